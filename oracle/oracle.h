@@ -1,0 +1,169 @@
+/*
+ * oracle.h -- plain, slow CPU oracle for one EAGLE-style verify/accept step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library is loaded by the test suite, by the
+ * package smoke check and by the CPU-baseline leg of the benchmark, and by
+ * nothing else.  It shares no code, header, table or helper with the GPU
+ * library: it includes none of its headers and the GPU library includes none
+ * of these.  Both sides meet only at the seeded input generator.
+ *
+ * Sources (web pages), cited in this file as [KEY section]:
+ *   [SGL-XI]  "SGLang 源码完全拆解(十一):投机解码——草稿生成、批量验证与 token 接受如何接进同一条前向"
+ *   [ACCEPT]  "投机解码 Accept从 Verify 行到最终输出路径"
+ *   [EVOL]    "SGLang 设计演进投机解码、PD 分离与大规模 EP（2025 上半年）", chapter "EAGLE 投机解码四部曲"
+ *   [INTERN]  "Speculative Decoding" (SGLang internals, part 3, execution model)
+ *   [EAGLE2]  "把投机采样讲透：以 SGLang 中的 EAGLE-2 为例"
+ *
+ * Arithmetic is fp64 except where the method itself hands values over in a
+ * narrower type: probabilities leave the softmax as fp32, a path score is one
+ * correctly rounded fp32 product, and the accept test compares fp32 values.
+ *
+ * Conventions shared by every function:
+ *   - every pointer is a host pointer owned by the caller; nothing is kept;
+ *   - "row" of a request b and tree node i is the flattened verify row b*n+i;
+ *   - -1 means "none" in every tree pointer and in accept_index padding;
+ *   - return value 0 = success; ORC_EARG = bad argument; ORC_EBOUNDS = an index
+ *     read from an input array is out of range; ORC_EINVARIANT = an input breaks
+ *     an invariant of the method (for example a selected node whose parent was
+ *     not selected).
+ *
+ * Parity status: every function is pinned by tests against values the pages
+ * print, closed forms, library routines or brute force, except the rejection
+ * sampler on trees with more than one child per node, whose multi-sibling rule
+ * is pinned only by its single-candidate special case, the T=0 == greedy
+ * identity and a distribution test: "parity unpinned" beyond those.
+ */
+#ifndef ACCEPT_SELECT_TOP_ORACLE_H
+#define ACCEPT_SELECT_TOP_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+#define ORC_OK 0
+#define ORC_EARG 1
+#define ORC_EBOUNDS 2
+#define ORC_EINVARIANT 3
+
+/* c1 -- per-row softmax and top-k of the draft distribution.
+ * [SGL-XI select_top_k_tokens]: each draft row yields topk_p (its top-k
+ * probabilities) and topk_index (their token ids).
+ * p_v = exp((l_v - max l)/T) / sum_w exp((l_w - max l)/T), fp64, rounded to fp32.
+ * The k tokens are the k largest logits ordered by (logit desc, token id asc).
+ * logits: [rows, V] of dtype (ORC_F32 or ORC_BF16 bit patterns).
+ * topk_p, topk_idx: [rows, k]. */
+int oracle_softmax_topk(int rows, int V, int dtype, const void* logits,
+                        double temperature, int k, float* topk_p, int32_t* topk_idx);
+
+/* c2 -- one step of select_top_k_tokens given the rows' top-k.
+ * [SGL-XI organize_draft_results] (_select_top_k_tokens_first / _later).
+ * step 0: rows = 1 per request; score block = topk_p [b,k]; tokens = topk_idx
+ *   [b,k]; parent block = [-1, 0, .., k-1] [b,k+1]; next scores = topk_p.
+ * step i>=1: rows = k per request; expand[r*k+j] = fp32(scores_in[r]*topk_p[r,j]);
+ *   score block = expand [b,k*k]; tokens = topk_idx [b,k*k]; the k best expand
+ *   values by (value desc, flat index asc), in that order, give
+ *   parent block = sel + k*k*(i-1) + k [b,k], next scores = expand[sel],
+ *   next input ids = tokens[sel]. */
+int oracle_path_step(int step, int b, int k, const float* topk_p,
+                     const int32_t* topk_idx, const float* scores_in,
+                     float* score_blk, int32_t* token_blk, int32_t* parent_blk,
+                     float* scores_out, int32_t* next_ids);
+
+/* c1 followed by c2 on draft logits [b*(step ? k : 1), V]; topk_p_out may be NULL. */
+int oracle_select_topk(int step, int b, int k, int V, int dtype,
+                       const void* draft_logits, double temperature,
+                       const float* scores_in, float* score_blk,
+                       int32_t* token_blk, int32_t* parent_blk,
+                       float* scores_out, int32_t* next_ids, float* topk_p_out);
+
+/* c3..c5 -- organize_draft_results followed by build_tree_kernel_efficient.
+ * [SGL-XI organize_draft_results], [SGL-XI build_tree_kernel_efficient],
+ * [ACCEPT section 2], [EAGLE2 sections 4.3, 5.3, 5.4].
+ * score_space, token_space: [b, C], C = k + (S-1)*k*k (all S blocks, in step order);
+ * parent_space: [b, 1 + (S-1)*k] (the parent blocks of steps 0..S-2).
+ * Outputs (all [b*n] unless stated): draft_tokens, positions, retrieve_index,
+ * next_token, next_sibling (node indices local to the request), mask_bits
+ * (one uint64 per row, bit j set iff node j is an ancestor of the row's node or
+ * the node itself), parent_node (optional, may be NULL). n <= 64. */
+int oracle_build_tree(int b, int k, int S, int n, const float* score_space,
+                      const int32_t* token_space, const int32_t* parent_space,
+                      const int32_t* bonus, const int32_t* seq_lens,
+                      int32_t* draft_tokens, int32_t* positions,
+                      int32_t* retrieve_index, int32_t* next_token,
+                      int32_t* next_sibling, uint64_t* mask_bits,
+                      int32_t* parent_node);
+
+/* c6 -- tree-masked verify attention, fp64.
+ * [EAGLE2 sections 4.2-4.3]: the queries are the tree nodes; the keys are the
+ * request's cached prefix (positions 0..seq_len-1 through req_to_token, all
+ * visible) followed by the tree nodes whose mask bit is set (through verify_loc).
+ * q: [b*n, Hq, D] bf16 bits; k_pool, v_pool: [num_slots, Hkv, D] bf16 bits;
+ * q head h reads kv head h / (Hq/Hkv).  out: [b*n, Hq, D] fp64 and lse:
+ * [b*n, Hq] fp64 (natural log), both optional.  With pairs != NULL only the
+ * n_pairs (row, head) pairs listed are computed and written (pairs is
+ * [n_pairs, 2]); other outputs are left untouched. */
+int oracle_verify_attention(int b, int n, int Hq, int Hkv, int D,
+                            const uint16_t* q, const uint16_t* k_pool,
+                            const uint16_t* v_pool, int64_t num_slots,
+                            const int32_t* req_to_token, int row_w,
+                            const int32_t* req_pool_idx, const int32_t* seq_lens,
+                            const int32_t* verify_loc, const uint64_t* mask_bits,
+                            double scale, int n_pairs, const int32_t* pairs,
+                            double* out, double* lse);
+
+/* c7 -- greedy accept.  [SGL-XI eagle_sample], [ACCEPT section 3], [EAGLE2 5.3].
+ * logits: [b*n, V]; accept_index, accepted_tokens: [b, S+1]; predict: [b*n];
+ * accept_lens, next_root: [b].  accepted_tokens and next_root may be NULL. */
+int oracle_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits,
+                         const int32_t* draft_tokens, const int32_t* retrieve_index,
+                         const int32_t* next_token, const int32_t* next_sibling,
+                         int32_t* predict, int32_t* accept_index,
+                         int32_t* accept_lens, int32_t* accepted_tokens,
+                         int32_t* next_root);
+
+/* c8 -- rejection-sampling accept.  [ACCEPT section 4], [INTERN accept/reject],
+ * [EAGLE2 5.6], [SGL-XI eagle_sample].
+ * draft_probs: [b*n, V] fp32, row of node i = the distribution node i's children
+ * were proposed from; temperatures: [b] (<= 0 means greedy); u: [b*n] (one coin
+ * per child node, u[b*n+0] unused); u_final: [b].  Outputs as c7. */
+int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits,
+                           const float* draft_probs, const float* temperatures,
+                           const float* u, const float* u_final,
+                           const int32_t* draft_tokens, const int32_t* retrieve_index,
+                           const int32_t* next_token, const int32_t* next_sibling,
+                           int32_t* predict, int32_t* accept_index,
+                           int32_t* accept_lens, int32_t* accepted_tokens,
+                           int32_t* next_root);
+
+/* c9 -- KV commit.  [SGL-XI KV 回写], [ACCEPT section 3 (input/output shift)],
+ * [EVOL 草稿、验证与槽位].
+ * For request b with L = accept_lens[b] and k < L:
+ *   dst_k = req_to_token[req_pool_idx[b]*row_w + seq_lens[b] + k],
+ *   src_k = verify_loc[accept_index[b*W + k]];
+ * every src row is read (all layers, K and V, [Hkv, D]) before any dst row is
+ * written.  new_seq_lens[b] = seq_lens[b] + L.
+ * Free list, request order, then ascending node order:
+ *   page_size == 1: every verify slot of the request that is no dst slot;
+ *   page_size  > 1: every page (slot / page_size) that holds a verify slot of
+ *   the request and no dst slot of the request, listed once, at its first node.
+ * k_layers, v_layers: arrays of num_layers host pointers to [num_slots, Hkv, D]
+ * bf16 pools (modified in place); free_ids: [>= b*n]; n_free: one int. */
+int oracle_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers,
+                     int page_size, uint16_t* const* k_layers,
+                     uint16_t* const* v_layers, int64_t num_slots,
+                     const int32_t* req_to_token, int row_w,
+                     const int32_t* req_pool_idx, const int32_t* seq_lens,
+                     const int32_t* verify_loc, const int32_t* accept_index,
+                     const int32_t* accept_lens, int32_t* new_seq_lens,
+                     int32_t* free_ids, int32_t* n_free);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

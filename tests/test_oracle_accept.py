@@ -1,0 +1,272 @@
+"""Oracle pins for the accept step: greedy walk and rejection sampling (CPU only)."""
+import numpy as np
+import pytest
+import scipy.stats
+
+import oracle
+from accept_select_top_gb300 import workloads as W
+from oracle import pipeline as P
+from tests.helpers import golden, onehot_logits, pointers_from_parents
+
+
+def _rabcd():
+    fx = golden("rabcd_greedy.json")
+    tok = fx["tokens"]
+    nodes = fx["nodes"]
+    n = len(nodes)
+    draft = np.array([tok[x] for x in nodes], np.int32)
+    nt, ns = pointers_from_parents(fx["parents"])
+    logits = onehot_logits([tok[fx["target_argmax"][x]] for x in nodes], fx["V"])
+    return fx, n, draft, nt, ns, logits
+
+
+def test_rabcd_greedy():
+    fx, n, draft, nt, ns, logits = _rabcd()
+    tok, ex = fx["tokens"], fx["expect"]
+    S = 2
+    o = oracle.verify_greedy(1, n, S, logits, draft, np.arange(n), nt, ns)
+    W_ = S + 1
+    assert o["accept_index"][0, : ex["accept_lens"]].tolist() == ex["accept_rows"]
+    assert (o["accept_index"][0, ex["accept_lens"]:] == -1).all()
+    assert o["accept_lens"].tolist() == [ex["num_correct_drafts"] + 1] == [ex["accept_lens"]]
+    expect_pred = np.zeros(n, np.int32)
+    for row, name in ex["predict"].items():
+        expect_pred[int(row)] = tok[name]
+    assert o["predict"].tolist() == expect_pred.tolist()
+    assert o["accepted_tokens"][0, : ex["accept_lens"]].tolist() == [tok[x] for x in ex["accepted_tokens"]]
+    assert o["next_root"].tolist() == [tok[ex["next_root"]]]
+    # the rows that feed the KV commit are the input rows R, A, C, not the output X
+    rows = o["accept_index"][0, : o["accept_lens"][0]]
+    assert [fx["nodes"][r] for r in rows] == ex["committed_rows"]
+    assert W_ == o["accept_index"].shape[1]
+
+
+def test_rabcd_greedy_batched_rows_are_global():
+    """accept_index holds flattened rows b*n+i of the whole batch."""
+    fx, n, draft, nt, ns, logits = _rabcd()
+    b = 3
+    o = oracle.verify_greedy(b, n, 2, np.tile(logits, (b, 1)), np.tile(draft, b),
+                             np.arange(b * n), np.tile(nt, b), np.tile(ns, b))
+    for r in range(b):
+        assert o["accept_index"][r].tolist() == [r * n + x for x in fx["expect"]["accept_rows"]]
+
+
+def test_eagle2_walk_root_a_d():
+    fx = golden("eagle2_child_sibling.json")
+    nodes = fx["nodes"]
+    n = len(nodes)
+    tok = {x: 10 + i for i, x in enumerate(nodes)}
+    tok["bonus"] = 30
+    draft = np.array([tok[x] for x in nodes], np.int32)
+    want = {"root": tok["A"], "A": tok["D"], "D": tok["bonus"]}
+    logits = onehot_logits([want.get(x, 31) for x in nodes], 32)
+    o = oracle.verify_greedy(1, n, 3, logits, draft, np.arange(n), np.array(fx["next_token"]),
+                             np.array(fx["next_sibling"]))
+    L = o["accept_lens"][0]
+    assert [nodes[i] for i in o["accept_index"][0, :L]] == fx["walk"]["accepted"]
+    assert L - 1 == fx["walk"]["num_correct_drafts"]
+
+
+def test_chain_the_cat_sat():
+    fx = golden("chain_topk1.json")
+    tok = fx["tokens"]
+    names = [fx["root"]] + fx["draft_chain"]
+    draft = np.array([tok[x] for x in names], np.int32)
+    nt, ns = pointers_from_parents([-1, 0, 1, 2])
+    logits = onehot_logits([tok[x] for x in fx["target_argmax"]], 8)
+    o = oracle.verify_greedy(1, 4, fx["S"], logits, draft, np.arange(4), nt, ns)
+    ex = fx["expect"]
+    assert o["accept_lens"][0] == ex["accept_lens"] == ex["num_correct_drafts"] + 1
+    assert o["accepted_tokens"][0, :3].tolist() == [tok[x] for x in ex["accepted_tokens"]]
+    assert o["accepted_tokens"][0, 3] == -1
+
+
+def test_dspark_chain_counts():
+    fx = golden("chain_commit.json")
+    tok = fx["tokens"]
+    draft = np.array([tok[x] for x in fx["nodes"]], np.int32)
+    nt, ns = pointers_from_parents([-1, 0, 1, 2])
+    logits = onehot_logits([tok[x] for x in fx["target_argmax"]], 8)
+    o = oracle.verify_greedy(1, 4, 3, logits, draft, np.arange(4), nt, ns)
+    ex = fx["expect"]
+    assert o["accept_lens"][0] - 1 == ex["correct_len"]
+    assert o["accept_lens"][0] == ex["commit_lens"]
+    assert o["accepted_tokens"][0, :3].tolist() == [tok[x] for x in ex["accepted_tokens"]]
+
+
+def test_greedy_first_sibling_wins_and_root_only():
+    """Two siblings with the same token: the first in sibling order is taken.
+    No matching child: only the root row, accept_lens 1, output = target at root."""
+    draft = np.array([1, 5, 5, 6], np.int32)
+    nt, ns = pointers_from_parents([-1, 0, 0, 1])
+    o = oracle.verify_greedy(1, 4, 3, onehot_logits([5, 6, 7, 7], 8), draft, np.arange(4), nt, ns)
+    assert o["accept_index"][0].tolist() == [0, 1, 3, -1]
+    o = oracle.verify_greedy(1, 4, 3, onehot_logits([4, 6, 7, 7], 8), draft, np.arange(4), nt, ns)
+    assert o["accept_index"][0].tolist() == [0, -1, -1, -1]
+    assert o["accept_lens"][0] == 1 and o["predict"].tolist() == [4, 0, 0, 0]
+
+
+def test_greedy_argmax_ties_lowest_index():
+    draft = np.array([1, 3, 2], np.int32)
+    nt, ns = pointers_from_parents([-1, 0, 0])
+    x = np.zeros((3, 8), np.float32)
+    x[0, [2, 3]] = 1.0  # tie between tokens 2 and 3: token 2 wins -> node 2
+    o = oracle.verify_greedy(1, 3, 1, x, draft, np.arange(3), nt, ns)
+    assert o["accept_index"][0].tolist() == [0, 2]
+
+
+def _tiny_case(seed=0, mode="sampling"):
+    wl = W.WORKLOADS["tiny"]
+    drafts_t = [W.draft_logits(wl, i, seed=seed) for i in range(wl.S)]
+    drafts = [W.host(d) for d in drafts_t]
+    lay = W.kv_layout(wl, seed=seed)
+    ch = P.select_chain(wl, drafts)
+    tree = P.tree_from_chain(wl, ch, W.host(W.bonus_tokens(wl, seed=seed)), lay["seq_lens"])
+    rows = W.draft_rows_of_nodes(wl, tree["draft_tokens"], tree["next_token"], tree["next_sibling"],
+                                 ch["token_space"], ch["parent_space"])
+    all_d = torch_cat(drafts_t)
+    logits = W.target_logits(wl, rows, all_d, seed=seed)
+    temps = W.request_temperatures(wl, mode)
+    q = W.draft_probs(wl, rows, all_d, temps)
+    u, uf = W.coins(wl, seed=seed)
+    return wl, tree, W.host(logits), W.host(q), temps, W.host(u), W.host(uf)
+
+
+def torch_cat(ts):
+    import torch
+    return torch.cat(ts, 0)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_t0_sampling_equals_greedy(seed):
+    wl, tree, logits, q, temps, u, uf = _tiny_case(seed, "greedy")
+    g = P.accept(wl, "greedy", tree, logits)
+    s = P.accept(wl, "sampling", tree, logits, q, np.zeros(wl.b, np.float32), u, uf)
+    for key in g:
+        np.testing.assert_array_equal(g[key], s[key], err_msg=key)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sampling"])
+@pytest.mark.parametrize("seed", range(5))
+def test_accept_invariants(mode, seed):
+    """accept_lens = drafts + 1; the valid prefix of accept_index is a root-to-
+    node path through parent -> child links; predict[accept_index] = accepted
+    draft tokens followed by the terminal token."""
+    wl, tree, logits, q, temps, u, uf = _tiny_case(seed, mode)
+    o = P.accept(wl, mode, tree, logits, q, temps, u, uf)
+    b, n = wl.b, wl.n
+    par = tree["parent_node"].reshape(b, n)
+    for r in range(b):
+        L = o["accept_lens"][r]
+        rows = o["accept_index"][r, :L]
+        assert (o["accept_index"][r, L:] == -1).all()
+        assert rows[0] == r * n
+        for d in range(1, L):
+            assert par[r, rows[d] - r * n] == rows[d - 1] - r * n
+        toks = o["predict"][rows]
+        assert toks[:-1].tolist() == tree["draft_tokens"][rows[1:]].tolist()
+        assert o["accepted_tokens"][r, :L].tolist() == toks.tolist()
+        assert o["next_root"][r] == toks[-1]
+        visited = set(rows.tolist())
+        for i in range(r * n, (r + 1) * n):
+            if i not in visited:
+                assert o["predict"][i] == 0
+        if mode == "greedy":
+            assert toks[-1] == np.argmax(logits[rows[-1]])
+
+
+def _single_candidate(p, q, u, uf, x, leaf_logits=None):
+    """b single-candidate chains: root (target p, draft q) with one child x."""
+    b = len(u)
+    V = len(p)
+    logits = np.empty((b * 2, V), np.float32)
+    logits[0::2] = np.log(np.asarray(p, np.float64)).astype(np.float32)
+    logits[1::2] = leaf_logits if leaf_logits is not None else np.log(np.full(V, 1.0 / V)).astype(np.float32)
+    qq = np.zeros((b * 2, V), np.float32)
+    qq[0::2] = np.asarray(q, np.float32)
+    draft = np.empty(b * 2, np.int32)
+    draft[0::2] = 0
+    draft[1::2] = x
+    uu = np.zeros(b * 2, np.float32)
+    uu[1::2] = u
+    nt = np.tile(np.array([1, -1], np.int32), b)
+    ns = np.full(b * 2, -1, np.int32)
+    return oracle.verify_sampling(b, 2, 1, logits, qq, np.ones(b, np.float32), uu,
+                                  np.asarray(uf, np.float32), draft, np.arange(b * 2), nt, ns)
+
+
+def test_rejection_example_points():
+    fx = golden("rejection_example.json")
+    p, q = fx["p"], fx["q"]
+    leaf = np.log(np.array([0.2, 0.5, 0.3])).astype(np.float32)
+    o = _single_candidate(p, q, [0.49, 0.49, 0.51, 0.51, 0.51], [0.1, 0.5, 0.3, 0.34, 0.99], 0, leaf)
+    # u < 0.5 accepts A; then A is a leaf and the bonus comes from its own p
+    assert o["accept_lens"].tolist() == [2, 2, 1, 1, 1]
+    assert o["accepted_tokens"][:2, :2].tolist() == [[0, 0], [0, 1]]
+    # rejected: residual (0, 0.1, 0.2)/0.3 -> B below 1/3, C above
+    assert o["accepted_tokens"][2:, 0].tolist() == [1, 2, 2]
+
+
+def test_rejection_example_distribution_closed_form():
+    """Quadrature over (x ~ q, u, u_final) on a midpoint grid: the first output
+    token is distributed as p, the accept probability of A is 0.5 and the
+    rejected mass lands on B and C as 1/3, 2/3."""
+    fx = golden("rejection_example.json")
+    p, q = np.array(fx["p"]), np.array(fx["q"])
+    G = 300
+    grid = (np.arange(G) + 0.5) / G
+    uu, ff = np.meshgrid(grid, grid, indexing="ij")
+    uu, ff = uu.ravel(), ff.ravel()
+    dist = np.zeros(3)
+    for x in range(3):
+        o = _single_candidate(p, q, uu, ff, x)
+        first = o["accepted_tokens"][:, 0]
+        acc = o["accept_lens"] == 2
+        if x == 0:
+            assert abs(acc.mean() - fx["expect"]["accept_prob_A"]) < 2.0 / G
+            rej = first[~acc]
+            frac = np.bincount(rej, minlength=3) / len(rej)
+            np.testing.assert_allclose(frac, fx["expect"]["residual_normalised"], atol=2.0 / G)
+        dist += q[x] * np.bincount(first, minlength=3) / len(first)
+    np.testing.assert_allclose(dist, fx["expect"]["combined"], atol=2.0 / G)
+
+
+def test_rejection_chi_square():
+    """V=16, 1e5 single-candidate trials with x drawn from q: the output is
+    distributed as p and the acceptance rate is sum(min(p, q))."""
+    rng = np.random.default_rng(7)
+    V, N = 16, 100_000
+    p = rng.dirichlet(np.full(V, 0.8))
+    q = rng.dirichlet(np.full(V, 0.8))
+    pf = np.exp(np.log(p).astype(np.float32).astype(np.float64))
+    pf /= pf.sum()
+    x = np.searchsorted(np.cumsum(q), rng.random(N), side="right").clip(0, V - 1)
+    u = rng.random(N).astype(np.float32)
+    uf = rng.random(N).astype(np.float32)
+    o = _single_candidate(p, q.astype(np.float32), u, uf, x)
+    first = o["accepted_tokens"][:, 0]
+    counts = np.bincount(first, minlength=V)
+    stat, pval = scipy.stats.chisquare(counts, pf * N)
+    assert pval > 1e-3, (stat, pval)
+    acc = (o["accept_lens"] == 2).mean()
+    a = np.minimum(pf, q).sum()
+    assert abs(acc - a) < 4 * np.sqrt(a * (1 - a) / N)
+
+
+def test_residual_zero_falls_back_to_p():
+    """q == p at the only child's row and the child rejected: Z would be 0 only
+    if p <= q everywhere; here q puts all mass on x, p does not, so the
+    residual is p without x."""
+    p = np.array([0.5, 0.25, 0.25])
+    q = np.array([1.0, 0.0, 0.0], np.float32)
+    o = _single_candidate(p, q, [0.9], [0.0], 0)
+    assert o["accept_lens"][0] == 1 and o["accepted_tokens"][0, 0] == 1
+    # q == p with the child on a zero-probability token: u*0 < 0 fails, the
+    # residual max(0, p - q) is zero everywhere (Z == 0) and the bonus comes from p
+    p = np.array([0.5, 0.5, 0.0])
+    o = _single_candidate(p, p.astype(np.float32), [0.3], [0.74], 2)
+    assert o["accept_lens"][0] == 1 and o["accepted_tokens"][0, 0] == 1
+    # with q == p > 0 at the child, u*q < p holds for every u < 1: always accepted
+    p = np.array([0.25, 0.25, 0.5])
+    o = _single_candidate(p, p.astype(np.float32), [0.999999], [0.74], 2)
+    assert o["accept_lens"][0] == 2
