@@ -1,0 +1,149 @@
+// build_tree.cu -- organize_draft_results followed by build_tree, one CTA per
+// request.
+//
+// [SGL-XI organize_draft_results (topk over the score list, sort of the
+// indices, gather of the tokens, parent list)], [SGL-XI build_tree_kernel_efficient
+// (bonus token at node 0, positions = prefix + depth, retrieve_* child/sibling
+// arrays, bit-packed QLEN_ONLY mask)], [ACCEPT section 2], [EAGLE2 sections 4.3, 5.3].
+//
+// Steps inside the CTA (all in shared memory):
+//   1. rank every score position among the C positions (value desc, index
+//      asc); the n-1 with rank < n-1 are selected;
+//   2. compact the selected positions in ascending order (warp ballots) ->
+//      node j = 1 + its rank among the selected positions;
+//   3. parent of node j: position parent_space[p / k] (-1 = root) mapped back
+//      to its node through a position -> node table;
+//   4. ancestors by walking parent pointers (<= n steps): mask row, depth;
+//   5. first child / next sibling by scanning the parent array.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace spec {
+
+namespace {
+
+constexpr int kBuildThreads = 512;
+
+__global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a) {
+  extern __shared__ unsigned char smem_raw[];
+  const int req = blockIdx.x;
+  const int C = a.k + (a.S - 1) * a.k * a.k;
+  const int P = 1 + (a.S - 1) * a.k;
+  const int n = a.n, need = n - 1;
+  float* sc = reinterpret_cast<float*>(smem_raw);                      // [C]
+  int* node_of = reinterpret_cast<int*>(sc + C);                       // [C]
+  unsigned char* sel = reinterpret_cast<unsigned char*>(node_of + C);  // [C]
+  __shared__ int sel_pos[kMaxN];
+  __shared__ int par[kMaxN];
+  __shared__ int warp_base[kBuildThreads / 32 + 1];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+
+  const float* srow = a.score_space + size_t(req) * C;
+  for (int p = tid; p < C; p += blockDim.x) sc[p] = srow[p];
+  __syncthreads();
+
+  // 1. selection by rank (counting stops once n-1 better ones are found)
+  for (int p = tid; p < C; p += blockDim.x) {
+    const float v = sc[p];
+    int rank = 0;
+    for (int q = 0; q < C && rank < need; ++q) rank += better(sc[q], q, v, p);
+    sel[p] = rank < need;
+    node_of[p] = -1;
+  }
+  __syncthreads();
+
+  // 2. ascending compaction: each warp counts its contiguous slice, then assigns
+  const int per_warp = (C + nw - 1) / nw;
+  const int lo = w * per_warp, hi = min(C, lo + per_warp);
+  int cnt = 0;
+  for (int p0 = lo; p0 < hi; p0 += 32) {
+    const int p = p0 + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, p < hi && sel[p]));
+  }
+  if (lane == 0) warp_base[w + 1] = cnt;
+  __syncthreads();
+  if (tid == 0) {
+    warp_base[0] = 0;
+    for (int i = 1; i <= nw; ++i) warp_base[i] += warp_base[i - 1];
+  }
+  __syncthreads();
+  int base = warp_base[w];
+  for (int p0 = lo; p0 < hi; p0 += 32) {
+    const int p = p0 + lane;
+    const bool s = p < hi && sel[p];
+    const unsigned bal = __ballot_sync(0xffffffffu, s);
+    if (s) {
+      const int j = base + __popc(bal & ((1u << lane) - 1));
+      if (j < need) {
+        sel_pos[j] = p;
+        node_of[p] = j + 1;
+      }
+    }
+    base += __popc(bal);
+  }
+  __syncthreads();
+
+  // 3. parents
+  const int* prow = a.parent_space + size_t(req) * P;
+  for (int j = tid; j < n; j += blockDim.x) {
+    if (j == 0) {
+      par[0] = -1;
+      continue;
+    }
+    const int p = sel_pos[j - 1];
+    const int t = p / a.k;
+    int parent = 0;
+    const int ppos = t < P ? prow[t] : -2;
+    if (ppos >= 0 && ppos < C && node_of[ppos] > 0 && node_of[ppos] < j) {
+      parent = node_of[ppos];
+    } else if (ppos != -1) {
+      raise_error(a.error, SPEC_DEV_INVARIANT);
+    }
+    par[j] = parent;
+  }
+  __syncthreads();
+
+  // 4.-5. per node outputs
+  const size_t rb = size_t(req) * n;
+  for (int i = tid; i < n; i += blockDim.x) {
+    uint64_t m = 0;
+    int depth = -1, x = i;
+    for (int g = 0; x >= 0 && g <= n; ++g) {
+      m |= uint64_t(1) << x;
+      ++depth;
+      x = par[x];
+    }
+    int first = -1;
+    for (int c = i + 1; c < n && first < 0; ++c)
+      if (par[c] == i) first = c;
+    int sib = -1;
+    if (i > 0)
+      for (int c = i + 1; c < n && sib < 0; ++c)
+        if (par[c] == par[i]) sib = c;
+    a.mask_bits[rb + i] = m;
+    a.positions[rb + i] = a.seq_lens[req] + depth;
+    a.retrieve_index[rb + i] = int(rb + i);
+    a.next_token[rb + i] = first;
+    a.next_sibling[rb + i] = sib;
+    a.draft_tokens[rb + i] = i == 0 ? a.bonus[req] : a.token_space[size_t(req) * C + sel_pos[i - 1]];
+  }
+}
+
+}  // namespace
+
+size_t build_tree_smem_bytes(int k, int S) {
+  const size_t C = size_t(k) + size_t(S - 1) * k * k;
+  return C * (sizeof(float) + sizeof(int) + 1);
+}
+
+int launch_build_tree(const BuildParams& p, cudaStream_t stream) {
+  const size_t smem = build_tree_smem_bytes(p.k, p.S);
+  if (smem > 200 * 1024) return SPEC_ERR_ARG;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  build_tree_kernel<<<p.b, kBuildThreads, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+}  // namespace spec

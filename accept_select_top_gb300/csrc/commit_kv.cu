@@ -1,0 +1,148 @@
+// commit_kv.cu -- move the accepted rows' KV into the sequence and release the
+// slots (or pages) the accepted path does not keep.
+//
+// [SGL-XI KV 回写: move_accept_tokens_to_target_kvcache -- target slots from
+// req_to_token over [seq_len, seq_len + accept_len), source slots
+// out_cache_loc[accept_index] (accept_index holds global rows, -1 unused),
+// size by accept_index's width, not by num_draft_tokens], [ACCEPT section 3:
+// the committed rows are the input rows R, A, C, not the output X],
+// [EVOL 草稿、验证与槽位: only the accepted path's slots are kept].
+//
+// Grid: one CTA per request.  The CTA reads every source row of the request
+// (all layers, K and V) into shared memory before writing any target row, in
+// column slices small enough for shared memory; a target that is also a later
+// source is therefore never clobbered.  Each CTA stages its request's free
+// units in the workspace; the CTA arriving last concatenates them in request
+// order into free_ids and writes n_free.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace spec {
+
+namespace {
+
+constexpr int kCommitThreads = 256;
+constexpr int kSliceBytes = 32 * 1024;  // shared staging per slice (K and V of all L rows)
+
+__global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) {
+  const int req = blockIdx.x;
+  const int n = a.n, W = a.W;
+  __shared__ long long src[kMaxN + 1], dst[kMaxN + 1];
+  __shared__ int s_ok, s_L;
+  __shared__ uint4 stage[kSliceBytes / 16];
+  int* stage_free = reinterpret_cast<int*>(a.partials) + size_t(req) * n;
+  int* counts = reinterpret_cast<int*>(a.partials) + size_t(a.b) * n;
+
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const int L = a.accept_lens[req];
+    const int s0 = a.seq_lens[req];
+    const int rq = a.req_pool_idx[req];
+    if (L < 1 || L > W || s0 < 0 || s0 + L > a.row_w) {
+      raise_error(a.error, SPEC_DEV_LENGTH);
+      ok = 0;
+    }
+    if (rq < 0 || rq >= a.req_rows) {
+      raise_error(a.error, SPEC_DEV_INDEX);
+      ok = 0;
+    }
+    s_L = ok ? L : 0;
+    s_ok = ok;
+  }
+  __syncthreads();
+  const int L = s_L;
+  for (int kk = threadIdx.x; kk < L; kk += blockDim.x) {
+    const int ai = a.accept_index[size_t(req) * W + kk];
+    long long s = -1, d = -1;
+    if (ai >= 0 && ai < a.b * n) s = a.verify_loc[ai];
+    d = a.req_to_token[size_t(a.req_pool_idx[req]) * a.row_w + a.seq_lens[req] + kk];
+    if (s < 0 || s >= a.num_slots || d < 0 || d >= a.num_slots) {
+      raise_error(a.error, SPEC_DEV_INDEX);
+      atomicExch(&s_ok, 0);
+    }
+    src[kk] = s;
+    dst[kk] = d;
+  }
+  __syncthreads();
+  const bool ok = s_ok;
+
+  if (ok) {
+    const int units = a.Hkv * a.D * 2 / 16;         // 16-byte units per slot row
+    const int slice = max(1, min(units, kSliceBytes / 16 / (2 * L)));
+    for (int layer = 0; layer < a.num_layers; ++layer) {
+      const uint4* kin = static_cast<const uint4*>(a.k_layers[layer]);
+      const uint4* vin = static_cast<const uint4*>(a.v_layers[layer]);
+      uint4* kout = static_cast<uint4*>(a.k_layers[layer]);
+      uint4* vout = static_cast<uint4*>(a.v_layers[layer]);
+      for (int c0 = 0; c0 < units; c0 += slice) {
+        const int cw = min(slice, units - c0);
+        const int tot = 2 * L * cw;
+        for (int t = threadIdx.x; t < tot; t += blockDim.x) {
+          const int which = t / (L * cw), rem = t % (L * cw), kk = rem / cw, col = rem % cw;
+          const uint4* pool = which ? vin : kin;
+          stage[t] = pool[size_t(src[kk]) * units + c0 + col];
+        }
+        __syncthreads();
+        for (int t = threadIdx.x; t < tot; t += blockDim.x) {
+          const int which = t / (L * cw), rem = t % (L * cw), kk = rem / cw, col = rem % cw;
+          uint4* pool = which ? vout : kout;
+          pool[size_t(dst[kk]) * units + c0 + col] = stage[t];
+        }
+        __syncthreads();
+      }
+    }
+  }
+  if (threadIdx.x == 0) a.new_seq_lens[req] = a.seq_lens[req] + (ok ? L : 0);
+
+  // free units of this request, in ascending node order (one thread: n <= 64)
+  if (threadIdx.x == 0) {
+    int cnt = 0;
+    if (ok) {
+      const long long ps = a.page_size;
+      for (int j = 0; j < n; ++j) {
+        const long long slot = a.verify_loc[size_t(req) * n + j];
+        if (slot < 0 || slot >= a.num_slots) {
+          raise_error(a.error, SPEC_DEV_INDEX);
+          continue;
+        }
+        const long long unit = slot / ps;
+        bool kept = false;
+        for (int kk = 0; kk < L && !kept; ++kk) kept = dst[kk] / ps == unit;
+        if (kept) continue;
+        bool listed = false;
+        for (int jj = 0; jj < j && !listed; ++jj) listed = a.verify_loc[size_t(req) * n + jj] / ps == unit;
+        if (listed) continue;
+        stage_free[cnt++] = int(unit);
+      }
+    }
+    counts[req] = cnt;
+  }
+
+  if (!arrive_last(a.counters, uint32_t(a.b))) return;
+
+  // ---- the last CTA concatenates the staged lists in request order ----
+  __shared__ int s_off;
+  if (threadIdx.x == 0) s_off = 0;
+  __syncthreads();
+  for (int r = 0; r < a.b; ++r) {
+    const int c = __ldcg(counts + r);
+    const int* from = reinterpret_cast<const int*>(a.partials) + size_t(r) * n;
+    for (int t = threadIdx.x; t < c; t += blockDim.x) a.free_ids[s_off + t] = __ldcg(from + t);
+    __syncthreads();
+    if (threadIdx.x == 0) s_off += c;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *a.n_free = s_off;
+  counter_reset(a.counters);
+}
+
+}  // namespace
+
+size_t commit_partial_bytes(int b, int n) { return align256(size_t(b) * n * 4 + size_t(b) * 4); }
+
+int launch_commit_kv(const CommitParams& p, cudaStream_t stream) {
+  commit_kernel<<<p.b, kCommitThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+}  // namespace spec

@@ -1,0 +1,151 @@
+// kernels.cuh -- launch parameters of the verify/accept kernels (device side of
+// the C ABI in accept_select_top.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spec {
+
+struct SelectParams {
+  int step, b, k, V, dtype;
+  const void* logits;
+  float temperature;
+  const float* scores_in;
+  float* score_blk;
+  int32_t* token_blk;
+  int score_ld;
+  int32_t* parent_blk;
+  int parent_ld;
+  float* scores_out;
+  int32_t* next_ids;
+  float* topk_p_out;
+  int rows, chunks, chunk_elems;
+  bool vec_ok;
+  uint32_t* error;
+  uint32_t* counters;
+  unsigned char* partials;
+};
+
+struct BuildParams {
+  int b, k, S, n;
+  const float* score_space;
+  const int32_t* token_space;
+  const int32_t* parent_space;
+  const int32_t* bonus;
+  const int32_t* seq_lens;
+  int32_t* draft_tokens;
+  int32_t* positions;
+  int32_t* retrieve_index;
+  int32_t* next_token;
+  int32_t* next_sibling;
+  uint64_t* mask_bits;
+  uint32_t* error;
+};
+
+struct GreedyParams {
+  int b, n, S, V, dtype;
+  const void* logits;
+  const int32_t* draft_tokens;
+  const int32_t* retrieve_index;
+  const int32_t* next_token;
+  const int32_t* next_sibling;
+  int32_t* predict;
+  int32_t* accept_index;
+  int32_t* accept_lens;
+  int32_t* accepted_tokens;
+  int32_t* next_root;
+  int chunks, chunk_elems;
+  bool vec_ok;
+  uint32_t* error;
+  uint32_t* counters;
+  unsigned char* partials;
+};
+
+struct SamplingParams {
+  int b, n, S, V, dtype;
+  const void* logits;
+  const float* draft_probs;
+  const float* temperatures;
+  const float* u;
+  const float* u_final;
+  const int32_t* draft_tokens;
+  const int32_t* retrieve_index;
+  const int32_t* next_token;
+  const int32_t* next_sibling;
+  int32_t* predict;
+  int32_t* accept_index;
+  int32_t* accept_lens;
+  int32_t* accepted_tokens;
+  int32_t* next_root;
+  int chunks, chunk_elems;    // pass 1 split of a verify row
+  int chunks2, chunk2_elems;  // pass 2 split of the terminal row
+  bool vec_ok;
+  uint32_t* error;
+  uint32_t* counters;
+  unsigned char* partials;   // pass 1 partials
+  unsigned char* state;      // per-request state handed from pass 1 to pass 2
+  unsigned char* partials2;  // pass 2 partials
+};
+
+struct AttentionParams {
+  int b, n, Hq, Hkv, D, page_size;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  long long num_slots;
+  const int32_t* req_to_token;
+  int req_rows, row_w;
+  const int32_t* req_pool_idx;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  const int32_t* verify_loc;
+  const uint64_t* mask_bits;
+  float scale;
+  void* out;
+  float* lse;
+  int splits;
+  uint32_t* error;
+  uint32_t* counters;
+  unsigned char* partials;
+};
+
+constexpr int kMaxLayers = 128;
+
+struct CommitParams {
+  int b, n, W, Hkv, D, num_layers, page_size;
+  void* k_layers[kMaxLayers];
+  void* v_layers[kMaxLayers];
+  long long num_slots;
+  const int32_t* req_to_token;
+  int req_rows, row_w;
+  const int32_t* req_pool_idx;
+  const int32_t* seq_lens;
+  const int32_t* verify_loc;
+  const int32_t* accept_index;
+  const int32_t* accept_lens;
+  int32_t* new_seq_lens;
+  int32_t* free_ids;
+  int32_t* n_free;
+  uint32_t* error;
+  uint32_t* counters;
+  unsigned char* partials;
+};
+
+int launch_select_topk(const SelectParams& p, cudaStream_t stream);
+int launch_build_tree(const BuildParams& p, cudaStream_t stream);
+int launch_verify_greedy(const GreedyParams& p, cudaStream_t stream);
+int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream);
+int launch_attention_simple(const AttentionParams& p, cudaStream_t stream);
+int launch_commit_kv(const CommitParams& p, cudaStream_t stream);
+
+size_t select_partial_bytes(int rows, int chunks);
+size_t build_tree_smem_bytes(int k, int S);
+size_t sampling_partial_bytes(int rows, int chunks);
+size_t sampling_state_bytes(int b);
+size_t sampling_partial2_bytes(int b, int chunks2);
+size_t commit_partial_bytes(int b, int n);
+int attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len);
+size_t attention_partial_bytes(int b, int n, int Hq, int D, int splits);
+
+}  // namespace spec

@@ -1,0 +1,348 @@
+// spec_api.cu -- the C ABI declared in accept_select_top.h: argument checks,
+// workspace sizing and layout, and kernel dispatch.  No call allocates memory
+// or synchronises the host, except spec_last_error.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "accept_select_top.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace spec;
+
+namespace {
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int elem_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : 2; }
+inline int vec_elems(int dtype) { return dtype == SPEC_F32 ? 4 : 8; }
+
+// Upper bound on the chunk count pick_split() returns for `rows` rows of V.
+inline int chunk_bound(long rows, int V) { return pick_split(rows, V, 1).chunks; }
+
+inline bool vec_ok(const void* logits, int V, int dtype) {
+  return aligned(logits, 16) && (size_t(V) * elem_bytes(dtype)) % 16 == 0;
+}
+
+size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
+  switch (op) {
+    case SPEC_OP_SELECT_TOPK: {
+      const size_t a = select_partial_bytes(b, chunk_bound(b, V));
+      const size_t c = select_partial_bytes(b * k, chunk_bound(long(b) * k, V));
+      return a > c ? a : c;
+    }
+    case SPEC_OP_BUILD_TREE:
+      return 0;
+    case SPEC_OP_VERIFY_GREEDY:
+      return align256(size_t(b) * n * chunk_bound(long(b) * n, V) * 8);
+    case SPEC_OP_VERIFY_SAMPLING:
+      return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
+             sampling_partial2_bytes(b, chunk_bound(b, V));
+    case SPEC_OP_VERIFY_ATTENTION:
+      return attention_partial_bytes(b, n, Hq, 128, attention_splits(b, n, Hq, Hkv, max_seq_len));
+    case SPEC_OP_COMMIT_KV:
+      return commit_partial_bytes(b, n);
+    default:
+      return 0;
+  }
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || !aligned(ws, 256)) return SPEC_ERR_WORKSPACE;
+  if (ws_bytes < need) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
+  if (b < 0 || op < 0 || op > SPEC_OP_COMMIT_KV) return 0;
+  if (b == 0) return kHeaderBytes + counters_bytes(0);
+  if (n < 1 || n > kMaxN || k < 1 || k > kMaxK || V < 1) return 0;
+  if (op == SPEC_OP_VERIFY_ATTENTION && (Hq < 1 || Hkv < 1 || Hq % Hkv || max_seq_len < 0)) return 0;
+  return kHeaderBytes + counters_bytes(b) + partial_bytes(op, b, n, k, V, Hq, Hkv, max_seq_len);
+}
+
+int spec_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return SPEC_ERR_WORKSPACE;
+  return cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_last_error(void* ws, void* stream) {
+  if (!ws) return SPEC_ERR_WORKSPACE;
+  uint32_t word = 0;
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaMemsetAsync(ws, 0, sizeof word, s) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  return int(word & 0x7fffffffu);
+}
+
+int spec_device_sm_count(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft_logits, float temperature,
+                     const float* scores_in, float* score_blk, int32_t* token_blk, int score_ld,
+                     int32_t* parent_blk, int parent_ld, float* scores_out, int32_t* next_input_ids,
+                     float* topk_p_out, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || step < 0 || k < 1 || k > kMaxK || V < k) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (!(temperature > 0.f)) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!draft_logits || !score_blk || !token_blk || !scores_out || !next_input_ids) return SPEC_ERR_ARG;
+  if (step > 0 && !scores_in) return SPEC_ERR_ARG;
+  if (score_ld < (step ? k * k : k)) return SPEC_ERR_ARG;
+  if (parent_blk && parent_ld < (step ? k : k + 1)) return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_SELECT_TOPK, b, 1, k, V, 0, 0, 0);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const WsView v = ws_view(ws, b);
+  SelectParams p{};
+  p.step = step;
+  p.b = b;
+  p.k = k;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = draft_logits;
+  p.temperature = temperature;
+  p.scores_in = scores_in;
+  p.score_blk = score_blk;
+  p.token_blk = token_blk;
+  p.score_ld = score_ld;
+  p.parent_blk = parent_blk;
+  p.parent_ld = parent_ld;
+  p.scores_out = scores_out;
+  p.next_ids = next_input_ids;
+  p.topk_p_out = topk_p_out;
+  p.rows = b * (step ? k : 1);
+  const RowSplit sp = pick_split(p.rows, V, vec_elems(dtype));
+  p.chunks = sp.chunks;
+  p.chunk_elems = sp.chunk_elems;
+  p.vec_ok = vec_ok(draft_logits, V, dtype);
+  p.error = v.error;
+  p.counters = v.counters;
+  p.partials = v.partials;
+  return launch_select_topk(p, as_stream(stream));
+}
+
+int spec_build_tree(int b, int k, int S, int n, const float* score_space, const int32_t* token_space,
+                    const int32_t* parent_space, const int32_t* bonus, const int32_t* seq_lens,
+                    int32_t* draft_tokens, int32_t* positions, int32_t* retrieve_index, int32_t* next_token,
+                    int32_t* next_sibling, uint64_t* mask_bits, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || k < 1 || k > kMaxK || S < 1 || n < 1 || n > kMaxN) return SPEC_ERR_ARG;
+  const long C = long(k) + long(S - 1) * k * k;
+  if (n - 1 > C || C > 16384) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!score_space || !token_space || !parent_space || !bonus || !seq_lens || !draft_tokens || !positions ||
+      !retrieve_index || !next_token || !next_sibling || !mask_bits)
+    return SPEC_ERR_ARG;
+  if (int rc = check_ws(ws, ws_bytes, kHeaderBytes)) return rc;
+  BuildParams p{};
+  p.b = b;
+  p.k = k;
+  p.S = S;
+  p.n = n;
+  p.score_space = score_space;
+  p.token_space = token_space;
+  p.parent_space = parent_space;
+  p.bonus = bonus;
+  p.seq_lens = seq_lens;
+  p.draft_tokens = draft_tokens;
+  p.positions = positions;
+  p.retrieve_index = retrieve_index;
+  p.next_token = next_token;
+  p.next_sibling = next_sibling;
+  p.mask_bits = mask_bits;
+  p.error = ws_view(ws, b).error;
+  return launch_build_tree(p, as_stream(stream));
+}
+
+int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, const void* q, const void* k_pool,
+                          const void* v_pool, int64_t num_slots, const int32_t* req_to_token, int req_rows,
+                          int row_w, const int32_t* req_pool_idx, const int32_t* seq_lens, int max_seq_len,
+                          const int32_t* verify_loc, const uint64_t* mask_bits, float scale, void* out,
+                          float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || n < 1 || n > kMaxN || Hq < 1 || Hkv < 1 || Hq % Hkv || page_size < 1) return SPEC_ERR_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (num_slots < 1 || req_rows < 1 || row_w < 1 || max_seq_len < 0) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!q || !k_pool || !v_pool || !req_to_token || !req_pool_idx || !seq_lens || !verify_loc || !mask_bits || !out)
+    return SPEC_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16)) return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_ATTENTION, b, n, 1, 1, Hq, Hkv, max_seq_len);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const WsView v = ws_view(ws, b);
+  AttentionParams p{};
+  p.b = b;
+  p.n = n;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.page_size = page_size;
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.num_slots = num_slots;
+  p.req_to_token = req_to_token;
+  p.req_rows = req_rows;
+  p.row_w = row_w;
+  p.req_pool_idx = req_pool_idx;
+  p.seq_lens = seq_lens;
+  p.max_seq_len = max_seq_len;
+  p.verify_loc = verify_loc;
+  p.mask_bits = mask_bits;
+  p.scale = scale;
+  p.out = out;
+  p.lse = lse;
+  p.splits = attention_splits(b, n, Hq, Hkv, max_seq_len);
+  p.error = v.error;
+  p.counters = v.counters;
+  p.partials = v.partials;
+  return launch_attention_simple(p, as_stream(stream));
+}
+
+int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
+                       const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,
+                       int32_t* predict, int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
+                       int32_t* next_root, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || n < 1 || n > kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (b == 0) return SPEC_OK;
+  if (!logits || !draft_tokens || !retrieve_index || !next_token || !next_sibling || !predict || !accept_index ||
+      !accept_lens)
+    return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const WsView v = ws_view(ws, b);
+  GreedyParams p{};
+  p.b = b;
+  p.n = n;
+  p.S = S;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = logits;
+  p.draft_tokens = draft_tokens;
+  p.retrieve_index = retrieve_index;
+  p.next_token = next_token;
+  p.next_sibling = next_sibling;
+  p.predict = predict;
+  p.accept_index = accept_index;
+  p.accept_lens = accept_lens;
+  p.accepted_tokens = accepted_tokens;
+  p.next_root = next_root;
+  const RowSplit sp = pick_split(long(b) * n, V, vec_elems(dtype));
+  p.chunks = sp.chunks;
+  p.chunk_elems = sp.chunk_elems;
+  p.vec_ok = vec_ok(logits, V, dtype);
+  p.error = v.error;
+  p.counters = v.counters;
+  p.partials = v.partials;
+  return launch_verify_greedy(p, as_stream(stream));
+}
+
+int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits, const float* draft_probs,
+                         const float* temperatures, const float* u, const float* u_final,
+                         const int32_t* draft_tokens, const int32_t* retrieve_index, const int32_t* next_token,
+                         const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
+                         int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (b < 0 || n < 1 || n > kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (b == 0) return SPEC_OK;
+  if (!logits || !draft_probs || !temperatures || !u || !u_final || !draft_tokens || !retrieve_index ||
+      !next_token || !next_sibling || !predict || !accept_index || !accept_lens)
+    return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_SAMPLING, b, n, 1, V, 0, 0, 0);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const WsView v = ws_view(ws, b);
+  SamplingParams p{};
+  p.b = b;
+  p.n = n;
+  p.S = S;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = logits;
+  p.draft_probs = draft_probs;
+  p.temperatures = temperatures;
+  p.u = u;
+  p.u_final = u_final;
+  p.draft_tokens = draft_tokens;
+  p.retrieve_index = retrieve_index;
+  p.next_token = next_token;
+  p.next_sibling = next_sibling;
+  p.predict = predict;
+  p.accept_index = accept_index;
+  p.accept_lens = accept_lens;
+  p.accepted_tokens = accepted_tokens;
+  p.next_root = next_root;
+  const RowSplit s1 = pick_split(long(b) * n, V, vec_elems(dtype));
+  const RowSplit s2 = pick_split(b, V, 1);
+  p.chunks = s1.chunks;
+  p.chunk_elems = s1.chunk_elems;
+  p.chunks2 = s2.chunks;
+  p.chunk2_elems = s2.chunk_elems;
+  p.vec_ok = vec_ok(logits, V, dtype);
+  p.error = v.error;
+  p.counters = v.counters;
+  p.partials = v.partials;
+  p.state = v.partials + sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V));
+  p.partials2 = p.state + sampling_state_bytes(b);
+  return launch_verify_sampling(p, as_stream(stream));
+}
+
+int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page_size, void* const* k_layers,
+                   void* const* v_layers, int64_t num_slots, const int32_t* req_to_token, int req_rows, int row_w,
+                   const int32_t* req_pool_idx, const int32_t* seq_lens, const int32_t* verify_loc,
+                   const int32_t* accept_index, const int32_t* accept_lens, int32_t* new_seq_lens,
+                   int32_t* free_ids, int32_t* n_free, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || n < 1 || n > kMaxN || W < 1 || W > kMaxN + 1 || Hkv < 1 || page_size < 1) return SPEC_ERR_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (num_layers < 1 || num_layers > kMaxLayers || num_slots < 1 || req_rows < 1 || row_w < 1) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!k_layers || !v_layers || !req_to_token || !req_pool_idx || !seq_lens || !verify_loc || !accept_index ||
+      !accept_lens || !new_seq_lens || !free_ids || !n_free)
+    return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_COMMIT_KV, b, n, 1, 1, 0, 0, 0);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const WsView v = ws_view(ws, b);
+  CommitParams p{};
+  p.b = b;
+  p.n = n;
+  p.W = W;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.num_layers = num_layers;
+  p.page_size = page_size;
+  for (int i = 0; i < num_layers; ++i) {
+    if (!k_layers[i] || !v_layers[i] || !aligned(k_layers[i], 16) || !aligned(v_layers[i], 16)) return SPEC_ERR_ARG;
+    p.k_layers[i] = k_layers[i];
+    p.v_layers[i] = v_layers[i];
+  }
+  p.num_slots = num_slots;
+  p.req_to_token = req_to_token;
+  p.req_rows = req_rows;
+  p.row_w = row_w;
+  p.req_pool_idx = req_pool_idx;
+  p.seq_lens = seq_lens;
+  p.verify_loc = verify_loc;
+  p.accept_index = accept_index;
+  p.accept_lens = accept_lens;
+  p.new_seq_lens = new_seq_lens;
+  p.free_ids = free_ids;
+  p.n_free = n_free;
+  p.error = v.error;
+  p.counters = v.counters;
+  p.partials = v.partials;
+  return launch_commit_kv(p, as_stream(stream));
+}
+
+}  // extern "C"

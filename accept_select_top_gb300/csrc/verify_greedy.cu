@@ -1,0 +1,185 @@
+// verify_greedy.cu -- greedy accept: per-row argmax over the vocabulary, then
+// the first-child / next-sibling walk from the root.
+//
+// [SGL-XI eagle_sample, 路径一:贪心验证], [ACCEPT section 3 (pseudocode of the
+// walk, row/output shift)], [EAGLE2 section 5.3].
+//
+// Grid: (chunks, b*n).  Each CTA reduces one chunk of one verify row to its
+// (max, lowest index) pair with 16-byte streaming loads; the CTA that finishes
+// last for a request merges the request's partials into target_predict and
+// runs the walk for that request (one thread: at most S levels of at most n
+// siblings), then writes predict / accept_index / accept_lens.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace spec {
+
+namespace {
+
+struct ArgPart {
+  float v;
+  int i;
+};
+
+// Argmax of row[begin, end) for this thread, elements visited in increasing
+// index order (so a strict > keeps the lowest index among equals).
+template <typename T>
+__device__ __forceinline__ void scan_argmax(const T* row, int begin, int end, bool vec, float& bv, int& bi) {
+  using Tr = LogitTraits<T>;
+  constexpr int E = Tr::kVec;
+  if (vec) {
+    const uint4* p = reinterpret_cast<const uint4*>(row);
+    const int vb = begin / E, ve = end / E;
+    constexpr int U = 4;
+    for (int v0 = vb + threadIdx.x; v0 < ve; v0 += blockDim.x * U) {
+      uint4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        int idx = v0 + u * blockDim.x;
+        if (idx < ve) x[u] = ld_stream(p + idx);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        int idx = v0 + u * blockDim.x;
+        if (idx >= ve) break;
+        float f[E];
+        Tr::unpack(x[u], f);
+        float m = f[0];
+#pragma unroll
+        for (int e = 1; e < E; ++e) m = fmaxf(m, f[e]);
+        if (m >= bv) {
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (better(f[e], idx * E + e, bv, bi)) {
+              bv = f[e];
+              bi = idx * E + e;
+            }
+        }
+      }
+    }
+  } else {
+    for (int i = begin + threadIdx.x; i < end; i += blockDim.x) {
+      float f = Tr::load(row, i);
+      if (better(f, i, bv, bi)) {
+        bv = f;
+        bi = i;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void block_argmax(float& v, int& i) {
+  __shared__ float sv[kThreads / 32];
+  __shared__ int si[kThreads / 32];
+  warp_argmax(v, i);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    sv[w] = v;
+    si[w] = i;
+  }
+  __syncthreads();
+  if (w == 0) {
+    v = l < int(blockDim.x >> 5) ? sv[l] : -INFINITY;
+    i = l < int(blockDim.x >> 5) ? si[l] : INT_MAX;
+    warp_argmax(v, i);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
+  const int row = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const int req = row / a.n;
+  const int begin = chunk * a.chunk_elems;
+  const int end = min(a.V, begin + a.chunk_elems);
+  const T* lrow = static_cast<const T*>(a.logits) + size_t(row) * a.V;
+
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  scan_argmax<T>(lrow, begin, end, a.vec_ok, bv, bi);
+  block_argmax(bv, bi);
+  ArgPart* part = reinterpret_cast<ArgPart*>(a.partials);
+  if (threadIdx.x == 0) part[size_t(row) * a.chunks + chunk] = ArgPart{bv, bi};
+
+  if (!arrive_last(a.counters + req, uint32_t(a.n * a.chunks))) return;
+
+  // ---- finalize request `req` (last CTA to arrive) ----
+  const int n = a.n, base = req * n, W = a.S + 1;
+  __shared__ int tp[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
+  __shared__ int s_len;
+  for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    const ArgPart* pr = part + size_t(base + t) * a.chunks;
+    float v = -INFINITY;
+    int i = INT_MAX;
+    for (int c = 0; c < a.chunks; ++c) {
+      // partials of other CTAs: read through L2 (__ldcg), not a stale L1 line
+      const int2 q = __ldcg(reinterpret_cast<const int2*>(pr + c));
+      const float qv = __int_as_float(q.x);
+      if (better(qv, q.y, v, i)) {
+        v = qv;
+        i = q.y;
+      }
+    }
+    tp[t] = i;
+    tok[t] = a.draft_tokens[base + t];
+    int x = a.next_token[base + t], y = a.next_sibling[base + t], r = a.retrieve_index[base + t];
+    if (x < -1 || x >= n || y < -1 || y >= n) {
+      raise_error(a.error, SPEC_DEV_INDEX);
+      x = x < -1 || x >= n ? -1 : x;
+      y = y < -1 || y >= n ? -1 : y;
+    }
+    if (r < base || r >= base + n) {
+      raise_error(a.error, SPEC_DEV_INDEX);
+      r = base + t;
+    }
+    nt[t] = x;
+    ns[t] = y;
+    ri[t] = r;
+    pred[t] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int cur = 0, ncd = 0;
+    path[0] = 0;
+    // a valid tree is at most n-1 deep; the bound also stops a malformed (cyclic) one
+    for (int d = 1; d <= a.S && ncd < n - 1; ++d) {
+      int c = nt[cur], hit = -1, guard = 0;
+      while (c != -1 && guard++ < n) {
+        if (tok[c] == tp[cur]) {
+          hit = c;
+          break;
+        }
+        c = ns[c];
+      }
+      if (hit < 0) break;
+      pred[cur] = tok[hit];
+      path[++ncd] = hit;
+      cur = hit;
+    }
+    pred[cur] = tp[cur];
+    s_len = ncd + 1;
+    a.accept_lens[req] = ncd + 1;
+    if (a.next_root) a.next_root[req] = tp[cur];
+  }
+  __syncthreads();
+  const int L = s_len;
+  for (int t = threadIdx.x; t < n; t += blockDim.x) a.predict[ri[t]] = pred[t];
+  for (int d = threadIdx.x; d < W; d += blockDim.x) {
+    a.accept_index[size_t(req) * W + d] = d < L ? ri[path[d]] : -1;
+    if (a.accepted_tokens) a.accepted_tokens[size_t(req) * W + d] = d < L ? pred[path[d]] : -1;
+  }
+  counter_reset(a.counters + req);
+}
+
+}  // namespace
+
+int launch_verify_greedy(const GreedyParams& p, cudaStream_t stream) {
+  dim3 grid(p.chunks, p.b * p.n);
+  if (p.dtype == SPEC_F32)
+    greedy_kernel<float><<<grid, kThreads, 0, stream>>>(p);
+  else
+    greedy_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+}  // namespace spec

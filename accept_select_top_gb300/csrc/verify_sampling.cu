@@ -1,0 +1,404 @@
+// verify_sampling.cu -- rejection-sampling accept with residual resampling and
+// the terminal bonus token.
+//
+// [ACCEPT section 4: accept x when u < min(1, p(x)/q(x)) tested without the
+// division as u*q(x) < p(x); on rejection sample max(p - q, 0)/Z; after a fully
+// accepted path sample the bonus from p], [INTERN 接受/拒绝], [EAGLE2 5.6: a
+// rejected child passes to the next sibling, all rejected -> residual],
+// [SGL-XI eagle_sample, 路径三:拒绝采样].
+//
+// Pass 1, grid (chunks, b*n): every verify row is reduced to (max, argmax,
+// sum of exp((x - max)/T)) by chunk; the CTA arriving last for a request merges
+// the request's rows and walks the tree with p(x) = exp((l_x - max)/T)/sum
+// (fp32) read at the children's tokens only.  It writes everything but the
+// terminal token, and leaves the request's state (terminal node, mode) in the
+// workspace: mode 0 = done (greedy request, terminal = argmax), 1 = sample the
+// terminal from p, 2 = sample it from the residual max(0, p - q).
+// Pass 2, grid (chunks, b): for requests of mode 1 or 2 each CTA sums, in fp64,
+// the residual and p over one chunk of the terminal row; the last CTA finds the
+// chunk where u_final * Z falls and the token inside it by an in-order scan.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace spec {
+
+namespace {
+
+struct StatPart {
+  float m;
+  int arg;
+  float s;
+  float pad;
+};
+
+struct ReqState {
+  int cur;    // terminal node
+  int mode;   // 0 done, 1 from p, 2 from residual
+  int ncd;    // accepted drafts
+  int row;    // verify row of the terminal node (logits / q row)
+  float M;    // max logit of that row
+  float S;    // sum of exp((x - M)/T) of that row
+  float T;
+  int out_row;  // retrieve_index row of the terminal node
+};
+
+struct MassPart {
+  double res;   // sum of max(0, p - q) over the chunk
+  double p;     // sum of p over the chunk
+  int last_res; // last index with a positive residual, -1 if none
+  int last_p;
+  int pad[2];
+};
+
+// p of one token given the row statistics (T > 0).
+__device__ __forceinline__ float p_of(float l, float M, float T, float S) { return expf((l - M) / T) / S; }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams a) {
+  using Tr = LogitTraits<T>;
+  constexpr int E = Tr::kVec;
+  const int row = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const int req = row / a.n;
+  const int begin = chunk * a.chunk_elems;
+  const int end = min(a.V, begin + a.chunk_elems);
+  const T* lrow = static_cast<const T*>(a.logits) + size_t(row) * a.V;
+  const float temp = a.temperatures[req];
+  const bool soft = temp > 0.f;
+  const float c = soft ? 1.4426950408889634f / temp : 0.f;
+
+  float m = -3.0e38f, s = 0.f, bv = -INFINITY;
+  int bi = INT_MAX;
+  auto consume = [&](const float* f, int n_el, int first) {
+    float vm = f[0];
+    for (int e = 1; e < n_el; ++e) vm = fmaxf(vm, f[e]);
+    if (vm >= bv) {
+      for (int e = 0; e < n_el; ++e)
+        if (better(f[e], first + e, bv, bi)) {
+          bv = f[e];
+          bi = first + e;
+        }
+    }
+    if (soft) {
+      if (vm > m) {
+        s *= exp2f((m - vm) * c);
+        m = vm;
+      }
+      for (int e = 0; e < n_el; ++e) s += exp2f((f[e] - m) * c);
+    }
+  };
+  if (a.vec_ok) {
+    const uint4* p = reinterpret_cast<const uint4*>(lrow);
+    const int vb = begin / E, ve = end / E;
+    constexpr int U = 4;
+    for (int v0 = vb + threadIdx.x; v0 < ve; v0 += blockDim.x * U) {
+      uint4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        int idx = v0 + u * blockDim.x;
+        if (idx < ve) x[u] = ld_stream(p + idx);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        int idx = v0 + u * blockDim.x;
+        if (idx >= ve) break;
+        float f[E];
+        Tr::unpack(x[u], f);
+        consume(f, E, idx * E);
+      }
+    }
+  } else {
+    for (int i = begin + threadIdx.x; i < end; i += blockDim.x) {
+      float f = Tr::load(lrow, i);
+      consume(&f, 1, i);
+    }
+  }
+  // CTA reduction
+  __shared__ float sm_[kThreads / 32], ss_[kThreads / 32], sv_[kThreads / 32];
+  __shared__ int si_[kThreads / 32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  {
+    float M = warp_max(m);
+    float sc = warp_sum(s * exp2f((m - M) * c));
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      sm_[w] = M;
+      ss_[w] = sc;
+      sv_[w] = bv;
+      si_[w] = bi;
+    }
+  }
+  __syncthreads();
+  StatPart* part = reinterpret_cast<StatPart*>(a.partials) + size_t(row) * a.chunks + chunk;
+  if (w == 0) {
+    float M = lane < nw ? sm_[lane] : -3.0e38f;
+    M = warp_max(M);
+    float sc = warp_sum(lane < nw ? ss_[lane] * exp2f((sm_[lane] - M) * c) : 0.f);
+    float v = lane < nw ? sv_[lane] : -INFINITY;
+    int i = lane < nw ? si_[lane] : INT_MAX;
+    warp_argmax(v, i);
+    if (lane == 0) *part = StatPart{soft ? M : v, i, sc, 0.f};
+  }
+
+  if (!arrive_last(a.counters + req, uint32_t(a.n * a.chunks))) return;
+
+  // ---- finalize request `req`: merge the row statistics, then walk ----
+  const int n = a.n, base = req * n, W = a.S + 1;
+  __shared__ float rM[kMaxN], rS[kMaxN];
+  __shared__ int rA[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
+  __shared__ int s_len, s_mode;
+  for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    const StatPart* pr = reinterpret_cast<const StatPart*>(a.partials) + size_t(base + t) * a.chunks;
+    float M = -3.0e38f, v = -INFINITY;
+    int arg = INT_MAX;
+    for (int ch = 0; ch < a.chunks; ++ch) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(pr + ch));
+      M = fmaxf(M, q.x);
+      // the argmax of a soft row is tracked through the chunk max
+      if (better(q.x, __float_as_int(q.y), v, arg)) {
+        v = q.x;
+        arg = __float_as_int(q.y);
+      }
+    }
+    float S = 0.f;
+    for (int ch = 0; ch < a.chunks; ++ch) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(pr + ch));
+      S += q.z * exp2f((q.x - M) * c);
+    }
+    rM[t] = M;
+    rS[t] = S;
+    rA[t] = arg;
+    tok[t] = a.draft_tokens[base + t];
+    int x = a.next_token[base + t], y = a.next_sibling[base + t], r = a.retrieve_index[base + t];
+    if (x < -1 || x >= n || y < -1 || y >= n || r < base || r >= base + n) {
+      raise_error(a.error, SPEC_DEV_INDEX);
+      x = x < -1 || x >= n ? -1 : x;
+      y = y < -1 || y >= n ? -1 : y;
+      r = r < base || r >= base + n ? base + t : r;
+    }
+    nt[t] = x;
+    ns[t] = y;
+    ri[t] = r;
+    pred[t] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const T* L = static_cast<const T*>(a.logits);
+    int cur = 0, ncd = 0, all_rejected = 0;
+    path[0] = 0;
+    for (int d = 0; d < a.S && ncd < n - 1; ++d) {  // bounded by the tree depth
+      const size_t vrow = size_t(base + cur);
+      const float* q = a.draft_probs + vrow * a.V;
+      int c2 = nt[cur], hit = -1, guard = 0;
+      const int had_child = c2 != -1;
+      while (c2 != -1 && guard++ < n) {
+        const int x = tok[c2];
+        if (x < 0 || x >= a.V) {
+          raise_error(a.error, SPEC_DEV_INDEX);
+          c2 = ns[c2];
+          continue;
+        }
+        float px;
+        if (soft) px = p_of(Tr::load(L, vrow * a.V + x), rM[cur], temp, rS[cur]);
+        else px = x == rA[cur] ? 1.f : 0.f;
+        if (__fmul_rn(a.u[base + c2], __ldg(q + x)) < px) {
+          hit = c2;
+          break;
+        }
+        c2 = ns[c2];
+      }
+      if (hit < 0) {
+        all_rejected = had_child;
+        break;
+      }
+      pred[cur] = tok[hit];
+      path[++ncd] = hit;
+      cur = hit;
+    }
+    int mode = soft ? (all_rejected ? 2 : 1) : 0;
+    if (mode == 0) pred[cur] = rA[cur];
+    ReqState* st = reinterpret_cast<ReqState*>(a.state) + req;
+    *st = ReqState{cur, mode, ncd, base + cur, rM[cur], rS[cur], temp, ri[cur]};
+    a.accept_lens[req] = ncd + 1;
+    if (mode == 0 && a.next_root) a.next_root[req] = pred[cur];
+    s_len = ncd + 1;
+    s_mode = mode;
+  }
+  __syncthreads();
+  const int Lp = s_len;
+  for (int t = threadIdx.x; t < n; t += blockDim.x) a.predict[ri[t]] = pred[t];
+  for (int d = threadIdx.x; d < W; d += blockDim.x) {
+    a.accept_index[size_t(req) * W + d] = d < Lp ? ri[path[d]] : -1;
+    if (a.accepted_tokens) {
+      const bool known = d < Lp - 1 || (d == Lp - 1 && s_mode == 0);
+      a.accepted_tokens[size_t(req) * W + d] = known ? pred[path[d]] : -1;
+    }
+  }
+  counter_reset(a.counters + req);
+}
+
+template <typename T>
+__device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqState& st, int begin, int end,
+                                           double& res, double& ps, int& last_res, int& last_p) {
+  using Tr = LogitTraits<T>;
+  const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
+  const float* q = a.draft_probs + size_t(st.row) * a.V;
+  for (int v = begin + threadIdx.x; v < end; v += blockDim.x) {
+    const float p = p_of(Tr::load(L, v), st.M, st.T, st.S);
+    const double r = st.mode == 2 ? fmax(double(p) - double(__ldg(q + v)), 0.0) : 0.0;
+    res += r;
+    ps += double(p);
+    if (r > 0.0) last_res = v;
+    if (p > 0.f) last_p = v;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams a) {
+  using Tr = LogitTraits<T>;
+  const int req = blockIdx.y;
+  const int chunk = blockIdx.x;
+  const ReqState st = reinterpret_cast<const ReqState*>(a.state)[req];
+  if (st.mode == 0) return;  // every CTA of this request agrees: nothing to sample
+  const int begin = chunk * a.chunk2_elems;
+  const int end = min(a.V, begin + a.chunk2_elems);
+  double res = 0.0, ps = 0.0;
+  int last_res = -1, last_p = -1;
+  chunk_mass<T>(a, st, begin, end, res, ps, last_res, last_p);
+  __shared__ double sres[kThreads / 32], sps[kThreads / 32];
+  __shared__ int slr[kThreads / 32], slp[kThreads / 32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  res = warp_sum_d(res);
+  ps = warp_sum_d(ps);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    last_res = max(last_res, __shfl_xor_sync(0xffffffffu, last_res, o));
+    last_p = max(last_p, __shfl_xor_sync(0xffffffffu, last_p, o));
+  }
+  if (lane == 0) {
+    sres[w] = res;
+    sps[w] = ps;
+    slr[w] = last_res;
+    slp[w] = last_p;
+  }
+  __syncthreads();
+  MassPart* parts = reinterpret_cast<MassPart*>(a.partials2) + size_t(req) * a.chunks2;
+  if (threadIdx.x == 0) {
+    MassPart mp{0.0, 0.0, -1, -1, {0, 0}};
+    for (int i = 0; i < nw; ++i) {
+      mp.res += sres[i];
+      mp.p += sps[i];
+      mp.last_res = max(mp.last_res, slr[i]);
+      mp.last_p = max(mp.last_p, slp[i]);
+    }
+    parts[chunk] = mp;
+  }
+
+  if (!arrive_last(a.counters + req, uint32_t(a.chunks2))) return;
+
+  // ---- finalize: locate u_final * Z on the cumulative mass ----
+  __shared__ int s_chunk, s_use_res, s_fallback;
+  __shared__ double s_before, s_target;
+  if (threadIdx.x == 0) {
+    double zr = 0.0, zp = 0.0;
+    int lr = -1, lp = -1;
+    for (int ch = 0; ch < a.chunks2; ++ch) {
+      zr += __ldcg(&parts[ch].res);
+      zp += __ldcg(&parts[ch].p);
+      lr = max(lr, __ldcg(&parts[ch].last_res));
+      lp = max(lp, __ldcg(&parts[ch].last_p));
+    }
+    const int use_res = st.mode == 2 && zr > 0.0;
+    const double Z = use_res ? zr : zp;
+    const double target = double(a.u_final[req]) * Z;
+    double acc = 0.0;
+    int found = -1;
+    for (int ch = 0; ch < a.chunks2; ++ch) {
+      const double m = use_res ? __ldcg(&parts[ch].res) : __ldcg(&parts[ch].p);
+      if (target < acc + m) {
+        found = ch;
+        break;
+      }
+      acc += m;
+    }
+    s_chunk = found;
+    s_use_res = use_res;
+    s_before = acc;
+    s_target = target;
+    s_fallback = use_res ? lr : lp;
+  }
+  __syncthreads();
+  __shared__ int s_bonus;
+  if (threadIdx.x == 0) s_bonus = s_fallback;
+  __syncthreads();
+  if (s_chunk >= 0) {
+    // in-order scan of the chunk: each thread owns a contiguous segment
+    const int cb = s_chunk * a.chunk2_elems;
+    const int ce = min(a.V, cb + a.chunk2_elems);
+    const int seg = (ce - cb + blockDim.x - 1) / blockDim.x;
+    const int sb = cb + threadIdx.x * seg, se = min(ce, sb + seg);
+    const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
+    const float* q = a.draft_probs + size_t(st.row) * a.V;
+    auto mass = [&](int v) {
+      const float p = p_of(Tr::load(L, v), st.M, st.T, st.S);
+      return s_use_res ? fmax(double(p) - double(__ldg(q + v)), 0.0) : double(p);
+    };
+    double mine = 0.0;
+    for (int v = sb; v < se; ++v) mine += mass(v);
+    __shared__ double pre[kThreads];
+    pre[threadIdx.x] = mine;
+    __syncthreads();
+    if (threadIdx.x == 0) {  // exclusive prefix over the segments, in element order
+      double run = s_before;
+      for (int t = 0; t < int(blockDim.x); ++t) {
+        const double x = pre[t];
+        pre[t] = run;
+        run += x;
+      }
+    }
+    __syncthreads();
+    __shared__ int s_hit;
+    if (threadIdx.x == 0) s_hit = INT_MAX;
+    __syncthreads();
+    double run = pre[threadIdx.x];
+    for (int v = sb; v < se; ++v) {
+      const double m = mass(v);
+      run += m;
+      if (s_target < run) {
+        atomicMin(&s_hit, v);
+        break;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_hit != INT_MAX) s_bonus = s_hit;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int bonus = s_bonus;
+    const int W = a.S + 1;
+    a.predict[st.out_row] = bonus;
+    if (a.accepted_tokens) a.accepted_tokens[size_t(req) * W + st.ncd] = bonus;
+    if (a.next_root) a.next_root[req] = bonus;
+  }
+  counter_reset(a.counters + req);
+}
+
+}  // namespace
+
+size_t sampling_partial_bytes(int rows, int chunks) { return align256(size_t(rows) * chunks * sizeof(StatPart)); }
+size_t sampling_state_bytes(int b) { return align256(size_t(b) * sizeof(ReqState)); }
+size_t sampling_partial2_bytes(int b, int chunks2) { return align256(size_t(b) * chunks2 * sizeof(MassPart)); }
+
+int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
+  dim3 g1(p.chunks, p.b * p.n), g2(p.chunks2, p.b);
+  if (p.dtype == SPEC_F32) {
+    sampling_stats_kernel<float><<<g1, kThreads, 0, stream>>>(p);
+    sampling_bonus_kernel<float><<<g2, kThreads, 0, stream>>>(p);
+  } else {
+    sampling_stats_kernel<uint16_t><<<g1, kThreads, 0, stream>>>(p);
+    sampling_bonus_kernel<uint16_t><<<g2, kThreads, 0, stream>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+}  // namespace spec

@@ -1,0 +1,255 @@
+/*
+ * accept_select_top.h -- C ABI of the GB300 (sm_103a) verify/accept step of
+ * EAGLE-style speculative decoding.
+ *
+ * One verify step is, in order:
+ *   spec_select_topk  x num_steps   draft-tree growth (select_top_k_tokens)
+ *   spec_build_tree                 organize_draft_results + build_tree
+ *   spec_verify_attention           tree-masked attention of the verify queries
+ *   spec_verify_greedy | spec_verify_sampling   accept
+ *   spec_commit_kv                  move accepted KV, release the rest
+ *
+ * Sources (web pages), cited below as [KEY section]:
+ *   [SGL-XI]  "SGLang 源码完全拆解(十一):投机解码——草稿生成、批量验证与 token 接受如何接进同一条前向"
+ *   [ACCEPT]  "投机解码 Accept从 Verify 行到最终输出路径"
+ *   [EVOL]    "SGLang 设计演进投机解码、PD 分离与大规模 EP（2025 上半年）", chapter "EAGLE 投机解码四部曲"
+ *   [INTERN]  "Speculative Decoding" (SGLang internals, part 3, execution model)
+ *   [EAGLE2]  "把投机采样讲透：以 SGLang 中的 EAGLE-2 为例"
+ *
+ * Conventions for every call:
+ *   - Every array pointer is a DEVICE pointer allocated and owned by the caller;
+ *     the library keeps no pointer after a call returns and allocates nothing.
+ *   - `stream` is a cudaStream_t passed as void*; every call is asynchronous on
+ *     it and never synchronises the host (except spec_last_error).
+ *   - `ws` / `ws_bytes` is caller-provided scratch memory sized by
+ *     spec_workspace_size() and zero-filled once (spec_workspace_init) before its
+ *     first use.  Every call leaves it zero again apart from the error word, so
+ *     one workspace serves any sequence of calls on one stream.  Calls that may
+ *     run concurrently (different streams) need separate workspaces.
+ *   - Return codes: SPEC_OK, SPEC_ERR_ARG (null pointer, bad size or shape, a
+ *     limit below exceeded), SPEC_ERR_WORKSPACE (ws too small or misaligned),
+ *     SPEC_ERR_LAUNCH (the CUDA launch failed; cudaGetLastError is consumed),
+ *     SPEC_ERR_UNSUPPORTED (dtype or head size not built).
+ *   - b == 0 (an idle batch) is a no-op that returns SPEC_OK [SGL-XI eagle_sample].
+ *   - Indices read from device arrays are bounds-checked on the device; a bad
+ *     one sets a bit in the workspace error word and the access is skipped (no
+ *     trap).  spec_last_error() reads and clears that word.
+ *   - Tree arrays use -1 for "none"; a verify row is the flattened index
+ *     b*n + i of request b's tree node i [ACCEPT section 3].
+ *   - Limits: 1 <= k <= 16, k <= V, 1 <= n <= 64, n - 1 <= k + (S-1)*k*k,
+ *     S >= 1, head_dim D in {64, 128}, Hq a multiple of Hkv.
+ *   - Ties in every top-k / argmax go to the lowest index.
+ */
+#ifndef ACCEPT_SELECT_TOP_H
+#define ACCEPT_SELECT_TOP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_OK 0
+#define SPEC_ERR_ARG (-1)
+#define SPEC_ERR_WORKSPACE (-2)
+#define SPEC_ERR_LAUNCH (-3)
+#define SPEC_ERR_UNSUPPORTED (-4)
+
+/* logits dtypes */
+#define SPEC_F32 0
+#define SPEC_BF16 1
+
+/* bits of the device error word */
+#define SPEC_DEV_INDEX 1u      /* an index read from an input array was out of range */
+#define SPEC_DEV_INVARIANT 2u  /* a selected node's parent was not selected (build_tree) */
+#define SPEC_DEV_LENGTH 4u     /* a length (seq_len, accept_len) outside its valid range */
+
+/* operation ids for spec_workspace_size */
+#define SPEC_OP_SELECT_TOPK 0
+#define SPEC_OP_BUILD_TREE 1
+#define SPEC_OP_VERIFY_ATTENTION 2
+#define SPEC_OP_VERIFY_GREEDY 3
+#define SPEC_OP_VERIFY_SAMPLING 4
+#define SPEC_OP_COMMIT_KV 5
+
+/* Bytes of workspace the operation needs for these sizes (b requests, n tree
+ * nodes, k = topk, V vocabulary, Hq query heads, Hkv kv heads, max_seq_len an
+ * upper bound on seq_lens).  Sizes an operation does not use are ignored.
+ * Returns 0 for an unknown op or invalid sizes. */
+size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len);
+
+/* Zero-fills a workspace (cudaMemsetAsync on `stream`). */
+int spec_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the device error word (SPEC_DEV_* bits, 0 if
+ * clean) and clears it; a negative SPEC_ERR_* on failure. */
+int spec_last_error(void* ws, void* stream);
+
+/* Number of streaming multiprocessors of the current device (0 on failure). */
+int spec_device_sm_count(void);
+
+/* ---------------------------------------------------------------------------
+ * spec_select_topk -- one step of select_top_k_tokens, with the draft
+ * distribution's softmax and top-k fused in.
+ * [SGL-XI organize_draft_results] (_select_top_k_tokens_first / _later) and
+ * [SGL-XI 草稿主循环: draft()].
+ *
+ * draft_logits: [b * rows, V] (rows = 1 at step 0, k after), dtype SPEC_F32 or
+ *   SPEC_BF16, row-major.  Per row: p = softmax(logits / temperature)
+ *   (temperature > 0), topk_p = the k largest p in descending order, with
+ *   their token ids.
+ * step 0:  score block [b, k] = topk_p; token block [b, k] = ids;
+ *          parent block [b, k+1] = -1, 0, .., k-1; scores_out = topk_p;
+ *          next_input_ids = ids.
+ * step i>0: scores_in [b, k] are the path scores of the current rows;
+ *          expand[r*k+j] = scores_in[r] * topk_p[r][j] (one fp32 multiply);
+ *          score block [b, k*k] = expand; token block [b, k*k] = ids;
+ *          the k best expand values (value desc, flat index asc) sel[0..k-1]
+ *          give parent block [b, k] = sel + k*k*(i-1) + k, scores_out [b, k]
+ *          = expand[sel], next_input_ids [b*k] = ids[sel].
+ * score_blk / token_blk rows are `score_ld` elements apart and parent_blk rows
+ * `parent_ld` apart, so the blocks can be written straight into the
+ * concatenated score / token space and parent list that spec_build_tree reads
+ * (score_ld = k + (S-1)*k*k, parent_ld = 1 + (S-1)*k).  parent_blk may be NULL
+ * (the last step's parent block is not part of the parent list).  topk_p_out
+ * [b*rows, k] is optional (NULL).
+ * ------------------------------------------------------------------------- */
+int spec_select_topk(int step, int b, int k, int V, int dtype,
+                     const void* draft_logits, float temperature,
+                     const float* scores_in,
+                     float* score_blk, int32_t* token_blk, int score_ld,
+                     int32_t* parent_blk, int parent_ld,
+                     float* scores_out, int32_t* next_input_ids,
+                     float* topk_p_out,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_build_tree -- organize_draft_results followed by build_tree.
+ * [SGL-XI organize_draft_results], [SGL-XI build_tree_kernel_efficient],
+ * [ACCEPT section 2], [EAGLE2 sections 4.3, 5.3].
+ *
+ * score_space, token_space: [b, C], C = k + (S-1)*k*k; parent_space: [b, P],
+ *   P = 1 + (S-1)*k; bonus, seq_lens: [b].
+ * The n-1 best scores (value desc, index asc), re-sorted by position, become
+ * nodes 1..n-1; node 0 is the bonus token.  The parent of the node at position
+ * p is the node at position parent_space[p / k] (-1 = the root).
+ * Outputs, [b*n] each: draft_tokens; positions = seq_len + depth;
+ *   retrieve_index = b*n + i; next_token = first (smallest) child;
+ *   next_sibling = next larger child of the same parent; mask_bits (uint64,
+ *   bit j of row b*n+i set iff node j is an ancestor of node i or i itself).
+ * A selected node whose parent is not selected sets SPEC_DEV_INVARIANT and is
+ * attached to the root.
+ * ------------------------------------------------------------------------- */
+int spec_build_tree(int b, int k, int S, int n,
+                    const float* score_space, const int32_t* token_space,
+                    const int32_t* parent_space,
+                    const int32_t* bonus, const int32_t* seq_lens,
+                    int32_t* draft_tokens, int32_t* positions,
+                    int32_t* retrieve_index, int32_t* next_token,
+                    int32_t* next_sibling, uint64_t* mask_bits,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_verify_attention -- tree-masked attention of the verify queries.
+ * [EAGLE2 sections 4.2, 4.3], [SGL-XI 三种 mask 形态 (QLEN_ONLY)].
+ *
+ * q: [b*n, Hq, D] bf16; k_pool, v_pool: [num_slots, Hkv, D] bf16 (post-RoPE);
+ * req_to_token: [req_rows, row_w] int32 slots; req_pool_idx, seq_lens: [b];
+ * verify_loc: [b*n] slots of the tree nodes; mask_bits: [b*n] from
+ * spec_build_tree.  For row b*n+i and q head h (kv head g = h / (Hq/Hkv)):
+ *   keys = prefix positions 0..seq_len[b]-1 (all visible), then tree nodes j
+ *   with mask bit (i, j) set;  out = softmax(scale * q.K^T) V.
+ * out: [b*n, Hq, D] bf16; lse: [b*n, Hq] fp32 natural-log sum-exp of the
+ * scaled scores (optional, NULL).  max_seq_len bounds every seq_len (a larger
+ * one sets SPEC_DEV_LENGTH and is clamped) and sizes the split-KV grid.
+ * page_size is the KV page size (1 or 16); slots of one page are consecutive.
+ * ------------------------------------------------------------------------- */
+int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size,
+                          const void* q, const void* k_pool, const void* v_pool,
+                          int64_t num_slots,
+                          const int32_t* req_to_token, int req_rows, int row_w,
+                          const int32_t* req_pool_idx, const int32_t* seq_lens,
+                          int max_seq_len,
+                          const int32_t* verify_loc, const uint64_t* mask_bits,
+                          float scale, void* out, float* lse,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_verify_greedy -- greedy accept.
+ * [SGL-XI eagle_sample (路径一:贪心验证)], [ACCEPT section 3], [EAGLE2 5.3].
+ *
+ * logits: [b*n, V] (SPEC_F32 or SPEC_BF16).  target_predict = per-row argmax.
+ * Walk per request: cur = node 0, accept_index[b,0] = row(0); up to S times,
+ * the first child c of cur in sibling order with draft_tokens[b*n+c] ==
+ * target_predict[b*n+cur] is accepted: predict[row(cur)] = its token,
+ * accept_index[b,d] = row(c), cur = c; stop when no child matches.  Then
+ * predict[row(cur)] = target_predict[b*n+cur].  row(i) = retrieve_index[b*n+i].
+ * Outputs: predict [b*n] (0 on rows not on the path), accept_index [b, S+1]
+ * (-1 padded), accept_lens [b] = accepted drafts + 1; optional (NULL):
+ * accepted_tokens [b, S+1] = predict[accept_index] (-1 padded), next_root [b]
+ * = the last accepted token.
+ * ------------------------------------------------------------------------- */
+int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits,
+                       const int32_t* draft_tokens, const int32_t* retrieve_index,
+                       const int32_t* next_token, const int32_t* next_sibling,
+                       int32_t* predict, int32_t* accept_index,
+                       int32_t* accept_lens, int32_t* accepted_tokens,
+                       int32_t* next_root,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_verify_sampling -- rejection-sampling accept with residual and bonus.
+ * [ACCEPT section 4], [INTERN 接受/拒绝], [EAGLE2 5.6], [SGL-XI eagle_sample].
+ *
+ * p = softmax(logits_row / T_b) (T_b = temperatures[b] > 0; T_b <= 0 means
+ * greedy: p is one-hot at the argmax).  draft_probs q: [b*n, V] fp32, row of
+ * node i = the distribution i's children were proposed from.  At node cur each
+ * child c (sibling order) with token x is accepted iff u[b*n+c] * q(x) < p(x)
+ * (fp32); the first accepted child is descended into.  When every child of cur
+ * is rejected the terminal token is the smallest v with
+ * u_final[b] * Z < sum_{w<=v} max(0, p_w - q_w) (Z = the total; from p itself
+ * when Z == 0); when cur has no child or S drafts were accepted it is drawn
+ * from p the same way.  Outputs as spec_verify_greedy.
+ * ------------------------------------------------------------------------- */
+int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits,
+                         const float* draft_probs, const float* temperatures,
+                         const float* u, const float* u_final,
+                         const int32_t* draft_tokens, const int32_t* retrieve_index,
+                         const int32_t* next_token, const int32_t* next_sibling,
+                         int32_t* predict, int32_t* accept_index,
+                         int32_t* accept_lens, int32_t* accepted_tokens,
+                         int32_t* next_root,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_commit_kv -- move the accepted rows' KV into the sequence, release the rest.
+ * [SGL-XI KV 回写 (move_accept_tokens_to_target_kvcache)], [ACCEPT section 3
+ * (input/output shift)], [EVOL 草稿、验证与槽位].
+ *
+ * For request b, L = accept_lens[b], k < L:
+ *   dst_k = req_to_token[req_pool_idx[b], seq_lens[b] + k],
+ *   src_k = verify_loc[accept_index[b, k]]   (accept_index is [b, W], global rows);
+ * K and V rows [Hkv, D] bf16 of every layer move src -> dst, every source row
+ * of a request being read before any of its targets is written.
+ * new_seq_lens[b] = seq_lens[b] + L.
+ * Free list (request order, then ascending node order): page_size == 1: each
+ * verify slot of the request that is no dst slot; page_size > 1: each page id
+ * (slot / page_size) holding a verify slot of the request and no dst slot of
+ * it, once.  free_ids: [b*n] capacity; n_free: one int32.
+ * k_layers / v_layers: HOST arrays of num_layers (<= 128) device pointers to
+ * [num_slots, Hkv, D] bf16 pools.
+ * ------------------------------------------------------------------------- */
+int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page_size,
+                   void* const* k_layers, void* const* v_layers, int64_t num_slots,
+                   const int32_t* req_to_token, int req_rows, int row_w,
+                   const int32_t* req_pool_idx, const int32_t* seq_lens,
+                   const int32_t* verify_loc, const int32_t* accept_index,
+                   const int32_t* accept_lens, int32_t* new_seq_lens,
+                   int32_t* free_ids, int32_t* n_free,
+                   void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ACCEPT_SELECT_TOP_H */

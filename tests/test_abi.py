@@ -1,0 +1,79 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point the header declares, and validates arguments on the host (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"^\s*(?:size_t|int)\s+(spec_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from accept_select_top_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10, names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_binding_names_match_header():
+    from accept_select_top_gb300 import ops
+    assert sorted(ops.EXPORTS) == _declared()
+    for name in _declared():
+        assert hasattr(ops.LIB, name)
+
+
+def test_workspace_sizes_host_only():
+    from accept_select_top_gb300 import ops
+    for op in range(6):
+        s = ops.spec_workspace_size(op, 8, 16, 4, 128256, 32, 8, 4096)
+        assert s >= 256 + 64
+    assert ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, 0, 16, 4, 1000) > 0  # idle batch
+    assert ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, 8, 65, 4, 1000) == 0  # n > 64
+    assert ops.spec_workspace_size(ops.OP_SELECT_TOPK, 8, 16, 17, 1000) == 0   # k > 16
+    assert ops.spec_workspace_size(99, 8, 16, 4, 1000) == 0
+
+
+def test_host_argument_checks_without_gpu(lib):
+    """Rejected arguments and the idle batch return before any CUDA call."""
+    P = ctypes.c_void_p
+    f = lib.spec_select_topk
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 5 + [P, ctypes.c_float, P, P, P, ctypes.c_int, P, ctypes.c_int, P, P, P, P,
+                                       ctypes.c_size_t, P]
+    args = lambda step, b, k, V, dt, T: (step, b, k, V, dt, None, T, None, None, None, 4, None, 5, None, None,
+                                         None, None, 0, None)
+    assert f(*args(0, 0, 4, 100, 1, 1.0)) == 0        # b == 0: no-op
+    assert f(*args(0, 2, 17, 100, 1, 1.0)) == -1      # k > 16
+    assert f(*args(0, 2, 4, 3, 1, 1.0)) == -1         # V < k
+    assert f(*args(0, 2, 4, 100, 7, 1.0)) == -4       # dtype
+    assert f(*args(0, 2, 4, 100, 1, 0.0)) == -1       # temperature
+    assert f(*args(0, 2, 4, 100, 1, 1.0)) == -1       # null pointers
+    g = lib.spec_verify_attention
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_int] * 6 + [P, P, P, ctypes.c_int64, P, ctypes.c_int, ctypes.c_int, P, P,
+                                       ctypes.c_int, P, P, ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+    base = [2, 4, 8, 2, 128, 1, None, None, None, 10, None, 1, 10, None, None, 10, None, None, 0.1, None, None,
+            None, 0, None]
+    bad_d = list(base)
+    bad_d[4] = 96
+    assert g(*bad_d) == -4
+    bad_g = list(base)
+    bad_g[3] = 3
+    assert g(*bad_g) == -1
+    assert g(*base) == -1  # null pointers

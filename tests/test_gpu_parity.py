@@ -1,0 +1,409 @@
+"""GPU-vs-oracle parity through the C ABI, stage by stage and end to end.
+
+Bars: integer / index / tree / accept / commit outputs bit-exact (a decision
+that floating point takes is allowed to differ only with a near-tie
+certificate); softmax probabilities within 1e-6 relative; attention within
+1e-2 * max(1, |ref|)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from accept_select_top_gb300 import workloads as W
+from tests.cases import (bf16_to_f64, certified_topk_difference, make_case, sampling_margin)
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["tiny", "llama8b_greedy", "sampling_heavy", "long_context", "mtp_chain"]
+
+
+def _ops():
+    from accept_select_top_gb300 import ops
+    return ops
+
+
+@pytest.fixture(scope="module")
+def cases():
+    store = {}
+
+    def get(name, mode):
+        key = (name, mode)
+        if key not in store:
+            wl = W.WORKLOADS[name] if isinstance(name, str) else name
+            store[key] = make_case(wl, mode)
+        return store[key]
+    yield get
+    store.clear()
+    torch.cuda.empty_cache()
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ------------------------------------------------------------- select_topk
+
+def _gpu_select_step(wl, step, logits, scores_in, ws):
+    ops = _ops()
+    b, k = wl.b, wl.k
+    blk = k * k if step else k
+    rows = b * (k if step else 1)
+    dev = logits.device
+    o = {"score_blk": torch.zeros(b, blk, device=dev), "token_blk": torch.zeros(b, blk, dtype=torch.int32, device=dev),
+         "parent_blk": torch.zeros(b, k if step else k + 1, dtype=torch.int32, device=dev),
+         "scores_out": torch.zeros(b, k, device=dev), "next_ids": torch.zeros(b * k, dtype=torch.int32, device=dev),
+         "topk_p": torch.zeros(rows, k, device=dev)}
+    ops.spec_select_topk(step, b, k, logits, 1.0, scores_in, o["score_blk"], o["token_blk"], blk, o["parent_blk"],
+                         o["parent_blk"].shape[1], o["scores_out"], o["next_ids"], o["topk_p"], ws)
+    return o
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_select_topk_parity(cases, name):
+    c = cases(name, "greedy")
+    wl = c.wl
+    ops = _ops()
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_SELECT_TOPK, wl.b, wl.n, wl.k, wl.V))
+    scores_in = None
+    certified = 0
+    for i in range(wl.S):
+        g = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws)
+        torch.cuda.synchronize()
+        # the oracle on the same inputs (its own scores chain until the first divergence)
+        o = oracle.select_topk(i, wl.b, wl.k, c.host_drafts[i], 1.0, None if scores_in is None else _np(scores_in))
+        np.testing.assert_array_equal(_np(g["token_blk"]), o["token_blk"])
+        np.testing.assert_allclose(_np(g["topk_p"]), o["topk_p"], rtol=1e-6, atol=0)
+        np.testing.assert_allclose(_np(g["score_blk"]), o["score_blk"], rtol=3e-6, atol=0)
+        if i == 0:
+            np.testing.assert_array_equal(_np(g["parent_blk"]), o["parent_blk"])
+        for r in range(wl.b):
+            gp, op_ = _np(g["parent_blk"])[r], o["parent_blk"][r]
+            if not np.array_equal(gp, op_):
+                assert certified_topk_difference(o["score_blk"][r], op_ - (wl.k * wl.k * (i - 1) + wl.k),
+                                                 gp - (wl.k * wl.k * (i - 1) + wl.k), wl.k), (name, i, r)
+                certified += 1
+        assert ws.last_error() == 0
+        # the next step consumes the GPU's own path scores
+        scores_in = g["scores_out"]
+    assert certified <= 1
+
+
+# -------------------------------------------------------------- build_tree
+
+@pytest.mark.parametrize("name", FULL)
+def test_build_tree_parity(cases, name):
+    c = cases(name, "greedy")
+    wl, ops = c.wl, _ops()
+    dev = "cuda"
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(dev)
+    out = {k_: torch.zeros(wl.b * wl.n, dtype=torch.int32, device=dev)
+           for k_ in ("draft_tokens", "positions", "retrieve_index", "next_token", "next_sibling")}
+    mask = torch.zeros(wl.b * wl.n, dtype=torch.int64, device=dev)
+    ws = ops.Workspace(1024)
+    ops.spec_build_tree(wl.b, wl.k, wl.S, wl.n, t(c.chain["score_space"]), t(c.chain["token_space"]),
+                        t(c.chain["parent_space"]), c.bonus, t(c.layout["seq_lens"]), out["draft_tokens"],
+                        out["positions"], out["retrieve_index"], out["next_token"], out["next_sibling"], mask, ws)
+    for k_, v in out.items():
+        np.testing.assert_array_equal(_np(v), c.tree[k_], err_msg=k_)
+    np.testing.assert_array_equal(_np(mask).view(np.uint64), c.tree["mask_bits"])
+    assert ws.last_error() == 0
+
+
+# ---------------------------------------------------------------- greedy
+
+def _accept_bufs(wl, dev="cuda"):
+    z = lambda *s: torch.zeros(*s, dtype=torch.int32, device=dev)
+    return {"predict": z(wl.b * wl.n), "accept_index": z(wl.b, wl.W), "accept_lens": z(wl.b),
+            "accepted_tokens": z(wl.b, wl.W), "next_root": z(wl.b)}
+
+
+def _tree_dev(c):
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    return tuple(t(c.tree[k_]) for k_ in ("draft_tokens", "retrieve_index", "next_token", "next_sibling"))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_verify_greedy_parity(cases, name):
+    c = cases(name, "greedy")
+    wl, ops = c.wl, _ops()
+    bufs = _accept_bufs(wl)
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, wl.b, wl.n, 1, wl.V))
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *bufs.values(), ws)
+    o = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), c.tree["draft_tokens"], c.tree["retrieve_index"],
+                             c.tree["next_token"], c.tree["next_sibling"])
+    for k_, v in bufs.items():
+        np.testing.assert_array_equal(_np(v), o[k_], err_msg=k_)
+    assert ws.last_error() == 0
+    if name == "llama8b_greedy":
+        assert 1.5 <= o["accept_lens"].mean() <= 5.0  # planted agreement: the few-token regime
+
+
+# -------------------------------------------------------------- sampling
+
+def _certify_sampling(c, o, g_lens, g_idx, r):
+    """Some accept test on the oracle's or the GPU's path of request r, or the
+    terminal draw's CDF boundary, is within 1e-5 relative: a near tie."""
+    wl = c.wl
+    n = wl.n
+    lg = W.host(c.logits)
+    lg = bf16_to_f64(lg) if lg.dtype == np.uint16 else lg.astype(np.float64)
+    q = W.host(c.q)
+    u = W.host(c.u)
+    T = float(c.temps[r])
+    if T <= 0:
+        return False
+    nt, ns, tok = c.tree["next_token"], c.tree["next_sibling"], c.tree["draft_tokens"]
+    margins = []
+    for path in (o["accept_index"][r], g_idx):
+        for row in path:
+            if row < 0:
+                break
+            ch = nt[row]                      # local node id of the first child
+            while ch != -1:
+                crow = r * n + ch             # the child's global row
+                margins.append(sampling_margin(lg[row], T, q[row], int(tok[crow]), float(u[crow])))
+                ch = ns[crow]
+    # the terminal draw: distance of u_final to the nearest normalised cumulative boundary
+    term = int(o["accept_index"][r, o["accept_lens"][r] - 1])
+    z = lg[term] / T
+    z -= z.max()
+    p = np.exp(z)
+    p /= p.sum()
+    for dist in (np.maximum(p - q[term], 0), p):
+        if dist.sum() > 0:
+            cs = np.cumsum(dist) / dist.sum()
+            margins.append(float(np.min(np.abs(cs - float(W.host(c.u_final)[r])))))
+    return min(margins) < 1e-5
+
+
+@pytest.mark.parametrize("name", ["tiny", "sampling_heavy", "mtp_chain"])
+def test_verify_sampling_parity(cases, name):
+    c = cases(name, "sampling")
+    wl, ops = c.wl, _ops()
+    bufs = _accept_bufs(wl)
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_SAMPLING, wl.b, wl.n, 1, wl.V))
+    temps = torch.as_tensor(c.temps).cuda()
+    ops.spec_verify_sampling(wl.b, wl.n, wl.S, c.logits, c.q, temps, c.u, c.u_final, *_tree_dev(c),
+                             *bufs.values(), ws)
+    o = oracle.verify_sampling(wl.b, wl.n, wl.S, W.host(c.logits), W.host(c.q), c.temps, W.host(c.u),
+                               W.host(c.u_final), c.tree["draft_tokens"], c.tree["retrieve_index"],
+                               c.tree["next_token"], c.tree["next_sibling"])
+    g = {k_: _np(v) for k_, v in bufs.items()}
+    assert ws.last_error() == 0
+    certified = 0
+    for r in range(wl.b):
+        same = (g["accept_lens"][r] == o["accept_lens"][r] and np.array_equal(g["accept_index"][r], o["accept_index"][r])
+                and np.array_equal(g["accepted_tokens"][r], o["accepted_tokens"][r])
+                and np.array_equal(g["predict"][r * wl.n:(r + 1) * wl.n], o["predict"][r * wl.n:(r + 1) * wl.n]))
+        if not same:
+            assert _certify_sampling(c, o, g["accept_lens"][r], g["accept_index"][r], r), (name, r)
+            certified += 1
+    assert certified <= max(1, wl.b // 50)
+    np.testing.assert_array_equal(g["next_root"], [g["accepted_tokens"][r, g["accept_lens"][r] - 1] for r in range(wl.b)])
+
+
+def test_sampling_t0_equals_greedy_on_gpu(cases):
+    c = cases("mtp_chain", "sampling")
+    wl, ops = c.wl, _ops()
+    a, b_ = _accept_bufs(wl), _accept_bufs(wl)
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_SAMPLING, wl.b, wl.n, 1, wl.V))
+    zeros = torch.zeros(wl.b, device="cuda")
+    ops.spec_verify_sampling(wl.b, wl.n, wl.S, c.logits, c.q, zeros, c.u, c.u_final, *_tree_dev(c), *a.values(), ws)
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *b_.values(), ws)
+    for k_ in a:
+        assert torch.equal(a[k_], b_[k_]), k_
+
+
+# -------------------------------------------------------------- attention
+
+def _attention_pairs(wl, rng, m=96):
+    rows = rng.integers(0, wl.b * wl.n, m)
+    heads = rng.integers(0, wl.Hq, m)
+    # always include every node of the first and the last request for head 0
+    extra = [(r, 0) for r in list(range(wl.n)) + list(range((wl.b - 1) * wl.n, wl.b * wl.n))]
+    return np.unique(np.concatenate([np.stack([rows, heads], 1), np.array(extra)]), axis=0)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_verify_attention_parity(cases, name):
+    c = cases(name, "greedy")
+    wl, ops = c.wl, _ops()
+    lay = c.layout
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    out = torch.zeros(wl.b * wl.n, wl.Hq, wl.D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(wl.b * wl.n, wl.Hq, device="cuda")
+    max_len = int(lay["seq_lens"].max())
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_ATTENTION, wl.b, wl.n, 1, 1, wl.Hq, wl.Hkv, max_len))
+    mask = t(c.tree["mask_bits"].view(np.int64))
+    ops.spec_verify_attention(wl.b, wl.n, wl.Hq, wl.Hkv, wl.D, wl.page_size, c.att["q"], c.att["k_pool"],
+                              c.att["v_pool"], t(lay["req_to_token"]), t(lay["req_pool_idx"]), t(lay["seq_lens"]),
+                              max_len, t(lay["verify_loc"]), mask, 1.0 / math.sqrt(wl.D), out, lse, ws)
+    assert ws.last_error() == 0
+    pairs = None if name == "tiny" else _attention_pairs(wl, np.random.default_rng(0))
+    ref = oracle.verify_attention(wl.b, wl.n, wl.Hq, wl.Hkv, wl.D, W.host(c.att["q"]), W.host(c.att["k_pool"]),
+                                  W.host(c.att["v_pool"]), lay["req_to_token"], lay["req_pool_idx"],
+                                  lay["seq_lens"], lay["verify_loc"], c.tree["mask_bits"], 1.0 / math.sqrt(wl.D),
+                                  pairs=pairs)
+    g = out.float().cpu().numpy()
+    gl = _np(lse)
+    sel = (slice(None), slice(None)) if pairs is None else (pairs[:, 0], pairs[:, 1])
+    r_o, g_o = ref["out"][sel], g[sel]
+    err = np.abs(g_o - r_o)
+    assert (err <= 1e-2 * np.maximum(1.0, np.abs(r_o))).all(), float(err.max())
+    np.testing.assert_allclose(gl[sel], ref["lse"][sel], rtol=1e-4, atol=1e-4)
+
+
+# ----------------------------------------------------------------- commit
+
+@pytest.mark.parametrize("name", FULL)
+def test_commit_kv_parity(cases, name):
+    c = cases(name, "greedy")
+    wl, ops = c.wl, _ops()
+    lay = c.layout
+    acc = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), c.tree["draft_tokens"], c.tree["retrieve_index"],
+                               c.tree["next_token"], c.tree["next_sibling"])
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    kp, vp = c.att["k_pool"].clone(), c.att["v_pool"].clone()
+    new_len = torch.zeros(wl.b, dtype=torch.int32, device="cuda")
+    free_ids = torch.zeros(wl.b * wl.n, dtype=torch.int32, device="cuda")
+    n_free = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_COMMIT_KV, wl.b, wl.n, 1, 1))
+    ops.spec_commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, [kp], [vp], t(lay["req_to_token"]),
+                       t(lay["req_pool_idx"]), t(lay["seq_lens"]), t(lay["verify_loc"]), t(acc["accept_index"]),
+                       t(acc["accept_lens"]), new_len, free_ids, n_free, ws)
+    assert ws.last_error() == 0
+    hk, hv = W.host(c.att["k_pool"]).copy(), W.host(c.att["v_pool"]).copy()
+    o = oracle.commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, [hk], [hv], lay["req_to_token"],
+                         lay["req_pool_idx"], lay["seq_lens"], lay["verify_loc"], acc["accept_index"],
+                         acc["accept_lens"])
+    np.testing.assert_array_equal(_np(new_len), o["new_seq_lens"])
+    nf = int(_np(n_free)[0])
+    np.testing.assert_array_equal(_np(free_ids)[:nf], o["free_ids"])
+    np.testing.assert_array_equal(W.host(kp), hk)
+    np.testing.assert_array_equal(W.host(vp), hv)
+
+
+# ------------------------------------------------------------- end to end
+
+@pytest.mark.parametrize("name,mode", [("tiny", "greedy"), ("tiny", "sampling"), ("llama8b_greedy", "greedy"),
+                                       ("sampling_heavy", "sampling"), ("long_context", "greedy"),
+                                       ("mtp_chain", "sampling")])
+def test_end_to_end_step(cases, name, mode):
+    """The whole GPU step (VerifyStep.run) against the oracle chain."""
+    from accept_select_top_gb300.pipeline import VerifyStep
+    c = cases(name, mode)
+    wl = c.wl
+    inp = c.device_inputs()
+    kp0, vp0 = W.host(inp.k_pool).copy(), W.host(inp.v_pool).copy()
+    inp.k_pool, inp.v_pool = inp.k_pool.clone(), inp.v_pool.clone()
+    step = VerifyStep(wl, inp, mode)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.ws.last_error() == 0
+    tr = c.tree
+    same_tree = all(np.array_equal(_np(getattr(step, k_)), tr[k_]) for k_ in
+                    ("draft_tokens", "positions", "next_token", "next_sibling"))
+    if not same_tree:
+        pytest.skip("draft tree differs through a certified near tie of path scores")  # counted by the select test
+    np.testing.assert_array_equal(_np(step.mask_bits).view(np.uint64), tr["mask_bits"])
+    if mode == "greedy":
+        o = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), tr["draft_tokens"], tr["retrieve_index"],
+                                 tr["next_token"], tr["next_sibling"])
+        for k_ in ("predict", "accept_index", "accept_lens", "accepted_tokens", "next_root"):
+            np.testing.assert_array_equal(_np(getattr(step, k_)), o[k_], err_msg=k_)
+    else:
+        o = oracle.verify_sampling(wl.b, wl.n, wl.S, W.host(c.logits), W.host(c.q), c.temps, W.host(c.u),
+                                   W.host(c.u_final), tr["draft_tokens"], tr["retrieve_index"], tr["next_token"],
+                                   tr["next_sibling"])
+        mism = int((_np(step.accept_lens) != o["accept_lens"]).sum())
+        assert mism <= max(1, wl.b // 50)
+        if mism:
+            pytest.skip(f"{mism} certified-size accept differences; exact commit check needs equal accepts")
+    # commit on the oracle side from the oracle's accept result
+    o2 = oracle.commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, [kp0], [vp0], c.layout["req_to_token"],
+                          c.layout["req_pool_idx"], c.layout["seq_lens"], c.layout["verify_loc"], o["accept_index"],
+                          o["accept_lens"])
+    np.testing.assert_array_equal(_np(step.new_seq_lens), o2["new_seq_lens"])
+    nf = int(_np(step.n_free)[0])
+    np.testing.assert_array_equal(_np(step.free_ids)[:nf], o2["free_ids"])
+    if name != "mtp_chain":  # the largest pools: committed rows are compared through the ids above
+        np.testing.assert_array_equal(W.host(inp.k_pool), kp0)
+
+
+# ------------------------------------------------------------- edge cases
+
+def test_idle_batch_and_bad_workspace():
+    ops = _ops()
+    ws = ops.Workspace(256)
+    x = torch.zeros(1, 16, device="cuda")
+    i = torch.zeros(16, dtype=torch.int32, device="cuda")
+    ops.spec_verify_greedy(0, 4, 2, x, i, i, i, i, i, i, i, i, i, ws)  # b == 0: no-op
+    with pytest.raises(ops.SpecError, match="workspace"):
+        ops.spec_verify_greedy(2, 4, 2, torch.zeros(8, 100000, device="cuda"), i, i, i, i, i, i, i, i, i, ws)
+
+
+@pytest.mark.parametrize("V,dtype", [(1000, torch.float32), (1001, torch.bfloat16), (33, torch.bfloat16),
+                                     (4096 + 8, torch.bfloat16)])
+def test_ragged_vocab_select_and_greedy(V, dtype):
+    """Vocabularies that are not a multiple of the 16-byte vector take the
+    scalar path; a vocabulary that is takes the vector path with a ragged last
+    chunk."""
+    wl = W.scaled(W.WORKLOADS["tiny"], name=f"ragged{V}", V=V, logits_dtype="f32" if dtype == torch.float32 else "bf16",
+                  k=4, S=3, n=9)
+    c = make_case(wl, "greedy", with_attention=False)
+    ops = _ops()
+    ws = ops.Workspace(max(ops.spec_workspace_size(op, wl.b, wl.n, wl.k, wl.V) for op in (0, 3)))
+    scores_in = None
+    for i in range(wl.S):
+        g = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws)
+        o = oracle.select_topk(i, wl.b, wl.k, c.host_drafts[i], 1.0, None if scores_in is None else _np(scores_in))
+        np.testing.assert_array_equal(_np(g["token_blk"]), o["token_blk"])
+        np.testing.assert_allclose(_np(g["topk_p"]), o["topk_p"], rtol=1e-6)
+        scores_in = g["scores_out"]
+    bufs = _accept_bufs(wl)
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *bufs.values(), ws)
+    o = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), c.tree["draft_tokens"], c.tree["retrieve_index"],
+                             c.tree["next_token"], c.tree["next_sibling"])
+    for k_, v in bufs.items():
+        np.testing.assert_array_equal(_np(v), o[k_], err_msg=k_)
+
+
+def test_max_sizes_k16_n64():
+    """topk 16 (the largest list), 64 tree nodes (a full mask word)."""
+    wl = W.scaled(W.WORKLOADS["tiny"], name="max", b=3, k=16, S=3, n=64, V=5000, logits_dtype="bf16", Hq=8, Hkv=2,
+                  D=128, ctx=("uniform", 100, 300))
+    c = make_case(wl, "greedy")
+    from accept_select_top_gb300.pipeline import VerifyStep
+    inp = c.device_inputs()
+    step = VerifyStep(wl, inp, "greedy")
+    step.select()
+    step.build()
+    torch.cuda.synchronize()
+    for k_ in ("draft_tokens", "positions", "next_token", "next_sibling"):
+        np.testing.assert_array_equal(_np(getattr(step, k_)), c.tree[k_], err_msg=k_)
+    step.attention()
+    ref = oracle.verify_attention(wl.b, wl.n, wl.Hq, wl.Hkv, wl.D, W.host(inp.q), W.host(inp.k_pool),
+                                  W.host(inp.v_pool), c.layout["req_to_token"], c.layout["req_pool_idx"],
+                                  c.layout["seq_lens"], c.layout["verify_loc"], c.tree["mask_bits"],
+                                  1.0 / math.sqrt(wl.D))
+    g = step.out.float().cpu().numpy()
+    assert (np.abs(g - ref["out"]) <= 1e-2 * np.maximum(1, np.abs(ref["out"]))).all()
+
+
+def test_bad_tree_index_sets_error_word_without_fault():
+    """A next_token pointing outside the tree is reported in the error word and
+    skipped; the context stays usable."""
+    c = make_case(W.WORKLOADS["tiny"], "greedy", with_attention=False)
+    wl, ops = c.wl, _ops()
+    dt, ri, nt, ns = _tree_dev(c)
+    nt = nt.clone()
+    nt[0] = 1000
+    bufs = _accept_bufs(wl)
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, wl.b, wl.n, 1, wl.V))
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, dt, ri, nt, ns, *bufs.values(), ws)
+    assert ws.last_error() & ops.DEV_INDEX
+    assert ws.last_error() == 0  # read-and-clear
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *bufs.values(), ws)
+    torch.cuda.synchronize()
