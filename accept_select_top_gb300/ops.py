@@ -27,7 +27,7 @@ _ERRORS = {-1: "bad argument", -2: "workspace too small or misaligned", -3: "CUD
 
 EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_last_error", "spec_device_sm_count",
            "spec_select_topk", "spec_build_tree", "spec_verify_attention", "spec_verify_greedy",
-           "spec_verify_sampling", "spec_commit_kv"]
+           "spec_verify_sampling", "spec_commit_kv", "spec_verify_greedy_noalloc"]
 
 
 class SpecError(RuntimeError):
@@ -50,6 +50,7 @@ def _load() -> ctypes.CDLL:
         "spec_verify_greedy": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_sampling": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_commit_kv": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, P, P, P, P, P, P, Z, P]),
+        "spec_verify_greedy_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -181,3 +182,15 @@ def spec_commit_kv(b: int, n: int, W: int, Hkv: int, D: int, page_size: int, k_l
                               req_to_token.shape[0], req_to_token.shape[1], _ptr(req_pool_idx), _ptr(seq_lens),
                               _ptr(verify_loc), _ptr(accept_index), _ptr(accept_lens), _ptr(new_seq_lens),
                               _ptr(free_ids), _ptr(n_free), ws.ptr, ws.nbytes, _stream(stream)), "spec_commit_kv")
+
+
+def spec_verify_greedy_noalloc(b: int, n: int, S: int, logits, draft_tokens, retrieve_index, next_token,
+                               next_sibling, predict, accept_index, accept_lens, accepted_tokens, next_root,
+                               stream=None):
+    """spec_verify_greedy for callers that cannot allocate device memory: the
+    library's fixed device scratch array stands in for the workspace."""
+    V = logits.shape[-1]
+    _check(LIB.spec_verify_greedy_noalloc(b, n, S, V, _dtype_code(logits), _ptr(logits), _ptr(draft_tokens),
+                                          _ptr(retrieve_index), _ptr(next_token), _ptr(next_sibling), _ptr(predict),
+                                          _ptr(accept_index), _ptr(accept_lens), _ptr(accepted_tokens),
+                                          _ptr(next_root), _stream(stream)), "spec_verify_greedy_noalloc")

@@ -249,6 +249,40 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
                    int32_t* free_ids, int32_t* n_free,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * spec_verify_greedy_noalloc -- spec_verify_greedy without a caller workspace.
+ * The pages have no counterpart: this exists for callers that cannot allocate
+ * device memory when they verify -- an engine whose allocator owns all device
+ * memory, a latency-critical path that must not pay cudaMalloc's implicit
+ * device synchronisation, or a plugin host that forbids allocation after
+ * start-up.
+ *
+ * Arguments, outputs and semantics are those of spec_verify_greedy.  The
+ * scratch memory is a fixed array of SPEC_NOALLOC_SCRATCH_BYTES inside the
+ * library's device image; every GPU that loads the library holds it until the
+ * process exits.  The entry point allocates nothing (no cudaMalloc, no
+ * allocating library call).
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Each call zeroes the array's error word and counters on `stream`, then
+ *     runs the greedy kernels with the array as their workspace.
+ *   - Every call shares the one array per device: calls that overlap on the
+ *     GPU (different streams, or concurrent host threads) race.  Serialise them.
+ *   - Returns SPEC_ERR_WORKSPACE when b, n and V need more scratch than the
+ *     array holds (spec_workspace_size(SPEC_OP_VERIFY_GREEDY, ...) bytes).
+ *   - Device index errors go to the array's error word, which this entry point
+ *     does not report; use spec_verify_greedy with a workspace to read them.
+ * ------------------------------------------------------------------------- */
+#define SPEC_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+int spec_verify_greedy_noalloc(int b, int n, int S, int V, int dtype, const void* logits,
+                               const int32_t* draft_tokens, const int32_t* retrieve_index,
+                               const int32_t* next_token, const int32_t* next_sibling,
+                               int32_t* predict, int32_t* accept_index,
+                               int32_t* accept_lens, int32_t* accepted_tokens,
+                               int32_t* next_root, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
