@@ -136,7 +136,6 @@ int launch_select_topk(const SelectParams& p, cudaStream_t stream);
 int launch_build_tree(const BuildParams& p, cudaStream_t stream);
 int launch_verify_greedy(const GreedyParams& p, cudaStream_t stream);
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream);
-int launch_attention_simple(const AttentionParams& p, cudaStream_t stream);
 int launch_commit_kv(const CommitParams& p, cudaStream_t stream);
 
 size_t select_partial_bytes(int rows, int chunks);
@@ -145,7 +144,15 @@ size_t sampling_partial_bytes(int rows, int chunks);
 size_t sampling_state_bytes(int b);
 size_t sampling_partial2_bytes(int b, int chunks2);
 size_t commit_partial_bytes(int b, int n);
-int attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len);
+
+// Split-KV geometry of the tensor-core attention: m_tiles CTAs of 128 query
+// rows per (request, kv head), splits of split_tiles 128-key tiles each.
+struct TcGeometry {
+  int m_tiles, split_tiles, splits;
+};
+TcGeometry attention_tc_geometry(int b, int n, int Hq, int Hkv, int max_seq_len);
+int launch_attention_tc(const AttentionParams& p, const TcGeometry& geo, cudaStream_t stream);
+int launch_attention_merge(const AttentionParams& p, cudaStream_t stream);
 size_t attention_partial_bytes(int b, int n, int Hq, int D, int splits);
 
 }  // namespace spec

@@ -42,7 +42,7 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
       return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
              sampling_partial2_bytes(b, chunk_bound(b, V));
     case SPEC_OP_VERIFY_ATTENTION:
-      return attention_partial_bytes(b, n, Hq, 128, attention_splits(b, n, Hq, Hkv, max_seq_len));
+      return attention_partial_bytes(b, n, Hq, 128, attention_tc_geometry(b, n, Hq, Hkv, max_seq_len).splits);
     case SPEC_OP_COMMIT_KV:
       return commit_partial_bytes(b, n);
     default:
@@ -174,6 +174,8 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   if (b < 0 || n < 1 || n > kMaxN || Hq < 1 || Hkv < 1 || Hq % Hkv || page_size < 1) return SPEC_ERR_ARG;
   if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
   if (num_slots < 1 || req_rows < 1 || row_w < 1 || max_seq_len < 0) return SPEC_ERR_ARG;
+  // TMA row coordinates of the gathers (slot * Hkv + head, node rows * Hq) are int32
+  if (num_slots * Hkv >= (int64_t(1) << 31) || int64_t(b) * n * Hq >= (int64_t(1) << 31)) return SPEC_ERR_ARG;
   if (b == 0) return SPEC_OK;
   if (!q || !k_pool || !v_pool || !req_to_token || !req_pool_idx || !seq_lens || !verify_loc || !mask_bits || !out)
     return SPEC_ERR_ARG;
@@ -203,11 +205,12 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   p.scale = scale;
   p.out = out;
   p.lse = lse;
-  p.splits = attention_splits(b, n, Hq, Hkv, max_seq_len);
+  const TcGeometry geo = attention_tc_geometry(b, n, Hq, Hkv, max_seq_len);
+  p.splits = geo.splits;
   p.error = v.error;
   p.counters = v.counters;
   p.partials = v.partials;
-  return launch_attention_simple(p, as_stream(stream));
+  return launch_attention_tc(p, geo, as_stream(stream));
 }
 
 int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,

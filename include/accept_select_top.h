@@ -64,6 +64,7 @@ extern "C" {
 #define SPEC_DEV_INDEX 1u      /* an index read from an input array was out of range */
 #define SPEC_DEV_INVARIANT 2u  /* a selected node's parent was not selected (build_tree) */
 #define SPEC_DEV_LENGTH 4u     /* a length (seq_len, accept_len) outside its valid range */
+#define SPEC_DEV_TIMEOUT 8u    /* a bounded device-side wait ran out; the kernel stopped cleanly */
 
 /* operation ids for spec_workspace_size */
 #define SPEC_OP_SELECT_TOPK 0
