@@ -37,28 +37,29 @@ namespace spec {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kKeys = 128;
+constexpr int kKeys = 64;
 constexpr int kStages = 2;
 constexpr int kTcThreads = 192;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 256;  // two CTAs share an SM's 512 columns
 constexpr uint32_t kColO = 0;
-// S buffer b lives at TMEM columns [128 + 128 b, 256 + 128 b)
-__host__ __device__ constexpr uint32_t col_s(int b) { return 128u + 128u * uint32_t(b); }
+// S buffer b lives at TMEM columns [128 + 64 b, 192 + 64 b)
+__host__ __device__ constexpr uint32_t col_s(int b) { return 128u + 64u * uint32_t(b); }
 constexpr float kRescaleLog2 = 8.f;       // O is rescaled only when the row max grows by more than 2^8
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz: bound of every mbarrier wait
 
 template <int D>
 struct Smem {
   static constexpr int kHalves = D / 64;
-  static constexpr int kBlock = kRows * 128;      // [128 rows x 64 bf16], 128B-swizzled: 16 KB
-  static constexpr int kTile = kHalves * kBlock;  // a Q, K or V tile
+  static constexpr int kQBlock = kRows * 128;      // [128 rows x 64 bf16], 128B-swizzled: 16 KB
+  static constexpr int kQTile = kHalves * kQBlock;
+  static constexpr int kKBlock = kKeys * 128;      // [64 keys x 64 bf16]: 8 KB
+  static constexpr int kKTile = kHalves * kKBlock; // a K or V tile
   static constexpr int kQ = 0;
-  static constexpr int kStage = kTile;            // stage s: K at kStage + 2*s*kTile, V at + kTile
-  static constexpr int kKinds = kStage + kStages * 2 * kTile;  // int16 kind per key and stage
-  static constexpr int kFlags = kKinds + kStages * kKeys * 2;  // int per stage: tile is all prefix
+  static constexpr int kStage = kQTile;            // stage s: K at kStage + 2*s*kKTile, V at + kKTile
+  static constexpr int kFlags = kStage + kStages * 2 * kKTile;  // per stage: 4 words of key flags
   static constexpr int kBars = kFlags + 64;
   static constexpr int kBytes = kBars + 256;
-  static constexpr int kTx = 2 * kTile;           // bytes one stage receives
+  static constexpr int kTx = 2 * kKTile;           // bytes one stage receives
 };
 
 // barriers (uint64 each), by index
@@ -190,8 +191,13 @@ struct TcArgs {
   int split_tiles;
 };
 
+// Per-stage key flags (4 words in shared memory):
+//   [0] bit j: key 2j of the tile has a valid slot      [1] same for key 2j+1
+//   [2] 1 when every key of the tile is a valid prefix key (no masking needed)
+__device__ __forceinline__ bool key_valid(const uint32_t* f, int c) { return (f[c & 1] >> (c >> 1)) & 1u; }
+
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     attention_tc_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = Smem<D>;
@@ -200,6 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int mt = blockIdx.x % args.m_tiles, g = blockIdx.x / args.m_tiles;
   const int req = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned FULL = 0xffffffffu;
 
   // ---- request geometry (bounds-checked) ----
   int Lp = a.seq_lens[req];
@@ -214,11 +221,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int k0 = split * args.split_tiles * kKeys;
   const int k1 = min(total, k0 + args.split_tiles * kKeys);
   const int T = k0 < k1 ? (k1 - k0 + kKeys - 1) / kKeys : 0;
+  const bool direct = a.splits == 1;  // one split: write the normalised output here
 
   float* po = reinterpret_cast<float*>(a.partials);
   float* pml = po + size_t(a.b) * a.n * a.Hq * a.splits * D;
   if (T == 0) {  // nothing in this split: an empty partial for every valid row
-    if (threadIdx.x < kRows) {
+    if (!direct && threadIdx.x < kRows) {
       const int rg = mt * kRows + threadIdx.x;
       if (rg < M) {
         const size_t idx = ((size_t(req) * a.n + rg / G) * a.Hq + g * G + rg % G) * a.splits + split;
@@ -234,8 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   unsigned char* sp = smem_raw + (sbase - raw);
-  int16_t* kinds = reinterpret_cast<int16_t*>(sp + L::kKinds);
-  int* prefix_flag = reinterpret_cast<int*>(sp + L::kFlags);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(sp + L::kFlags);  // [stage][4]
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sp + L::kBars + 8 * kNumBars);
@@ -283,60 +290,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int rg = mt * kRows + 4 * lane + e;
         y[e] = rg < M ? (req * a.n + rg / G) * a.Hq + g * G + rg % G : -1;  // -1: zero-filled
       }
-      if (lane == 0) mbar_expect_tx(bar(kQFull), L::kTile);
+      if (lane == 0) mbar_expect_tx(bar(kQFull), L::kQTile);
       __syncwarp();
 #pragma unroll
       for (int h = 0; h < L::kHalves; ++h)
-        tma_gather4(sbase + L::kQ + h * L::kBlock + 512u * lane, &tm_q, 64 * h, y[0], y[1], y[2], y[3], bar(kQFull));
+        tma_gather4(sbase + L::kQ + h * L::kQBlock + 512u * lane, &tm_q, 64 * h, y[0], y[1], y[2], y[3],
+                    bar(kQFull));
     }
+    // Keys 2*lane and 2*lane+1 of tile t: the slot loads are issued one tile
+    // ahead (issue) and their values consumed only after this tile's gathers
+    // are out (finish), so the lookup latency hides behind the pipeline.
+    auto issue = [&](int t, int (&slot)[2], int (&kind)[2]) {  // kind: 0 none, 1 prefix, 2 tree node
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kg = k0 + t * kKeys + 2 * lane + e;
+        slot[e] = -1;
+        kind[e] = 0;
+        if (kg < k1) {
+          if (kg < Lp) {
+            slot[e] = a.req_to_token[size_t(rq) * a.row_w + kg];
+            kind[e] = 1;
+          } else {
+            slot[e] = a.verify_loc[size_t(req) * a.n + (kg - Lp)];
+            kind[e] = 2;
+          }
+        }
+      }
+    };
+    auto finish = [&](const int (&slot)[2], const int (&kind)[2], int (&row)[2], bool (&pre)[2]) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool ok_slot = slot[e] >= 0 && slot[e] < a.num_slots;
+        if (kind[e] != 0 && !ok_slot) raise_error(a.error, SPEC_DEV_INDEX);
+        const bool v = kind[e] != 0 && ok_slot;
+        row[e] = v ? int(slot[e] * a.Hkv + g) : -1;  // -1: zero-filled, masked out
+        pre[e] = v && kind[e] == 1;
+      }
+    };
+    int row[2], slot_n[2], kind_n[2];
+    bool pre[2];
+    issue(0, slot_n, kind_n);
+    finish(slot_n, kind_n, row, pre);
     int issued = 0;
     for (int t = 0; t < T; ++t) {
       const int s = t & 1;
+      if (t + 1 < T) issue(t + 1, slot_n, kind_n);  // in flight while this warp waits
       const bool e_ok = (t < 2 || mbar_wait(bar(kEmpty0 + s), ((t >> 1) - 1) & 1)) && !*abort_flag;
-      if (!__all_sync(0xffffffffu, e_ok)) {  // the warp leaves the loop together
+      if (!__all_sync(FULL, e_ok)) {  // the warp leaves the loop together
         if (!*abort_flag) fail();
         break;
       }
-      int y[4];
-      bool all_prefix = true;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = 4 * lane + e;
-        const int kg = k0 + t * kKeys + c;
-        long long slot = -1;
-        int kind = -2;
-        if (kg < k1) {
-          if (kg < Lp) {
-            slot = a.req_to_token[size_t(rq) * a.row_w + kg];
-            kind = -1;
-          } else {
-            slot = a.verify_loc[size_t(req) * a.n + (kg - Lp)];
-            kind = kg - Lp;
-          }
-          if (slot < 0 || slot >= a.num_slots) {
-            raise_error(a.error, SPEC_DEV_INDEX);
-            slot = -1;
-            kind = -2;
-          }
-        }
-        y[e] = slot >= 0 ? int(slot * a.Hkv + g) : -1;
-        kinds[s * kKeys + c] = int16_t(kind);
-        all_prefix = all_prefix && kind == -1;
-      }
-      const bool tile_prefix = __all_sync(0xffffffffu, all_prefix);
+      const unsigned v0 = __ballot_sync(FULL, row[0] >= 0), v1 = __ballot_sync(FULL, row[1] >= 0);
+      const bool all_pre = __all_sync(FULL, pre[0] && pre[1]);
       if (lane == 0) {
-        prefix_flag[s] = tile_prefix ? 1 : 0;
+        flags[4 * s + 0] = v0;
+        flags[4 * s + 1] = v1;
+        flags[4 * s + 2] = all_pre ? 1u : 0u;
+        mbar_expect_tx(bar(kFull0 + s), L::kTx);
       }
+      // lane l gathers keys 4(l%16) .. 4(l%16)+3 of K (l < 16) or V (l >= 16)
+      const int grp = lane & 15;
+      const int y0 = __shfl_sync(FULL, row[0], 2 * grp), y1 = __shfl_sync(FULL, row[1], 2 * grp);
+      const int y2 = __shfl_sync(FULL, row[0], 2 * grp + 1), y3 = __shfl_sync(FULL, row[1], 2 * grp + 1);
       __syncwarp();
-      if (lane == 0) mbar_expect_tx(bar(kFull0 + s), L::kTx);
-      __syncwarp();
-      const uint32_t kdst = sbase + L::kStage + 2u * s * L::kTile + 512u * lane;
+      const bool is_v = lane >= 16;
+      const uint32_t dst = sbase + L::kStage + 2u * s * L::kKTile + (is_v ? L::kKTile : 0) + 512u * grp;
 #pragma unroll
-      for (int h = 0; h < L::kHalves; ++h) {
-        tma_gather4(kdst + h * L::kBlock, &tm_k, 64 * h, y[0], y[1], y[2], y[3], bar(kFull0 + s));
-        tma_gather4(kdst + L::kTile + h * L::kBlock, &tm_v, 64 * h, y[0], y[1], y[2], y[3], bar(kFull0 + s));
-      }
+      for (int h = 0; h < L::kHalves; ++h)
+        tma_gather4(dst + h * L::kKBlock, is_v ? &tm_v : &tm_k, 64 * h, y0, y1, y2, y3, bar(kFull0 + s));
       issued = t + 1;
+      if (t + 1 < T) finish(slot_n, kind_n, row, pre);
     }
     // drain: every stage this warp filled has landed before the CTA can exit
     for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(bar(kFull0 + (t & 1)), (t >> 1) & 1);
@@ -350,13 +373,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(bar(kPReady0 + b), (u >> 1) & 1)) return false;
         if (*abort_flag) return false;
         tc_fence_after();
-        const uint32_t vbase = sbase + L::kStage + 2u * b * L::kTile + L::kTile;
+        const uint32_t vbase = sbase + L::kStage + 2u * b * L::kKTile + L::kKTile;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h) {
             // V half h, keys 16kk..16kk+15: MN-major, 8-key groups 1024 B apart
-            const uint64_t bd = sdesc(vbase + h * L::kBlock + kk * 16 * 128, 1024, 1024);
+            const uint64_t bd = sdesc(vbase + h * L::kKBlock + kk * 16 * 128, 1024, 1024);
             mma_ts(tmem + kColO + 64 * h, tmem + col_s(b) + 8 * kk, bd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
           }
         }
@@ -373,12 +396,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = sbase + L::kStage + 2u * s * L::kTile;
+        const uint32_t kbase = sbase + L::kStage + 2u * s * L::kKTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kBlock + (kk & 3) * 32;
-          const uint64_t ad = sdesc(sbase + L::kQ + off, 16, 1024);
-          const uint64_t bd = sdesc(kbase + off, 16, 1024);
+          const uint32_t ko = (kk >> 2) * L::kKBlock + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * L::kQBlock + (kk & 3) * 32;
+          const uint64_t ad = sdesc(sbase + L::kQ + qo, 16, 1024);
+          const uint64_t bd = sdesc(kbase + ko, 16, 1024);
           mma_ss(tmem + col_s(s), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kSFull0 + s));
@@ -399,7 +423,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // tcgen05.ld / tcgen05.st are .sync.aligned: every lane of the warp issues
     // them together, so every branch around them and every loop exit below is
     // warp-uniform (padding rows compute and store zeros instead of skipping).
-    const unsigned FULL = 0xffffffffu;
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int r = 32 * quarter + lane;
     const int rg = mt * kRows + r;
@@ -427,14 +450,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[32 * q + i] = v[i];
       }
-      const bool all_prefix = prefix_flag[s] != 0;
+      const uint32_t* f = flags + 4 * s;
+      const bool all_pre = f[2] != 0;
+      const int kbase = k0 + t * kKeys;
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kKeys; ++c) {
         float v = x[c] * sl2;
-        if (!all_prefix) {
-          const int kind = kinds[s * kKeys + c];
-          const bool vis = kind == -1 || (kind >= 0 && ((mask >> kind) & 1ull));
+        if (!all_pre) {
+          const int kg = kbase + c;
+          const bool vis = key_valid(f, c) && (kg < Lp || ((mask >> (kg - Lp)) & 1ull));
           v = vis ? v : -INFINITY;
         }
         x[c] = v;
@@ -482,24 +507,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive(bar(kPReady0 + s));
     }
     if (!ok && !*abort_flag) fail();
-    // epilogue: wait for the last P V, then write this row's partial
+    // epilogue: wait for the last P V, then write this row's output or partial
     const bool e_ok = ok && mbar_wait(bar(kODone), (T - 1) & 1);
     if (__all_sync(FULL, e_ok)) {
       tc_fence_after();
-      const size_t idx = ((size_t(req) * a.n + node) * a.Hq + g * G + rg % G) * a.splits + split;
-      float4* dst = reinterpret_cast<float4*>(po + idx * D);
+      const int head = g * G + rg % G;
+      const size_t orow = (size_t(req) * a.n + node) * a.Hq + head;
+      const size_t idx = orow * a.splits + split;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         float v[32];
         tmem_ld32(tl + kColO + 32 * q, v);
         if (valid) {
+          if (direct) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D) + 4 * q;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) dst[8 * q + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                  pack_bf16(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                  pack_bf16(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                  pack_bf16(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(po + idx * D);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[8 * q + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
         }
       }
       if (valid) {
-        pml[idx * 2] = m_ref;
-        pml[idx * 2 + 1] = lsum;
+        if (direct) {
+          if (a.lse) a.lse[orow] = lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+        } else {
+          pml[idx * 2] = m_ref;
+          pml[idx * 2 + 1] = lsum;
+        }
       }
     } else if (!*abort_flag) {
       fail();
@@ -561,7 +604,7 @@ int launch_t(const AttentionParams& p, const TcGeometry& geo, cudaStream_t strea
   dim3 grid(p.Hkv * geo.m_tiles, p.b, p.splits);
   attention_tc_kernel<D><<<grid, kTcThreads, smem, stream>>>(args, tq, tk, tv);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
-  return launch_attention_merge(p, stream);
+  return p.splits == 1 ? SPEC_OK : launch_attention_merge(p, stream);
 }
 
 }  // namespace
@@ -572,15 +615,14 @@ TcGeometry attention_tc_geometry(int b, int n, int Hq, int Hkv, int max_seq_len)
   geo.m_tiles = (n * G + kRows - 1) / kRows;
   const long units = long(b) * Hkv * geo.m_tiles;
   const long tiles = (long(max_seq_len) + n + kKeys - 1) / kKeys;
-  long want = (4L * 152 + units - 1) / units;  // about four waves of one CTA per SM
-  if (want < 1) want = 1;
-  long split_tiles = (tiles + want - 1) / want;
-  if (split_tiles < 4) split_tiles = 4;       // keep the pipeline warm
-  if (split_tiles > tiles) split_tiles = tiles;
-  if (split_tiles < 1) split_tiles = 1;
-  geo.split_tiles = int(split_tiles);
-  geo.splits = int((tiles + split_tiles - 1) / split_tiles);
-  if (geo.splits < 1) geo.splits = 1;
+  // aim at two waves of two CTAs per SM, splits of at least 8 tiles, and at
+  // most 16 splits (each split adds a partial per row to write and merge)
+  long splits = (2L * 2 * 152 + units - 1) / units;
+  if (splits > tiles / 8) splits = tiles / 8;
+  if (splits > 16) splits = 16;
+  if (splits < 1) splits = 1;
+  geo.split_tiles = int((tiles + splits - 1) / splits);
+  geo.splits = int((tiles + geo.split_tiles - 1) / geo.split_tiles);
   return geo;
 }
 

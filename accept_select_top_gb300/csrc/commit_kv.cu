@@ -27,7 +27,7 @@ constexpr int kSliceBytes = 32 * 1024;  // shared staging per slice (K and V of 
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) {
   const int req = blockIdx.x;
   const int n = a.n, W = a.W;
-  __shared__ long long src[kMaxN + 1], dst[kMaxN + 1];
+  __shared__ int src[kMaxN + 1], dst[kMaxN + 1];
   __shared__ int s_ok, s_L;
   __shared__ uint4 stage[kSliceBytes / 16];
   int* stage_free = reinterpret_cast<int*>(a.partials) + size_t(req) * n;
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) 
   const int L = s_L;
   for (int kk = threadIdx.x; kk < L; kk += blockDim.x) {
     const int ai = a.accept_index[size_t(req) * W + kk];
-    long long s = -1, d = -1;
+    int s = -1, d = -1;
     if (ai >= 0 && ai < a.b * n) s = a.verify_loc[ai];
     d = a.req_to_token[size_t(a.req_pool_idx[req]) * a.row_w + a.seq_lens[req] + kk];
     if (s < 0 || s >= a.num_slots || d < 0 || d >= a.num_slots) {
@@ -94,45 +94,88 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) 
   }
   if (threadIdx.x == 0) a.new_seq_lens[req] = a.seq_lens[req] + (ok ? L : 0);
 
-  // free units of this request, in ascending node order (one thread: n <= 64)
-  if (threadIdx.x == 0) {
-    int cnt = 0;
-    if (ok) {
-      const long long ps = a.page_size;
-      for (int j = 0; j < n; ++j) {
-        const long long slot = a.verify_loc[size_t(req) * n + j];
-        if (slot < 0 || slot >= a.num_slots) {
-          raise_error(a.error, SPEC_DEV_INDEX);
-          continue;
-        }
-        const long long unit = slot / ps;
-        bool kept = false;
-        for (int kk = 0; kk < L && !kept; ++kk) kept = dst[kk] / ps == unit;
-        if (kept) continue;
-        bool listed = false;
-        for (int jj = 0; jj < j && !listed; ++jj) listed = a.verify_loc[size_t(req) * n + jj] / ps == unit;
-        if (listed) continue;
-        stage_free[cnt++] = int(unit);
-      }
+  // free units of this request, in ascending node order: node j's unit
+  // (slot, or page = slot / page_size) is released when no target slot of the
+  // request lies in it, at the first node that holds it.  One node per thread.
+  __shared__ int unit_s[kMaxN];
+  __shared__ int dst_unit_s[kMaxN + 1];
+  __shared__ int s_count;
+  const int ps = a.page_size;
+  for (int kk = threadIdx.x; kk < L; kk += blockDim.x) dst_unit_s[kk] = int(dst[kk] / ps);
+  bool free_j = false;
+  int j = threadIdx.x;
+  if (j < n) {
+    const int slot = a.verify_loc[size_t(req) * n + j];
+    unit_s[j] = (slot >= 0 && slot < a.num_slots) ? slot / ps : -1;
+  }
+  __syncthreads();
+  if (j < n && ok) {
+    const int u = unit_s[j];
+    if (u < 0) {
+      raise_error(a.error, SPEC_DEV_INDEX);
+    } else {
+      bool kept = false;
+      for (int kk = 0; kk < L && !kept; ++kk) kept = dst_unit_s[kk] == u;
+      bool listed = false;
+      for (int jj = 0; jj < j && !listed; ++jj) listed = unit_s[jj] == u;
+      free_j = !kept && !listed;
     }
-    counts[req] = cnt;
+  }
+  // compaction in node order (n <= 64: the first two warps)
+  __shared__ int warp_cnt[2];
+  if (threadIdx.x < 64) {
+    const unsigned bal = __ballot_sync(0xffffffffu, free_j);
+    if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = __popc(bal);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const unsigned bal = __ballot_sync(0xffffffffu, free_j);
+    const int before = (threadIdx.x >= 32 ? warp_cnt[0] : 0) + __popc(bal & ((1u << (threadIdx.x & 31)) - 1u));
+    if (free_j) stage_free[before] = unit_s[j];
+    if (threadIdx.x == 0) {
+      s_count = warp_cnt[0] + warp_cnt[1];
+      counts[req] = s_count;
+    }
   }
 
   if (!arrive_last(a.counters, uint32_t(a.b))) return;
 
-  // ---- the last CTA concatenates the staged lists in request order ----
-  __shared__ int s_off;
-  if (threadIdx.x == 0) s_off = 0;
+  // ---- the last CTA concatenates the staged lists in request order:
+  // a block-wide exclusive scan of the counts, then each thread copies its
+  // request's entries ----
+  __shared__ int warp_sum[kCommitThreads / 32];
+  __shared__ int s_running;
+  if (threadIdx.x == 0) s_running = 0;
   __syncthreads();
-  for (int r = 0; r < a.b; ++r) {
-    const int c = __ldcg(counts + r);
-    const int* from = reinterpret_cast<const int*>(a.partials) + size_t(r) * n;
-    for (int t = threadIdx.x; t < c; t += blockDim.x) a.free_ids[s_off + t] = __ldcg(from + t);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int r0 = 0; r0 < a.b; r0 += blockDim.x) {
+    const int r = r0 + threadIdx.x;
+    const int c = r < a.b ? __ldcg(counts + r) : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[w] = incl;
     __syncthreads();
-    if (threadIdx.x == 0) s_off += c;
+    int before = s_running;
+    for (int i = 0; i < w; ++i) before += warp_sum[i];
+    const int off = before + incl - c;
+    if (r < a.b) {
+      const int* from = reinterpret_cast<const int*>(a.partials) + size_t(r) * n;
+      for (int e = 0; e < c; ++e) a.free_ids[off + e] = __ldcg(from + e);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int i = 0; i < nw; ++i) tot += warp_sum[i];
+      s_running += tot;
+    }
     __syncthreads();
   }
-  if (threadIdx.x == 0) *a.n_free = s_off;
+  if (threadIdx.x == 0) *a.n_free = s_running;
   counter_reset(a.counters);
 }
 

@@ -153,4 +153,23 @@ inline RowSplit pick_split(long rows, int V, int vec, int max_chunks = kMaxChunk
   return RowSplit{chunks, per};
 }
 
+// The split select_topk uses: as pick_split, but never more than 8192 logits
+// (32 per thread) per CTA, so a thread's share of a chunk fits in registers.
+// More than kMaxChunks chunks (a vocabulary above 262144) is not supported.
+constexpr int kSelectChunkMax = kThreads * 32;
+
+inline RowSplit select_split(long rows, int V, int vec) {
+  long want = (kTargetCtas + rows - 1) / rows;
+  if (want < 1) want = 1;
+  if (want > kMaxChunks) want = kMaxChunks;
+  long by_size = V / 2048;
+  if (by_size < 1) by_size = 1;
+  if (want > by_size) want = by_size;
+  const long need = (long(V) + kSelectChunkMax - 1) / kSelectChunkMax;
+  if (want < need) want = need;
+  int per = int((V + want - 1) / want);
+  per = (per + vec - 1) / vec * vec;
+  return RowSplit{(V + per - 1) / per, per};
+}
+
 }  // namespace spec

@@ -65,49 +65,67 @@ struct TopList {
   }
 };
 
-template <typename T, int K>
-__device__ __forceinline__ void scan_row(const T* row, int begin, int end, bool vec, float c,
-                                         float& m, float& s, TopList<K>& top) {
+// Elements one thread holds: its share of the chunk fits in registers.
+constexpr int kPerThread = 32;
+
+// Loads this thread's elements of row[begin, end) into f: vectors
+// vb + tid + u*blockDim (16-byte loads) or single elements
+// begin + tid + j*blockDim; -inf where there is none.  share_index() gives
+// the vocabulary index of f[j].
+template <typename T>
+__device__ __forceinline__ void load_share(const T* row, int begin, int end, bool vec, float (&f)[kPerThread]) {
   using Tr = LogitTraits<T>;
   constexpr int E = Tr::kVec;
-  auto consume = [&](const float* f, int n_el, int first) {
-    float vm = f[0];
-    for (int e = 1; e < n_el; ++e) vm = fmaxf(vm, f[e]);
-    if (vm >= top.v[K - 1]) {
-      for (int e = 0; e < n_el; ++e) top.push(f[e], first + e);
-    }
-    if (vm > m) {
-      s *= exp2f((m - vm) * c);
-      m = vm;
-    }
-    for (int e = 0; e < n_el; ++e) s += exp2f((f[e] - m) * c);
-  };
+  constexpr int U = kPerThread / E;
   if (vec) {
     const uint4* p = reinterpret_cast<const uint4*>(row);
     const int vb = begin / E, ve = end / E;
-    constexpr int U = 4;
-    for (int v0 = vb + threadIdx.x; v0 < ve; v0 += blockDim.x * U) {
-      uint4 x[U];
+    uint4 x[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int idx = v0 + u * blockDim.x;
-        if (idx < ve) x[u] = ld_stream(p + idx);
+    for (int u = 0; u < U; ++u) {
+      const int v = vb + threadIdx.x + u * blockDim.x;
+      if (v < ve) x[u] = ld_stream(p + v);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = vb + threadIdx.x + u * blockDim.x;
+      float g[E];
+      if (v < ve) {
+        Tr::unpack(x[u], g);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) g[e] = -INFINITY;
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int idx = v0 + u * blockDim.x;
-        if (idx >= ve) break;
-        float f[E];
-        Tr::unpack(x[u], f);
-        consume(f, E, idx * E);
-      }
+      for (int e = 0; e < E; ++e) f[u * E + e] = g[e];
     }
   } else {
-    for (int i = begin + threadIdx.x; i < end; i += blockDim.x) {
-      float f = Tr::load(row, i);
-      consume(&f, 1, i);
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int i = begin + threadIdx.x + j * blockDim.x;
+      f[j] = i < end ? Tr::load(row, i) : -INFINITY;
     }
   }
+}
+
+template <typename T>
+__device__ __forceinline__ int share_index(int begin, bool vec, int j) {
+  constexpr int E = LogitTraits<T>::kVec;
+  return vec ? (begin / E + int(threadIdx.x) + (j / E) * int(blockDim.x)) * E + j % E
+             : begin + int(threadIdx.x) + j * int(blockDim.x);
+}
+
+// The k-th largest of the lanes' values (-inf when fewer than k lanes hold one).
+__device__ __forceinline__ float warp_kth_largest(float v, int k) {
+  float kth = -INFINITY;
+  for (int r = 0; r < k; ++r) {
+    const float mx = warp_max(v);
+    kth = mx;
+    const unsigned holders = __ballot_sync(0xffffffffu, v == mx);
+    if (holders == 0u) break;  // only NaN left
+    if ((threadIdx.x & 31) == __ffs(holders) - 1) v = -INFINITY;
+  }
+  return kth;
 }
 
 // Merge the lanes' sorted lists of a warp into the warp's best K (written by
@@ -138,10 +156,35 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   const T* lrow = static_cast<const T*>(a.logits) + size_t(row) * a.V;
   const float c = 1.4426950408889634f / a.temperature;  // log2(e) / T
 
-  float m = -3.0e38f, s = 0.f;
+  // this thread's share of the chunk, in registers
+  float f[kPerThread];
+  load_share<T>(lrow, begin, end, a.vec_ok, f);
+  float tm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) tm = fmaxf(tm, f[j]);
+  // online-softmax partial of the share: max m and sum of exp((x - m) / T)
+  const float m = fmaxf(tm, -3.0e38f);
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) s += exp2f((f[j] - m) * c);
+  // Pruning threshold: a warp's k-th largest thread maximum tau_w stands for k
+  // distinct elements >= tau_w, so no element below max_w tau_w can be among
+  // the chunk's k best; only elements >= that bound enter the top-K lists.
+  __shared__ float tau_w[kThreads / 32];
+  {
+    const float kth = warp_kth_largest(tm, a.k);
+    if ((threadIdx.x & 31) == 0) tau_w[threadIdx.x >> 5] = kth;
+  }
+  __syncthreads();
+  float tau = -INFINITY;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) tau = fmaxf(tau, tau_w[w]);
   TopList<K> top;
   top.init();
-  scan_row<T, K>(lrow, begin, end, a.vec_ok, c, m, s, top);
+  if (tm >= tau) {
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j)
+      if (f[j] >= tau) top.push(f[j], share_index<T>(begin, a.vec_ok, j));
+  }
 
   // ---- CTA merge: softmax stats and top-K ----
   __shared__ float wm[kThreads / 32], ws_[kThreads / 32];
@@ -229,9 +272,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
         else ++h1;
       }
       if (lane == 0) {
-        // p = exp((x - M) / T) / S with the exponential in fp64
-        const double e = exp((double(bv) - double(M)) / double(a.temperature));
-        p_s[r][j] = float(e / double(S));
+        // p = exp((x - M) / T) / S; x - M is exact for bf16 logits, so fp32
+        // expf (about 1 ulp) keeps p within 1e-6 relative of the fp64 value
+        p_s[r][j] = expf((bv - M) / a.temperature) / S;
         id_s[r][j] = bi;
       }
     }

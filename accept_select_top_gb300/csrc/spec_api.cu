@@ -30,8 +30,8 @@ inline bool vec_ok(const void* logits, int V, int dtype) {
 size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
   switch (op) {
     case SPEC_OP_SELECT_TOPK: {
-      const size_t a = select_partial_bytes(b, chunk_bound(b, V));
-      const size_t c = select_partial_bytes(b * k, chunk_bound(long(b) * k, V));
+      const size_t a = select_partial_bytes(b, select_split(b, V, 1).chunks);
+      const size_t c = select_partial_bytes(b * k, select_split(long(b) * k, V, 1).chunks);
       return a > c ? a : c;
     }
     case SPEC_OP_BUILD_TREE:
@@ -124,7 +124,8 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   p.next_ids = next_input_ids;
   p.topk_p_out = topk_p_out;
   p.rows = b * (step ? k : 1);
-  const RowSplit sp = pick_split(p.rows, V, vec_elems(dtype));
+  const RowSplit sp = select_split(p.rows, V, vec_elems(dtype));
+  if (sp.chunks > kMaxChunks || sp.chunk_elems > kSelectChunkMax) return SPEC_ERR_UNSUPPORTED;
   p.chunks = sp.chunks;
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(draft_logits, V, dtype);

@@ -106,14 +106,18 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
   // ---- finalize request `req` (last CTA to arrive) ----
   const int n = a.n, base = req * n, W = a.S + 1;
   __shared__ int tp[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
+  __shared__ int2 stage[kMaxN * kMaxChunks];
   __shared__ int s_len;
+  // every (row, chunk) partial in one round of loads; partials of other CTAs
+  // are read through L2 (__ldcg), not a stale L1 line
+  for (int t = threadIdx.x; t < n * a.chunks; t += blockDim.x)
+    stage[t] = __ldcg(reinterpret_cast<const int2*>(part + size_t(base) * a.chunks) + t);
+  __syncthreads();
   for (int t = threadIdx.x; t < n; t += blockDim.x) {
-    const ArgPart* pr = part + size_t(base + t) * a.chunks;
     float v = -INFINITY;
     int i = INT_MAX;
     for (int c = 0; c < a.chunks; ++c) {
-      // partials of other CTAs: read through L2 (__ldcg), not a stale L1 line
-      const int2 q = __ldcg(reinterpret_cast<const int2*>(pr + c));
+      const int2 q = stage[t * a.chunks + c];
       const float qv = __int_as_float(q.x);
       if (better(qv, q.y, v, i)) {
         v = qv;

@@ -147,12 +147,18 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
   __shared__ float rM[kMaxN], rS[kMaxN];
   __shared__ int rA[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
   __shared__ int s_len, s_mode;
+  __shared__ float4 stage[kMaxN * kMaxChunks];
+  // every (row, chunk) partial in one round of loads, through L2 (__ldcg)
+  for (int t = threadIdx.x; t < n * a.chunks; t += blockDim.x)
+    stage[t] = __ldcg(reinterpret_cast<const float4*>(
+        reinterpret_cast<const StatPart*>(a.partials) + size_t(base) * a.chunks) + t);
+  __syncthreads();
   for (int t = threadIdx.x; t < n; t += blockDim.x) {
-    const StatPart* pr = reinterpret_cast<const StatPart*>(a.partials) + size_t(base + t) * a.chunks;
+    const float4* pr = stage + t * a.chunks;
     float M = -3.0e38f, v = -INFINITY;
     int arg = INT_MAX;
     for (int ch = 0; ch < a.chunks; ++ch) {
-      const float4 q = __ldcg(reinterpret_cast<const float4*>(pr + ch));
+      const float4 q = pr[ch];
       M = fmaxf(M, q.x);
       // the argmax of a soft row is tracked through the chunk max
       if (better(q.x, __float_as_int(q.y), v, arg)) {
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
     }
     float S = 0.f;
     for (int ch = 0; ch < a.chunks; ++ch) {
-      const float4 q = __ldcg(reinterpret_cast<const float4*>(pr + ch));
+      const float4 q = pr[ch];
       S += q.z * exp2f((q.x - M) * c);
     }
     rM[t] = M;
@@ -237,20 +243,49 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
   counter_reset(a.counters + req);
 }
 
+// Compensated (Kahan) fp32 accumulation: the per-element work stays off the
+// slow fp64 pipe; the few per-thread totals are combined in fp64.
+struct Kahan {
+  float sum = 0.f, comp = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+  }
+};
+
+// Residual max(0, p - q) (mode 2) or p (otherwise) of token v of the terminal row.
+template <typename T>
+__device__ __forceinline__ float terminal_mass(const SamplingParams& a, const ReqState& st, bool use_res, int v) {
+  using Tr = LogitTraits<T>;
+  const float p = p_of(Tr::load(static_cast<const T*>(a.logits) + size_t(st.row) * a.V, v), st.M, st.T, st.S);
+  if (!use_res) return p;
+  const float q = __ldg(a.draft_probs + size_t(st.row) * a.V + v);
+  return p > q ? p - q : 0.f;  // the fp32 difference of the two values
+}
+
 template <typename T>
 __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqState& st, int begin, int end,
                                            double& res, double& ps, int& last_res, int& last_p) {
   using Tr = LogitTraits<T>;
   const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
   const float* q = a.draft_probs + size_t(st.row) * a.V;
+  Kahan kr, kp;
   for (int v = begin + threadIdx.x; v < end; v += blockDim.x) {
     const float p = p_of(Tr::load(L, v), st.M, st.T, st.S);
-    const double r = st.mode == 2 ? fmax(double(p) - double(__ldg(q + v)), 0.0) : 0.0;
-    res += r;
-    ps += double(p);
-    if (r > 0.0) last_res = v;
+    float r = 0.f;
+    if (st.mode == 2) {
+      const float qq = __ldg(q + v);
+      r = p > qq ? p - qq : 0.f;
+    }
+    kr.add(r);
+    kp.add(p);
+    if (r > 0.f) last_res = v;
     if (p > 0.f) last_p = v;
   }
+  res = double(kr.sum) - double(kr.comp);
+  ps = double(kp.sum) - double(kp.comp);
 }
 
 template <typename T>
@@ -337,34 +372,33 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
     const int ce = min(a.V, cb + a.chunk2_elems);
     const int seg = (ce - cb + blockDim.x - 1) / blockDim.x;
     const int sb = cb + threadIdx.x * seg, se = min(ce, sb + seg);
-    const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
-    const float* q = a.draft_probs + size_t(st.row) * a.V;
-    auto mass = [&](int v) {
-      const float p = p_of(Tr::load(L, v), st.M, st.T, st.S);
-      return s_use_res ? fmax(double(p) - double(__ldg(q + v)), 0.0) : double(p);
-    };
-    double mine = 0.0;
-    for (int v = sb; v < se; ++v) mine += mass(v);
-    __shared__ double pre[kThreads];
-    pre[threadIdx.x] = mine;
-    __syncthreads();
-    if (threadIdx.x == 0) {  // exclusive prefix over the segments, in element order
-      double run = s_before;
-      for (int t = 0; t < int(blockDim.x); ++t) {
-        const double x = pre[t];
-        pre[t] = run;
-        run += x;
-      }
+    const bool use_res = s_use_res != 0;
+    Kahan mine;
+    for (int v = sb; v < se; ++v) mine.add(terminal_mass<T>(a, st, use_res, v));
+    // exclusive prefix of the segment totals in element order (fp64 shuffles)
+    __shared__ double wtot[kThreads / 32];
+    const double own = double(mine.sum) - double(mine.comp);
+    double incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    if (lane == 31) wtot[w] = incl;
     __syncthreads();
+    double before = s_before;
+    for (int i = 0; i < w; ++i) before += wtot[i];
+    before += incl - own;
     __shared__ int s_hit;
     if (threadIdx.x == 0) s_hit = INT_MAX;
     __syncthreads();
-    double run = pre[threadIdx.x];
+    // the first positive-mass token where the running sum passes the target
+    const float gap = float(s_target - before);
+    Kahan run;
     for (int v = sb; v < se; ++v) {
-      const double m = mass(v);
-      run += m;
-      if (s_target < run) {
+      const float mv = terminal_mass<T>(a, st, use_res, v);
+      run.add(mv);
+      if (mv > 0.f && gap < run.sum - run.comp) {
         atomicMin(&s_hit, v);
         break;
       }
