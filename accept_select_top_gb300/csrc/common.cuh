@@ -15,6 +15,8 @@
 #include <climits>
 #include <cmath>
 
+#include <cuda_bf16.h>
+
 #include "accept_select_top.h"
 
 namespace spec {
@@ -134,6 +136,124 @@ __device__ __forceinline__ void counter_reset(uint32_t* counter) {
   if (threadIdx.x == 0) atomicExch(counter, 0u);
 }
 
+// Batches of a row chunk row[begin, end).  In each batch every thread holds
+// U = 32 / E raw 16-byte vectors (vector v of the batch = v0 + tid + u *
+// blockDim, E logits each) in registers; fn(x, v0) is called once per batch
+// with absent vectors filled with -inf.  Logit (u, e) of the batch has index
+// (v0 + tid + u * blockDim) * E + e, so each thread sees its logits in
+// increasing index order.  Used only when rows are 16-byte aligned.
+constexpr int kBatch = 32;
+
+template <typename T>
+struct VecOps;
+template <>
+struct VecOps<uint16_t> {
+  static constexpr int E = 8;
+  __device__ static uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+  // maximum of the 8 bf16 values (packed bf16x2 max)
+  __device__ static float vmax(const uint4& x) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&x.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&x.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&x.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&x.w);
+    const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+  __device__ static float at(const uint4& x, int e) {
+    const uint32_t w = e < 2 ? x.x : e < 4 ? x.y : e < 6 ? x.z : x.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+};
+template <>
+struct VecOps<float> {
+  static constexpr int E = 4;
+  __device__ static uint4 neg_inf() {
+    const uint32_t n = 0xFF800000u;
+    return make_uint4(n, n, n, n);
+  }
+  __device__ static float vmax(const uint4& x) {
+    return fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)), fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)));
+  }
+  __device__ static float at(const uint4& x, int e) {
+    return __uint_as_float(e == 0 ? x.x : e == 1 ? x.y : e == 2 ? x.z : x.w);
+  }
+};
+
+template <typename T, typename Fn>
+__device__ __forceinline__ void for_each_vec_batch(const T* row, int begin, int end, Fn&& fn) {
+  constexpr int E = VecOps<T>::E;
+  constexpr int U = kBatch / E;
+  const int nt = blockDim.x, tid = threadIdx.x;
+  const uint4* p = reinterpret_cast<const uint4*>(row);
+  const int ve = end / E;
+  for (int v0 = begin / E; v0 < ve; v0 += U * nt) {
+    uint4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + tid + u * nt;
+      x[u] = v < ve ? ld_stream(p + v) : VecOps<T>::neg_inf();
+    }
+    fn(x, v0);
+  }
+}
+
+// Argmax (lowest index among equals) of this thread's logits of
+// row[begin, end), plus an online softmax when `soft` (running max m and
+// sum s of exp2((x - m) * c)), rescaled once per batch.
+template <typename T>
+__device__ __forceinline__ void scan_row_stats(const T* row, int begin, int end, bool vec, bool soft, float c,
+                                               float& bv, int& bi, float& m, float& s) {
+  using Tr = LogitTraits<T>;
+  constexpr int E = VecOps<T>::E;
+  constexpr int U = kBatch / E;
+  if (vec) {
+    const int nt = blockDim.x;
+    for_each_vec_batch<T>(row, begin, end, [&](const uint4 (&x)[U], int v0) {
+      float bm = VecOps<T>::vmax(x[0]);
+#pragma unroll
+      for (int u = 1; u < U; ++u) bm = fmaxf(bm, VecOps<T>::vmax(x[u]));
+      if (bm > bv || (bm == bv && bi == INT_MAX)) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float f = VecOps<T>::at(x[u], e);
+            const int i = (v0 + int(threadIdx.x) + u * nt) * E + e;
+            if (better(f, i, bv, bi)) {
+              bv = f;
+              bi = i;
+            }
+          }
+      }
+      if (soft) {
+        const float mb = fmaxf(m, bm);
+        float sb = 0.f;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < E; ++e) sb += exp2f((VecOps<T>::at(x[u], e) - mb) * c);
+        s = s * exp2f((m - mb) * c) + sb;
+        m = mb;
+      }
+    });
+  } else {
+    for (int i = begin + threadIdx.x; i < end; i += blockDim.x) {
+      const float f = Tr::load(row, i);
+      if (better(f, i, bv, bi)) {
+        bv = f;
+        bi = i;
+      }
+      if (soft) {
+        if (f > m) {
+          s *= exp2f((m - f) * c);
+          m = f;
+        }
+        s += exp2f((f - m) * c);
+      }
+    }
+  }
+}
+
 // How a row of V logits is split over CTAs.
 struct RowSplit {
   int chunks;
@@ -151,6 +271,13 @@ inline RowSplit pick_split(long rows, int V, int vec, int max_chunks = kMaxChunk
   per = (per + vec - 1) / vec * vec;
   int chunks = (V + per - 1) / per;
   return RowSplit{chunks, per};
+}
+
+// The split of the terminal row in the second sampling pass: fixed
+// 4096-token chunks, so the in-order search of one chunk is 16 block scans.
+inline RowSplit terminal_split(int V) {
+  const int per = V < 4096 ? V : 4096;
+  return RowSplit{(V + per - 1) / per, per};
 }
 
 // The split select_topk uses: as pick_split, but never more than 8192 logits

@@ -178,18 +178,29 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   __syncthreads();
   float tau = -INFINITY;
   for (int w = 0; w < int(blockDim.x >> 5); ++w) tau = fmaxf(tau, tau_w[w]);
-  TopList<K> top;
-  top.init();
+  // Common case: few elements reach tau; they are appended to a shared
+  // candidate list and one warp picks the K best in K rounds.  Heavy ties can
+  // overflow the list, and then every thread keeps its own sorted top-K and the
+  // lists are merged (the general path).
+  constexpr int kCap = 512;
+  __shared__ float cand_v[kCap];
+  __shared__ int cand_i[kCap];
+  __shared__ int cand_n;
+  if (threadIdx.x == 0) cand_n = 0;
+  __syncthreads();
   if (tm >= tau) {
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j)
-      if (f[j] >= tau) top.push(f[j], share_index<T>(begin, a.vec_ok, j));
+      if (f[j] >= tau) {
+        const int pos = atomicAdd(&cand_n, 1);
+        if (pos < kCap) {
+          cand_v[pos] = f[j];
+          cand_i[pos] = share_index<T>(begin, a.vec_ok, j);
+        }
+      }
   }
-
-  // ---- CTA merge: softmax stats and top-K ----
+  // softmax statistics of the CTA
   __shared__ float wm[kThreads / 32], ws_[kThreads / 32];
-  __shared__ float lv[kThreads / 32][K];
-  __shared__ int li[kThreads / 32][K];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   {
     float M = warp_max(m);
@@ -200,29 +211,64 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
       ws_[w] = sc;
     }
   }
-  warp_merge<K>(top, lv[w], li[w]);
   __syncthreads();
   SelPart* part = reinterpret_cast<SelPart*>(a.partials) + size_t(row) * a.chunks + chunk;
-  if (w == 0) {
-    float M = lane < nw ? wm[lane] : -3.0e38f;
-    M = warp_max(M);
-    float sc = lane < nw ? ws_[lane] * exp2f((wm[lane] - M) * c) : 0.f;
-    sc = warp_sum(sc);
-    // rank each of the nw*K candidates among all of them (lowest-index ties)
-    for (int t = lane; t < nw * K; t += 32) {
-      const float v = lv[t / K][t % K];
-      const int ix = li[t / K][t % K];
-      int rank = 0;
-      for (int u = 0; u < nw * K; ++u) rank += better(lv[u / K][u % K], li[u / K][u % K], v, ix);
-      if (rank < K) {
-        part->v[rank] = v;
-        part->i[rank] = ix;
+  const int ncand = cand_n;
+  if (ncand <= kCap) {
+    if (w == 0) {
+      for (int r = 0; r < K; ++r) {
+        float v = -INFINITY;
+        int ix = INT_MAX, slot = -1;
+        for (int t = lane; t < ncand; t += 32)
+          if (cand_i[t] != INT_MIN && better(cand_v[t], cand_i[t], v, ix)) {
+            v = cand_v[t];
+            ix = cand_i[t];
+            slot = t;
+          }
+        float bv = v;
+        int bi = ix;
+        warp_argmax(bv, bi);
+        if (slot >= 0 && bv == v && bi == ix) cand_i[slot] = INT_MIN;  // taken
+        __syncwarp();
+        if (lane == 0) {
+          part->v[r] = bv;
+          part->i[r] = bi;
+        }
       }
     }
-    if (lane == 0) {
-      part->m = M;
-      part->s = sc;
+  } else {
+    TopList<K> top;
+    top.init();
+    if (tm >= tau) {
+#pragma unroll
+      for (int j = 0; j < kPerThread; ++j)
+        if (f[j] >= tau) top.push(f[j], share_index<T>(begin, a.vec_ok, j));
     }
+    __shared__ float lv[kThreads / 32][K];
+    __shared__ int li[kThreads / 32][K];
+    warp_merge<K>(top, lv[w], li[w]);
+    __syncthreads();
+    if (w == 0) {
+      // rank each of the nw*K candidates among all of them (lowest-index ties)
+      for (int t = lane; t < nw * K; t += 32) {
+        const float v = lv[t / K][t % K];
+        const int ix = li[t / K][t % K];
+        int rank = 0;
+        for (int u = 0; u < nw * K; ++u) rank += better(lv[u / K][u % K], li[u / K][u % K], v, ix);
+        if (rank < K) {
+          part->v[rank] = v;
+          part->i[rank] = ix;
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    float M = -3.0e38f;
+    for (int i = 0; i < nw; ++i) M = fmaxf(M, wm[i]);
+    float sc = 0.f;
+    for (int i = 0; i < nw; ++i) sc += ws_[i] * exp2f((wm[i] - M) * c);
+    part->m = M;
+    part->s = sc;
   }
 
   if (!arrive_last(a.counters + req, uint32_t(rows_per_req * a.chunks))) return;

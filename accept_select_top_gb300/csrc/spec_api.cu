@@ -40,7 +40,7 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
       return align256(size_t(b) * n * chunk_bound(long(b) * n, V) * 8);
     case SPEC_OP_VERIFY_SAMPLING:
       return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
-             sampling_partial2_bytes(b, chunk_bound(b, V));
+             sampling_partial2_bytes(b, terminal_split(V).chunks);
     case SPEC_OP_VERIFY_ATTENTION:
       return attention_partial_bytes(b, n, Hq, 128, attention_tc_geometry(b, n, Hq, Hkv, max_seq_len).splits);
     case SPEC_OP_COMMIT_KV:
@@ -214,6 +214,11 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   return launch_attention_tc(p, geo, as_stream(stream));
 }
 
+int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len) {
+  if (b < 1 || n < 1 || n > kMaxN || Hq < 1 || Hkv < 1 || Hq % Hkv || max_seq_len < 0) return 0;
+  return attention_tc_geometry(b, n, Hq, Hkv, max_seq_len).splits;
+}
+
 int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
                        const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,
                        int32_t* predict, int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
@@ -289,7 +294,7 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
   p.accepted_tokens = accepted_tokens;
   p.next_root = next_root;
   const RowSplit s1 = pick_split(long(b) * n, V, vec_elems(dtype));
-  const RowSplit s2 = pick_split(b, V, 1);
+  const RowSplit s2 = terminal_split(V);
   p.chunks = s1.chunks;
   p.chunk_elems = s1.chunk_elems;
   p.chunks2 = s2.chunks;

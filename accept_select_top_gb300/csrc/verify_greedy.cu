@@ -21,53 +21,6 @@ struct ArgPart {
   int i;
 };
 
-// Argmax of row[begin, end) for this thread, elements visited in increasing
-// index order (so a strict > keeps the lowest index among equals).
-template <typename T>
-__device__ __forceinline__ void scan_argmax(const T* row, int begin, int end, bool vec, float& bv, int& bi) {
-  using Tr = LogitTraits<T>;
-  constexpr int E = Tr::kVec;
-  if (vec) {
-    const uint4* p = reinterpret_cast<const uint4*>(row);
-    const int vb = begin / E, ve = end / E;
-    constexpr int U = 4;
-    for (int v0 = vb + threadIdx.x; v0 < ve; v0 += blockDim.x * U) {
-      uint4 x[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int idx = v0 + u * blockDim.x;
-        if (idx < ve) x[u] = ld_stream(p + idx);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int idx = v0 + u * blockDim.x;
-        if (idx >= ve) break;
-        float f[E];
-        Tr::unpack(x[u], f);
-        float m = f[0];
-#pragma unroll
-        for (int e = 1; e < E; ++e) m = fmaxf(m, f[e]);
-        if (m >= bv) {
-#pragma unroll
-          for (int e = 0; e < E; ++e)
-            if (better(f[e], idx * E + e, bv, bi)) {
-              bv = f[e];
-              bi = idx * E + e;
-            }
-        }
-      }
-    }
-  } else {
-    for (int i = begin + threadIdx.x; i < end; i += blockDim.x) {
-      float f = Tr::load(row, i);
-      if (better(f, i, bv, bi)) {
-        bv = f;
-        bi = i;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ void block_argmax(float& v, int& i) {
   __shared__ float sv[kThreads / 32];
   __shared__ int si[kThreads / 32];
@@ -96,7 +49,8 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
 
   float bv = -INFINITY;
   int bi = INT_MAX;
-  scan_argmax<T>(lrow, begin, end, a.vec_ok, bv, bi);
+  float unused_m = 0.f, unused_s = 0.f;
+  scan_row_stats<T>(lrow, begin, end, a.vec_ok, false, 0.f, bv, bi, unused_m, unused_s);
   block_argmax(bv, bi);
   ArgPart* part = reinterpret_cast<ArgPart*>(a.partials);
   if (threadIdx.x == 0) part[size_t(row) * a.chunks + chunk] = ArgPart{bv, bi};

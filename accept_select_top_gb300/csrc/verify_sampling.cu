@@ -56,7 +56,6 @@ __device__ __forceinline__ float p_of(float l, float M, float T, float S) { retu
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams a) {
   using Tr = LogitTraits<T>;
-  constexpr int E = Tr::kVec;
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const int req = row / a.n;
@@ -69,50 +68,7 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
 
   float m = -3.0e38f, s = 0.f, bv = -INFINITY;
   int bi = INT_MAX;
-  auto consume = [&](const float* f, int n_el, int first) {
-    float vm = f[0];
-    for (int e = 1; e < n_el; ++e) vm = fmaxf(vm, f[e]);
-    if (vm >= bv) {
-      for (int e = 0; e < n_el; ++e)
-        if (better(f[e], first + e, bv, bi)) {
-          bv = f[e];
-          bi = first + e;
-        }
-    }
-    if (soft) {
-      if (vm > m) {
-        s *= exp2f((m - vm) * c);
-        m = vm;
-      }
-      for (int e = 0; e < n_el; ++e) s += exp2f((f[e] - m) * c);
-    }
-  };
-  if (a.vec_ok) {
-    const uint4* p = reinterpret_cast<const uint4*>(lrow);
-    const int vb = begin / E, ve = end / E;
-    constexpr int U = 4;
-    for (int v0 = vb + threadIdx.x; v0 < ve; v0 += blockDim.x * U) {
-      uint4 x[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int idx = v0 + u * blockDim.x;
-        if (idx < ve) x[u] = ld_stream(p + idx);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        int idx = v0 + u * blockDim.x;
-        if (idx >= ve) break;
-        float f[E];
-        Tr::unpack(x[u], f);
-        consume(f, E, idx * E);
-      }
-    }
-  } else {
-    for (int i = begin + threadIdx.x; i < end; i += blockDim.x) {
-      float f = Tr::load(lrow, i);
-      consume(&f, 1, i);
-    }
-  }
+  scan_row_stats<T>(lrow, begin, end, a.vec_ok, soft, c, bv, bi, m, s);
   // CTA reduction
   __shared__ float sm_[kThreads / 32], ss_[kThreads / 32], sv_[kThreads / 32];
   __shared__ int si_[kThreads / 32];
@@ -367,43 +323,44 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   if (threadIdx.x == 0) s_bonus = s_fallback;
   __syncthreads();
   if (s_chunk >= 0) {
-    // in-order scan of the chunk: each thread owns a contiguous segment
+    // In-order search of the chunk, 256 tokens per round: each round is a
+    // coalesced load and a block-wide inclusive scan of the masses; the first
+    // positive-mass token whose running sum passes the target is the draw.
     const int cb = s_chunk * a.chunk2_elems;
     const int ce = min(a.V, cb + a.chunk2_elems);
-    const int seg = (ce - cb + blockDim.x - 1) / blockDim.x;
-    const int sb = cb + threadIdx.x * seg, se = min(ce, sb + seg);
     const bool use_res = s_use_res != 0;
-    Kahan mine;
-    for (int v = sb; v < se; ++v) mine.add(terminal_mass<T>(a, st, use_res, v));
-    // exclusive prefix of the segment totals in element order (fp64 shuffles)
-    __shared__ double wtot[kThreads / 32];
-    const double own = double(mine.sum) - double(mine.comp);
-    double incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) wtot[w] = incl;
-    __syncthreads();
-    double before = s_before;
-    for (int i = 0; i < w; ++i) before += wtot[i];
-    before += incl - own;
+    __shared__ float wtot[kThreads / 32];
+    __shared__ double s_run;
     __shared__ int s_hit;
-    if (threadIdx.x == 0) s_hit = INT_MAX;
-    __syncthreads();
-    // the first positive-mass token where the running sum passes the target
-    const float gap = float(s_target - before);
-    Kahan run;
-    for (int v = sb; v < se; ++v) {
-      const float mv = terminal_mass<T>(a, st, use_res, v);
-      run.add(mv);
-      if (mv > 0.f && gap < run.sum - run.comp) {
-        atomicMin(&s_hit, v);
-        break;
-      }
+    if (threadIdx.x == 0) {
+      s_run = s_before;
+      s_hit = INT_MAX;
     }
     __syncthreads();
+    for (int r0 = cb; r0 < ce; r0 += blockDim.x) {
+      const int v = r0 + threadIdx.x;
+      const float mv = v < ce ? terminal_mass<T>(a, st, use_res, v) : 0.f;
+      float incl = mv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wtot[w] = incl;
+      __syncthreads();
+      float before = 0.f;
+      for (int i = 0; i < w; ++i) before += wtot[i];
+      const float gap = float(s_target - s_run);
+      if (v < ce && mv > 0.f && gap < before + incl) atomicMin(&s_hit, v);
+      __syncthreads();
+      if (s_hit != INT_MAX) break;  // uniform: every thread reads the same value
+      if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int i = 0; i < nw; ++i) tot += wtot[i];
+        s_run += double(tot);
+      }
+      __syncthreads();
+    }
     if (threadIdx.x == 0 && s_hit != INT_MAX) s_bonus = s_hit;
     __syncthreads();
   }

@@ -26,7 +26,7 @@ _ERRORS = {-1: "bad argument", -2: "workspace too small or misaligned", -3: "CUD
            -4: "unsupported dtype or head size"}
 
 EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_last_error", "spec_device_sm_count",
-           "spec_select_topk", "spec_build_tree", "spec_verify_attention", "spec_verify_greedy",
+           "spec_select_topk", "spec_build_tree", "spec_verify_attention", "spec_verify_attention_splits", "spec_verify_greedy",
            "spec_verify_sampling", "spec_commit_kv", "spec_verify_greedy_noalloc"]
 
 
@@ -47,6 +47,7 @@ def _load() -> ctypes.CDLL:
         "spec_select_topk": (I, [I, I, I, I, I, P, F, P, P, P, I, P, I, P, P, P, P, Z, P]),
         "spec_build_tree": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_attention": (I, [I, I, I, I, I, I, P, P, P, L, P, I, I, P, P, I, P, P, F, P, P, P, Z, P]),
+        "spec_verify_attention_splits": (I, [I, I, I, I, I]),
         "spec_verify_greedy": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_sampling": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_commit_kv": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, P, P, P, P, P, P, Z, P]),
@@ -115,6 +116,11 @@ def spec_workspace_size(op: int, b: int, n: int, k: int, V: int, Hq: int = 0, Hk
 
 def spec_device_sm_count() -> int:
     return int(LIB.spec_device_sm_count())
+
+
+def spec_verify_attention_splits(b: int, n: int, Hq: int, Hkv: int, max_seq_len: int) -> int:
+    """Key splits of spec_verify_attention for these sizes (1: no merge launch)."""
+    return int(LIB.spec_verify_attention_splits(b, n, Hq, Hkv, max_seq_len))
 
 
 def spec_select_topk(step: int, b: int, k: int, draft_logits: torch.Tensor, temperature: float,

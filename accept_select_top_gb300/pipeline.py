@@ -135,13 +135,17 @@ class VerifyStep:
         self.commit(stream)
 
     def launches_per_step(self) -> int:
-        return launches_per_step(self.wl, self.mode)
+        return launches_per_step(self.wl, self.mode, self.inp.max_seq_len)
 
 
-def launches_per_step(wl: Workload, mode: str) -> int:
-    """Kernels one VerifyStep.run() launches: S selects, build, attention and
-    its split merge, accept (sampling: two passes), commit."""
-    return wl.S + 1 + 2 + (1 if mode == "greedy" else 2) + 1
+def launches_per_step(wl: Workload, mode: str, max_seq_len: int) -> int:
+    """Kernels one VerifyStep.run() launches: S selects, build, attention (plus
+    a merge when the key lists are split), accept (sampling: two passes),
+    commit."""
+    splits = ops.spec_verify_attention_splits(wl.b, wl.n, wl.Hq, wl.Hkv, max_seq_len)
+    if splits < 1:
+        raise ValueError("invalid attention sizes")
+    return wl.S + 1 + (1 if splits == 1 else 2) + (1 if mode == "greedy" else 2) + 1
 
 
 def _view_from(t: torch.Tensor, offset: int) -> torch.Tensor:

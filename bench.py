@@ -525,7 +525,7 @@ def main(argv=None):
         roof.update({"traffic": None if tr is None else tr["dram_bytes_per_launch"], "stage": dom,
                      "stage_us": ms * 1e3, "algorithmic_bytes": bytes_[dom],
                      "peak_kind": f"{peaks_kind} ({'sustained' if tensor_bound else 'copy'})"})
-    launches = launches_per_step(wl, mode)
+    launches = launches_per_step(wl, mode, int(lay["seq_lens"].max()))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "step_us": ms_per_step * 1e3,

@@ -177,6 +177,13 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size,
                           float scale, void* out, float* lse,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Number of pieces spec_verify_attention splits each request's key list into
+ * for these sizes (host only, no device call).  1 means the kernel writes the
+ * output itself (one launch); more means a second, merge launch combines the
+ * per-split partials.  0 for invalid sizes.  (An implementation detail the
+ * method itself has no counterpart for: it lets a caller count launches.) */
+int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len);
+
 /* ---------------------------------------------------------------------------
  * spec_verify_greedy -- greedy accept.
  * [SGL-XI eagle_sample (路径一:贪心验证)], [ACCEPT section 3], [EAGLE2 5.3].
