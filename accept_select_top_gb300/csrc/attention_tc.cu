@@ -47,7 +47,7 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kKeys = 64;
 constexpr int kStages = 4;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;  // warps: 0 lead copy, 1 MMA, 2-5 softmax, 6 7 9 copy, 8 idle
 constexpr uint32_t kTmemCols = 512;
 // O buffer i at TMEM columns [128 i, 128 i + 128); S buffer b at [256 + 64 b, 320 + 64 b)
 __host__ __device__ constexpr uint32_t col_o(int i) { return 128u * uint32_t(i); }
@@ -67,7 +67,7 @@ struct Smem {
   static constexpr int kPBuf = kRows * kKeys * 2;  // P: [128 rows x 64 keys] bf16, 128B-swizzled: 16 KB
   static constexpr int kP = kStage + kStages * 2 * kKTile;      // two P buffers
   static constexpr int kFlags = kP + 2 * kPBuf;                 // per stage: 4 words of key flags
-  static constexpr int kItems = kFlags + kStages * 16;          // two published item ids
+  static constexpr int kItems = kFlags + kStages * 32;          // two published item ids
   static constexpr int kBars = kItems + 64;
   static constexpr int kBytes = kBars + 512;
 };
@@ -103,17 +103,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// One try_wait: the thread may sleep in hardware until the phase completes or
+// kSuspendNs pass, so waiting warps take no issue slots from their neighbours.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
 // Bounded wait for the phase of the given parity: false once kWaitCycles SM
-// cycles have passed (try_wait itself may suspend the thread for a while).
+// cycles have passed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
@@ -266,9 +269,9 @@ __device__ __forceinline__ Item item_of(const TcArgs& args, int id, bool report)
   return it;
 }
 
-// Per-stage key flags (4 words in shared memory):
-//   [0] bit j: key j of the tile has a valid slot        [1] same for key 32+j
-//   [2] 1 when every key of the tile is a valid prefix key (no masking needed)
+// Per-stage key flags (8 words in shared memory), written by copy warp p:
+//   [p]     bit j: key 16p+j of the tile has a valid slot
+//   [4+p]   1 when each of keys 16p..16p+15 is a valid prefix key
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -298,12 +301,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kFull0 + i), 32 + 1);
+      mbar_init(bar(kFull0 + i), 4 * 32 + 4);  // four copy warps: cp.async arrivals + flag arrivals
       mbar_init(bar(kEmpty0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kItemFull0 + i), 1);
-      mbar_init(bar(kItemEmpty0 + i), 1 + kRows);  // the MMA thread and the softmax rows
+      mbar_init(bar(kItemEmpty0 + i), 1 + kRows + 3);  // the MMA thread, the softmax rows, three copy warps
       mbar_init(bar(kQFull0 + i), 1);
       mbar_init(bar(kQEmpty0 + i), 1);
       mbar_init(bar(kSFull0 + i), 1);
@@ -332,86 +335,88 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *abort_flag = 1;
   };
 
-  if (warp == 0) {
-    // =========================== producer ===========================
-    // Keys lane and 32+lane of tile t of an item: slot loads issued one tile
-    // ahead (issue), values consumed after that tile's copies (finish).
-    auto issue = [&](const Item& it, int t, int (&slot)[2], int (&kind)[2]) {  // kind: 0 none, 1 prefix, 2 tree
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int kg = it.k0 + t * kKeys + 32 * e + lane;
-        slot[e] = -1;
-        kind[e] = 0;
-        if (kg < it.k1) {
-          if (kg < it.Lp) {
-            slot[e] = a.req_to_token[size_t(it.rq) * a.row_w + kg];
-            kind[e] = 1;
-          } else {
-            slot[e] = a.verify_loc[size_t(it.req) * a.n + (kg - it.Lp)];
-            kind[e] = 2;
-          }
+  if (warp == 0 || warp == 6 || warp == 7 || warp == 9) {
+    // ============================ producers ============================
+    // Four copy warps, one per SM sub-partition (warp & 3), so the copy
+    // instructions do not all land next to one softmax warp.  Copy warp
+    // `part` looks up and copies keys 16*part .. 16*part+15 of every tile;
+    // warp 0 (the lead) also takes the items from the work counter,
+    // publishes them and gathers each item's Q rows.
+    const int part = warp & 3;
+    const bool lead = warp == 0;
+    // Key 16*part + lane (lanes 0..15) of tile t: slot load issued one tile
+    // ahead (issue), value consumed after that tile's copies (finish).
+    auto issue = [&](const Item& it, int t, int& slot, int& kind) {  // kind: 0 none, 1 prefix, 2 tree
+      const int kg = it.k0 + t * kKeys + 16 * part + lane;
+      slot = -1;
+      kind = 0;
+      if (lane < 16 && kg < it.k1) {
+        if (kg < it.Lp) {
+          slot = a.req_to_token[size_t(it.rq) * a.row_w + kg];
+          kind = 1;
+        } else {
+          slot = a.verify_loc[size_t(it.req) * a.n + (kg - it.Lp)];
+          kind = 2;
         }
       }
     };
-    auto finish = [&](const Item& it, const int (&slot)[2], const int (&kind)[2], int (&row)[2], bool (&pre)[2]) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const bool ok_slot = slot[e] >= 0 && slot[e] < a.num_slots;
-        if (kind[e] != 0 && !ok_slot) raise_error(a.error, SPEC_DEV_INDEX);
-        const bool v = kind[e] != 0 && ok_slot;
-        row[e] = v ? int(slot[e] * a.Hkv + it.g) : -1;  // -1: zero-filled, masked out
-        pre[e] = v && kind[e] == 1;
-      }
+    auto finish = [&](const Item& it, int slot, int kind, int& row, bool& pre) {
+      const bool ok_slot = slot >= 0 && slot < a.num_slots;
+      if (kind != 0 && !ok_slot) raise_error(a.error, SPEC_DEV_INDEX);
+      const bool v = kind != 0 && ok_slot;
+      row = v ? int(slot * a.Hkv + it.g) : -1;  // -1: zero-filled, masked out
+      pre = lane >= 16 || (v && kind == 1);
     };
     int ct = 0, ci = 0;
     bool ok = true;
     while (ok) {
-      int id = 0;
-      if (lane == 0) id = int(atomicAdd(args.work_counter, 1u));
-      id = __shfl_sync(FULL, id, 0);
-      const bool last = id >= args.num_items;
       Item it{};
-      if (!last) {
-        it = item_of(args, id, lane == 0);
-        if (it.T == 0) {  // nothing in this split (or a rejected request): not published
+      if (lead) {
+        int id = 0;
+        if (lane == 0) id = int(atomicAdd(args.work_counter, 1u));
+        id = __shfl_sync(FULL, id, 0);
+        const bool last = id >= args.num_items;
+        if (!last) {
+          it = item_of(args, id, lane == 0);
+          if (it.T == 0) {  // nothing in this split (or a rejected request): not published
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rg = it.mt * kRows + 4 * lane + e;
-            if (rg < M) {
-              const size_t orow = (size_t(it.req) * a.n + rg / G) * a.Hq + it.g * G + rg % G;
-              if (direct) {  // zero output, empty lse
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D);
-                for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (a.lse) a.lse[orow] = -INFINITY;
-              } else {  // an empty partial, skipped by the merge
-                const size_t idx = orow * a.splits + it.split;
-                pml[idx * 2] = -INFINITY;
-                pml[idx * 2 + 1] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int rg = it.mt * kRows + 4 * lane + e;
+              if (rg < M) {
+                const size_t orow = (size_t(it.req) * a.n + rg / G) * a.Hq + it.g * G + rg % G;
+                if (direct) {  // zero output, empty lse
+                  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D);
+                  for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+                  if (a.lse) a.lse[orow] = -INFINITY;
+                } else {  // an empty partial, skipped by the merge
+                  const size_t idx = orow * a.splits + it.split;
+                  pml[idx * 2] = -INFINITY;
+                  pml[idx * 2 + 1] = 0.f;
+                }
               }
             }
+            continue;
           }
-          continue;
         }
-      }
-      // publish the item (or the end marker) in slot ci % 2
-      const bool slot_ok = (ci < 2 || mbar_wait(bar(kItemEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
-      if (!__all_sync(FULL, slot_ok)) {
-        if (!*abort_flag) fail();
-        break;
-      }
-      if (lane == 0) {
-        items[ci & 1] = last ? -1 : id;
-        mbar_arrive(bar(kItemFull0 + (ci & 1)));
-      }
-      __syncwarp();
-      if (last) break;
-      // the item's Q rows into Q buffer ci % 2, rows 4*lane .. 4*lane+3
-      const bool q_ok = (ci < 2 || mbar_wait(bar(kQEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
-      if (!__all_sync(FULL, q_ok)) {
-        if (!*abort_flag) fail();
-        break;
-      }
-      {
+        // publish the item (or the end marker) in slot ci % 2
+        const bool slot_ok =
+            (ci < 2 || mbar_wait(bar(kItemEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
+        if (!__all_sync(FULL, slot_ok)) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        if (lane == 0) {
+          items[ci & 1] = last ? -1 : id;
+          mbar_arrive(bar(kItemFull0 + (ci & 1)));
+        }
+        __syncwarp();
+        if (last) break;
+        // the item's Q rows into Q buffer ci % 2, rows 4*lane .. 4*lane+3
+        const bool q_ok = (ci < 2 || mbar_wait(bar(kQEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
+        if (!__all_sync(FULL, q_ok)) {
+          if (!*abort_flag) fail();
+          break;
+        }
         int y[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -424,9 +429,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = 0; h < L::kHalves; ++h)
           tma_gather4(sbase + L::kQ + (ci & 1) * L::kQTile + h * L::kQBlock + 512u * lane, &tm_q, 64 * h, y[0], y[1],
                       y[2], y[3], bar(kQFull0 + (ci & 1)));
+      } else {
+        const bool i_ok = mbar_wait(bar(kItemFull0 + (ci & 1)), (ci >> 1) & 1) && !*abort_flag;
+        if (!__all_sync(FULL, i_ok)) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        const int id = items[ci & 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kItemEmpty0 + (ci & 1)));
+        if (id < 0) break;
+        it = item_of(args, id, false);
       }
-      int row[2], slot_n[2], kind_n[2];
-      bool pre[2];
+      int row = -1, slot_n = -1, kind_n = 0;
+      bool pre = true;
       issue(it, 0, slot_n, kind_n);
       finish(it, slot_n, kind_n, row, pre);
       for (int t = 0; t < it.T; ++t, ++ct) {
@@ -438,26 +454,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = false;
           break;
         }
-        const unsigned v0 = __ballot_sync(FULL, row[0] >= 0), v1 = __ballot_sync(FULL, row[1] >= 0);
-        const bool all_pre = __all_sync(FULL, pre[0] && pre[1]);
+        const unsigned vbits = __ballot_sync(FULL, row >= 0);  // lanes 16..31 hold no key
+        const bool all_pre = __all_sync(FULL, pre);
         if (lane == 0) {
-          flags[4 * s + 0] = v0;
-          flags[4 * s + 1] = v1;
-          flags[4 * s + 2] = all_pre ? 1u : 0u;
+          flags[8 * s + part] = vbits;
+          flags[8 * s + 4 + part] = all_pre ? 1u : 0u;
           mbar_arrive(bar(kFull0 + s));
         }
         // lane: 16-byte chunk c of key row r; one instruction covers kRowsPerOp
-        // whole rows (coalesced), rows spread over the tile.  Shared address:
-        // half c/8 of the row, 128-byte line r, chunk (c%8) ^ (r%8) (128B swizzle).
+        // whole rows (coalesced).  Shared address: half c/8 of the row,
+        // 128-byte line r, chunk (c%8) ^ (r%8) (128B swizzle).
         constexpr int kChunks = D / 8;
         constexpr int kRowsPerOp = 32 / kChunks;
         const int c = lane % kChunks, rsub = lane / kChunks;
         const uint32_t kdst = sbase + L::kStage + 2u * s * L::kKTile + uint32_t(c >> 3) * L::kKBlock;
-#pragma unroll 8
-        for (int i = 0; i < kKeys / kRowsPerOp; ++i) {
-          const int r = kRowsPerOp * i + rsub;
-          // key r's pool row is held by lane r%32 (element r/32, the same for the whole warp)
-          const int y = __shfl_sync(FULL, (kRowsPerOp * i) >= 32 ? row[1] : row[0], r & 31);
+#pragma unroll
+        for (int i = 0; i < 16 / kRowsPerOp; ++i) {
+          const int rl = kRowsPerOp * i + rsub, r = 16 * part + rl;
+          const int y = __shfl_sync(FULL, row, rl);  // key r's pool row, held by lane rl
           const uint32_t dst = kdst + uint32_t(r) * 128u + (uint32_t((c & 7) ^ (r & 7)) << 4);
           const size_t off = size_t(y < 0 ? 0 : y) * (D * 2) + size_t(c) * 16;
           const uint32_t nb = y < 0 ? 0u : 16u;
@@ -545,7 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(bar(kDrain), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ============================ softmax rows ============================
     // tcgen05.ld / tcgen05.st are .sync.aligned: every lane of the warp issues
     // them together, so every branch around them and every loop exit below is
@@ -589,8 +603,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[32 * q + i] = v[i];
         }
-        const uint32_t* f = flags + 4 * s;
-        const bool all_pre = f[2] != 0;
+        const uint32_t* f = flags + 8 * s;
+        const bool all_pre = (f[4] & f[5] & f[6] & f[7]) != 0u;
         const int kbase = it.k0 + t * kKeys;
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (all_pre) {  // history keys only: all visible
@@ -606,7 +620,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int c0 = it.Lp - kbase;
           const uint64_t hist = c0 <= 0 ? 0ull : (c0 >= kKeys ? ~0ull : ((1ull << c0) - 1ull));
           const uint64_t tree = c0 >= kKeys ? 0ull : (c0 >= 0 ? (mask << c0) : (mask >> (-c0)));
-          const uint64_t vis = ((uint64_t(f[1]) << 32) | f[0]) & (hist | tree);
+          const uint64_t valid = uint64_t(f[0] | (f[1] << 16)) | (uint64_t(f[2] | (f[3] << 16)) << 32);
+          const uint64_t vis = valid & (hist | tree);
           const uint32_t vlo = uint32_t(vis), vhi = uint32_t(vis >> 32);
 #pragma unroll
           for (int c = 0; c < kKeys; ++c) {
