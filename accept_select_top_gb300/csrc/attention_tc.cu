@@ -210,13 +210,6 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32])
   tmem_st16(taddr + 16, b);
 }
 
-// 2^x by the hardware approximation (relative error about 2^-22, results
-// below 2^-126 flushed to zero): far below the bf16 rounding of P.
-__device__ __forceinline__ float exp2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // two floats to bf16 (round to nearest even), lower key in the low half
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -633,7 +626,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         // lazy rescaling: move the reference max only when it grows by > 2^8
         const bool need = valid && mx > m_ref + kRescaleLog2;
-        const float factor = need ? exp2_approx(m_ref - mx) : 1.f;  // 0 when nothing was seen yet
+        const float factor = need ? fast_exp2(m_ref - mx) : 1.f;  // 0 when nothing was seen yet
         if (t > 0 && __any_sync(FULL, need)) {
           // O holds P V up to tile ct-1; PV(ct-2) is known complete
           const bool o_ok = mbar_wait(bar(kODone0 + ((ct - 1) & 1)), ((ct - 1) >> 1) & 1);
@@ -665,8 +658,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float p0 = live ? exp2_approx(x[8 * j + 2 * i] - m_ref) : 0.f;
-            const float p1 = live ? exp2_approx(x[8 * j + 2 * i + 1] - m_ref) : 0.f;
+            const float p0 = live ? fast_exp2(x[8 * j + 2 * i] - m_ref) : 0.f;
+            const float p1 = live ? fast_exp2(x[8 * j + 2 * i + 1] - m_ref) : 0.f;
             part4[i] += p0 + p1;
             pk[i] = pack_bf16(p0, p1);
           }

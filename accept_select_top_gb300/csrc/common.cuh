@@ -98,6 +98,15 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
+// 2^x by the hardware approximation: relative error about 2^-22, results
+// below 2^-126 flushed to zero.  For sums of exponentials whose total is at
+// least 1 (a softmax denominator), far below fp32's own accumulated rounding.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -231,7 +240,7 @@ __device__ __forceinline__ void scan_row_stats(const T* row, int begin, int end,
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int e = 0; e < E; ++e) sb += exp2f((VecOps<T>::at(x[u], e) - mb) * c);
+          for (int e = 0; e < E; ++e) sb += fast_exp2((VecOps<T>::at(x[u], e) - mb) * c);
         s = s * exp2f((m - mb) * c) + sb;
         m = mb;
       }
@@ -248,7 +257,7 @@ __device__ __forceinline__ void scan_row_stats(const T* row, int begin, int end,
           s *= exp2f((m - f) * c);
           m = f;
         }
-        s += exp2f((f - m) * c);
+        s += fast_exp2((f - m) * c);
       }
     }
   }

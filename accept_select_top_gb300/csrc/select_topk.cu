@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   const float m = fmaxf(tm, -3.0e38f);
   float s = 0.f;
 #pragma unroll
-  for (int j = 0; j < kPerThread; ++j) s += exp2f((f[j] - m) * c);
+  for (int j = 0; j < kPerThread; ++j) s += fast_exp2((f[j] - m) * c);
   // Pruning threshold: a warp's k-th largest thread maximum tau_w stands for k
   // distinct elements >= tau_w, so no element below max_w tau_w can be among
   // the chunk's k best; only elements >= that bound enter the top-K lists.
@@ -214,7 +214,23 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   __syncthreads();
   SelPart* part = reinterpret_cast<SelPart*>(a.partials) + size_t(row) * a.chunks + chunk;
   const int ncand = cand_n;
-  if (ncand <= kCap) {
+  if (ncand <= int(blockDim.x)) {
+    // one candidate per thread: its rank among the candidates (a strict
+    // order: no NaN passes the threshold, indices are distinct) is its slot
+    if (int(threadIdx.x) < ncand) {
+      const float v = cand_v[threadIdx.x];
+      const int ix = cand_i[threadIdx.x];
+      int rank = 0;
+      for (int u = 0; u < ncand; ++u) rank += better(cand_v[u], cand_i[u], v, ix);
+      if (rank < K) {
+        part->v[rank] = v;
+        part->i[rank] = ix;
+      }
+    } else if (int(threadIdx.x) < K) {  // fewer candidates than K: empty slots
+      part->v[threadIdx.x] = -INFINITY;
+      part->i[threadIdx.x] = INT_MAX;
+    }
+  } else if (ncand <= kCap) {
     if (w == 0) {
       for (int r = 0; r < K; ++r) {
         float v = -INFINITY;
@@ -274,7 +290,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   if (!arrive_last(a.counters + req, uint32_t(rows_per_req * a.chunks))) return;
 
   // ---- finalize request `req` ----
-  const int k = a.k;
+  // Every load of the finalize is issued before any of them is used (one
+  // round trip through L2: the partials were written by other CTAs), then
+  // one warp per row works from registers and shared memory.
+  const int k = a.k, kk = k * k;
+  const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
   __shared__ float heads_v[kThreads / 32][kMaxChunks * K];  // one warp per row
   __shared__ int heads_i[kThreads / 32][kMaxChunks * K];
   __shared__ float p_s[kMaxK][kMaxK];
@@ -282,19 +302,33 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   for (int r = w; r < rows_per_req; r += nw) {
     const int grow = req * rows_per_req + r;
     const SelPart* pr = reinterpret_cast<const SelPart*>(a.partials) + size_t(grow) * a.chunks;
-    // softmax denominator of the whole row
-    float M = -3.0e38f;
-    for (int ch = lane; ch < a.chunks; ch += 32) M = fmaxf(M, __ldcg(&pr[ch].m));
-    M = warp_max(M);
-    float S = 0.f;
-    for (int ch = lane; ch < a.chunks; ch += 32) S += __ldcg(&pr[ch].s) * exp2f((__ldcg(&pr[ch].m) - M) * c);
-    S = warp_sum(S);
-    // stage the chunk lists, then k rounds of a tournament over list heads
-    for (int t = lane; t < a.chunks * K; t += 32) {
-      heads_v[w][t] = __ldcg(&pr[t / K].v[t % K]);
-      heads_i[w][t] = __ldcg(&pr[t / K].i[t % K]);
+    float hv[K], pm = -3.0e38f, psum = 0.f;
+    int hi[K];
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      const int t = lane + 32 * q;
+      if (t < a.chunks * K) {
+        hv[q] = __ldcg(&pr[t / K].v[t % K]);
+        hi[q] = __ldcg(&pr[t / K].i[t % K]);
+      }
     }
+    if (lane < a.chunks) {
+      pm = __ldcg(&pr[lane].m);
+      psum = __ldcg(&pr[lane].s);
+    }
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      const int t = lane + 32 * q;
+      if (t < a.chunks * K) {
+        heads_v[w][t] = hv[q];
+        heads_i[w][t] = hi[q];
+      }
+    }
+    // softmax denominator of the whole row
+    const float M = warp_max(pm);
+    const float S = warp_sum(psum * exp2f((pm - M) * c));
     __syncwarp();
+    // k rounds of a tournament over the chunk lists' heads
     int h0 = 0, h1 = 0;  // list heads of chunks lane and lane + 32
     for (int j = 0; j < k; ++j) {
       float v = -INFINITY;
@@ -317,13 +351,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
         if (src == 0) ++h0;
         else ++h1;
       }
-      if (lane == 0) {
-        // p = exp((x - M) / T) / S; x - M is exact for bf16 logits, so fp32
-        // expf (about 1 ulp) keeps p within 1e-6 relative of the fp64 value
-        p_s[r][j] = expf((bv - M) / a.temperature) / S;
+      if (lane == j) {
+        p_s[r][j] = bv;  // the logit for now; turned into p below, in parallel
         id_s[r][j] = bi;
       }
     }
+    __syncwarp();
+    // p = exp((x - M) / T) / S; x - M is exact for bf16 logits, so fp32 expf
+    // (about 1 ulp) keeps p within 1e-6 relative of the fp64 value
+    if (lane < k) p_s[r][lane] = expf((p_s[r][lane] - M) / a.temperature) / S;
     __syncwarp();
   }
   __syncthreads();
@@ -343,10 +379,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
       for (int j = threadIdx.x; j <= k; j += blockDim.x) a.parent_blk[size_t(req) * a.parent_ld + j] = j - 1;
   } else if (w == 0) {
     // expand[r*k + j] = scores_in[r] * p[r][j] (one fp32 multiply); top-k of k*k
-    const int kk = k * k;
     __shared__ float ex[kMaxK * kMaxK];
     for (int f = lane; f < kk; f += 32) {
-      ex[f] = __fmul_rn(a.scores_in[size_t(req) * k + f / k], p_s[f / k][f % k]);
+      const float sin = f < 32 ? sc_in : a.scores_in[size_t(req) * k + f / k];
+      ex[f] = __fmul_rn(sin, p_s[f / k][f % k]);
       a.score_blk[sb + f] = ex[f];
       a.token_blk[sb + f] = id_s[f / k][f % k];
     }

@@ -38,6 +38,43 @@ __device__ __forceinline__ void block_argmax(float& v, int& i) {
   }
 }
 
+// Argmax (max value, lowest index) of bf16 row[begin, end) by 16-byte
+// vectors: per vector one packed max and one compare; the thread keeps its
+// best vector (the first one with the best maximum) and resolves the element
+// inside it at the end.  The thread's first vector is always taken, so a
+// row of -inf still yields its lowest index.
+__device__ __forceinline__ void scan_argmax_bf16(const uint16_t* row, int begin, int end, float& bv, int& bi) {
+  constexpr int U = kBatch / 8;
+  const uint4* p = reinterpret_cast<const uint4*>(row);
+  const int nt = blockDim.x, ve = end / 8;
+  int bvi = -1;
+  uint4 bx = make_uint4(0u, 0u, 0u, 0u);
+  for (int v0 = begin / 8 + int(threadIdx.x); v0 < ve; v0 += U * nt) {
+    uint4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * nt;
+      x[u] = v < ve ? ld_stream(p + v) : VecOps<uint16_t>::neg_inf();
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * nt;
+      const float mf = VecOps<uint16_t>::vmax(x[u]);
+      if (v < ve && (mf > bv || (bvi < 0 && mf == mf))) {
+        bv = mf;
+        bvi = v;
+        bx = x[u];
+      }
+    }
+  }
+  bi = INT_MAX;
+  if (bvi >= 0) {
+#pragma unroll
+    for (int e = 7; e >= 0; --e)
+      if (VecOps<uint16_t>::at(bx, e) == bv) bi = bvi * 8 + e;
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
   const int row = blockIdx.y;
@@ -49,8 +86,17 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
 
   float bv = -INFINITY;
   int bi = INT_MAX;
-  float unused_m = 0.f, unused_s = 0.f;
-  scan_row_stats<T>(lrow, begin, end, a.vec_ok, false, 0.f, bv, bi, unused_m, unused_s);
+  if constexpr (sizeof(T) == 2) {
+    if (a.vec_ok) {
+      scan_argmax_bf16(lrow, begin, end, bv, bi);
+    } else {
+      float unused_m = 0.f, unused_s = 0.f;
+      scan_row_stats<T>(lrow, begin, end, false, false, 0.f, bv, bi, unused_m, unused_s);
+    }
+  } else {
+    float unused_m = 0.f, unused_s = 0.f;
+    scan_row_stats<T>(lrow, begin, end, a.vec_ok, false, 0.f, bv, bi, unused_m, unused_s);
+  }
   block_argmax(bv, bi);
   ArgPart* part = reinterpret_cast<ArgPart*>(a.partials);
   if (threadIdx.x == 0) part[size_t(row) * a.chunks + chunk] = ArgPart{bv, bi};
@@ -62,8 +108,14 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
   __shared__ int tp[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
   __shared__ int2 stage[kMaxN * kMaxChunks];
   __shared__ int s_len;
-  // every (row, chunk) partial in one round of loads; partials of other CTAs
-  // are read through L2 (__ldcg), not a stale L1 line
+  // the request's tree arrays and every (row, chunk) partial in one round
+  // of loads; partials of other CTAs are read through L2 (__ldcg), not a
+  // stale L1 line
+  const int tt = threadIdx.x;
+  const int tok0 = tt < n ? a.draft_tokens[base + tt] : 0;
+  const int x0 = tt < n ? a.next_token[base + tt] : -1;
+  const int y0 = tt < n ? a.next_sibling[base + tt] : -1;
+  const int r0 = tt < n ? a.retrieve_index[base + tt] : base;
   for (int t = threadIdx.x; t < n * a.chunks; t += blockDim.x)
     stage[t] = __ldcg(reinterpret_cast<const int2*>(part + size_t(base) * a.chunks) + t);
   __syncthreads();
@@ -79,8 +131,8 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
       }
     }
     tp[t] = i;
-    tok[t] = a.draft_tokens[base + t];
-    int x = a.next_token[base + t], y = a.next_sibling[base + t], r = a.retrieve_index[base + t];
+    tok[t] = tok0;  // t == threadIdx.x: n <= kMaxN < blockDim.x
+    int x = x0, y = y0, r = r0;
     if (x < -1 || x >= n || y < -1 || y >= n) {
       raise_error(a.error, SPEC_DEV_INDEX);
       x = x < -1 || x >= n ? -1 : x;
