@@ -5,27 +5,29 @@
 // query sees only its ancestors and itself; history KV is read once and shared
 // by all candidates], [SGL-XI QLEN_ONLY mask: prefix columns implicitly visible].
 //
-// Persistent kernel, one CTA per SM.  A work item is 128 query rows of one
-// (request, kv head) -- row r is (node r / G, q head g*G + r % G), G = Hq/Hkv --
-// and one split of that request's key list (prefix positions, then the n tree
-// nodes).  Items are taken from a global counter; every role walks the same
-// flat stream of 64-key tiles:
-//   warp 0      producer: takes items, publishes them in a two-slot ring,
-//               gathers each item's Q rows (cp.async.bulk.tensor tile::gather4)
-//               and, per tile, looks the keys' slots up (req_to_token /
-//               verify_loc, one tile ahead) and copies their K and V rows into
-//               a four-stage ring with 16-byte cp.async, 128B-swizzled by hand
-//               (the same layout a swizzled TMA box would give; per-lane copies
+// Persistent kernel, one CTA per SM, with a stream-K partition: the units
+// (request, kv head, 128 query rows -- row r is (node r / G, q head g*G + r %
+// G), G = Hq/Hkv) are laid end to end in tile space (64 keys a tile: prefix
+// positions, then the n tree nodes) and each CTA takes an equal contiguous
+// range of tiles, cut into one piece per unit it touches.  A unit inside one
+// range is written directly; a unit split over CTAs leaves one partial per
+// piece and the piece arriving last merges them (no second launch).  Every
+// role walks the same pieces and the same flat stream of tiles:
+//   warps 0,6,7,9  copy warps, one per SM sub-partition: each looks up the
+//               slots of 16 keys of every tile (req_to_token / verify_loc,
+//               one tile ahead) and copies their K and V rows into a
+//               four-stage ring with 16-byte cp.async, 128B-swizzled by hand
+//               (the layout a swizzled TMA box would give; per-lane copies
 //               keep far more scattered rows in flight than gather4 does);
+//               warp 0 also gathers each piece's Q rows (tile::gather4);
 //   warp 1      MMA issuer (one thread): S = Q K^T (M=128, N=64, K=D) into one
 //               of two TMEM S buffers; O += P V (M=128, N=D, K=64) with both
-//               operands in shared memory, into the item's O buffer (two);
+//               operands in shared memory, into the piece's O buffer (two);
 //   warps 2..5  one query row per thread: masked online softmax of the S row
 //               (tcgen05.ld), P as bf16 into one of two shared-memory P
 //               buffers (128B-swizzled, K-major), lazy rescaling of O in TMEM,
-//               and the item's epilogue (bf16 output directly when the key
-//               list is not split, else partials that attention_merge_kernel
-//               combines).
+//               and the piece's epilogue;
+//   warp 8      idle.
 // P goes through shared memory rather than TMEM because an MMA that reads its
 // A operand from TMEM measured about three times slower on this part than the
 // same MMA reading shared memory.
@@ -66,9 +68,9 @@ struct Smem {
   static constexpr int kStage = 2 * kQTile;        // stage s: K at kStage + 2*s*kKTile, V at + kKTile
   static constexpr int kPBuf = kRows * kKeys * 2;  // P: [128 rows x 64 keys] bf16, 128B-swizzled: 16 KB
   static constexpr int kP = kStage + kStages * 2 * kKTile;      // two P buffers
-  static constexpr int kFlags = kP + 2 * kPBuf;                 // per stage: 4 words of key flags
-  static constexpr int kItems = kFlags + kStages * 32;          // two published item ids
-  static constexpr int kBars = kItems + 64;
+  static constexpr int kFlags = kP + 2 * kPBuf;                 // per stage: 8 words of key flags
+  static constexpr int kScratch = kFlags + kStages * 32;        // partition and merge scratch
+  static constexpr int kBars = kScratch + 512;
   static constexpr int kBytes = kBars + 512;
 };
 
@@ -78,15 +80,14 @@ static_assert(Smem<128>::kBytes + 1024 <= 227 * 1024, "shared memory of one CTA"
 enum {
   kFull0 = 0,                  // + stage: K/V landed (the producer's 32 cp.async arrivals + its flags arrival)
   kEmpty0 = kFull0 + kStages,  // + stage: PV of the tile done (stage free)
-  kItemFull0 = kEmpty0 + kStages,
-  kItemEmpty0 = kItemFull0 + 2,
-  kQFull0 = kItemEmpty0 + 2,
+  kQFull0 = kEmpty0 + kStages,
   kQEmpty0 = kQFull0 + 2,
   kSFull0 = kQEmpty0 + 2,
   kPReady0 = kSFull0 + 2,
   kOFree0 = kPReady0 + 2,
   kODone0 = kOFree0 + 2,  // + (PV index & 1): two barriers, so no wait is ever two phases behind
-  kDrain = kODone0 + 2,
+  kSmGroup = kODone0 + 2,  // the 128 softmax threads meet (merge of split units)
+  kDrain,
   kNumBars
 };
 
@@ -219,48 +220,106 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 
+constexpr int kMaxCtas = 192;  // upper bound of the grid (one CTA per SM); sizes the partial slots
+// partial region of the workspace: [slot m, l][slot O (D <= 128)]; the
+// arrival counters are the workspace's counter words (zero between calls)
+constexpr size_t kSlotMLOffset = 0;
+constexpr size_t kSlotOOffset = kSlotMLOffset + size_t(2) * kMaxCtas * kRows * 2 * 4;
+
 struct TcArgs {
   AttentionParams p;
   int m_tiles;
-  int split_tiles;
-  int num_items;
-  uint32_t* work_counter;  // next item to take (zero between launches)
-  uint32_t* exit_counter;  // CTAs done (zero between launches)
+  uint32_t* counters;   // [kMaxCtas] arrivals per split unit (workspace counter words, zero between launches)
+  float* slot_o;        // [2 * kMaxCtas][128 rows][D] unnormalised O of a piece of a split unit
+  float* slot_ml;       // [2 * kMaxCtas][128 rows][2]: running max (log2 domain), sum
 };
 
-// Geometry of a work item, computed alike by every role from the item id.
-// id = ((split * b + req) * Hkv + g) * m_tiles + mt: the row tiles of one
-// (request, kv head, split) are consecutive, so they run together and share
-// their K/V reads through L2.
-struct Item {
-  int req, g, mt, split, Lp, rq, k0, k1, T;
+// Keys, history length and pool row of request r, validated like the C ABI
+// describes: a bad length is clamped, a bad pool row leaves no keys.
+struct ReqInfo {
+  int Lp, rq, total, tiles;
 };
-
-__device__ __forceinline__ Item item_of(const TcArgs& args, int id, bool report) {
-  const AttentionParams& a = args.p;
-  Item it;
-  it.mt = id % args.m_tiles;
-  int rest = id / args.m_tiles;
-  it.g = rest % a.Hkv;
-  rest /= a.Hkv;
-  it.req = rest % a.b;
-  it.split = rest / a.b;
-  const bool first = report && it.g == 0 && it.mt == 0 && it.split == 0;
-  int Lp = a.seq_lens[it.req];
-  it.rq = a.req_pool_idx[it.req];
-  const bool req_ok = it.rq >= 0 && it.rq < a.req_rows;
+__device__ __forceinline__ ReqInfo req_check(const AttentionParams& a, int Lp, int rq, bool report) {
+  ReqInfo q;
+  q.rq = rq;
+  const bool req_ok = q.rq >= 0 && q.rq < a.req_rows;
   if (Lp < 0 || Lp > a.max_seq_len || Lp > a.row_w) {
-    if (first) raise_error(a.error, SPEC_DEV_LENGTH);
+    if (report) raise_error(a.error, SPEC_DEV_LENGTH);
     Lp = max(0, min(Lp, min(a.max_seq_len, a.row_w)));
   }
-  if (!req_ok && first) raise_error(a.error, SPEC_DEV_INDEX);
-  it.Lp = Lp;
-  const int total = req_ok ? Lp + a.n : 0;
-  it.k0 = it.split * args.split_tiles * kKeys;
-  it.k1 = min(total, it.k0 + args.split_tiles * kKeys);
-  it.T = it.k0 < it.k1 ? (it.k1 - it.k0 + kKeys - 1) / kKeys : 0;
-  return it;
+  if (!req_ok && report) raise_error(a.error, SPEC_DEV_INDEX);
+  q.Lp = Lp;
+  q.total = req_ok ? Lp + a.n : 0;
+  q.tiles = max(1, (q.total + kKeys - 1) / kKeys);  // a request without keys still owns one (empty) tile
+  return q;
 }
+__device__ __forceinline__ ReqInfo req_info(const AttentionParams& a, int r, bool report) {
+  return req_check(a, a.seq_lens[r], a.req_pool_idx[r], report);
+}
+
+// Stream-K partition.  The units (request, kv head, 128-row tile) are laid
+// end to end in tile space, request by request; unit (r, j) has the tiles of
+// request r.  CTA c takes tiles [c*T/G, (c+1)*T/G) and cuts them into pieces,
+// one per unit it touches.
+__host__ __device__ __forceinline__ long long cta_start(long long c, long long T, long long G) { return c * T / G; }
+// the CTA whose range holds tile x
+__host__ __device__ __forceinline__ int cta_of(long long x, long long T, long long G) {
+  return int(((x + 1) * G - 1) / T);
+}
+
+struct Piece {
+  int req, g, mt, t0, T, Tr, Lp, rq, k0, k1, idx;  // idx: ordinal of the piece within its CTA
+  long long unit_start;                           // first tile of the unit in tile space
+  bool complete;                                  // the piece is the whole unit
+};
+
+struct PieceIter {
+  int r, j, t0, idx;
+  long long cur, end;
+  int nr, nlen, nrq;  // request nr's raw seq_len and pool row, loaded one piece ahead
+  __device__ __forceinline__ bool next(const AttentionParams& a, int m_tiles, Piece& p, bool report) {
+    if (cur >= end) return false;
+    const int upr = a.Hkv * m_tiles;
+    const ReqInfo q = nr == r ? req_check(a, nlen, nrq, report && j == 0 && t0 == 0)
+                              : req_info(a, r, report && j == 0 && t0 == 0);
+    const long long left = end - cur;
+    const int take = int(left < (long long)(q.tiles - t0) ? left : (long long)(q.tiles - t0));
+    p.req = r;
+    p.g = j / m_tiles;
+    p.mt = j % m_tiles;
+    p.t0 = t0;
+    p.T = take;
+    p.Tr = q.tiles;
+    p.Lp = q.Lp;
+    p.rq = q.rq;
+    p.k0 = t0 * kKeys;
+    p.k1 = min(q.total, (t0 + take) * kKeys);
+    p.idx = idx++;
+    p.unit_start = cur - t0;
+    p.complete = t0 == 0 && take == q.tiles;
+    cur += take;
+    t0 += take;
+    if (t0 == q.tiles) {
+      t0 = 0;
+      if (++j == upr) {
+        j = 0;
+        ++r;
+      }
+    }
+    if (r != nr && cur < end) {  // the next piece's request: loads in flight meanwhile
+      nr = r;
+      nlen = a.seq_lens[r];
+      nrq = a.req_pool_idx[r];
+    } else if (nr != r) {
+      nr = -1;
+    }
+    if (nr == r && r == p.req) {  // same request: keep the values already checked
+      nlen = q.Lp;
+      nrq = q.rq;
+    }
+    return true;
+  }
+};
 
 // Per-stage key flags (8 words in shared memory), written by copy warp p:
 //   [p]     bit j: key 16p+j of the tile has a valid slot
@@ -274,9 +333,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int G = a.Hq / a.Hkv, M = a.n * G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
-  const bool direct = a.splits == 1;  // one split: the normalised output is written here
-  float* po = reinterpret_cast<float*>(a.partials);
-  float* pml = po + size_t(a.b) * a.n * a.Hq * a.splits * D;
   const unsigned char* kbytes = static_cast<const unsigned char*>(a.k_pool);
   const unsigned char* vbytes = static_cast<const unsigned char*>(a.v_pool);
 
@@ -285,12 +341,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   unsigned char* sp = smem_raw + (sbase - raw);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(sp + L::kFlags);  // [stage][4]
-  volatile int* items = reinterpret_cast<volatile int*>(sp + L::kItems);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(sp + L::kFlags);  // [stage][8]
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sp + L::kBars + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + L::kBars + 8 * kNumBars + 8);
+  long long* scratch = reinterpret_cast<long long*>(sp + L::kScratch);  // [0..15] block sums, [16..] partition
+  // split units this CTA merges at the end: count, then (unit_start, Tr, req, g, mt, c1, c2, -) each
+  int* merges = reinterpret_cast<int*>(sp + L::kScratch + 8 * 24);
+  constexpr int kMaxMerges = 2;  // a CTA finishes at most its first and its last piece
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -298,8 +357,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(kEmpty0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kItemFull0 + i), 1);
-      mbar_init(bar(kItemEmpty0 + i), 1 + kRows + 3);  // the MMA thread, the softmax rows, three copy warps
       mbar_init(bar(kQFull0 + i), 1);
       mbar_init(bar(kQEmpty0 + i), 1);
       mbar_init(bar(kSFull0 + i), 1);
@@ -307,8 +364,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(kOFree0 + i), kRows);
       mbar_init(bar(kODone0 + i), 1);
     }
+    mbar_init(bar(kSmGroup), kRows);
     mbar_init(bar(kDrain), 1);
     *abort_flag = 0;
+    merges[0] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -318,10 +377,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+
+  // ---- partition: total tiles T, this CTA's range, and where it starts ----
+  const int upr = a.Hkv * args.m_tiles;
+  const int nwarps = blockDim.x >> 5;
+  {
+    long long tot = 0;
+    for (int r = threadIdx.x; r < a.b; r += blockDim.x) tot += (long long)req_info(a, r, false).tiles * upr;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+    if (lane == 0) scratch[warp] = tot;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long T = 0;
+      for (int w = 0; w < nwarps; ++w) T += scratch[w];
+      scratch[16] = T;
+    }
+    __syncthreads();
+    const long long T = scratch[16];
+    // Ge = min(grid, T) CTAs share the tiles, so every one of them has at
+    // least one (a unit's pieces are then in consecutive CTAs); the others idle
+    const long long Ge = T < gridDim.x ? T : gridDim.x;
+    const bool part = blockIdx.x < Ge;
+    const long long S = part ? cta_start(blockIdx.x, T, Ge) : 0, E = part ? cta_start(blockIdx.x + 1, T, Ge) : 0;
+    // the request holding tile S: chunks of blockDim requests, a block scan each
+    long long run = 0;
+    for (int rb = 0; rb < a.b; rb += blockDim.x) {
+      const int r = rb + threadIdx.x;
+      const long long v = r < a.b ? (long long)req_info(a, r, false).tiles * upr : 0;
+      long long incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      __syncthreads();  // scratch[0..] reused
+      if (lane == 31) scratch[warp] = incl;
+      __syncthreads();
+      long long before = run;
+      for (int w = 0; w < warp; ++w) before += scratch[w];
+      const long long excl = before + incl - v;
+      if (r < a.b && v > 0 && excl <= S && S < excl + v) {
+        const long long o = S - excl;  // offset inside request r
+        const ReqInfo q = req_info(a, r, false);
+        scratch[17] = r;
+        scratch[18] = o / q.tiles;  // unit within the request
+        scratch[19] = o % q.tiles;  // tile within the unit
+      }
+      for (int w = 0; w < nwarps; ++w) run += scratch[w];
+    }
+    if (threadIdx.x == 0) {
+      scratch[20] = S;
+      scratch[21] = E;
+      scratch[22] = Ge;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  const long long T_all = scratch[16], G_eff = scratch[22];
+  auto start_iter = [&]() {
+    PieceIter it;
+    it.cur = scratch[20];
+    it.end = scratch[21];
+    it.r = it.cur < it.end ? int(scratch[17]) : 0;
+    it.j = it.cur < it.end ? int(scratch[18]) : 0;
+    it.t0 = it.cur < it.end ? int(scratch[19]) : 0;
+    it.idx = 0;
+    it.nr = -1;
+    it.nlen = 0;
+    it.nrq = -1;
+    return it;
+  };
 
   auto fail = [&]() {
     raise_error(a.error, SPEC_DEV_TIMEOUT);
@@ -333,78 +461,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Four copy warps, one per SM sub-partition (warp & 3), so the copy
     // instructions do not all land next to one softmax warp.  Copy warp
     // `part` looks up and copies keys 16*part .. 16*part+15 of every tile;
-    // warp 0 (the lead) also takes the items from the work counter,
-    // publishes them and gathers each item's Q rows.
+    // warp 0 (the lead) also gathers each piece's Q rows.
     const int part = warp & 3;
     const bool lead = warp == 0;
     // Key 16*part + lane (lanes 0..15) of tile t: slot load issued one tile
     // ahead (issue), value consumed after that tile's copies (finish).
-    auto issue = [&](const Item& it, int t, int& slot, int& kind) {  // kind: 0 none, 1 prefix, 2 tree
-      const int kg = it.k0 + t * kKeys + 16 * part + lane;
+    auto issue = [&](const Piece& pc, int t, int& slot, int& kind) {  // kind: 0 none, 1 prefix, 2 tree
+      const int kg = pc.k0 + t * kKeys + 16 * part + lane;
       slot = -1;
       kind = 0;
-      if (lane < 16 && kg < it.k1) {
-        if (kg < it.Lp) {
-          slot = a.req_to_token[size_t(it.rq) * a.row_w + kg];
+      if (lane < 16 && kg < pc.k1) {
+        if (kg < pc.Lp) {
+          slot = a.req_to_token[size_t(pc.rq) * a.row_w + kg];
           kind = 1;
         } else {
-          slot = a.verify_loc[size_t(it.req) * a.n + (kg - it.Lp)];
+          slot = a.verify_loc[size_t(pc.req) * a.n + (kg - pc.Lp)];
           kind = 2;
         }
       }
     };
-    auto finish = [&](const Item& it, int slot, int kind, int& row, bool& pre) {
+    auto finish = [&](const Piece& pc, int slot, int kind, int& row, bool& pre) {
       const bool ok_slot = slot >= 0 && slot < a.num_slots;
       if (kind != 0 && !ok_slot) raise_error(a.error, SPEC_DEV_INDEX);
       const bool v = kind != 0 && ok_slot;
-      row = v ? int(slot * a.Hkv + it.g) : -1;  // -1: zero-filled, masked out
+      row = v ? int(slot * a.Hkv + pc.g) : -1;  // -1: zero-filled, masked out
       pre = lane >= 16 || (v && kind == 1);
     };
+    PieceIter pit = start_iter();
+    Piece pc;
     int ct = 0, ci = 0;
     bool ok = true;
-    while (ok) {
-      Item it{};
+    int row = -1, slot_n = -1, kind_n = 0;
+    bool pre = true, have_first = false;
+    while (ok && pit.next(a, args.m_tiles, pc, lead && lane == 0)) {
       if (lead) {
-        int id = 0;
-        if (lane == 0) id = int(atomicAdd(args.work_counter, 1u));
-        id = __shfl_sync(FULL, id, 0);
-        const bool last = id >= args.num_items;
-        if (!last) {
-          it = item_of(args, id, lane == 0);
-          if (it.T == 0) {  // nothing in this split (or a rejected request): not published
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int rg = it.mt * kRows + 4 * lane + e;
-              if (rg < M) {
-                const size_t orow = (size_t(it.req) * a.n + rg / G) * a.Hq + it.g * G + rg % G;
-                if (direct) {  // zero output, empty lse
-                  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D);
-                  for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-                  if (a.lse) a.lse[orow] = -INFINITY;
-                } else {  // an empty partial, skipped by the merge
-                  const size_t idx = orow * a.splits + it.split;
-                  pml[idx * 2] = -INFINITY;
-                  pml[idx * 2 + 1] = 0.f;
-                }
-              }
-            }
-            continue;
-          }
-        }
-        // publish the item (or the end marker) in slot ci % 2
-        const bool slot_ok =
-            (ci < 2 || mbar_wait(bar(kItemEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
-        if (!__all_sync(FULL, slot_ok)) {
-          if (!*abort_flag) fail();
-          break;
-        }
-        if (lane == 0) {
-          items[ci & 1] = last ? -1 : id;
-          mbar_arrive(bar(kItemFull0 + (ci & 1)));
-        }
-        __syncwarp();
-        if (last) break;
-        // the item's Q rows into Q buffer ci % 2, rows 4*lane .. 4*lane+3
+        // the piece's Q rows into Q buffer ci % 2, rows 4*lane .. 4*lane+3
         const bool q_ok = (ci < 2 || mbar_wait(bar(kQEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
         if (!__all_sync(FULL, q_ok)) {
           if (!*abort_flag) fail();
@@ -413,8 +504,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int y[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int rg = it.mt * kRows + 4 * lane + e;
-          y[e] = rg < M ? (it.req * a.n + rg / G) * a.Hq + it.g * G + rg % G : -1;  // -1: zero-filled
+          const int rg = pc.mt * kRows + 4 * lane + e;
+          y[e] = rg < M ? (pc.req * a.n + rg / G) * a.Hq + pc.g * G + rg % G : -1;  // -1: zero-filled
         }
         if (lane == 0) mbar_expect_tx(bar(kQFull0 + (ci & 1)), L::kQTile);
         __syncwarp();
@@ -422,25 +513,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = 0; h < L::kHalves; ++h)
           tma_gather4(sbase + L::kQ + (ci & 1) * L::kQTile + h * L::kQBlock + 512u * lane, &tm_q, 64 * h, y[0], y[1],
                       y[2], y[3], bar(kQFull0 + (ci & 1)));
-      } else {
-        const bool i_ok = mbar_wait(bar(kItemFull0 + (ci & 1)), (ci >> 1) & 1) && !*abort_flag;
-        if (!__all_sync(FULL, i_ok)) {
-          if (!*abort_flag) fail();
-          break;
-        }
-        const int id = items[ci & 1];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kItemEmpty0 + (ci & 1)));
-        if (id < 0) break;
-        it = item_of(args, id, false);
       }
-      int row = -1, slot_n = -1, kind_n = 0;
-      bool pre = true;
-      issue(it, 0, slot_n, kind_n);
-      finish(it, slot_n, kind_n, row, pre);
-      for (int t = 0; t < it.T; ++t, ++ct) {
+      if (!have_first) {  // tile 0's lookups, unless the previous piece started them
+        issue(pc, 0, slot_n, kind_n);
+        finish(pc, slot_n, kind_n, row, pre);
+      }
+      have_first = false;
+      Piece nxt;  // the next piece: its tile-0 lookups go out during this piece's last tile
+      bool has_next = false;
+      for (int t = 0; t < pc.T; ++t, ++ct) {
         const int s = ct % kStages;
-        if (t + 1 < it.T) issue(it, t + 1, slot_n, kind_n);  // in flight while this warp waits
+        if (t + 1 < pc.T) {
+          issue(pc, t + 1, slot_n, kind_n);  // in flight while this warp waits
+        } else {
+          PieceIter peek = pit;
+          has_next = peek.next(a, args.m_tiles, nxt, false);
+          if (has_next) issue(nxt, 0, slot_n, kind_n);
+        }
         const bool e_ok = (ct < kStages || mbar_wait(bar(kEmpty0 + s), ((ct / kStages) - 1) & 1)) && !*abort_flag;
         if (!__all_sync(FULL, e_ok)) {
           if (!*abort_flag) fail();
@@ -472,7 +561,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cp_async16(dst + L::kKTile, vbytes + off, nb);
         }
         cp_async_arrive(bar(kFull0 + s));
-        if (t + 1 < it.T) finish(it, slot_n, kind_n, row, pre);
+        if (t + 1 < pc.T) {
+          finish(pc, slot_n, kind_n, row, pre);
+        } else if (has_next) {
+          finish(nxt, slot_n, kind_n, row, pre);
+          have_first = true;
+        }
       }
       ++ci;
     }
@@ -483,7 +577,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, D, true);
-      // O += P V for global tile u, local tile lt of the item with ordinal ic
+      // O += P V for global tile u, local tile lt of the piece with ordinal ic
       auto issue_pv = [&](int u, int ic, int lt) -> bool {
         const int b = u & 1, s = u % kStages;
         if (lt == 0 && ic >= 2 && !mbar_wait(bar(kOFree0 + (ic & 1)), ((ic >> 1) - 1) & 1)) return false;
@@ -502,23 +596,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(bar(kEmpty0 + s));
         return true;
       };
-      int ct = 0, ci = 0, pend_ic = 0, pend_lt = 0;
+      PieceIter pit = start_iter();
+      Piece pc;
+      // P V of a tile is issued after the next tile's Q K^T (so the softmax of
+      // the next tile overlaps it), except at the end of a piece: there it
+      // follows at once, so the piece's epilogue does not wait on the next
+      // piece's first loads
+      int ct = 0, ci = 0, pend_u = -1, pend_ic = 0, pend_lt = 0;
       bool ok = true;
-      while (ok) {
-        if (!mbar_wait(bar(kItemFull0 + (ci & 1)), (ci >> 1) & 1) || *abort_flag) {
-          ok = false;
-          break;
-        }
-        const int id = items[ci & 1];
-        mbar_arrive(bar(kItemEmpty0 + (ci & 1)));
-        if (id < 0) break;
-        const Item it = item_of(args, id, false);
-        if (!mbar_wait(bar(kQFull0 + (ci & 1)), (ci >> 1) & 1)) {
+      while (ok && pit.next(a, args.m_tiles, pc, false)) {
+        if (!mbar_wait(bar(kQFull0 + (ci & 1)), (ci >> 1) & 1) || *abort_flag) {
           ok = false;
           break;
         }
         const uint32_t qbase = sbase + L::kQ + (ci & 1) * L::kQTile;
-        for (int t = 0; t < it.T; ++t, ++ct) {
+        for (int t = 0; t < pc.T; ++t, ++ct) {
           const int s = ct % kStages;
           if (!mbar_wait(bar(kFull0 + s), (ct / kStages) & 1) || *abort_flag) {
             ok = false;
@@ -535,17 +627,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(kSFull0 + (ct & 1)));
-          if (t == it.T - 1) mma_commit(bar(kQEmpty0 + (ci & 1)));  // the item's Q is no longer read
-          if (ct > 0 && !issue_pv(ct - 1, pend_ic, pend_lt)) {
+          if (t == pc.T - 1) mma_commit(bar(kQEmpty0 + (ci & 1)));  // the piece's Q is no longer read
+          if (pend_u >= 0 && !issue_pv(pend_u, pend_ic, pend_lt)) {
             ok = false;
             break;
           }
+          pend_u = ct;
           pend_ic = ci;
           pend_lt = t;
+          if (t == pc.T - 1) {
+            if (!issue_pv(pend_u, pend_ic, pend_lt)) {
+              ok = false;
+              break;
+            }
+            pend_u = -1;
+          }
         }
         ++ci;
       }
-      if (ok && ct > 0) ok = issue_pv(ct - 1, pend_ic, pend_lt);
+      if (ok && pend_u >= 0) ok = issue_pv(pend_u, pend_ic, pend_lt);
       if (!ok && !*abort_flag) fail();
       // drain: every MMA issued has completed before TMEM is released
       mma_commit(bar(kDrain));
@@ -561,25 +661,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = 32 * quarter + lane;
     const uint32_t tl = tmem + (uint32_t(32 * quarter) << 16);
     const float sl2 = a.scale * 1.4426950408889634f;
-    int ct = 0, ci = 0;
+    PieceIter pit = start_iter();
+    Piece pc;
+    int ct = 0, ci = 0, gph = 0;
     bool ok = true;
-    while (ok) {
-      const bool i_ok = mbar_wait(bar(kItemFull0 + (ci & 1)), (ci >> 1) & 1) && !*abort_flag;
-      if (!__all_sync(FULL, i_ok)) {
-        ok = false;
-        break;
-      }
-      const int id = items[ci & 1];
-      mbar_arrive(bar(kItemEmpty0 + (ci & 1)));
-      if (id < 0) break;
-      const Item it = item_of(args, id, false);
-      const int rg = it.mt * kRows + r;
+    // the 128 softmax threads meet (bounded wait, so a timeout never hangs)
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(bar(kSmGroup));
+      const bool w_ok = mbar_wait(bar(kSmGroup), gph & 1);
+      ++gph;
+      return __all_sync(FULL, w_ok);
+    };
+    while (ok && pit.next(a, args.m_tiles, pc, false)) {
+      const int rg = pc.mt * kRows + r;
       const bool valid = rg < M;
       const int node = valid ? rg / G : 0;
-      const uint64_t mask = valid ? a.mask_bits[size_t(it.req) * a.n + node] : 0ull;
+      const uint64_t mask = valid ? a.mask_bits[size_t(pc.req) * a.n + node] : 0ull;
       const uint32_t ocol = col_o(ci & 1);
       float m_ref = -INFINITY, lsum = 0.f;
-      for (int t = 0; t < it.T; ++t, ++ct) {
+      for (int t = 0; t < pc.T; ++t, ++ct) {
         const int s = ct % kStages, b = ct & 1;
         const bool w_ok = mbar_wait(bar(kSFull0 + b), (ct >> 1) & 1) &&
                           mbar_wait(bar(kFull0 + s), (ct / kStages) & 1) && !*abort_flag;
@@ -598,7 +698,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const uint32_t* f = flags + 8 * s;
         const bool all_pre = (f[4] & f[5] & f[6] & f[7]) != 0u;
-        const int kbase = it.k0 + t * kKeys;
+        const int kbase = pc.k0 + t * kKeys;
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (all_pre) {  // history keys only: all visible
 #pragma unroll
@@ -610,11 +710,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // visibility of the tile's keys for this row: a valid slot, and a
           // history key or a tree node on the row's ancestor mask; key c is
           // tree node c - c0
-          const int c0 = it.Lp - kbase;
+          const int c0 = pc.Lp - kbase;
           const uint64_t hist = c0 <= 0 ? 0ull : (c0 >= kKeys ? ~0ull : ((1ull << c0) - 1ull));
           const uint64_t tree = c0 >= kKeys ? 0ull : (c0 >= 0 ? (mask << c0) : (mask >> (-c0)));
-          const uint64_t valid = uint64_t(f[0] | (f[1] << 16)) | (uint64_t(f[2] | (f[3] << 16)) << 32);
-          const uint64_t vis = valid & (hist | tree);
+          const uint64_t vw = uint64_t(f[0] | (f[1] << 16)) | (uint64_t(f[2] | (f[3] << 16)) << 32);
+          const uint64_t vis = vw & (hist | tree);
           const uint32_t vlo = uint32_t(vis), vhi = uint32_t(vis >> 32);
 #pragma unroll
           for (int c = 0; c < kKeys; ++c) {
@@ -671,7 +771,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive(bar(kPReady0 + b));
       }
       if (!ok) break;
-      // epilogue: wait for the PV of the item's last tile ct-1 (its commit
+      // epilogue: wait for the PV of the piece's last tile ct-1 (its commit
       // covers every earlier PV; PV(ct-3) is known complete from S(ct-1))
       const bool e_ok = mbar_wait(bar(kODone0 + ((ct - 1) & 1)), ((ct - 1) >> 1) & 1);
       if (!__all_sync(FULL, e_ok)) {
@@ -679,16 +779,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const int head = it.g * G + rg % G;
-      const size_t orow = (size_t(it.req) * a.n + node) * a.Hq + head;
-      const size_t idx = orow * a.splits + it.split;
+      const int head = pc.g * G + rg % G;
+      const size_t orow = (size_t(pc.req) * a.n + node) * a.Hq + head;
+      const int slot = 2 * int(blockIdx.x) + (pc.idx == 0 ? 0 : 1);
+      float* so = args.slot_o + (size_t(slot) * kRows + r) * D;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         float v[32];
         tmem_ld32(tl + ocol + 32 * q, v);
         if (valid) {
-          if (direct) {
+          if (pc.complete) {  // the whole unit: normalised bf16 output
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D) + 4 * q;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -696,24 +797,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                   pack_bf16(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
                                   pack_bf16(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
                                   pack_bf16(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(po + idx * D);
+          } else {  // a piece of a split unit: unnormalised partial in this CTA's slot
+            float4* dst = reinterpret_cast<float4*>(so) + 8 * q;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[8 * q + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
       }
-      if (valid) {
-        if (direct) {
-          if (a.lse) a.lse[orow] = lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
-        } else {
-          pml[idx * 2] = m_ref;
-          pml[idx * 2 + 1] = lsum;
+      tc_fence_before();
+      mbar_arrive(bar(kOFree0 + (ci & 1)));  // this O buffer may take the piece after next
+      if (pc.complete) {
+        if (valid && a.lse) a.lse[orow] = lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+      } else {
+        // split unit: publish this piece; the piece arriving last records the
+        // unit, and the whole CTA merges it once the pipeline is done
+        if (valid) {
+          float* sml = args.slot_ml + (size_t(slot) * kRows + r) * 2;
+          sml[0] = m_ref;
+          sml[1] = lsum;
+        }
+        __threadfence();
+        if (!group_sync()) {
+          ok = false;
+          break;
+        }
+        if (r == 0) {
+          const int c1 = cta_of(pc.unit_start, T_all, G_eff);
+          const int c2 = cta_of(pc.unit_start + pc.Tr - 1, T_all, G_eff);
+          if (atomicAdd(args.counters + c1, 1u) == uint32_t(c2 - c1) && merges[0] < kMaxMerges) {
+            int* m = merges + 1 + 8 * merges[0];
+            m[0] = int(pc.unit_start);  // tile space fits in int: < 2^31 tiles
+            m[1] = pc.Tr;
+            m[2] = pc.req;
+            m[3] = pc.g;
+            m[4] = pc.mt;
+            m[5] = c1;
+            m[6] = c2;
+            merges[0] += 1;
+          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(kOFree0 + (ci & 1)));  // this O buffer may take the item after next
       ++ci;
     }
     if (!ok && !*abort_flag) fail();
@@ -726,13 +849,127 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
-  // the CTA that finishes last puts the work counters back to zero
-  if (threadIdx.x == 0) {
+
+  // ---- merge the split units whose last piece this CTA finished: every
+  // thread, many independent loads in flight; the K/V ring (idle now) holds
+  // the per-row weights ----
+  const int nmerge = *abort_flag ? 0 : merges[0];
+  // [pieces][128 rows] weights, [128] 1/L, [pieces][128] sums
+  float* wsm = reinterpret_cast<float*>(sp + L::kStage);
+  // pieces the ring can hold per-row data for: max then weight, sum, and 1/L
+  const int wcap = ((2 * kStages * L::kKTile) / (4 * kRows) - 1) / 2;
+  for (int mi = 0; mi < nmerge; ++mi) {
+    const int* m = merges + 1 + 8 * mi;
+    const long long ustart = m[0];
+    const int mreq = m[2], mg = m[3], mmt = m[4], c1 = m[5], c2 = m[6];
+    const int np = c2 - c1 + 1;
     __threadfence();
-    if (atomicAdd(args.exit_counter, 1u) == gridDim.x - 1) {
-      atomicExch(args.work_counter, 0u);
-      atomicExch(args.exit_counter, 0u);
+    auto slot_of = [&](int c) { return 2 * c + ((c == c1 && cta_start(c1, T_all, G_eff) < ustart) ? 1 : 0); };
+    const int rows = min(kRows, M - mmt * kRows);
+    const float2* ml2 = reinterpret_cast<const float2*>(args.slot_ml);
+    if (np <= wcap) {
+      // per row: the largest running max, each piece's weight, 1 / total
+      // ((m, l) pairs loaded eight pieces at a time)
+      for (int rr = threadIdx.x; rr < rows; rr += blockDim.x) {
+        float Mx = -INFINITY;
+        for (int q0 = 0; q0 < np; q0 += 8) {
+          float2 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            v[u] = q0 + u < np ? __ldcg(ml2 + size_t(slot_of(c1 + q0 + u)) * kRows + rr) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (v[u].y > 0.f) Mx = fmaxf(Mx, v[u].x);
+            if (q0 + u < np) {
+              wsm[(q0 + u) * kRows + rr] = v[u].x;  // the piece's max for now
+              wsm[(np + 1 + q0 + u) * kRows + rr] = v[u].y;
+            }
+          }
+        }
+        float Ls = 0.f;
+        for (int q = 0; q < np; ++q) {
+          const float lc = wsm[(np + 1 + q) * kRows + rr];
+          const float wq = lc > 0.f ? exp2f(wsm[q * kRows + rr] - Mx) : 0.f;
+          wsm[q * kRows + rr] = wq;
+          Ls += lc * wq;
+        }
+        wsm[np * kRows + rr] = Ls > 0.f ? 1.f / Ls : 0.f;
+        const int rg = mmt * kRows + rr;
+        const size_t orow = (size_t(mreq) * a.n + rg / G) * a.Hq + mg * G + rg % G;
+        if (a.lse) a.lse[orow] = Ls > 0.f ? (Mx + log2f(Ls)) * 0.6931471805599453f : -INFINITY;
+      }
+      __syncthreads();
+      // every (row, 4 columns) of the output: the weighted sum over pieces;
+      // each thread loads its whole share of one piece before using any of it
+      constexpr int C4 = D / 4;
+      constexpr int U = (kRows * C4 + kTcThreads - 1) / kTcThreads;
+      const int total = rows * C4;
+      float4 acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < np; ++q) {
+        const float4* src = reinterpret_cast<const float4*>(args.slot_o) + size_t(slot_of(c1 + q)) * kRows * C4;
+        float4 o4[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = threadIdx.x + u * kTcThreads;
+          o4[u] = e < total ? __ldcg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = threadIdx.x + u * kTcThreads;
+          const float wq = e < total ? wsm[q * kRows + e / C4] : 0.f;
+          acc[u].x += wq * o4[u].x;
+          acc[u].y += wq * o4[u].y;
+          acc[u].z += wq * o4[u].z;
+          acc[u].w += wq * o4[u].w;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = threadIdx.x + u * kTcThreads;
+        if (e < total) {
+          const int rr = e / C4, c4 = e % C4;
+          const float li = wsm[np * kRows + rr];
+          const int rg = mmt * kRows + rr;
+          const size_t orow = (size_t(mreq) * a.n + rg / G) * a.Hq + mg * G + rg % G;
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * D + 4 * c4) =
+              make_uint2(pack_bf16(acc[u].x * li, acc[u].y * li), pack_bf16(acc[u].z * li, acc[u].w * li));
+        }
+      }
+    } else if (threadIdx.x < rows) {
+      // more pieces than the ring holds weights for: one thread per row, two passes
+      const int rr = threadIdx.x;
+      float Mx = -INFINITY, Ls = 0.f;
+      for (int q = 0; q < np; ++q) Mx = fmaxf(Mx, __ldcg(args.slot_ml + (size_t(slot_of(c1 + q)) * kRows + rr) * 2));
+      for (int q = 0; q < np; ++q) {
+        const float* ml = args.slot_ml + (size_t(slot_of(c1 + q)) * kRows + rr) * 2;
+        const float lc = __ldcg(ml + 1);
+        if (lc > 0.f) Ls += lc * exp2f(__ldcg(ml) - Mx);
+      }
+      const float linv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const int rg = mmt * kRows + rr;
+      const size_t orow = (size_t(mreq) * a.n + rg / G) * a.Hq + mg * G + rg % G;
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < np; ++q) {
+          const float* ml = args.slot_ml + (size_t(slot_of(c1 + q)) * kRows + rr) * 2;
+          const float lc = __ldcg(ml + 1);
+          if (!(lc > 0.f)) continue;
+          const float wq = exp2f(__ldcg(ml) - Mx) * linv;
+          const float4 o4 = __ldcg(reinterpret_cast<const float4*>(args.slot_o + (size_t(slot_of(c1 + q)) * kRows + rr) * D) + c4);
+          acc.x += wq * o4.x;
+          acc.y += wq * o4.y;
+          acc.z += wq * o4.z;
+          acc.w += wq * o4.w;
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * D + 4 * c4) =
+            make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+      }
+      if (a.lse) a.lse[orow] = Ls > 0.f ? (Mx + log2f(Ls)) * 0.6931471805599453f : -INFINITY;
     }
+    __syncthreads();
+    if (threadIdx.x == 0) atomicExch(args.counters + c1, 0u);  // ready for the next launch
   }
 }
 
@@ -783,34 +1020,28 @@ int launch_t(const AttentionParams& p, const TcGeometry& geo, cudaStream_t strea
       return SPEC_ERR_LAUNCH;
     attr_set = true;
   }
-  const long items = long(p.splits) * p.b * p.Hkv * geo.m_tiles;
-  if (items > 0x7fffffffL) return SPEC_ERR_UNSUPPORTED;
-  TcArgs args{p, geo.m_tiles, geo.split_tiles, int(items), p.counters, p.counters + 1};
-  const int grid = int(items < sm_count ? items : sm_count);
+  unsigned char* base = p.partials;
+  TcArgs args{p, geo.m_tiles, p.counters,
+              reinterpret_cast<float*>(base + kSlotOOffset),
+              reinterpret_cast<float*>(base + kSlotMLOffset)};
+  const int grid = sm_count < kMaxCtas ? sm_count : kMaxCtas;
   attention_tc_kernel<D><<<grid, kTcThreads, smem, stream>>>(args, tq);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
-  return p.splits == 1 ? SPEC_OK : launch_attention_merge(p, stream);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 }  // namespace
 
 TcGeometry attention_tc_geometry(int b, int n, int Hq, int Hkv, int max_seq_len) {
+  (void)b;
+  (void)max_seq_len;
   TcGeometry geo{};
-  const int G = Hq / Hkv;
-  geo.m_tiles = (n * G + kRows - 1) / kRows;
-  const long units = long(b) * Hkv * geo.m_tiles;
-  const long tiles = (long(max_seq_len) + n + kKeys - 1) / kKeys;
-  // about four items per SM for the dynamic schedule to balance, splits of at
-  // least 8 tiles (each split adds a partial per row to write and merge), at
-  // most 32 splits
-  long splits = (kTargetCtas + units - 1) / units;
-  if (splits > tiles / 8) splits = tiles / 8;
-  if (splits > 32) splits = 32;
-  if (splits < 1) splits = 1;
-  geo.split_tiles = int((tiles + splits - 1) / splits);
-  geo.splits = int((tiles + geo.split_tiles - 1) / geo.split_tiles);
+  geo.m_tiles = (n * (Hq / Hkv) + kRows - 1) / kRows;
+  geo.split_tiles = 0;
+  geo.splits = 1;  // split units are merged inside the kernel: always one launch
   return geo;
 }
+
+size_t attention_partial_bytes() { return kSlotOOffset + size_t(2) * kMaxCtas * kRows * 128 * 4; }
 
 int launch_attention_tc(const AttentionParams& p, const TcGeometry& geo, cudaStream_t stream) {
   if (p.D == 128) return launch_t<128>(p, geo, stream);

@@ -31,7 +31,8 @@ constexpr size_t kHeaderBytes = 256;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline size_t counters_bytes(int b) { return align256(size_t(b + 1) * 4); }
+// at least 256 words: the attention merge counts arrivals per CTA (<= 192)
+__host__ __device__ inline size_t counters_bytes(int b) { return align256(size_t(b + 1 > 256 ? b + 1 : 256) * 4); }
 
 struct WsView {
   uint32_t* error;

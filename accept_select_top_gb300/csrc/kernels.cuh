@@ -145,14 +145,14 @@ size_t sampling_state_bytes(int b);
 size_t sampling_partial2_bytes(int b, int chunks2);
 size_t commit_partial_bytes(int b, int n);
 
-// Split-KV geometry of the tensor-core attention: m_tiles CTAs of 128 query
-// rows per (request, kv head), splits of split_tiles 128-key tiles each.
+// Geometry of the tensor-core attention: m_tiles units of 128 query rows per
+// (request, kv head); splits is the number of launches' worth of key splits
+// (always 1: units split over CTAs are merged inside the kernel).
 struct TcGeometry {
   int m_tiles, split_tiles, splits;
 };
 TcGeometry attention_tc_geometry(int b, int n, int Hq, int Hkv, int max_seq_len);
 int launch_attention_tc(const AttentionParams& p, const TcGeometry& geo, cudaStream_t stream);
-int launch_attention_merge(const AttentionParams& p, cudaStream_t stream);
-size_t attention_partial_bytes(int b, int n, int Hq, int D, int splits);
+size_t attention_partial_bytes();  // merge slots and counters, any D <= 128
 
 }  // namespace spec

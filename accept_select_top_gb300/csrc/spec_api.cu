@@ -42,7 +42,7 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
       return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
              sampling_partial2_bytes(b, terminal_split(V).chunks);
     case SPEC_OP_VERIFY_ATTENTION:
-      return attention_partial_bytes(b, n, Hq, 128, attention_tc_geometry(b, n, Hq, Hkv, max_seq_len).splits);
+      return attention_partial_bytes();
     case SPEC_OP_COMMIT_KV:
       return commit_partial_bytes(b, n);
     default:

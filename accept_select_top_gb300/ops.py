@@ -119,7 +119,7 @@ def spec_device_sm_count() -> int:
 
 
 def spec_verify_attention_splits(b: int, n: int, Hq: int, Hkv: int, max_seq_len: int) -> int:
-    """Key splits of spec_verify_attention for these sizes (1: no merge launch)."""
+    """Kernel launches spec_verify_attention makes for these sizes (0: invalid sizes)."""
     return int(LIB.spec_verify_attention_splits(b, n, Hq, Hkv, max_seq_len))
 
 

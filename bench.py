@@ -503,7 +503,7 @@ def main(argv=None):
     roof = None
     if stage is not None:
         dom = max(stage, key=stage.get)
-        sources = {"attention": ["accept_select_top_gb300/csrc/attention_tc.cu", "accept_select_top_gb300/csrc/attention_merge.cu"],
+        sources = {"attention": ["accept_select_top_gb300/csrc/attention_tc.cu"],
                    "select_build": ["accept_select_top_gb300/csrc/select_topk.cu",
                                     "accept_select_top_gb300/csrc/build_tree.cu"],
                    "accept_commit": ["accept_select_top_gb300/csrc/verify_greedy.cu",

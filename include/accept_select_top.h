@@ -164,8 +164,11 @@ int spec_build_tree(int b, int k, int S, int n,
  *   with mask bit (i, j) set;  out = softmax(scale * q.K^T) V.
  * out: [b*n, Hq, D] bf16; lse: [b*n, Hq] fp32 natural-log sum-exp of the
  * scaled scores (optional, NULL).  max_seq_len bounds every seq_len (a larger
- * one sets SPEC_DEV_LENGTH and is clamped) and sizes the split-KV grid.
- * page_size is the KV page size (1 or 16); slots of one page are consecutive.
+ * one sets SPEC_DEV_LENGTH and is clamped).  page_size is the KV page size (1
+ * or 16); slots of one page are consecutive.  One launch: the key lists are
+ * spread evenly over one CTA per SM, and a (request, kv head) split between
+ * CTAs is merged by the CTA that finishes it last.  The workspace holds the
+ * merge slots (about 26 MB, independent of the sizes).
  * ------------------------------------------------------------------------- */
 int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size,
                           const void* q, const void* k_pool, const void* v_pool,
@@ -177,11 +180,10 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size,
                           float scale, void* out, float* lse,
                           void* ws, size_t ws_bytes, void* stream);
 
-/* Number of pieces spec_verify_attention splits each request's key list into
- * for these sizes (host only, no device call).  1 means the kernel writes the
- * output itself (one launch); more means a second, merge launch combines the
- * per-split partials.  0 for invalid sizes.  (An implementation detail the
- * method itself has no counterpart for: it lets a caller count launches.) */
+/* Kernel launches spec_verify_attention makes for these sizes (host only, no
+ * device call): 1 with the current kernel, which merges split key lists
+ * itself.  0 for invalid sizes.  (An implementation detail the method itself
+ * has no counterpart for: it lets a caller count launches.) */
 int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len);
 
 /* ---------------------------------------------------------------------------

@@ -49,14 +49,12 @@ def test_workspace_sizes_host_only():
     assert ops.spec_workspace_size(99, 8, 16, 4, 1000) == 0
 
 
-def test_attention_splits_host_only():
-    """The split count covers the key list and shrinks as the batch grows."""
+def test_attention_launch_count_host_only():
+    """One launch for any valid sizes (split key lists are merged in the kernel)."""
     from accept_select_top_gb300 import ops
-    assert ops.spec_verify_attention_splits(8, 16, 32, 8, 4096) >= 1
-    assert ops.spec_verify_attention_splits(1, 4, 8, 8, 0) == 1          # one tile: no split
-    big = ops.spec_verify_attention_splits(2, 64, 64, 8, 131072)
-    assert 1 < big <= 32
-    assert ops.spec_verify_attention_splits(4096, 16, 32, 8, 4096) == 1  # enough work unsplit
+    assert ops.spec_verify_attention_splits(8, 16, 32, 8, 4096) == 1
+    assert ops.spec_verify_attention_splits(1, 4, 8, 8, 0) == 1
+    assert ops.spec_verify_attention_splits(2, 64, 64, 8, 131072) == 1
     assert ops.spec_verify_attention_splits(8, 65, 32, 8, 4096) == 0     # n > 64
     assert ops.spec_verify_attention_splits(8, 16, 30, 8, 4096) == 0     # Hq % Hkv
 
