@@ -328,6 +328,7 @@ struct PieceIter {
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attention_tc_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q) {
+  pdl_trigger();
   using L = Smem<D>;
   const AttentionParams& a = args.p;
   const int G = a.Hq / a.Hkv, M = a.n * G;
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
+  pdl_wait();  // nothing above reads global memory
   // ---- partition: total tiles T, this CTA's range, and where it starts ----
   const int upr = a.Hkv * args.m_tiles;
   const int nwarps = blockDim.x >> 5;
@@ -1025,8 +1027,8 @@ int launch_t(const AttentionParams& p, const TcGeometry& geo, cudaStream_t strea
               reinterpret_cast<float*>(base + kSlotOOffset),
               reinterpret_cast<float*>(base + kSlotMLOffset)};
   const int grid = sm_count < kMaxCtas ? sm_count : kMaxCtas;
-  attention_tc_kernel<D><<<grid, kTcThreads, smem, stream>>>(args, tq);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  const cudaError_t e = launch_pdl(attention_tc_kernel<D>, dim3(grid), dim3(kTcThreads), smem, stream, args, tq);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 }  // namespace

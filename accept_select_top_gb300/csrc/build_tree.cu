@@ -25,6 +25,8 @@ namespace {
 constexpr int kBuildThreads = 512;
 
 __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   const int req = blockIdx.x;
   const int C = a.k + (a.S - 1) * a.k * a.k;
@@ -142,7 +144,8 @@ int launch_build_tree(const BuildParams& p, cudaStream_t stream) {
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return SPEC_ERR_LAUNCH;
-  build_tree_kernel<<<p.b, kBuildThreads, smem, stream>>>(p);
+  if (launch_pdl(build_tree_kernel, dim3(p.b), dim3(kBuildThreads), smem, stream, p) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

@@ -27,6 +27,8 @@ constexpr int kCommitThreads = 256;
 constexpr int kSliceBytes = 32 * 1024;  // shared staging per slice (K and V of all L rows)
 
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) {
+  pdl_trigger();
+  pdl_wait();
   const int req = blockIdx.x, grp = blockIdx.y, G = gridDim.y;
   const int n = a.n, W = a.W, tid = threadIdx.x;
   __shared__ int src[kMaxN + 1], dst[kMaxN + 1], unit_s[kMaxN], dst_unit_s[kMaxN + 1];
@@ -185,7 +187,8 @@ int launch_commit_kv(const CommitParams& p, cudaStream_t stream) {
   const int cap = p.b > 0 ? (kTargetCtas + p.b - 1) / p.b : 1;
   if (G > cap) G = cap;
   if (G < 1) G = 1;
-  commit_kernel<<<dim3(p.b, G), kCommitThreads, 0, stream>>>(p);
+  if (launch_pdl(commit_kernel, dim3(p.b, G), dim3(kCommitThreads), 0, stream, p) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

@@ -99,6 +99,31 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation (launch_pdl): it lets the grid
+// that follows be scheduled early (pdl_trigger, first thing in each kernel),
+// and waits for the grid before it -- its completion and its memory -- before
+// reading any global memory (pdl_wait).  Stream order is kept: no kernel
+// reads anything before its predecessor has finished.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // 2^x by the hardware approximation: relative error about 2^-22, results
 // below 2^-126 flushed to zero.  For sums of exponentials whose total is at
 // least 1 (a softmax denominator), far below fp32's own accumulated rounding.

@@ -145,8 +145,53 @@ __device__ __forceinline__ void warp_merge(TopList<K>& top, float* out_v, int* o
   }
 }
 
+// Outputs of request req once p_s / id_s hold its rows' k probabilities and
+// tokens (best first): topk_p_out, and for step 0 the first score block, else
+// the path-score expansion scores_in[r] * p[r][j] (one fp32 multiply) and its
+// top-k with parent offsets.  Called by every thread of the CTA after a
+// __syncthreads; sc_in is scores_in[req*k + lane/k] prefetched by warp 0.
+__device__ __forceinline__ void write_request(const SelectParams& a, int req, int rows_per_req,
+                                              const float (*p_s)[kMaxK], const int (*id_s)[kMaxK], float sc_in) {
+  const int k = a.k, kk = k * k, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.topk_p_out) {
+    for (int t = threadIdx.x; t < rows_per_req * k; t += blockDim.x)
+      a.topk_p_out[size_t(req * rows_per_req + t / k) * k + t % k] = p_s[t / k][t % k];
+  }
+  const size_t sb = size_t(req) * a.score_ld;
+  if (a.step == 0) {
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      a.score_blk[sb + j] = p_s[0][j];
+      a.token_blk[sb + j] = id_s[0][j];
+      a.scores_out[size_t(req) * k + j] = p_s[0][j];
+      a.next_ids[size_t(req) * k + j] = id_s[0][j];
+    }
+    if (a.parent_blk)
+      for (int j = threadIdx.x; j <= k; j += blockDim.x) a.parent_blk[size_t(req) * a.parent_ld + j] = j - 1;
+  } else if (w == 0) {
+    __shared__ float ex[kMaxK * kMaxK];
+    for (int f = lane; f < kk; f += 32) {
+      const float sin = f < 32 ? sc_in : a.scores_in[size_t(req) * k + f / k];
+      ex[f] = __fmul_rn(sin, p_s[f / k][f % k]);
+      a.score_blk[sb + f] = ex[f];
+      a.token_blk[sb + f] = id_s[f / k][f % k];
+    }
+    __syncwarp();
+    for (int f = lane; f < kk; f += 32) {
+      int rank = 0;
+      for (int g = 0; g < kk; ++g) rank += better(ex[g], g, ex[f], f);
+      if (rank < k) {
+        if (a.parent_blk) a.parent_blk[size_t(req) * a.parent_ld + rank] = f + kk * (a.step - 1) + k;
+        a.scores_out[size_t(req) * k + rank] = ex[f];
+        a.next_ids[size_t(req) * k + rank] = id_s[f / k][f % k];
+      }
+    }
+  }
+}
+
 template <typename T, int K>
 __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const int rows_per_req = a.step ? a.k : 1;
@@ -363,55 +408,24 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
     __syncwarp();
   }
   __syncthreads();
-  if (a.topk_p_out) {
-    for (int t = threadIdx.x; t < rows_per_req * k; t += blockDim.x)
-      a.topk_p_out[size_t(req * rows_per_req + t / k) * k + t % k] = p_s[t / k][t % k];
-  }
-  const size_t sb = size_t(req) * a.score_ld;
-  if (a.step == 0) {
-    for (int j = threadIdx.x; j < k; j += blockDim.x) {
-      a.score_blk[sb + j] = p_s[0][j];
-      a.token_blk[sb + j] = id_s[0][j];
-      a.scores_out[size_t(req) * k + j] = p_s[0][j];
-      a.next_ids[size_t(req) * k + j] = id_s[0][j];
-    }
-    if (a.parent_blk)
-      for (int j = threadIdx.x; j <= k; j += blockDim.x) a.parent_blk[size_t(req) * a.parent_ld + j] = j - 1;
-  } else if (w == 0) {
-    // expand[r*k + j] = scores_in[r] * p[r][j] (one fp32 multiply); top-k of k*k
-    __shared__ float ex[kMaxK * kMaxK];
-    for (int f = lane; f < kk; f += 32) {
-      const float sin = f < 32 ? sc_in : a.scores_in[size_t(req) * k + f / k];
-      ex[f] = __fmul_rn(sin, p_s[f / k][f % k]);
-      a.score_blk[sb + f] = ex[f];
-      a.token_blk[sb + f] = id_s[f / k][f % k];
-    }
-    __syncwarp();
-    for (int f = lane; f < kk; f += 32) {
-      int rank = 0;
-      for (int g = 0; g < kk; ++g) rank += better(ex[g], g, ex[f], f);
-      if (rank < k) {
-        if (a.parent_blk) a.parent_blk[size_t(req) * a.parent_ld + rank] = f + kk * (a.step - 1) + k;
-        a.scores_out[size_t(req) * k + rank] = ex[f];
-        a.next_ids[size_t(req) * k + rank] = id_s[f / k][f % k];
-      }
-    }
-  }
+  write_request(a, req, rows_per_req, p_s, id_s, sc_in);
   counter_reset(a.counters + req);
 }
+
 
 template <typename T>
 int launch_t(const SelectParams& p, cudaStream_t stream) {
   dim3 grid(p.chunks, p.rows);
   const int K = p.k <= 1 ? 1 : p.k <= 2 ? 2 : p.k <= 4 ? 4 : p.k <= 8 ? 8 : 16;
+  cudaError_t e = cudaSuccess;
   switch (K) {
-    case 1: select_kernel<T, 1><<<grid, kThreads, 0, stream>>>(p); break;
-    case 2: select_kernel<T, 2><<<grid, kThreads, 0, stream>>>(p); break;
-    case 4: select_kernel<T, 4><<<grid, kThreads, 0, stream>>>(p); break;
-    case 8: select_kernel<T, 8><<<grid, kThreads, 0, stream>>>(p); break;
-    default: select_kernel<T, 16><<<grid, kThreads, 0, stream>>>(p); break;
+    case 1: e = launch_pdl(select_kernel<T, 1>, grid, dim3(kThreads), 0, stream, p); break;
+    case 2: e = launch_pdl(select_kernel<T, 2>, grid, dim3(kThreads), 0, stream, p); break;
+    case 4: e = launch_pdl(select_kernel<T, 4>, grid, dim3(kThreads), 0, stream, p); break;
+    case 8: e = launch_pdl(select_kernel<T, 8>, grid, dim3(kThreads), 0, stream, p); break;
+    default: e = launch_pdl(select_kernel<T, 16>, grid, dim3(kThreads), 0, stream, p); break;
   }
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 }  // namespace

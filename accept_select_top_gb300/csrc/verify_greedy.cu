@@ -77,6 +77,8 @@ __device__ __forceinline__ void scan_argmax_bf16(const uint16_t* row, int begin,
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const int req = row / a.n;
@@ -185,10 +187,9 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
 
 int launch_verify_greedy(const GreedyParams& p, cudaStream_t stream) {
   dim3 grid(p.chunks, p.b * p.n);
-  if (p.dtype == SPEC_F32)
-    greedy_kernel<float><<<grid, kThreads, 0, stream>>>(p);
-  else
-    greedy_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(p);
+  const cudaError_t e = p.dtype == SPEC_F32 ? launch_pdl(greedy_kernel<float>, grid, dim3(kThreads), 0, stream, p)
+                                             : launch_pdl(greedy_kernel<uint16_t>, grid, dim3(kThreads), 0, stream, p);
+  if (e != cudaSuccess) return SPEC_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

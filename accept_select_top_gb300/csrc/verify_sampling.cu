@@ -55,6 +55,8 @@ __device__ __forceinline__ float p_of(float l, float M, float T, float S) { retu
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams a) {
+  pdl_trigger();
+  pdl_wait();
   using Tr = LogitTraits<T>;
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
@@ -246,6 +248,8 @@ __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqSta
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams a) {
+  pdl_trigger();
+  pdl_wait();
   using Tr = LogitTraits<T>;
   const int req = blockIdx.y;
   const int chunk = blockIdx.x;
@@ -382,14 +386,15 @@ size_t sampling_partial2_bytes(int b, int chunks2) { return align256(size_t(b) *
 
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
   dim3 g1(p.chunks, p.b * p.n), g2(p.chunks2, p.b);
+  cudaError_t e;
   if (p.dtype == SPEC_F32) {
-    sampling_stats_kernel<float><<<g1, kThreads, 0, stream>>>(p);
-    sampling_bonus_kernel<float><<<g2, kThreads, 0, stream>>>(p);
+    e = launch_pdl(sampling_stats_kernel<float>, g1, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float>, g2, dim3(kThreads), 0, stream, p);
   } else {
-    sampling_stats_kernel<uint16_t><<<g1, kThreads, 0, stream>>>(p);
-    sampling_bonus_kernel<uint16_t><<<g2, kThreads, 0, stream>>>(p);
+    e = launch_pdl(sampling_stats_kernel<uint16_t>, g1, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t>, g2, dim3(kThreads), 0, stream, p);
   }
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 }  // namespace spec
