@@ -493,8 +493,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Piece pc;
     int ct = 0, ci = 0;
     bool ok = true;
-    int row = -1, slot_n = -1, kind_n = 0;
-    bool pre = true, have_first = false;
+    // Slot lookups run two tiles ahead of the copies: cur (row, pre) is the
+    // looked-up tile about to be copied, q1 the lookup already in flight for
+    // the tile after it (also across a piece boundary, for the next piece's
+    // first two tiles).
+    int row = -1, q1s = -1, q1k = 0;
+    bool pre = true, cur_ready = false, q1v = false;
     while (ok && pit.next(a, args.m_tiles, pc, lead && lane == 0)) {
       if (lead) {
         // the piece's Q rows into Q buffer ci % 2, rows 4*lane .. 4*lane+3
@@ -516,21 +520,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_gather4(sbase + L::kQ + (ci & 1) * L::kQTile + h * L::kQBlock + 512u * lane, &tm_q, 64 * h, y[0], y[1],
                       y[2], y[3], bar(kQFull0 + (ci & 1)));
       }
-      if (!have_first) {  // tile 0's lookups, unless the previous piece started them
-        issue(pc, 0, slot_n, kind_n);
-        finish(pc, slot_n, kind_n, row, pre);
+      if (!cur_ready) {  // tile 0's lookups, unless the previous piece started them
+        int s0 = -1, k0 = 0;
+        issue(pc, 0, s0, k0);
+        finish(pc, s0, k0, row, pre);
       }
-      have_first = false;
-      Piece nxt;  // the next piece: its tile-0 lookups go out during this piece's last tile
-      bool has_next = false;
+      if (!q1v && pc.T > 1) {
+        issue(pc, 1, q1s, q1k);
+        q1v = true;
+      }
+      cur_ready = false;
+      Piece nxt;  // the next piece: its first lookups go out during this piece's last two tiles
+      bool has_next = false, peeked = false;
       for (int t = 0; t < pc.T; ++t, ++ct) {
         const int s = ct % kStages;
-        if (t + 1 < pc.T) {
-          issue(pc, t + 1, slot_n, kind_n);  // in flight while this warp waits
-        } else {
+        if (!peeked && t + 2 >= pc.T) {
           PieceIter peek = pit;
           has_next = peek.next(a, args.m_tiles, nxt, false);
-          if (has_next) issue(nxt, 0, slot_n, kind_n);
+          peeked = true;
+        }
+        // the lookup for the tile two ahead
+        int q2s = -1, q2k = 0;
+        bool q2v = false;
+        if (t + 2 < pc.T) {
+          issue(pc, t + 2, q2s, q2k);
+          q2v = true;
+        } else if (has_next && t + 2 - pc.T < min(nxt.T, 2)) {
+          issue(nxt, t + 2 - pc.T, q2s, q2k);
+          q2v = true;
         }
         const bool e_ok = (ct < kStages || mbar_wait(bar(kEmpty0 + s), ((ct / kStages) - 1) & 1)) && !*abort_flag;
         if (!__all_sync(FULL, e_ok)) {
@@ -563,12 +580,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cp_async16(dst + L::kKTile, vbytes + off, nb);
         }
         cp_async_arrive(bar(kFull0 + s));
+        // the next tile's lookup, issued an iteration ago, becomes cur
         if (t + 1 < pc.T) {
-          finish(pc, slot_n, kind_n, row, pre);
+          finish(pc, q1s, q1k, row, pre);
         } else if (has_next) {
-          finish(nxt, slot_n, kind_n, row, pre);
-          have_first = true;
+          if (!q1v) issue(nxt, 0, q1s, q1k);  // (only when this piece had a single tile)
+          finish(nxt, q1s, q1k, row, pre);
+          cur_ready = true;
         }
+        q1s = q2s;
+        q1k = q2k;
+        q1v = q2v;
       }
       ++ci;
     }
