@@ -60,6 +60,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def job_elapsed_ms(elapsed_ms, world, device, torch):
+    """The job's elapsed time: the slowest rank's (every rank verifies its own
+    batch; the job ends when the last one does)."""
+    if world <= 1:
+        return float(elapsed_ms)
+    tt = torch.tensor([float(elapsed_ms)], device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tokens_per_s(b, n, steps, world, elapsed_ms):
+    """Verified tree tokens of all ranks (weak scaling: b*n per rank per step)
+    over the job's elapsed time."""
+    return b * n * steps * world / (elapsed_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -300,11 +316,7 @@ def run_ours(args, torch):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler is not None else None
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = job_elapsed_ms(t0.elapsed_time(t1), world, device, torch)
     assert steps[0].ws.last_error() == 0, "device error word set during the timed region"
 
     stage = None
@@ -498,7 +510,7 @@ def main(argv=None):
         return 0
     from accept_select_top_gb300.pipeline import launches_per_step
     ms_per_step = elapsed_ms / args.steps
-    value = wl.b * wl.n * args.steps * world / (elapsed_ms / 1e3)
+    value = job_tokens_per_s(wl.b, wl.n, args.steps, world, elapsed_ms)
     bytes_ = step_bytes(wl, None, lay, mode)
     roof = None
     if stage is not None:
