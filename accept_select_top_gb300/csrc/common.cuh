@@ -156,14 +156,17 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 // CTA must reset the counter (counter_reset) once it is done.
 __device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t total) {
   __shared__ int s_last;
-  __threadfence();  // every thread's partial writes are ordered before the arrival
+  // The barrier orders every thread's partial writes before thread 0's
+  // arrival, an acquire-release atomic at GPU scope: the CTA that sees the
+  // count complete also sees every other CTA's partials (read after the
+  // second barrier).
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t prev = atomicAdd(counter, 1u);
+    uint32_t prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
     s_last = prev == total - 1;
   }
   __syncthreads();
-  if (s_last) __threadfence();
   return s_last;
 }
 

@@ -44,7 +44,7 @@ __device__ __forceinline__ void block_argmax(float& v, int& i) {
 // inside it at the end.  The thread's first vector is always taken, so a
 // row of -inf still yields its lowest index.
 __device__ __forceinline__ void scan_argmax_bf16(const uint16_t* row, int begin, int end, float& bv, int& bi) {
-  constexpr int U = kBatch / 8;
+  constexpr int U = 8;  // 128 bytes per thread in flight: a chunk in about two round trips
   const uint4* p = reinterpret_cast<const uint4*>(row);
   const int nt = blockDim.x, ve = end / 8;
   int bvi = -1;
