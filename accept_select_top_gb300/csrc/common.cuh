@@ -312,7 +312,9 @@ inline RowSplit pick_split(long rows, int V, int vec, int max_chunks = kMaxChunk
 }
 
 // The split of the terminal row in the second sampling pass: fixed
-// 4096-token chunks, so the in-order search of one chunk is 16 block scans.
+// 4096-token chunks (16 tokens per thread of a 256-thread CTA, so the
+// in-order search of one chunk is a single pass); at most kMaxChunks2 chunks.
+constexpr int kMaxChunks2 = 64;
 inline RowSplit terminal_split(int V) {
   const int per = V < 4096 ? V : 4096;
   return RowSplit{(V + per - 1) / per, per};

@@ -295,6 +295,7 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
   p.next_root = next_root;
   const RowSplit s1 = pick_split(long(b) * n, V, vec_elems(dtype));
   const RowSplit s2 = terminal_split(V);
+  if (s2.chunks > kMaxChunks2) return SPEC_ERR_UNSUPPORTED;
   p.chunks = s1.chunks;
   p.chunk_elems = s1.chunk_elems;
   p.chunks2 = s2.chunks;

@@ -213,34 +213,54 @@ struct Kahan {
   }
 };
 
-// Residual max(0, p - q) (mode 2) or p (otherwise) of token v of the terminal row.
-template <typename T>
-__device__ __forceinline__ float terminal_mass(const SamplingParams& a, const ReqState& st, bool use_res, int v) {
-  using Tr = LogitTraits<T>;
-  const float p = p_of(Tr::load(static_cast<const T*>(a.logits) + size_t(st.row) * a.V, v), st.M, st.T, st.S);
+// p of a token of the terminal row from its logit: 2^((l - M) c) / S with
+// c = log2(e) / T, by the hardware exp2 (relative error about 2^-22) and one
+// multiply.  The chunk sums and the in-chunk search use the same p.
+struct TermP {
+  float M, c, invS;
+  __device__ __forceinline__ explicit TermP(const ReqState& st)
+      : M(st.M), c(1.4426950408889634f / st.T), invS(1.f / st.S) {}
+  __device__ __forceinline__ float p(float l) const { return fast_exp2((l - M) * c) * invS; }
+};
+
+// Residual max(0, p - q) (mode 2) or p of a token given its logit l and q.
+__device__ __forceinline__ float term_mass(const TermP& tp, bool use_res, float l, float qv) {
+  const float p = tp.p(l);
   if (!use_res) return p;
-  const float q = __ldg(a.draft_probs + size_t(st.row) * a.V + v);
-  return p > q ? p - q : 0.f;  // the fp32 difference of the two values
+  return p > qv ? p - qv : 0.f;  // the fp32 difference of the two values
 }
 
+constexpr int kTermPer = 16;  // terminal tokens a thread holds at once
+
+// Sums of the residual and of p over row[begin, end) of the terminal row,
+// each thread loading kTermPer tokens (logit and q) before using any.
 template <typename T>
 __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqState& st, int begin, int end,
                                            double& res, double& ps, int& last_res, int& last_p) {
   using Tr = LogitTraits<T>;
   const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
   const float* q = a.draft_probs + size_t(st.row) * a.V;
+  const TermP tp(st);
+  const int nt = blockDim.x;
   Kahan kr, kp;
-  for (int v = begin + threadIdx.x; v < end; v += blockDim.x) {
-    const float p = p_of(Tr::load(L, v), st.M, st.T, st.S);
-    float r = 0.f;
-    if (st.mode == 2) {
-      const float qq = __ldg(q + v);
-      r = p > qq ? p - qq : 0.f;
+  for (int b0 = begin + int(threadIdx.x); b0 < end; b0 += kTermPer * nt) {
+    float lv[kTermPer], qv[kTermPer];
+#pragma unroll
+    for (int u = 0; u < kTermPer; ++u) {
+      const int v = b0 + u * nt;
+      lv[u] = v < end ? Tr::load(L, v) : -INFINITY;
+      qv[u] = (st.mode == 2 && v < end) ? __ldg(q + v) : 0.f;
     }
-    kr.add(r);
-    kp.add(p);
-    if (r > 0.f) last_res = v;
-    if (p > 0.f) last_p = v;
+#pragma unroll
+    for (int u = 0; u < kTermPer; ++u) {
+      const int v = b0 + u * nt;
+      const float p = v < end ? tp.p(lv[u]) : 0.f;
+      const float r = (st.mode == 2 && p > qv[u]) ? p - qv[u] : 0.f;
+      kr.add(r);
+      kp.add(p);
+      if (r > 0.f) last_res = v;
+      if (p > 0.f) last_p = v;
+    }
   }
   res = double(kr.sum) - double(kr.comp);
   ps = double(kp.sum) - double(kp.comp);
@@ -292,16 +312,26 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   if (!arrive_last(a.counters + req, uint32_t(a.chunks2))) return;
 
   // ---- finalize: locate u_final * Z on the cumulative mass ----
+  // every chunk's partial in one round of loads, then the prefix in shared memory
+  __shared__ double s_res[kMaxChunks2], s_p[kMaxChunks2];
+  __shared__ int s_lr[kMaxChunks2], s_lp[kMaxChunks2];
+  for (int ch = threadIdx.x; ch < a.chunks2; ch += blockDim.x) {
+    s_res[ch] = __ldcg(&parts[ch].res);
+    s_p[ch] = __ldcg(&parts[ch].p);
+    s_lr[ch] = __ldcg(&parts[ch].last_res);
+    s_lp[ch] = __ldcg(&parts[ch].last_p);
+  }
+  __syncthreads();
   __shared__ int s_chunk, s_use_res, s_fallback;
   __shared__ double s_before, s_target;
   if (threadIdx.x == 0) {
     double zr = 0.0, zp = 0.0;
     int lr = -1, lp = -1;
     for (int ch = 0; ch < a.chunks2; ++ch) {
-      zr += __ldcg(&parts[ch].res);
-      zp += __ldcg(&parts[ch].p);
-      lr = max(lr, __ldcg(&parts[ch].last_res));
-      lp = max(lp, __ldcg(&parts[ch].last_p));
+      zr += s_res[ch];
+      zp += s_p[ch];
+      lr = max(lr, s_lr[ch]);
+      lp = max(lp, s_lp[ch]);
     }
     const int use_res = st.mode == 2 && zr > 0.0;
     const double Z = use_res ? zr : zp;
@@ -309,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
     double acc = 0.0;
     int found = -1;
     for (int ch = 0; ch < a.chunks2; ++ch) {
-      const double m = use_res ? __ldcg(&parts[ch].res) : __ldcg(&parts[ch].p);
+      const double m = use_res ? s_res[ch] : s_p[ch];
       if (target < acc + m) {
         found = ch;
         break;
@@ -327,44 +357,59 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   if (threadIdx.x == 0) s_bonus = s_fallback;
   __syncthreads();
   if (s_chunk >= 0) {
-    // In-order search of the chunk, 256 tokens per round: each round is a
-    // coalesced load and a block-wide inclusive scan of the masses; the first
+    // In-order search of the chunk in one pass: thread t holds tokens
+    // [cb + t*per, cb + (t+1)*per) (loaded at once), a block-wide exclusive
+    // scan of the threads' totals gives each its running start, and the first
     // positive-mass token whose running sum passes the target is the draw.
+    using Tr = LogitTraits<T>;
     const int cb = s_chunk * a.chunk2_elems;
     const int ce = min(a.V, cb + a.chunk2_elems);
     const bool use_res = s_use_res != 0;
+    const TermP tp(st);
+    const T* Lr = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
+    const float* qr = a.draft_probs + size_t(st.row) * a.V;
     __shared__ float wtot[kThreads / 32];
-    __shared__ double s_run;
     __shared__ int s_hit;
-    if (threadIdx.x == 0) {
-      s_run = s_before;
-      s_hit = INT_MAX;
+    if (threadIdx.x == 0) s_hit = INT_MAX;
+    const int per = (ce - cb + int(blockDim.x) - 1) / int(blockDim.x);  // <= kTermPer
+    const int t0 = cb + int(threadIdx.x) * per;
+    float mv[kTermPer];
+    float lv[kTermPer], qv[kTermPer];
+#pragma unroll
+    for (int u = 0; u < kTermPer; ++u) {
+      const int v = t0 + u;
+      const bool in = u < per && v < ce;
+      lv[u] = in ? Tr::load(Lr, v) : -INFINITY;
+      qv[u] = (in && use_res) ? __ldg(qr + v) : 0.f;
+    }
+    float tot = 0.f;
+#pragma unroll
+    for (int u = 0; u < kTermPer; ++u) {
+      const int v = t0 + u;
+      mv[u] = (u < per && v < ce) ? term_mass(tp, use_res, lv[u], qv[u]) : 0.f;
+      tot += mv[u];
+    }
+    float incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wtot[w] = incl;
+    __syncthreads();
+    float before = incl - tot;
+    for (int i = 0; i < w; ++i) before += wtot[i];
+    const float gap = float(s_target - s_before);
+    float run = before;
+#pragma unroll
+    for (int u = 0; u < kTermPer; ++u) {
+      if (mv[u] > 0.f && gap < run + mv[u]) {
+        atomicMin(&s_hit, t0 + u);
+        break;
+      }
+      run += mv[u];
     }
     __syncthreads();
-    for (int r0 = cb; r0 < ce; r0 += blockDim.x) {
-      const int v = r0 + threadIdx.x;
-      const float mv = v < ce ? terminal_mass<T>(a, st, use_res, v) : 0.f;
-      float incl = mv;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) wtot[w] = incl;
-      __syncthreads();
-      float before = 0.f;
-      for (int i = 0; i < w; ++i) before += wtot[i];
-      const float gap = float(s_target - s_run);
-      if (v < ce && mv > 0.f && gap < before + incl) atomicMin(&s_hit, v);
-      __syncthreads();
-      if (s_hit != INT_MAX) break;  // uniform: every thread reads the same value
-      if (threadIdx.x == 0) {
-        float tot = 0.f;
-        for (int i = 0; i < nw; ++i) tot += wtot[i];
-        s_run += double(tot);
-      }
-      __syncthreads();
-    }
     if (threadIdx.x == 0 && s_hit != INT_MAX) s_bonus = s_hit;
     __syncthreads();
   }

@@ -38,7 +38,8 @@
  *     b*n + i of request b's tree node i [ACCEPT section 3].
  *   - Limits: 1 <= k <= 16, k <= V, 1 <= n <= 64, n - 1 <= k + (S-1)*k*k,
  *     S >= 1, head_dim D in {64, 128}, Hq a multiple of Hkv; spec_select_topk
- *     takes V <= 262144 (larger returns SPEC_ERR_UNSUPPORTED).
+ *     and spec_verify_sampling take V <= 262144 (larger returns
+ *     SPEC_ERR_UNSUPPORTED).
  *   - Ties in every top-k / argmax go to the lowest index.
  */
 #ifndef ACCEPT_SELECT_TOP_H
