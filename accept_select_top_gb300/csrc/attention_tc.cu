@@ -19,7 +19,9 @@
 //               four-stage ring with 16-byte cp.async, 128B-swizzled by hand
 //               (the layout a swizzled TMA box would give; per-lane copies
 //               keep far more scattered rows in flight than gather4 does);
-//               warp 0 also gathers each piece's Q rows (tile::gather4);
+//               each also copies 32 of the piece's 128 Q rows the same way
+//               (a tile::gather4 of Q stalled the copies for ~2.7 us a piece:
+//               the TMA unit takes about 42 ns per 4-row gather);
 //   warp 1      MMA issuer (one thread): S = Q K^T (M=128, N=64, K=D) into one
 //               of two TMEM S buffers; O += P V (M=128, N=D, K=64) with both
 //               operands in shared memory, into the piece's O buffer (two);
@@ -34,11 +36,6 @@
 // TMEM columns: O0 [0,128), O1 [128,256), S0 [256,320), S1 [320,384).  Every
 // mbarrier wait is bounded: on timeout the CTA sets SPEC_DEV_TIMEOUT, stops,
 // drains and frees its TMEM.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -49,7 +46,7 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kKeys = 64;
 constexpr int kStages = 4;
-constexpr int kTcThreads = 320;  // warps: 0 lead copy, 1 MMA, 2-5 softmax, 6 7 9 copy, 8 idle
+constexpr int kTcThreads = 320;  // warps: 0 6 7 9 copy, 1 MMA, 2-5 softmax, 8 idle
 constexpr uint32_t kTmemCols = 512;
 // O buffer i at TMEM columns [128 i, 128 i + 128); S buffer b at [256 + 64 b, 320 + 64 b)
 __host__ __device__ constexpr uint32_t col_o(int i) { return 128u * uint32_t(i); }
@@ -98,9 +95,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) { return static_cast
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -126,14 +120,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int y0, int y1, int y2, int y3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
 
 // 16-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -327,13 +313,14 @@ struct PieceIter {
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    attention_tc_kernel(const __grid_constant__ TcArgs args, const __grid_constant__ CUtensorMap tm_q) {
+    attention_tc_kernel(const __grid_constant__ TcArgs args) {
   pdl_trigger();
   using L = Smem<D>;
   const AttentionParams& a = args.p;
   const int G = a.Hq / a.Hkv, M = a.n * G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
+  const unsigned char* qbytes = static_cast<const unsigned char*>(a.q);
   const unsigned char* kbytes = static_cast<const unsigned char*>(a.k_pool);
   const unsigned char* vbytes = static_cast<const unsigned char*>(a.v_pool);
 
@@ -358,7 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(kEmpty0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kQFull0 + i), 1);
+      mbar_init(bar(kQFull0 + i), 4 * 32);  // four copy warps' cp.async arrivals
       mbar_init(bar(kQEmpty0 + i), 1);
       mbar_init(bar(kSFull0 + i), 1);
       mbar_init(bar(kPReady0 + i), kRows);
@@ -463,9 +450,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Four copy warps, one per SM sub-partition (warp & 3), so the copy
     // instructions do not all land next to one softmax warp.  Copy warp
     // `part` looks up and copies keys 16*part .. 16*part+15 of every tile;
-    // warp 0 (the lead) also gathers each piece's Q rows.
+    // each also copies 32 of each piece's 128 Q rows.
     const int part = warp & 3;
-    const bool lead = warp == 0;
+    const bool lead = warp == 0;  // reports a request's bad length or pool row
     // Key 16*part + lane (lanes 0..15) of tile t: slot load issued one tile
     // ahead (issue), value consumed after that tile's copies (finish).
     auto issue = [&](const Piece& pc, int t, int& slot, int& kind) {  // kind: 0 none, 1 prefix, 2 tree
@@ -493,61 +480,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Piece pc;
     int ct = 0, ci = 0;
     bool ok = true;
-    // Slot lookups run two tiles ahead of the copies: cur (row, pre) is the
-    // looked-up tile about to be copied, q1 the lookup already in flight for
-    // the tile after it (also across a piece boundary, for the next piece's
-    // first two tiles).
-    int row = -1, q1s = -1, q1k = 0;
-    bool pre = true, cur_ready = false, q1v = false;
+    // Slot lookups run kLook tiles ahead of the copies, like the copies run
+    // ahead of the MMA: cur (row, pre) is the looked-up tile about to be
+    // copied, ring[j] the lookup in flight for the (j+1)-th tile after it --
+    // across a piece boundary, the next piece's first tiles.
+    constexpr int kLook = 4;
+    int row = -1;
+    bool pre = true, cur_ready = false;
+    int rs[kLook], rk[kLook];
+    bool rv[kLook];
+#pragma unroll
+    for (int j = 0; j < kLook; ++j) {
+      rs[j] = -1;
+      rk[j] = 0;
+      rv[j] = false;
+    }
     while (ok && pit.next(a, args.m_tiles, pc, lead && lane == 0)) {
-      if (lead) {
-        // the piece's Q rows into Q buffer ci % 2, rows 4*lane .. 4*lane+3
+      {
+        // the piece's Q rows into Q buffer ci % 2 (same 16-byte cp.async and
+        // swizzle as K): copy warp `part` copies rows 32*part .. 32*part+31;
+        // padding rows are zero-filled
         const bool q_ok = (ci < 2 || mbar_wait(bar(kQEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
         if (!__all_sync(FULL, q_ok)) {
           if (!*abort_flag) fail();
           break;
         }
-        int y[4];
+        constexpr int kChunks = D / 8;
+        constexpr int kRowsPerOp = 32 / kChunks;
+        const int c = lane % kChunks, rsub = lane / kChunks;
+        const uint32_t qdst = sbase + L::kQ + uint32_t(ci & 1) * L::kQTile + uint32_t(c >> 3) * L::kQBlock;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int rg = pc.mt * kRows + 4 * lane + e;
-          y[e] = rg < M ? (pc.req * a.n + rg / G) * a.Hq + pc.g * G + rg % G : -1;  // -1: zero-filled
+        for (int i = 0; i < 32 / kRowsPerOp; ++i) {
+          const int r = 32 * part + kRowsPerOp * i + rsub;
+          const int rg = pc.mt * kRows + r;
+          const int y = rg < M ? (pc.req * a.n + rg / G) * a.Hq + pc.g * G + rg % G : -1;
+          const uint32_t dst = qdst + uint32_t(r) * 128u + (uint32_t((c & 7) ^ (r & 7)) << 4);
+          const size_t off = size_t(y < 0 ? 0 : y) * (D * 2) + size_t(c) * 16;
+          cp_async16(dst, qbytes + off, y < 0 ? 0u : 16u);
         }
-        if (lane == 0) mbar_expect_tx(bar(kQFull0 + (ci & 1)), L::kQTile);
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_gather4(sbase + L::kQ + (ci & 1) * L::kQTile + h * L::kQBlock + 512u * lane, &tm_q, 64 * h, y[0], y[1],
-                      y[2], y[3], bar(kQFull0 + (ci & 1)));
+        cp_async_arrive(bar(kQFull0 + (ci & 1)));
       }
       if (!cur_ready) {  // tile 0's lookups, unless the previous piece started them
         int s0 = -1, k0 = 0;
         issue(pc, 0, s0, k0);
         finish(pc, s0, k0, row, pre);
       }
-      if (!q1v && pc.T > 1) {
-        issue(pc, 1, q1s, q1k);
-        q1v = true;
-      }
       cur_ready = false;
-      Piece nxt;  // the next piece: its first lookups go out during this piece's last two tiles
+#pragma unroll
+      for (int j = 0; j < kLook; ++j)  // this piece's tiles 1..kLook not yet looked up
+        if (!rv[j] && 1 + j < pc.T) {
+          issue(pc, 1 + j, rs[j], rk[j]);
+          rv[j] = true;
+        }
+      Piece nxt;  // the next piece: its first lookups go out during this piece's last kLook tiles
       bool has_next = false, peeked = false;
       for (int t = 0; t < pc.T; ++t, ++ct) {
         const int s = ct % kStages;
-        if (!peeked && t + 2 >= pc.T) {
+        if (!peeked && t + 1 + kLook >= pc.T) {
           PieceIter peek = pit;
           has_next = peek.next(a, args.m_tiles, nxt, false);
           peeked = true;
+#pragma unroll
+          for (int j = 0; j < kLook; ++j) {  // ring slots that fall in the next piece
+            const int x = t + 1 + j - pc.T;
+            if (!rv[j] && x >= 0 && has_next && x < nxt.T) {
+              issue(nxt, x, rs[j], rk[j]);
+              rv[j] = true;
+            }
+          }
         }
-        // the lookup for the tile two ahead
-        int q2s = -1, q2k = 0;
-        bool q2v = false;
-        if (t + 2 < pc.T) {
-          issue(pc, t + 2, q2s, q2k);
-          q2v = true;
-        } else if (has_next && t + 2 - pc.T < min(nxt.T, 2)) {
-          issue(nxt, t + 2 - pc.T, q2s, q2k);
-          q2v = true;
+        // the lookup for the tile kLook+1 ahead
+        int ns = -1, nk = 0;
+        bool nv = false;
+        {
+          const int x = t + 1 + kLook;
+          if (x < pc.T) {
+            issue(pc, x, ns, nk);
+            nv = true;
+          } else if (has_next && x - pc.T < nxt.T) {
+            issue(nxt, x - pc.T, ns, nk);
+            nv = true;
+          }
         }
         const bool e_ok = (ct < kStages || mbar_wait(bar(kEmpty0 + s), ((ct / kStages) - 1) & 1)) && !*abort_flag;
         if (!__all_sync(FULL, e_ok)) {
@@ -580,17 +593,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cp_async16(dst + L::kKTile, vbytes + off, nb);
         }
         cp_async_arrive(bar(kFull0 + s));
-        // the next tile's lookup, issued an iteration ago, becomes cur
+        // the next tile's lookup (the ring's head) becomes cur
         if (t + 1 < pc.T) {
-          finish(pc, q1s, q1k, row, pre);
+          if (!rv[0]) issue(pc, t + 1, rs[0], rk[0]);  // (not reached: the ring holds it)
+          finish(pc, rs[0], rk[0], row, pre);
         } else if (has_next) {
-          if (!q1v) issue(nxt, 0, q1s, q1k);  // (only when this piece had a single tile)
-          finish(nxt, q1s, q1k, row, pre);
+          if (!rv[0]) issue(nxt, 0, rs[0], rk[0]);
+          finish(nxt, rs[0], rk[0], row, pre);
           cur_ready = true;
         }
-        q1s = q2s;
-        q1k = q2k;
-        q1v = q2v;
+#pragma unroll
+        for (int j = 0; j + 1 < kLook; ++j) {
+          rs[j] = rs[j + 1];
+          rk[j] = rk[j + 1];
+          rv[j] = rv[j + 1];
+        }
+        rs[kLook - 1] = ns;
+        rk[kLook - 1] = nk;
+        rv[kLook - 1] = nv;
       }
       ++ci;
     }
@@ -633,6 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = false;
           break;
         }
+        fence_proxy_async();  // Q was written by cp.async
         const uint32_t qbase = sbase + L::kQ + (ci & 1) * L::kQTile;
         for (int t = 0; t < pc.T; ++t, ++ct) {
           const int s = ct % kStages;
@@ -999,37 +1020,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 2D bf16 view [rows, D] (row pitch D*2 bytes), boxes of 64 columns x 1 row,
-// 128B swizzle: the tile::gather4 operand.
-bool encode_rows(CUtensorMap* m, const void* base, long long rows, int D) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 int launch_t(const AttentionParams& p, const TcGeometry& geo, cudaStream_t stream) {
-  alignas(64) CUtensorMap tq;
-  if (!encode_rows(&tq, p.q, (long long)p.b * p.n * p.Hq, D)) return SPEC_ERR_LAUNCH;
   // at least 120 KB, so that two CTAs never share an SM (each holds all 512
   // TMEM columns)
   const int smem = Smem<D>::kBytes + 1024 > 120 * 1024 ? Smem<D>::kBytes + 1024 : 120 * 1024;
@@ -1049,7 +1041,7 @@ int launch_t(const AttentionParams& p, const TcGeometry& geo, cudaStream_t strea
               reinterpret_cast<float*>(base + kSlotOOffset),
               reinterpret_cast<float*>(base + kSlotMLOffset)};
   const int grid = sm_count < kMaxCtas ? sm_count : kMaxCtas;
-  const cudaError_t e = launch_pdl(attention_tc_kernel<D>, dim3(grid), dim3(kTcThreads), smem, stream, args, tq);
+  const cudaError_t e = launch_pdl(attention_tc_kernel<D>, dim3(grid), dim3(kTcThreads), smem, stream, args);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
