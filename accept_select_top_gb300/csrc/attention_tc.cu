@@ -19,9 +19,6 @@
 //               four-stage ring with 16-byte cp.async, 128B-swizzled by hand
 //               (the layout a swizzled TMA box would give; per-lane copies
 //               keep far more scattered rows in flight than gather4 does);
-//               each also copies 32 of the piece's 128 Q rows the same way
-//               (a tile::gather4 of Q stalled the copies for ~2.7 us a piece:
-//               the TMA unit takes about 42 ns per 4-row gather);
 //   warp 1      MMA issuer (one thread): S = Q K^T (M=128, N=64, K=D) into one
 //               of two TMEM S buffers; O += P V (M=128, N=D, K=64) with both
 //               operands in shared memory, into the piece's O buffer (two);
@@ -29,7 +26,12 @@
 //               (tcgen05.ld), P as bf16 into one of two shared-memory P
 //               buffers (128B-swizzled, K-major), lazy rescaling of O in TMEM,
 //               and the piece's epilogue;
-//   warp 8      idle.
+//   warp 8      Q rows: copies each piece's real query rows into one of two
+//               Q buffers as soon as it frees (issuing a piece's Q took the
+//               copy warp ~4000 cycles under load, which drained the K/V
+//               ring at every piece boundary); and counts the CTA's split
+//               pieces in on their units (fence + atomic), which kept the
+//               softmax rows waiting when they did it themselves.
 // P goes through shared memory rather than TMEM because an MMA that reads its
 // A operand from TMEM measured about three times slower on this part than the
 // same MMA reading shared memory.
@@ -46,7 +48,7 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kKeys = 64;
 constexpr int kStages = 4;
-constexpr int kTcThreads = 320;  // warps: 0 6 7 9 copy, 1 MMA, 2-5 softmax, 8 idle
+constexpr int kTcThreads = 320;  // warps: 0 6 7 9 copy, 1 MMA, 2-5 softmax, 8 Q rows
 constexpr uint32_t kTmemCols = 512;
 // O buffer i at TMEM columns [128 i, 128 i + 128); S buffer b at [256 + 64 b, 320 + 64 b)
 __host__ __device__ constexpr uint32_t col_o(int i) { return 128u * uint32_t(i); }
@@ -83,8 +85,9 @@ enum {
   kPReady0 = kSFull0 + 2,
   kOFree0 = kPReady0 + 2,
   kODone0 = kOFree0 + 2,  // + (PV index & 1): two barriers, so no wait is ever two phases behind
-  kSmGroup = kODone0 + 2,  // the 128 softmax threads meet (merge of split units)
-  kDrain,
+  kPub0 = kODone0 + 2,  // + k: the 128 softmax rows stored the CTA's k-th split piece (k < 2; one phase each)
+  kDrain = kPub0 + 2,
+  kQIssued,  // the first piece's Q copies are issued (the K/V copies queue behind them)
   kNumBars
 };
 
@@ -117,6 +120,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   const long long start = clock64();
   while (clock64() - start < kWaitCycles)
     if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// the same bound, for a warp off the critical path that may wait a whole
+// piece: it sleeps between polls so that it takes no issue slots from the
+// copy and softmax warps of its sub-partition
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (clock64() - start < kWaitCycles && !*abort_flag) {
+    __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+  }
   return false;
 }
 
@@ -338,6 +353,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // split units this CTA merges at the end: count, then (unit_start, Tr, req, g, mt, c1, c2, -) each
   int* merges = reinterpret_cast<int*>(sp + L::kScratch + 8 * 24);
   constexpr int kMaxMerges = 2;  // a CTA finishes at most its first and its last piece
+  // split pieces of this CTA awaiting their arrival: (unit_start, Tr, req, g, mt, -, -, -) each
+  int* pend = merges + 1 + 8 * kMaxMerges;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -345,15 +362,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(kEmpty0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kQFull0 + i), 4 * 32);  // four copy warps' cp.async arrivals
+      mbar_init(bar(kQFull0 + i), 32);  // the Q warp's cp.async arrivals
       mbar_init(bar(kQEmpty0 + i), 1);
       mbar_init(bar(kSFull0 + i), 1);
       mbar_init(bar(kPReady0 + i), kRows);
       mbar_init(bar(kOFree0 + i), kRows);
       mbar_init(bar(kODone0 + i), 1);
     }
-    mbar_init(bar(kSmGroup), kRows);
+    mbar_init(bar(kPub0), kRows);
+    mbar_init(bar(kPub0 + 1), kRows);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kQIssued), 1);
     *abort_flag = 0;
     merges[0] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -449,8 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ producers ============================
     // Four copy warps, one per SM sub-partition (warp & 3), so the copy
     // instructions do not all land next to one softmax warp.  Copy warp
-    // `part` looks up and copies keys 16*part .. 16*part+15 of every tile;
-    // each also copies 32 of each piece's 128 Q rows.
+    // `part` looks up and copies keys 16*part .. 16*part+15 of every tile.
     const int part = warp & 3;
     const bool lead = warp == 0;  // reports a request's bad length or pool row
     // Key 16*part + lane (lanes 0..15) of tile t: slot load issued one tile
@@ -496,42 +514,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       rv[j] = false;
     }
     while (ok && pit.next(a, args.m_tiles, pc, lead && lane == 0)) {
-      {
-        // the piece's Q rows into Q buffer ci % 2 (same 16-byte cp.async and
-        // swizzle as K): copy warp `part` copies rows 32*part .. 32*part+31;
-        // padding rows are zero-filled
-        const bool q_ok = (ci < 2 || mbar_wait(bar(kQEmpty0 + (ci & 1)), ((ci >> 1) - 1) & 1)) && !*abort_flag;
-        if (!__all_sync(FULL, q_ok)) {
-          if (!*abort_flag) fail();
-          break;
-        }
-        constexpr int kChunks = D / 8;
-        constexpr int kRowsPerOp = 32 / kChunks;
-        const int c = lane % kChunks, rsub = lane / kChunks;
-        const uint32_t qdst = sbase + L::kQ + uint32_t(ci & 1) * L::kQTile + uint32_t(c >> 3) * L::kQBlock;
-#pragma unroll
-        for (int i = 0; i < 32 / kRowsPerOp; ++i) {
-          const int r = 32 * part + kRowsPerOp * i + rsub;
-          const int rg = pc.mt * kRows + r;
-          const int y = rg < M ? (pc.req * a.n + rg / G) * a.Hq + pc.g * G + rg % G : -1;
-          const uint32_t dst = qdst + uint32_t(r) * 128u + (uint32_t((c & 7) ^ (r & 7)) << 4);
-          const size_t off = size_t(y < 0 ? 0 : y) * (D * 2) + size_t(c) * 16;
-          cp_async16(dst, qbytes + off, y < 0 ? 0u : 16u);
-        }
-        cp_async_arrive(bar(kQFull0 + (ci & 1)));
-      }
-      if (!cur_ready) {  // tile 0's lookups, unless the previous piece started them
-        int s0 = -1, k0 = 0;
-        issue(pc, 0, s0, k0);
-        finish(pc, s0, k0, row, pre);
-      }
-      cur_ready = false;
+      int s0 = -1, k0 = 0;
+      if (!cur_ready) issue(pc, 0, s0, k0);  // tile 0's lookups, unless the previous piece started them
 #pragma unroll
       for (int j = 0; j < kLook; ++j)  // this piece's tiles 1..kLook not yet looked up
         if (!rv[j] && 1 + j < pc.T) {
           issue(pc, 1 + j, rs[j], rk[j]);
           rv[j] = true;
         }
+      if (!cur_ready) finish(pc, s0, k0, row, pre);
+      cur_ready = false;
       Piece nxt;  // the next piece: its first lookups go out during this piece's last kLook tiles
       bool has_next = false, peeked = false;
       for (int t = 0; t < pc.T; ++t, ++ct) {
@@ -564,6 +556,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const bool e_ok = (ct < kStages || mbar_wait(bar(kEmpty0 + s), ((ct / kStages) - 1) & 1)) && !*abort_flag;
         if (!__all_sync(FULL, e_ok)) {
+          if (!*abort_flag) fail();
+          ok = false;
+          break;
+        }
+        if (ct == 0 && !__all_sync(FULL, mbar_wait(bar(kQIssued), 0))) {
           if (!*abort_flag) fail();
           ok = false;
           break;
@@ -615,6 +612,109 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++ci;
     }
     // drain: every copy this warp issued has landed before the CTA can exit
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == 8) {
+    // ============================ Q rows ============================
+    // Each piece's Q rows go into Q buffer ci % 2 as soon as the MMA is done
+    // with the piece two back, so neither the K/V copies nor the MMA wait
+    // on them.  Only real query rows are copied (same 16-byte cp.async and
+    // swizzle as K).  The rows past them keep whatever they hold: their S
+    // rows are never read as output, their P rows are written as zeros (a
+    // padding row is never live), so their O rows stay out of every result.
+    // The first piece's Q goes out before any K/V copy, so that the first
+    // QK does not wait behind four stages of K/V.
+    //   The same warp counts this CTA's split pieces (its first and last at
+    // most) in on their units: once the softmax rows have stored a piece's
+    // partial and arrived, lane 0 fences (covering those stores, which the
+    // barrier ordered before it) and adds one to the unit's counter; the
+    // piece arriving last records the unit, and the whole CTA merges it
+    // after teardown.  A piece is counted in after the Q of the piece two
+    // later is out, which is the order the two events come in.
+    PieceIter pit = start_iter();
+    Piece pc;
+    int ci = 0;
+    int nsplit = 0, npub = 0;  // split pieces seen / counted in
+    int split_ci0 = 0, split_ci1 = 0;  // their piece ordinals
+    auto publish = [&]() -> bool {
+      const bool w = mbar_wait_idle(bar(kPub0 + npub), 0, abort_flag);
+      if (!__all_sync(FULL, w)) return false;
+      if (lane == 0) {
+        const int* e = pend + 8 * npub;
+        const int c1 = cta_of(e[0], T_all, G_eff);
+        const int c2 = cta_of((long long)e[0] + e[1] - 1, T_all, G_eff);
+        __threadfence();
+        if (atomicAdd(args.counters + c1, 1u) == uint32_t(c2 - c1) && merges[0] < kMaxMerges) {
+          __threadfence();  // the other pieces' partials, read in the merge
+          int* m = merges + 1 + 8 * merges[0];
+          for (int k = 0; k < 5; ++k) m[k] = e[k];
+          m[5] = c1;
+          m[6] = c2;
+          merges[0] += 1;
+        }
+      }
+      ++npub;
+      return true;
+    };
+    bool q_run = true;
+    constexpr int kChunks = D / 8;
+    constexpr int kRowsPerOp = 32 / kChunks;
+    const int c = lane % kChunks, rsub = lane / kChunks;
+    while (pit.next(a, args.m_tiles, pc, false)) {
+      const int b = ci & 1;
+      if (!pc.complete && nsplit < kMaxMerges) {
+        if (lane == 0) {
+          int* e = pend + 8 * nsplit;
+          e[0] = int(pc.unit_start);  // tile space fits in int: < 2^31 tiles
+          e[1] = pc.Tr;
+          e[2] = pc.req;
+          e[3] = pc.g;
+          e[4] = pc.mt;
+        }
+        if (nsplit == 0) split_ci0 = ci;
+        else split_ci1 = ci;
+        ++nsplit;
+      }
+      const bool q_ok = (ci < 2 || mbar_wait_idle(bar(kQEmpty0 + b), ((ci >> 1) - 1) & 1, abort_flag)) && !*abort_flag;
+      if (!__all_sync(FULL, q_ok)) {
+        q_run = false;
+        break;
+      }
+      const int v = min(kRows, M - pc.mt * kRows);  // real query rows of the tile
+      const uint32_t qdst = sbase + L::kQ + uint32_t(b) * L::kQTile + uint32_t(c >> 3) * L::kQBlock;
+      // row r = query (token tok, head h of the group): one division per
+      // piece, then stepped (a runtime divide per row cost ~200 cycles)
+      const int rg0 = pc.mt * kRows + rsub;
+      int tok = rg0 / G, h = rg0 - (rg0 / G) * G;
+      const long long qbase = (long long)pc.req * a.n;
+#pragma unroll 4
+      for (int r0 = 0; r0 < v; r0 += kRowsPerOp) {
+        const int r = r0 + rsub;
+        if (r < v) {
+          const size_t y = size_t((qbase + tok) * a.Hq + pc.g * G + h);
+          const uint32_t dst = qdst + uint32_t(r) * 128u + (uint32_t((c & 7) ^ (r & 7)) << 4);
+          cp_async16(dst, qbytes + y * (D * 2) + size_t(c) * 16, 16u);
+        }
+        h += kRowsPerOp;
+        while (h >= G) {  // at most kRowsPerOp steps
+          h -= G;
+          ++tok;
+        }
+      }
+      cp_async_arrive(bar(kQFull0 + b));
+      if (ci == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kQIssued));
+      }
+      if (npub < nsplit && (npub == 0 ? split_ci0 : split_ci1) <= ci - 2 && !publish()) {
+        q_run = false;
+        break;
+      }
+      ++ci;
+    }
+    if (ci == 0 && lane == 0) mbar_arrive(bar(kQIssued));  // (no piece, or stopped)
+    while (q_run && npub < nsplit)
+      if (!publish()) q_run = false;
+    if (!q_run && !*abort_flag) fail();
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
@@ -708,15 +808,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sl2 = a.scale * 1.4426950408889634f;
     PieceIter pit = start_iter();
     Piece pc;
-    int ct = 0, ci = 0, gph = 0;
+    int ct = 0, ci = 0, nsp = 0;  // nsp: split pieces so far
     bool ok = true;
-    // the 128 softmax threads meet (bounded wait, so a timeout never hangs)
-    auto group_sync = [&]() -> bool {
-      mbar_arrive(bar(kSmGroup));
-      const bool w_ok = mbar_wait(bar(kSmGroup), gph & 1);
-      ++gph;
-      return __all_sync(FULL, w_ok);
-    };
     while (ok && pit.next(a, args.m_tiles, pc, false)) {
       const int rg = pc.mt * kRows + r;
       const bool valid = rg < M;
@@ -854,33 +947,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (pc.complete) {
         if (valid && a.lse) a.lse[orow] = lsum > 0.f ? (m_ref + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
       } else {
-        // split unit: publish this piece; the piece arriving last records the
-        // unit, and the whole CTA merges it once the pipeline is done
+        // split unit: this piece's partial (O above, then m and l); the Q
+        // warp, once all 128 rows arrive, fences and counts the piece in on
+        // its unit, off this path
         if (valid) {
           float* sml = args.slot_ml + (size_t(slot) * kRows + r) * 2;
           sml[0] = m_ref;
           sml[1] = lsum;
         }
-        __threadfence();
-        if (!group_sync()) {
-          ok = false;
-          break;
-        }
-        if (r == 0) {
-          const int c1 = cta_of(pc.unit_start, T_all, G_eff);
-          const int c2 = cta_of(pc.unit_start + pc.Tr - 1, T_all, G_eff);
-          if (atomicAdd(args.counters + c1, 1u) == uint32_t(c2 - c1) && merges[0] < kMaxMerges) {
-            int* m = merges + 1 + 8 * merges[0];
-            m[0] = int(pc.unit_start);  // tile space fits in int: < 2^31 tiles
-            m[1] = pc.Tr;
-            m[2] = pc.req;
-            m[3] = pc.g;
-            m[4] = pc.mt;
-            m[5] = c1;
-            m[6] = c2;
-            merges[0] += 1;
-          }
-        }
+        if (nsp < kMaxMerges) mbar_arrive(bar(kPub0 + nsp));  // release (CTA scope): the stores above come first
+        ++nsp;
       }
       ++ci;
     }
