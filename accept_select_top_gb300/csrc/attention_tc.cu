@@ -625,10 +625,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // QK does not wait behind four stages of K/V.
     //   The same warp counts this CTA's split pieces (its first and last at
     // most) in on their units: once the softmax rows have stored a piece's
-    // partial and arrived, lane 0 fences (covering those stores, which the
-    // barrier ordered before it) and adds one to the unit's counter; the
-    // piece arriving last records the unit, and the whole CTA merges it
-    // after teardown.  A piece is counted in after the Q of the piece two
+    // partial and arrived (release, CTA scope), lane 0 adds one to the
+    // unit's counter with an acquire-release atomic at GPU scope, whose
+    // release covers those stores; the piece arriving last records the unit
+    // (its acquire covers every other piece's partial, and the teardown
+    // barrier passes that on to the whole CTA, which merges it).  A piece is counted in after the Q of the piece two
     // later is out, which is the order the two events come in.
     PieceIter pit = start_iter();
     Piece pc;
@@ -642,9 +643,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int* e = pend + 8 * npub;
         const int c1 = cta_of(e[0], T_all, G_eff);
         const int c2 = cta_of((long long)e[0] + e[1] - 1, T_all, G_eff);
-        __threadfence();
-        if (atomicAdd(args.counters + c1, 1u) == uint32_t(c2 - c1) && merges[0] < kMaxMerges) {
-          __threadfence();  // the other pieces' partials, read in the merge
+        if (atom_add_acq_rel(args.counters + c1) == uint32_t(c2 - c1) && merges[0] < kMaxMerges) {
           int* m = merges + 1 + 8 * merges[0];
           for (int k = 0; k < 5; ++k) m[k] = e[k];
           m[5] = c1;
@@ -984,11 +983,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const long long ustart = m[0];
     const int mreq = m[2], mg = m[3], mmt = m[4], c1 = m[5], c2 = m[6];
     const int np = c2 - c1 + 1;
-    __threadfence();
     auto slot_of = [&](int c) { return 2 * c + ((c == c1 && cta_start(c1, T_all, G_eff) < ustart) ? 1 : 0); };
     const int rows = min(kRows, M - mmt * kRows);
     const float2* ml2 = reinterpret_cast<const float2*>(args.slot_ml);
-    if (np <= wcap) {
+    constexpr int C4 = D / 4;
+    static_assert(32 % C4 == 0, "a warp instruction covers whole output rows");
+    if (np <= 2) {
+      // the common split (a unit over two CTAs): each warp takes a block of
+      // rows and issues every load for them -- both pieces' (m, l) and O --
+      // before using any, so the merge is one round trip; no shared memory,
+      // no block barrier.  Lane: row offset lane / C4, 4 columns lane % C4.
+      constexpr int kRPI = 32 / C4;  // rows per warp instruction
+      constexpr int kRB = 8;         // warp instructions per piece per batch
+      const int rsub = lane / C4, c4 = lane % C4;
+      const int per_warp = (rows + kTcThreads / 32 - 1) / (kTcThreads / 32);
+      const int w0 = warp * per_warp, w1 = min(rows, w0 + per_warp);
+      const int s0 = slot_of(c1), s1 = np > 1 ? slot_of(c1 + 1) : s0;
+      const float4* o4s = reinterpret_cast<const float4*>(args.slot_o);
+      for (int r0 = w0; r0 < w1; r0 += kRPI * kRB) {
+        float2 m0[kRB], m1[kRB];
+        float4 o0[kRB], o1[kRB];
+#pragma unroll
+        for (int i = 0; i < kRB; ++i) {
+          const int rr = r0 + i * kRPI + rsub;
+          const bool on = rr < w1;
+          m0[i] = on ? __ldcg(ml2 + size_t(s0) * kRows + rr) : make_float2(-INFINITY, 0.f);
+          o0[i] = on ? __ldcg(o4s + (size_t(s0) * kRows + rr) * C4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          m1[i] = on && np > 1 ? __ldcg(ml2 + size_t(s1) * kRows + rr) : make_float2(-INFINITY, 0.f);
+          o1[i] = on && np > 1 ? __ldcg(o4s + (size_t(s1) * kRows + rr) * C4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kRB; ++i) {
+          const int rr = r0 + i * kRPI + rsub;
+          if (rr < w1) {
+            float Mx = -INFINITY;
+            if (m0[i].y > 0.f) Mx = m0[i].x;
+            if (m1[i].y > 0.f) Mx = fmaxf(Mx, m1[i].x);
+            const float wa = m0[i].y > 0.f ? exp2f(m0[i].x - Mx) : 0.f;
+            const float wb = m1[i].y > 0.f ? exp2f(m1[i].x - Mx) : 0.f;
+            const float Ls = m0[i].y * wa + m1[i].y * wb;
+            const float li = Ls > 0.f ? 1.f / Ls : 0.f;
+            const float ka = wa * li, kb = wb * li;
+            const int rg = mmt * kRows + rr;
+            const size_t orow = (size_t(mreq) * a.n + rg / G) * a.Hq + mg * G + rg % G;
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * D + 4 * c4) =
+                make_uint2(pack_bf16(ka * o0[i].x + kb * o1[i].x, ka * o0[i].y + kb * o1[i].y),
+                           pack_bf16(ka * o0[i].z + kb * o1[i].z, ka * o0[i].w + kb * o1[i].w));
+            if (c4 == 0 && a.lse) a.lse[orow] = Ls > 0.f ? (Mx + log2f(Ls)) * 0.6931471805599453f : -INFINITY;
+          }
+        }
+      }
+    } else if (np <= wcap) {
       // per row: the largest running max, each piece's weight, 1 / total
       // ((m, l) pairs loaded eight pieces at a time)
       for (int rr = threadIdx.x; rr < rows; rr += blockDim.x) {
@@ -1022,7 +1067,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncthreads();
       // every (row, 4 columns) of the output: the weighted sum over pieces;
       // each thread loads its whole share of one piece before using any of it
-      constexpr int C4 = D / 4;
       constexpr int U = (kRows * C4 + kTcThreads - 1) / kTcThreads;
       const int total = rows * C4;
       float4 acc[U];

@@ -154,6 +154,12 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 // Returns true in every thread of the CTA that arrives last among `total` CTAs
 // sharing `counter`.  Call after the CTA's partial result is written.  The last
 // CTA must reset the counter (counter_reset) once it is done.
+// counter += 1 with acquire-release order at GPU scope; returns the old value
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* counter) {
+  uint32_t prev;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
+  return prev;
+}
 __device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t total) {
   __shared__ int s_last;
   // The barrier orders every thread's partial writes before thread 0's
@@ -161,11 +167,7 @@ __device__ __forceinline__ bool arrive_last(uint32_t* counter, uint32_t total) {
   // count complete also sees every other CTA's partials (read after the
   // second barrier).
   __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t prev;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
-    s_last = prev == total - 1;
-  }
+  if (threadIdx.x == 0) s_last = atom_add_acq_rel(counter) == total - 1;
   __syncthreads();
   return s_last;
 }
