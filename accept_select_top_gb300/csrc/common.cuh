@@ -86,19 +86,29 @@ struct LogitTraits<uint16_t> {  // bf16 bit patterns
 // Streaming 16-byte load: the logits are read once per step.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 
-// (value, index) argmax across a warp; every lane ends with the winner.
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
+// Order-preserving key of a float for the unsigned warp reductions: a larger
+// key is a larger value; -0 counts as +0 (they compare equal) and NaN ranks
+// below everything.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  v = v + 0.0f;  // -0 -> +0
+  const uint32_t b = __float_as_uint(v);
+  if (v != v) return 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// (value, index) argmax across a warp, in the order of better(); every lane
+// ends with the winner.  Two warp reductions (redux.sync): the largest key,
+// then the smallest index among the lanes that hold it.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+  const uint32_t key = order_key(v);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  const uint32_t imin = __reduce_min_sync(0xffffffffu, key == kmax ? uint32_t(i) : 0xffffffffu);
+  v = key_value(kmax);
+  i = int(imin);
+}
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialisation (launch_pdl): it lets the grid
 // that follows be scheduled early (pdl_trigger, first thing in each kernel),
@@ -134,11 +144,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  return key_value(__reduce_max_sync(0xffffffffu, order_key(v)));
 }
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
