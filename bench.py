@@ -515,12 +515,13 @@ def main(argv=None):
     roof = None
     if stage is not None:
         dom = max(stage, key=stage.get)
-        sources = {"attention": ["accept_select_top_gb300/csrc/attention_tc.cu"],
+        common = "accept_select_top_gb300/csrc/common.cuh"  # helpers compiled into every kernel
+        sources = {"attention": ["accept_select_top_gb300/csrc/attention_tc.cu", common],
                    "select_build": ["accept_select_top_gb300/csrc/select_topk.cu",
-                                    "accept_select_top_gb300/csrc/build_tree.cu"],
+                                    "accept_select_top_gb300/csrc/build_tree.cu", common],
                    "accept_commit": ["accept_select_top_gb300/csrc/verify_greedy.cu",
                                      "accept_select_top_gb300/csrc/verify_sampling.cu",
-                                     "accept_select_top_gb300/csrc/commit_kv.cu"]}[dom]
+                                     "accept_select_top_gb300/csrc/commit_kv.cu", common]}[dom]
         flops = attention_flops(wl, lay, mask_bits)
         tensor_bound = dom == "attention" and flops / bytes_["attention"] > \
             peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
