@@ -167,6 +167,26 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
     }
     if (a.parent_blk)
       for (int j = threadIdx.x; j <= k; j += blockDim.x) a.parent_blk[size_t(req) * a.parent_ld + j] = j - 1;
+  } else if (w == 0 && kk <= 32) {
+    // lane f: expansion f = (parent f / k, its j = f % k); rank among the k*k
+    // by shuffles
+    const bool on = lane < kk;
+    const float ex = on ? __fmul_rn(sc_in, p_s[lane / k][lane % k]) : -INFINITY;
+    const int id = on ? id_s[lane / k][lane % k] : 0;
+    if (on) {
+      a.score_blk[sb + lane] = ex;
+      a.token_blk[sb + lane] = id;
+    }
+    int rank = 0;
+    for (int g = 0; g < kk; ++g) {
+      const float o = __shfl_sync(0xffffffffu, ex, g);
+      rank += better(o, g, ex, lane) ? 1 : 0;
+    }
+    if (on && rank < k) {
+      if (a.parent_blk) a.parent_blk[size_t(req) * a.parent_ld + rank] = lane + kk * (a.step - 1) + k;
+      a.scores_out[size_t(req) * k + rank] = ex;
+      a.next_ids[size_t(req) * k + rank] = id;
+    }
   } else if (w == 0) {
     __shared__ float ex[kMaxK * kMaxK];
     for (int f = lane; f < kk; f += 32) {
@@ -201,38 +221,62 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   const T* lrow = static_cast<const T*>(a.logits) + size_t(row) * a.V;
   const float c = 1.4426950408889634f / a.temperature;  // log2(e) / T
 
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  constexpr int kCap = 512;
+  __shared__ float cand_v[kCap];
+  __shared__ int cand_i[kCap];
+  __shared__ int cand_n;
+  if (threadIdx.x == 0) cand_n = 0;  // first used after the barrier below
+
   // this thread's share of the chunk, in registers
   float f[kPerThread];
   load_share<T>(lrow, begin, end, a.vec_ok, f);
   float tm = -INFINITY;
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) tm = fmaxf(tm, f[j]);
-  // online-softmax partial of the share: max m and sum of exp((x - m) / T)
-  const float m = fmaxf(tm, -3.0e38f);
+  // The warp's max Mw, and the warp's sum of exp((x - Mw) / T): every exponent
+  // is <= 0, and a warp with no element (past the row's end) sums to 0.
+  const float Mw = warp_max(tm);
+  const float mref = fmaxf(Mw, -3.0e38f);
   float s = 0.f;
 #pragma unroll
-  for (int j = 0; j < kPerThread; ++j) s += fast_exp2((f[j] - m) * c);
-  // Pruning threshold: a warp's k-th largest thread maximum tau_w stands for k
-  // distinct elements >= tau_w, so no element below max_w tau_w can be among
-  // the chunk's k best; only elements >= that bound enter the top-K lists.
+  for (int j = 0; j < kPerThread; ++j) s += fast_exp2((f[j] - mref) * c);
+  s = warp_sum(s);
+  __shared__ float wmax[kThreads / 32], wsum[kThreads / 32];
   __shared__ float tau_w[kThreads / 32];
-  {
+  if (lane == 0) {
+    wmax[w] = Mw;
+    wsum[w] = s;
+  }
+  if (a.k > nw) {
+    // more picks than warps: a warp's k-th largest thread maximum stands
+    // for k distinct elements at or above it
     const float kth = warp_kth_largest(tm, a.k);
-    if ((threadIdx.x & 31) == 0) tau_w[threadIdx.x >> 5] = kth;
+    if (lane == 0) tau_w[w] = kth;
   }
   __syncthreads();
+  // Pruning bound tau: no element below it can be among the chunk's k best.
+  // With k <= warps it is the k-th largest warp maximum (k distinct
+  // elements, in k different warps, reach it): each warp ranks the nw warp
+  // maxima by shuffles, with no dependent rounds.
   float tau = -INFINITY;
-  for (int w = 0; w < int(blockDim.x >> 5); ++w) tau = fmaxf(tau, tau_w[w]);
+  if (a.k <= nw) {
+    const float v = lane < nw ? wmax[lane] : -INFINITY;
+    int rank = 0;
+    for (int q = 0; q < nw; ++q) {
+      const float o = __shfl_sync(0xffffffffu, v, q);
+      rank += (o > v || (o == v && q < lane)) ? 1 : 0;
+    }
+    const unsigned at = __ballot_sync(0xffffffffu, lane < nw && rank == a.k - 1);
+    tau = __shfl_sync(0xffffffffu, v, at ? __ffs(at) - 1 : 0);
+    if (!at) tau = -INFINITY;
+  } else {
+    for (int q = 0; q < nw; ++q) tau = fmaxf(tau, tau_w[q]);
+  }
   // Common case: few elements reach tau; they are appended to a shared
-  // candidate list and one warp picks the K best in K rounds.  Heavy ties can
-  // overflow the list, and then every thread keeps its own sorted top-K and the
-  // lists are merged (the general path).
-  constexpr int kCap = 512;
-  __shared__ float cand_v[kCap];
-  __shared__ int cand_i[kCap];
-  __shared__ int cand_n;
-  if (threadIdx.x == 0) cand_n = 0;
-  __syncthreads();
+  // candidate list and ranked.  Heavy ties can overflow the list, and then
+  // every thread keeps its own sorted top-K and the lists are merged (the
+  // general path).
   if (tm >= tau) {
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j)
@@ -244,21 +288,20 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
         }
       }
   }
-  // softmax statistics of the CTA
-  __shared__ float wm[kThreads / 32], ws_[kThreads / 32];
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  {
-    float M = warp_max(m);
-    float sc = s * exp2f((m - M) * c);
-    sc = warp_sum(sc);
-    if (lane == 0) {
-      wm[w] = M;
-      ws_[w] = sc;
-    }
-  }
   __syncthreads();
   SelPart* part = reinterpret_cast<SelPart*>(a.partials) + size_t(row) * a.chunks + chunk;
   const int ncand = cand_n;
+  if (w == nw - 1) {
+    // the chunk's softmax statistics from the warps' (Mw, sum): one warp
+    const float wm = lane < nw ? wmax[lane] : -INFINITY;
+    const float M = fmaxf(warp_max(wm), -3.0e38f);
+    const float t = lane < nw ? wsum[lane] * exp2f((fmaxf(wm, -3.0e38f) - M) * c) : 0.f;
+    const float S = warp_sum(t);
+    if (lane == 0) {
+      part->m = M;
+      part->s = S;
+    }
+  }
   if (ncand <= int(blockDim.x)) {
     // one candidate per thread: its rank among the candidates (a strict
     // order: no NaN passes the threshold, indices are distinct) is its slot
@@ -323,89 +366,64 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
       }
     }
   }
-  if (threadIdx.x == 0) {
-    float M = -3.0e38f;
-    for (int i = 0; i < nw; ++i) M = fmaxf(M, wm[i]);
-    float sc = 0.f;
-    for (int i = 0; i < nw; ++i) sc += ws_[i] * exp2f((wm[i] - M) * c);
-    part->m = M;
-    part->s = sc;
-  }
 
   if (!arrive_last(a.counters + req, uint32_t(rows_per_req * a.chunks))) return;
 
   // ---- finalize request `req` ----
-  // Every load of the finalize is issued before any of them is used (one
-  // round trip through L2: the partials were written by other CTAs), then
-  // one warp per row works from registers and shared memory.
+  // One warp per row: lane l holds chunk l's (m, s) and sorted top-K list in
+  // registers (every load issued before any is used: one round trip through
+  // L2, the partials were written by other CTAs); k rounds of a tournament
+  // over the lanes' list heads give the row's k best, lane j keeping the
+  // j-th.  Then the path step of the request.
   const int k = a.k, kk = k * k;
+  // this lane's parent score for the path step (lane f < k*k: parent f / k)
   const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
-  __shared__ float heads_v[kThreads / 32][kMaxChunks * K];  // one warp per row
-  __shared__ int heads_i[kThreads / 32][kMaxChunks * K];
   __shared__ float p_s[kMaxK][kMaxK];
   __shared__ int id_s[kMaxK][kMaxK];
   for (int r = w; r < rows_per_req; r += nw) {
     const int grow = req * rows_per_req + r;
     const SelPart* pr = reinterpret_cast<const SelPart*>(a.partials) + size_t(grow) * a.chunks;
+    const bool has = lane < a.chunks;
     float hv[K], pm = -3.0e38f, psum = 0.f;
     int hi[K];
 #pragma unroll
     for (int q = 0; q < K; ++q) {
-      const int t = lane + 32 * q;
-      if (t < a.chunks * K) {
-        hv[q] = __ldcg(&pr[t / K].v[t % K]);
-        hi[q] = __ldcg(&pr[t / K].i[t % K]);
-      }
+      hv[q] = has ? __ldcg(&pr[lane].v[q]) : -INFINITY;
+      hi[q] = has ? __ldcg(&pr[lane].i[q]) : INT_MAX;
     }
-    if (lane < a.chunks) {
+    if (has) {
       pm = __ldcg(&pr[lane].m);
       psum = __ldcg(&pr[lane].s);
-    }
-#pragma unroll
-    for (int q = 0; q < K; ++q) {
-      const int t = lane + 32 * q;
-      if (t < a.chunks * K) {
-        heads_v[w][t] = hv[q];
-        heads_i[w][t] = hi[q];
-      }
     }
     // softmax denominator of the whole row
     const float M = warp_max(pm);
     const float S = warp_sum(psum * exp2f((pm - M) * c));
-    __syncwarp();
-    // k rounds of a tournament over the chunk lists' heads
-    int h0 = 0, h1 = 0;  // list heads of chunks lane and lane + 32
+    float myv = -INFINITY;
+    int myi = INT_MAX;
     for (int j = 0; j < k; ++j) {
-      float v = -INFINITY;
-      int ix = INT_MAX, src = -1;
-      if (lane < a.chunks && h0 < K && better(heads_v[w][lane * K + h0], heads_i[w][lane * K + h0], v, ix)) {
-        v = heads_v[w][lane * K + h0];
-        ix = heads_i[w][lane * K + h0];
-        src = 0;
-      }
-      if (lane + 32 < a.chunks && h1 < K &&
-          better(heads_v[w][(lane + 32) * K + h1], heads_i[w][(lane + 32) * K + h1], v, ix)) {
-        v = heads_v[w][(lane + 32) * K + h1];
-        ix = heads_i[w][(lane + 32) * K + h1];
-        src = 1;
-      }
-      float bv = v;
-      int bi = ix;
+      float bv = hv[0];
+      int bi = hi[0];
       warp_argmax(bv, bi);
-      if (src >= 0 && bv == v && bi == ix) {
-        if (src == 0) ++h0;
-        else ++h1;
+      if (hi[0] == bi && bi != INT_MAX) {  // this lane's head won: next entry up
+#pragma unroll
+        for (int q = 0; q + 1 < K; ++q) {
+          hv[q] = hv[q + 1];
+          hi[q] = hi[q + 1];
+        }
+        hv[K - 1] = -INFINITY;
+        hi[K - 1] = INT_MAX;
       }
       if (lane == j) {
-        p_s[r][j] = bv;  // the logit for now; turned into p below, in parallel
-        id_s[r][j] = bi;
+        myv = bv;
+        myi = bi;
       }
     }
-    __syncwarp();
     // p = exp((x - M) / T) / S; x - M is exact for bf16 logits, so fp32 expf
     // (about 1 ulp) keeps p within 1e-6 relative of the fp64 value
-    if (lane < k) p_s[r][lane] = expf((p_s[r][lane] - M) / a.temperature) / S;
-    __syncwarp();
+    if (lane < k) {
+      p_s[r][lane] = expf((myv - M) / a.temperature) / S;
+      id_s[r][lane] = myi;
+    }
   }
   __syncthreads();
   write_request(a, req, rows_per_req, p_s, id_s, sc_in);
