@@ -34,21 +34,43 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a
   const int n = a.n, need = n - 1;
   float* sc = reinterpret_cast<float*>(smem_raw);                      // [C]
   int* node_of = reinterpret_cast<int*>(sc + C);                       // [C]
-  unsigned char* sel = reinterpret_cast<unsigned char*>(node_of + C);  // [C]
+  int* tok = node_of + C;                                              // [C]
+  int* prow_s = tok + C;                                               // [P]
+  unsigned char* sel = reinterpret_cast<unsigned char*>(prow_s + P);  // [C]
   __shared__ int sel_pos[kMaxN];
   __shared__ int par[kMaxN];
   __shared__ int warp_base[kBuildThreads / 32 + 1];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
 
+  // one round trip: the request's scores, tokens, parent list, prefix length
+  // and bonus token (nothing below reads global memory again)
   const float* srow = a.score_space + size_t(req) * C;
-  for (int p = tid; p < C; p += blockDim.x) sc[p] = srow[p];
+  const int* trow = a.token_space + size_t(req) * C;
+  const int* prow = a.parent_space + size_t(req) * P;
+  __shared__ int s_len, s_bonus;
+  for (int p = tid; p < C; p += blockDim.x) {
+    const float v = srow[p];
+    const int t = trow[p];
+    sc[p] = v;
+    tok[p] = t;
+  }
+  for (int t = tid; t < P; t += blockDim.x) prow_s[t] = prow[t];
+  if (tid == 0) {
+    s_len = a.seq_lens[req];
+    s_bonus = a.bonus[req];
+  }
   __syncthreads();
 
   // 1. selection by rank (counting stops once n-1 better ones are found)
   for (int p = tid; p < C; p += blockDim.x) {
     const float v = sc[p];
     int rank = 0;
-    for (int q = 0; q < C && rank < need; ++q) rank += better(sc[q], q, v, p);
+    int q = 0;
+    for (; q + 8 <= C && rank < need; q += 8) {  // eight independent reads per check
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rank += better(sc[q + u], q + u, v, p);
+    }
+    for (; q < C && rank < need; ++q) rank += better(sc[q], q, v, p);
     sel[p] = rank < need;
     node_of[p] = -1;
   }
@@ -86,7 +108,6 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a
   __syncthreads();
 
   // 3. parents
-  const int* prow = a.parent_space + size_t(req) * P;
   for (int j = tid; j < n; j += blockDim.x) {
     if (j == 0) {
       par[0] = -1;
@@ -95,7 +116,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a
     const int p = sel_pos[j - 1];
     const int t = p / a.k;
     int parent = 0;
-    const int ppos = t < P ? prow[t] : -2;
+    const int ppos = t < P ? prow_s[t] : -2;
     if (ppos >= 0 && ppos < C && node_of[ppos] > 0 && node_of[ppos] < j) {
       parent = node_of[ppos];
     } else if (ppos != -1) {
@@ -123,11 +144,11 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a
       for (int c = i + 1; c < n && sib < 0; ++c)
         if (par[c] == par[i]) sib = c;
     a.mask_bits[rb + i] = m;
-    a.positions[rb + i] = a.seq_lens[req] + depth;
+    a.positions[rb + i] = s_len + depth;
     a.retrieve_index[rb + i] = int(rb + i);
     a.next_token[rb + i] = first;
     a.next_sibling[rb + i] = sib;
-    a.draft_tokens[rb + i] = i == 0 ? a.bonus[req] : a.token_space[size_t(req) * C + sel_pos[i - 1]];
+    a.draft_tokens[rb + i] = i == 0 ? s_bonus : tok[sel_pos[i - 1]];
   }
 }
 
@@ -135,7 +156,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a
 
 size_t build_tree_smem_bytes(int k, int S) {
   const size_t C = size_t(k) + size_t(S - 1) * k * k;
-  return C * (sizeof(float) + sizeof(int) + 1);
+  const size_t P = 1 + size_t(S - 1) * k;
+  return C * (sizeof(float) + 2 * sizeof(int) + 1) + P * sizeof(int);
 }
 
 int launch_build_tree(const BuildParams& p, cudaStream_t stream) {

@@ -14,8 +14,9 @@
 // that is also a source is never clobbered.  All loads that do not depend on
 // one another are issued together (the kernel is a handful of short dependent
 // round trips, not bandwidth).  CTA (req, 0) also writes new_seq_lens and
-// stages the request's free units in the workspace; the CTA arriving last
-// concatenates them in request order into free_ids and writes n_free.
+// stages the request's free units in the workspace; of those b CTAs the one
+// arriving last concatenates the lists in request order into free_ids and
+// writes n_free (the other layer groups take no part in it).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -132,20 +133,33 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) 
     }
   }
 
-  if (!arrive_last(a.counters, uint32_t(a.b) * uint32_t(G))) return;
+  // only the group-0 CTAs stage free lists; the others are done
+  if (grp != 0 || !arrive_last(a.counters, uint32_t(a.b))) return;
 
-  // ---- the last CTA concatenates the staged lists in request order: per
-  // block of requests, an exclusive scan of the counts, then every entry of
-  // the block copied in parallel ----
+  // ---- the last group-0 CTA concatenates the staged lists in request
+  // order: per block of requests, the counts and every staged entry are
+  // loaded together (one round trip), then an exclusive scan of the counts
+  // places the entries ----
   __shared__ int warp_sum[kCommitThreads / 32];
   __shared__ int s_off[kCommitThreads], s_cnt[kCommitThreads];
   __shared__ int s_running;
   if (tid == 0) s_running = 0;
   __syncthreads();
   const int lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
-  for (int r0 = 0; r0 < a.b; r0 += blockDim.x) {
+  // requests per block: each thread holds at most kEnt staged entries
+  constexpr int kEnt = 8;
+  const int rblk = max(1, min(int(blockDim.x), kEnt * int(blockDim.x) / n));
+  for (int r0 = 0; r0 < a.b; r0 += rblk) {
+    const int nr = min(rblk, a.b - r0);
     const int r = r0 + tid;
-    const int c = r < a.b ? __ldcg(counts + r) : 0;
+    const int c = tid < nr ? __ldcg(counts + r) : 0;
+    const int* from = reinterpret_cast<const int*>(a.partials) + size_t(r0) * n;
+    int ent[kEnt];
+#pragma unroll
+    for (int j = 0; j < kEnt; ++j) {
+      const int x = tid + j * int(blockDim.x);
+      ent[j] = x < nr * n ? __ldcg(from + x) : 0;
+    }
     int incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -155,20 +169,22 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) 
     if (lane == 31) warp_sum[w] = incl;
     __syncthreads();
     int before = s_running;
-    for (int i = 0; i < w; ++i) before += warp_sum[i];
+    for (int q = 0; q < w; ++q) before += warp_sum[q];
     s_off[tid] = before + incl - c;
     s_cnt[tid] = c;
     __syncthreads();
-    const int nr = min(int(blockDim.x), a.b - r0);
-    const int* from = reinterpret_cast<const int*>(a.partials) + size_t(r0) * n;
-    for (int x = tid; x < nr * n; x += blockDim.x) {
-      const int ri = x / n, e = x - ri * n;
-      if (e < s_cnt[ri]) a.free_ids[s_off[ri] + e] = __ldcg(from + x);
+#pragma unroll
+    for (int j = 0; j < kEnt; ++j) {
+      const int x = tid + j * int(blockDim.x);
+      if (x < nr * n) {
+        const int ri = x / n, e = x - ri * n;
+        if (e < s_cnt[ri]) a.free_ids[s_off[ri] + e] = ent[j];
+      }
     }
     __syncthreads();
     if (tid == 0) {
       int tot = 0;
-      for (int i = 0; i < nw; ++i) tot += warp_sum[i];
+      for (int q = 0; q < nw; ++q) tot += warp_sum[q];
       s_running += tot;
     }
     __syncthreads();
