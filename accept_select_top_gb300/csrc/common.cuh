@@ -320,6 +320,21 @@ inline RowSplit pick_split(long rows, int V, int vec, int max_chunks = kMaxChunk
   return RowSplit{chunks, per};
 }
 
+// The split greedy accept uses: one wave of 8 CTAs of 256 threads per SM
+// (a 32-register kernel), so that a thread's share of a chunk is about one
+// batch of 16-byte loads in flight (one round trip instead of two).
+inline RowSplit greedy_split(long rows, int V, int vec) {
+  long want = (2 * kTargetCtas) / rows;
+  if (want < 1) want = 1;
+  if (want > kMaxChunks) want = kMaxChunks;
+  long by_size = V / 2048;
+  if (by_size < 1) by_size = 1;
+  if (want > by_size) want = by_size;
+  int per = int((V + want - 1) / want);
+  per = (per + vec - 1) / vec * vec;
+  return RowSplit{(V + per - 1) / per, per};
+}
+
 // The split of the terminal row in the second sampling pass: fixed
 // 4096-token chunks (16 tokens per thread of a 256-thread CTA, so the
 // in-order search of one chunk is a single pass); at most kMaxChunks2 chunks.

@@ -37,7 +37,7 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
     case SPEC_OP_BUILD_TREE:
       return 0;
     case SPEC_OP_VERIFY_GREEDY:
-      return align256(size_t(b) * n * chunk_bound(long(b) * n, V) * 8);
+      return align256(size_t(b) * n * greedy_split(long(b) * n, V, 1).chunks * 8);
     case SPEC_OP_VERIFY_SAMPLING:
       return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
              sampling_partial2_bytes(b, terminal_split(V).chunks);
@@ -248,7 +248,7 @@ int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits
   p.accept_lens = accept_lens;
   p.accepted_tokens = accepted_tokens;
   p.next_root = next_root;
-  const RowSplit sp = pick_split(long(b) * n, V, vec_elems(dtype));
+  const RowSplit sp = greedy_split(long(b) * n, V, vec_elems(dtype));
   p.chunks = sp.chunks;
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(logits, V, dtype);
