@@ -18,11 +18,13 @@ namespace spec {
 
 namespace {
 
-struct SelPart {
-  float m;   // max logit of the chunk
-  float s;   // sum of exp((x - m) / T) over the chunk
+// 16-byte aligned, lists first, so that a lane reads a chunk's partial with
+// 16-byte loads
+struct alignas(16) SelPart {
   float v[kMaxK];
   int i[kMaxK];
+  float m;   // max logit of the chunk
+  float s;   // sum of exp((x - m) / T) over the chunk
 };
 
 template <int K>
@@ -178,9 +180,10 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
       a.token_blk[sb + lane] = id;
     }
     int rank = 0;
-    for (int g = 0; g < kk; ++g) {
+#pragma unroll
+    for (int g = 0; g < 32; ++g) {  // all lanes shuffle; lanes past k*k hold -inf
       const float o = __shfl_sync(0xffffffffu, ex, g);
-      rank += better(o, g, ex, lane) ? 1 : 0;
+      rank += (g < kk && better(o, g, ex, lane)) ? 1 : 0;
     }
     if (on && rank < k) {
       if (a.parent_blk) a.parent_blk[size_t(req) * a.parent_ld + rank] = lane + kk * (a.step - 1) + k;
@@ -386,14 +389,27 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
     const bool has = lane < a.chunks;
     float hv[K], pm = -3.0e38f, psum = 0.f;
     int hi[K];
+    if constexpr (K % 4 == 0) {
 #pragma unroll
-    for (int q = 0; q < K; ++q) {
-      hv[q] = has ? __ldcg(&pr[lane].v[q]) : -INFINITY;
-      hi[q] = has ? __ldcg(&pr[lane].i[q]) : INT_MAX;
+      for (int q = 0; q < K; q += 4) {
+        const float4 v4 = has ? __ldcg(reinterpret_cast<const float4*>(&pr[lane].v[q]))
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        const int4 i4 = has ? __ldcg(reinterpret_cast<const int4*>(&pr[lane].i[q]))
+                            : make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
+        hv[q] = v4.x, hv[q + 1] = v4.y, hv[q + 2] = v4.z, hv[q + 3] = v4.w;
+        hi[q] = i4.x, hi[q + 1] = i4.y, hi[q + 2] = i4.z, hi[q + 3] = i4.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < K; ++q) {
+        hv[q] = has ? __ldcg(&pr[lane].v[q]) : -INFINITY;
+        hi[q] = has ? __ldcg(&pr[lane].i[q]) : INT_MAX;
+      }
     }
     if (has) {
-      pm = __ldcg(&pr[lane].m);
-      psum = __ldcg(&pr[lane].s);
+      const float2 ms = __ldcg(reinterpret_cast<const float2*>(&pr[lane].m));
+      pm = ms.x;
+      psum = ms.y;
     }
     // softmax denominator of the whole row
     const float M = warp_max(pm);
@@ -420,8 +436,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
     }
     // p = exp((x - M) / T) / S; x - M is exact for bf16 logits, so fp32 expf
     // (about 1 ulp) keeps p within 1e-6 relative of the fp64 value
+    const float invS = 1.f / S;  // one more rounding than a division: within 1 ulp
     if (lane < k) {
-      p_s[r][lane] = expf((myv - M) / a.temperature) / S;
+      p_s[r][lane] = expf((myv - M) / a.temperature) * invS;
       id_s[r][lane] = myi;
     }
   }
