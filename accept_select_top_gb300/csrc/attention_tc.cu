@@ -329,7 +329,6 @@ struct PieceIter {
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attention_tc_kernel(const __grid_constant__ TcArgs args) {
-  pdl_trigger();
   using L = Smem<D>;
   const AttentionParams& a = args.p;
   const int G = a.Hq / a.Hkv, M = a.n * G;
@@ -386,6 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   pdl_wait();  // nothing above reads global memory
+  pdl_trigger();
   // ---- partition: total tiles T, this CTA's range, and where it starts ----
   const int upr = a.Hkv * args.m_tiles;
   const int nwarps = blockDim.x >> 5;

@@ -25,8 +25,8 @@ namespace {
 constexpr int kBuildThreads = 512;
 
 __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned char smem_raw[];
   const int req = blockIdx.x;
   const int C = a.k + (a.S - 1) * a.k * a.k;

@@ -28,8 +28,8 @@ constexpr int kCommitThreads = 256;
 constexpr int kSliceBytes = 32 * 1024;  // shared staging per slice (K and V of all L rows)
 
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(CommitParams a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int req = blockIdx.x, grp = blockIdx.y, G = gridDim.y;
   const int n = a.n, W = a.W, tid = threadIdx.x;
   __shared__ int src[kMaxN + 1], dst[kMaxN + 1], unit_s[kMaxN], dst_unit_s[kMaxN + 1];

@@ -32,7 +32,11 @@ constexpr size_t kHeaderBytes = 256;
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // at least 256 words: the attention merge counts arrivals per CTA (<= 192)
-__host__ __device__ inline size_t counters_bytes(int b) { return align256(size_t(b + 1 > 256 ? b + 1 : 256) * 4); }
+// arrival counters: at least 256 words (the attention's merge counters) and
+// two per request (the two halves select alternates between), plus one
+__host__ __device__ inline size_t counters_bytes(int b) {
+  return align256(size_t(2 * b + 1 > 256 ? 2 * b + 1 : 256) * 4);
+}
 
 struct WsView {
   uint32_t* error;
@@ -110,11 +114,14 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   i = int(imin);
 }
 // Programmatic dependent launch.  Every kernel of the library is launched
-// with programmatic stream serialisation (launch_pdl): it lets the grid
-// that follows be scheduled early (pdl_trigger, first thing in each kernel),
-// and waits for the grid before it -- its completion and its memory -- before
-// reading any global memory (pdl_wait).  Stream order is kept: no kernel
-// reads anything before its predecessor has finished.
+// with programmatic stream serialisation (launch_pdl).  A kernel waits for the
+// grid before it -- its completion and its memory -- before reading anything
+// that grid may write (pdl_wait), and only then lets the grid after it be
+// scheduled (pdl_trigger).  So a kernel's work before its wait can overlap
+// only the one kernel right before it, never an earlier one.  The select's
+// chunk pass is such work when the kernel before it is the previous select
+// on the same workspace (the two use different halves of the workspace);
+// every other kernel waits first.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

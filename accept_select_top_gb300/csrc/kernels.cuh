@@ -22,9 +22,15 @@ struct SelectParams {
   float* topk_p_out;
   int rows, chunks, chunk_elems;
   bool vec_ok;
+  // The chunk pass may run before the launch waits on the kernel ahead of
+  // it (early): only when that kernel is the previous select on the same
+  // workspace, which uses the other half (1 - half) of the partials and
+  // counters.
+  bool early;
+  int half;
   uint32_t* error;
-  uint32_t* counters;
-  unsigned char* partials;
+  uint32_t* counters;    // this call's half: b counters
+  unsigned char* partials;  // this call's half
 };
 
 struct BuildParams {

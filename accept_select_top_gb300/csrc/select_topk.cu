@@ -213,8 +213,15 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
-  pdl_trigger();
-  pdl_wait();
+  // The chunk pass reads only the draft logits (which no kernel of the
+  // library writes) and this call's half of the workspace.  When the kernel
+  // before is the previous select on the same workspace (the other half),
+  // the pass runs before waiting on it; only the finalize, which reads its
+  // scores and writes this step's outputs, waits.
+  if (!a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const int rows_per_req = a.step ? a.k : 1;
@@ -371,6 +378,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   }
 
   if (!arrive_last(a.counters + req, uint32_t(rows_per_req * a.chunks))) return;
+  if (a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // ---- finalize request `req` ----
   // One warp per row: lane l holds chunk l's (m, s) and sorted top-K list in

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 
 #include "accept_select_top.h"
 #include "common.cuh"
@@ -27,13 +29,18 @@ inline bool vec_ok(const void* logits, int V, int dtype) {
   return aligned(logits, 16) && (size_t(V) * elem_bytes(dtype)) % 16 == 0;
 }
 
+// One half of the select partials: the larger of step 0 (b rows) and a
+// later step (b*k rows).
+size_t select_half_bytes(int b, int k, int V) {
+  const size_t a = select_partial_bytes(b, select_split(b, V, 1).chunks);
+  const size_t c = select_partial_bytes(b * k, select_split(long(b) * k, V, 1).chunks);
+  return a > c ? a : c;
+}
+
 size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
   switch (op) {
-    case SPEC_OP_SELECT_TOPK: {
-      const size_t a = select_partial_bytes(b, select_split(b, V, 1).chunks);
-      const size_t c = select_partial_bytes(b * k, select_split(long(b) * k, V, 1).chunks);
-      return a > c ? a : c;
-    }
+    case SPEC_OP_SELECT_TOPK:
+      return 2 * select_half_bytes(b, k, V);
     case SPEC_OP_BUILD_TREE:
       return 0;
     case SPEC_OP_VERIFY_GREEDY:
@@ -48,6 +55,36 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
     default:
       return 0;
   }
+}
+
+// Per workspace: whether the last call enqueued on it was a select, and the
+// half (of the select partials and counters) that select used.  A select
+// enqueued right after another select on the same workspace takes the other
+// half and runs its chunk pass before waiting on that select (programmatic
+// dependent launch); after any other call it waits first.  Every kernel lets
+// its successor start only after its own wait, so a kernel overlaps only the
+// one kernel before it.
+struct WsState {
+  bool last_select = false;
+  int half = 1;
+};
+std::mutex g_ws_mu;
+std::unordered_map<const void*, WsState> g_ws_state;
+
+void note_other(const void* ws) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  auto it = g_ws_state.find(ws);
+  if (it != g_ws_state.end()) it->second.last_select = false;
+}
+
+// (early, half) for a select about to be enqueued on ws
+std::pair<bool, int> take_select(const void* ws) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  WsState& st = g_ws_state[ws];
+  const bool early = st.last_select;
+  st.half ^= 1;
+  st.last_select = true;
+  return {early, st.half};
 }
 
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -70,6 +107,7 @@ size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, 
 
 int spec_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws) return SPEC_ERR_WORKSPACE;
+  note_other(ws);
   return cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -130,8 +168,11 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(draft_logits, V, dtype);
   p.error = v.error;
-  p.counters = v.counters;
-  p.partials = v.partials;
+  const std::pair<bool, int> eh = take_select(ws);
+  p.early = eh.first;
+  p.half = eh.second;
+  p.counters = v.counters + size_t(eh.second) * b;
+  p.partials = v.partials + size_t(eh.second) * select_half_bytes(b, k, V);
   return launch_select_topk(p, as_stream(stream));
 }
 
@@ -147,6 +188,7 @@ int spec_build_tree(int b, int k, int S, int n, const float* score_space, const 
       !retrieve_index || !next_token || !next_sibling || !mask_bits)
     return SPEC_ERR_ARG;
   if (int rc = check_ws(ws, ws_bytes, kHeaderBytes)) return rc;
+  note_other(ws);
   BuildParams p{};
   p.b = b;
   p.k = k;
@@ -183,6 +225,7 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16)) return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_VERIFY_ATTENTION, b, n, 1, 1, Hq, Hkv, max_seq_len);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  note_other(ws);
   const WsView v = ws_view(ws, b);
   AttentionParams p{};
   p.b = b;
@@ -231,6 +274,7 @@ int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits
     return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  note_other(ws);
   const WsView v = ws_view(ws, b);
   GreedyParams p{};
   p.b = b;
@@ -272,6 +316,7 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
     return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_VERIFY_SAMPLING, b, n, 1, V, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  note_other(ws);
   const WsView v = ws_view(ws, b);
   SamplingParams p{};
   p.b = b;
@@ -323,6 +368,7 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
     return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_COMMIT_KV, b, n, 1, 1, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  note_other(ws);
   const WsView v = ws_view(ws, b);
   CommitParams p{};
   p.b = b;

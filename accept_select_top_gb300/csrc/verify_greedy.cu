@@ -77,8 +77,8 @@ __device__ __forceinline__ void scan_argmax_bf16(const uint16_t* row, int begin,
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const int req = row / a.n;

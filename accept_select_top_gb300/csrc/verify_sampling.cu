@@ -55,8 +55,8 @@ __device__ __forceinline__ float p_of(float l, float M, float T, float S) { retu
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   using Tr = LogitTraits<T>;
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
@@ -268,8 +268,8 @@ __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqSta
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   using Tr = LogitTraits<T>;
   const int req = blockIdx.y;
   const int chunk = blockIdx.x;

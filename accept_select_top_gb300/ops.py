@@ -96,7 +96,11 @@ class Workspace:
 
     def __init__(self, nbytes: int, device=None, stream=None):
         self.nbytes = max(int(nbytes), 256)
-        self.tensor = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        self.tensor = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        # zero-filled through the C ABI, which also forgets any earlier
+        # workspace that lived at this address
+        _check(LIB.spec_workspace_init(self.ptr, ctypes.c_size_t(self.nbytes), _stream(stream)),
+               "spec_workspace_init")
 
     @property
     def ptr(self):

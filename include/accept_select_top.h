@@ -25,7 +25,10 @@
  *     spec_workspace_size() and zero-filled once (spec_workspace_init) before its
  *     first use.  Every call leaves it zero again apart from the error word, so
  *     one workspace serves any sequence of calls on one stream.  Calls that may
- *     run concurrently (different streams) need separate workspaces.
+ *     run concurrently (different streams) need separate workspaces.  Every
+ *     kernel is launched with programmatic dependent launch and lets the next
+ *     kernel start only after it has waited for the one before it, so at most
+ *     two consecutive kernels overlap (see spec_select_topk).
  *   - Return codes: SPEC_OK, SPEC_ERR_ARG (null pointer, bad size or shape, a
  *     limit below exceeded), SPEC_ERR_WORKSPACE (ws too small or misaligned),
  *     SPEC_ERR_LAUNCH (the CUDA launch failed; cudaGetLastError is consumed),
@@ -117,6 +120,13 @@ int spec_device_sm_count(void);
  * (score_ld = k + (S-1)*k*k, parent_ld = 1 + (S-1)*k).  parent_blk may be NULL
  * (the last step's parent block is not part of the parent list).  topk_p_out
  * [b*rows, k] is optional (NULL).
+ * Overlap: the library remembers, per workspace pointer, whether the last call
+ * enqueued on it was spec_select_topk.  If it was, this call uses the other
+ * half of the select's workspace area and starts its pass over draft_logits
+ * before the previous select has finished (programmatic dependent launch);
+ * only the step's outputs wait for it.  draft_logits must therefore be ready
+ * when this call is enqueued (any producer other than this library's kernels
+ * is), as for every input.  spec_workspace_init resets the record.
  * ------------------------------------------------------------------------- */
 int spec_select_topk(int step, int b, int k, int V, int dtype,
                      const void* draft_logits, float temperature,
