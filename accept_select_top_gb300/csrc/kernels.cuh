@@ -63,6 +63,11 @@ struct GreedyParams {
   int32_t* next_root;
   int chunks, chunk_elems;
   bool vec_ok;
+  // The scan may run before the launch waits on the kernel ahead of it
+  // (early): only when that kernel is the verify attention on the same
+  // workspace, whose merge slots and counters the scan's partials and
+  // counters do not share.
+  bool early;
   uint32_t* error;
   uint32_t* counters;
   unsigned char* partials;
@@ -160,5 +165,14 @@ struct TcGeometry {
 TcGeometry attention_tc_geometry(int b, int n, int Hq, int Hkv, int max_seq_len);
 int launch_attention_tc(const AttentionParams& p, const TcGeometry& geo, cudaStream_t stream);
 size_t attention_partial_bytes();  // merge slots and counters, any D <= 128
+
+// spec_verify_greedy on a workspace laid out for greedy accept alone (the
+// partials straight after the counters; never overlaps the kernel before):
+// the no-allocation entry point's fixed scratch.
+size_t greedy_compact_bytes(int b, int n, int V);
+int verify_greedy_compact(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
+                          const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,
+                          int32_t* predict, int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
+                          int32_t* next_root, void* ws, size_t ws_bytes, void* stream);
 
 }  // namespace spec

@@ -15,6 +15,7 @@
 
 #include "accept_select_top.h"
 #include "common.cuh"
+#include "kernels.cuh"
 
 namespace {
 
@@ -52,8 +53,7 @@ extern "C" int spec_verify_greedy_noalloc(int b, int n, int S, int V, int dtype,
   if (b < 0 || n < 1 || n > spec::kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (b == 0) return SPEC_OK;
-  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
-  if (need == 0) return SPEC_ERR_ARG;
+  const size_t need = spec::greedy_compact_bytes(b, n, V);
   if (need > kScratchBytes) return SPEC_ERR_WORKSPACE;  // too large for the fixed scratch
   void* ws = nullptr;
   if (int rc = scratch_of_current_device(&ws)) return rc;
@@ -61,7 +61,7 @@ extern "C" int spec_verify_greedy_noalloc(int b, int n, int S, int V, int dtype,
   // arrival counters must start at zero (the partials are always written first).
   const size_t zero_bytes = spec::kHeaderBytes + spec::counters_bytes(b);
   if (cudaMemsetAsync(ws, 0, zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  return spec_verify_greedy(b, n, S, V, dtype, logits, draft_tokens, retrieve_index, next_token, next_sibling,
-                            predict, accept_index, accept_lens, accepted_tokens, next_root, ws, kScratchBytes,
-                            stream);
+  return spec::verify_greedy_compact(b, n, S, V, dtype, logits, draft_tokens, retrieve_index, next_token,
+                                     next_sibling, predict, accept_index, accept_lens, accepted_tokens, next_root,
+                                     ws, kScratchBytes, stream);
 }

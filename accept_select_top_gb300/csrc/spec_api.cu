@@ -29,6 +29,9 @@ inline bool vec_ok(const void* logits, int V, int dtype) {
   return aligned(logits, 16) && (size_t(V) * elem_bytes(dtype)) % 16 == 0;
 }
 
+// Greedy accept's per-chunk argmax partials.
+size_t greedy_part_bytes(int b, int n, int V) { return align256(size_t(b) * n * greedy_split(long(b) * n, V, 1).chunks * 8); }
+
 // One half of the select partials: the larger of step 0 (b rows) and a
 // later step (b*k rows).
 size_t select_half_bytes(int b, int k, int V) {
@@ -43,8 +46,8 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
       return 2 * select_half_bytes(b, k, V);
     case SPEC_OP_BUILD_TREE:
       return 0;
-    case SPEC_OP_VERIFY_GREEDY:
-      return align256(size_t(b) * n * greedy_split(long(b) * n, V, 1).chunks * 8);
+    case SPEC_OP_VERIFY_GREEDY:  // after the attention's merge region (see spec_verify_greedy)
+      return attention_partial_bytes() + greedy_part_bytes(b, n, V);
     case SPEC_OP_VERIFY_SAMPLING:
       return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
              sampling_partial2_bytes(b, terminal_split(V).chunks);
@@ -66,15 +69,32 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
 // one kernel before it.
 struct WsState {
   bool last_select = false;
+  bool last_attention = false;
   int half = 1;
 };
 std::mutex g_ws_mu;
 std::unordered_map<const void*, WsState> g_ws_state;
 
-void note_other(const void* ws) {
+void note_other(const void* ws, bool attention = false) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  if (!attention) {
+    auto it = g_ws_state.find(ws);
+    if (it != g_ws_state.end()) it->second.last_select = it->second.last_attention = false;
+    return;
+  }
+  WsState& st = g_ws_state[ws];
+  st.last_select = false;
+  st.last_attention = true;
+}
+
+// whether the last call enqueued on ws was the verify attention (and forget it)
+bool take_after_attention(const void* ws) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   auto it = g_ws_state.find(ws);
-  if (it != g_ws_state.end()) it->second.last_select = false;
+  if (it == g_ws_state.end()) return false;
+  const bool r = it->second.last_attention;
+  it->second.last_select = it->second.last_attention = false;
+  return r;
 }
 
 // (early, half) for a select about to be enqueued on ws
@@ -84,6 +104,7 @@ std::pair<bool, int> take_select(const void* ws) {
   const bool early = st.last_select;
   st.half ^= 1;
   st.last_select = true;
+  st.last_attention = false;
   return {early, st.half};
 }
 
@@ -91,6 +112,53 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (!ws || !aligned(ws, 256)) return SPEC_ERR_WORKSPACE;
   if (ws_bytes < need) return SPEC_ERR_WORKSPACE;
   return SPEC_OK;
+}
+
+// compact: the no-allocation layout (partials straight after the counters,
+// never early).  Otherwise the partials sit after the attention's merge
+// region, and the scan runs before waiting on the kernel ahead when that
+// kernel is the verify attention on this workspace.
+int greedy_call(bool compact, int b, int n, int S, int V, int dtype, const void* logits,
+                const int32_t* draft_tokens, const int32_t* retrieve_index, const int32_t* next_token,
+                const int32_t* next_sibling, int32_t* predict, int32_t* accept_index, int32_t* accept_lens,
+                int32_t* accepted_tokens, int32_t* next_root, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || n < 1 || n > kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (b == 0) return SPEC_OK;
+  if (!logits || !draft_tokens || !retrieve_index || !next_token || !next_sibling || !predict || !accept_index ||
+      !accept_lens)
+    return SPEC_ERR_ARG;
+  const size_t need = compact ? kHeaderBytes + counters_bytes(b) + greedy_part_bytes(b, n, V)
+                              : spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const bool early = !compact && take_after_attention(ws);
+  if (compact) note_other(ws);
+  const WsView v = ws_view(ws, b);
+  GreedyParams p{};
+  p.b = b;
+  p.n = n;
+  p.S = S;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = logits;
+  p.draft_tokens = draft_tokens;
+  p.retrieve_index = retrieve_index;
+  p.next_token = next_token;
+  p.next_sibling = next_sibling;
+  p.predict = predict;
+  p.accept_index = accept_index;
+  p.accept_lens = accept_lens;
+  p.accepted_tokens = accepted_tokens;
+  p.next_root = next_root;
+  const RowSplit sp = greedy_split(long(b) * n, V, vec_elems(dtype));
+  p.chunks = sp.chunks;
+  p.chunk_elems = sp.chunk_elems;
+  p.vec_ok = vec_ok(logits, V, dtype);
+  p.early = early;
+  p.error = v.error;
+  p.counters = v.counters + greedy_counter_base(b);
+  p.partials = v.partials + (compact ? 0 : attention_partial_bytes());
+  return launch_verify_greedy(p, as_stream(stream));
 }
 
 }  // namespace
@@ -225,7 +293,7 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16)) return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_VERIFY_ATTENTION, b, n, 1, 1, Hq, Hkv, max_seq_len);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  note_other(ws);
+  note_other(ws, true);
   const WsView v = ws_view(ws, b);
   AttentionParams p{};
   p.b = b;
@@ -262,44 +330,13 @@ int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len)
   return attention_tc_geometry(b, n, Hq, Hkv, max_seq_len).splits;
 }
 
+
 int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
                        const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,
                        int32_t* predict, int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
                        int32_t* next_root, void* ws, size_t ws_bytes, void* stream) {
-  if (b < 0 || n < 1 || n > kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
-  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
-  if (b == 0) return SPEC_OK;
-  if (!logits || !draft_tokens || !retrieve_index || !next_token || !next_sibling || !predict || !accept_index ||
-      !accept_lens)
-    return SPEC_ERR_ARG;
-  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
-  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  note_other(ws);
-  const WsView v = ws_view(ws, b);
-  GreedyParams p{};
-  p.b = b;
-  p.n = n;
-  p.S = S;
-  p.V = V;
-  p.dtype = dtype;
-  p.logits = logits;
-  p.draft_tokens = draft_tokens;
-  p.retrieve_index = retrieve_index;
-  p.next_token = next_token;
-  p.next_sibling = next_sibling;
-  p.predict = predict;
-  p.accept_index = accept_index;
-  p.accept_lens = accept_lens;
-  p.accepted_tokens = accepted_tokens;
-  p.next_root = next_root;
-  const RowSplit sp = greedy_split(long(b) * n, V, vec_elems(dtype));
-  p.chunks = sp.chunks;
-  p.chunk_elems = sp.chunk_elems;
-  p.vec_ok = vec_ok(logits, V, dtype);
-  p.error = v.error;
-  p.counters = v.counters;
-  p.partials = v.partials;
-  return launch_verify_greedy(p, as_stream(stream));
+  return greedy_call(false, b, n, S, V, dtype, logits, draft_tokens, retrieve_index, next_token, next_sibling,
+                     predict, accept_index, accept_lens, accepted_tokens, next_root, ws, ws_bytes, stream);
 }
 
 int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits, const float* draft_probs,
@@ -402,3 +439,20 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
 }
 
 }  // extern "C"
+
+namespace spec {
+
+size_t greedy_compact_bytes(int b, int n, int V) {
+  if (b < 1 || n < 1 || V < 1) return kHeaderBytes + counters_bytes(0);
+  return kHeaderBytes + counters_bytes(b) + greedy_part_bytes(b, n, V);
+}
+
+int verify_greedy_compact(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
+                          const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,
+                          int32_t* predict, int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
+                          int32_t* next_root, void* ws, size_t ws_bytes, void* stream) {
+  return greedy_call(true, b, n, S, V, dtype, logits, draft_tokens, retrieve_index, next_token, next_sibling,
+                     predict, accept_index, accept_lens, accepted_tokens, next_root, ws, ws_bytes, stream);
+}
+
+}  // namespace spec

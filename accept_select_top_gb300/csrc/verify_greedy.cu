@@ -77,8 +77,14 @@ __device__ __forceinline__ void scan_argmax_bf16(const uint16_t* row, int begin,
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
-  pdl_wait();
-  pdl_trigger();
+  // The scan reads only the target logits (which no kernel of the library
+  // writes) and greedy's own partials and counters.  When the kernel before
+  // is the verify attention on the same workspace, the scan runs before
+  // waiting on it; only the finalize waits.
+  if (!a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const int req = row / a.n;
@@ -104,6 +110,10 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
   if (threadIdx.x == 0) part[size_t(row) * a.chunks + chunk] = ArgPart{bv, bi};
 
   if (!arrive_last(a.counters + req, uint32_t(a.n * a.chunks))) return;
+  if (a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // ---- finalize request `req` (last CTA to arrive) ----
   const int n = a.n, base = req * n, W = a.S + 1;

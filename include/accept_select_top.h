@@ -211,6 +211,12 @@ int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len)
  * (-1 padded), accept_lens [b] = accepted drafts + 1; optional (NULL):
  * accepted_tokens [b, S+1] = predict[accept_index] (-1 padded), next_root [b]
  * = the last accepted token.
+ * Overlap: when the last call enqueued on the workspace was
+ * spec_verify_attention, the argmax pass over logits starts before that call
+ * has finished (programmatic dependent launch; logits must be ready when this
+ * call is enqueued, as for every input); the walk and the outputs wait for
+ * it.  The workspace keeps the attention's merge area untouched for this, so
+ * spec_workspace_size(SPEC_OP_VERIFY_GREEDY, ...) includes it (about 26 MB).
  * ------------------------------------------------------------------------- */
 int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits,
                        const int32_t* draft_tokens, const int32_t* retrieve_index,
@@ -292,7 +298,11 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
  *   - Every call shares the one array per device: calls that overlap on the
  *     GPU (different streams, or concurrent host threads) race.  Serialise them.
  *   - Returns SPEC_ERR_WORKSPACE when b, n and V need more scratch than the
- *     array holds (spec_workspace_size(SPEC_OP_VERIFY_GREEDY, ...) bytes).
+ *     array holds.  The array is laid out for greedy accept alone (no room
+ *     kept for the attention's merge area, so the pass never overlaps the
+ *     call before it): 256 bytes of header, the arrival counters
+ *     (4 * max(256, 2b+1) + 4b bytes, rounded up to 256) and 8 bytes per
+ *     verify row and row chunk (about 9 chunks per row for 128 rows of 128K).
  *   - Device index errors go to the array's error word, which this entry point
  *     does not report; use spec_verify_greedy with a workspace to read them.
  * ------------------------------------------------------------------------- */

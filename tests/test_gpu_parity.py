@@ -208,7 +208,8 @@ def test_sampling_t0_equals_greedy_on_gpu(cases):
     c = cases("mtp_chain", "sampling")
     wl, ops = c.wl, _ops()
     a, b_ = _accept_bufs(wl), _accept_bufs(wl)
-    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_SAMPLING, wl.b, wl.n, 1, wl.V))
+    ws = ops.Workspace(max(ops.spec_workspace_size(op, wl.b, wl.n, 1, wl.V)  # both calls share it
+                           for op in (ops.OP_VERIFY_SAMPLING, ops.OP_VERIFY_GREEDY)))
     zeros = torch.zeros(wl.b, device="cuda")
     ops.spec_verify_sampling(wl.b, wl.n, wl.S, c.logits, c.q, zeros, c.u, c.u_final, *_tree_dev(c), *a.values(), ws)
     ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *b_.values(), ws)
