@@ -121,8 +121,9 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 // scheduled (pdl_trigger).  So a kernel's work before its wait can overlap
 // only the one kernel right before it, never an earlier one.  The select's
 // chunk pass is such work when the kernel before it is the previous select
-// on the same workspace (the two use different halves of the workspace);
-// every other kernel waits first.
+// (the two use different halves of the select's area) or the KV commit on
+// the same workspace, and greedy accept's scan when the kernel before it is
+// the verify attention; every other kernel waits first.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -25,7 +25,7 @@ struct SelectParams {
   // The chunk pass may run before the launch waits on the kernel ahead of
   // it (early): only when that kernel is the previous select on the same
   // workspace, which uses the other half (1 - half) of the partials and
-  // counters.
+  // counters, or the KV commit, which uses neither.
   bool early;
   int half;
   uint32_t* error;

@@ -214,10 +214,11 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
 template <typename T, int K>
 __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
   // The chunk pass reads only the draft logits (which no kernel of the
-  // library writes) and this call's half of the workspace.  When the kernel
-  // before is the previous select on the same workspace (the other half),
-  // the pass runs before waiting on it; only the finalize, which reads its
-  // scores and writes this step's outputs, waits.
+  // library writes) and this call's half of the select's workspace area.
+  // When the kernel before is the previous select (which uses the other
+  // half) or the KV commit on the same workspace, the pass runs before
+  // waiting on it; only the finalize, which reads the previous step's scores
+  // and writes this step's outputs, waits.
   if (!a.early) {
     pdl_wait();
     pdl_trigger();

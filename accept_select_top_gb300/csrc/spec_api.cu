@@ -32,6 +32,11 @@ inline bool vec_ok(const void* logits, int V, int dtype) {
 // Greedy accept's per-chunk argmax partials.
 size_t greedy_part_bytes(int b, int n, int V) { return align256(size_t(b) * n * greedy_split(long(b) * n, V, 1).chunks * 8); }
 
+// The select's partials start past the largest area the KV commit uses (its
+// staged free lists and counts, for any tree of at most kMaxN nodes), so that
+// a select may also overlap a commit before it.
+size_t select_base_bytes(int b) { return align256(size_t(b) * (kMaxN + 1) * 4); }
+
 // One half of the select partials: the larger of step 0 (b rows) and a
 // later step (b*k rows).
 size_t select_half_bytes(int b, int k, int V) {
@@ -43,7 +48,7 @@ size_t select_half_bytes(int b, int k, int V) {
 size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
   switch (op) {
     case SPEC_OP_SELECT_TOPK:
-      return 2 * select_half_bytes(b, k, V);
+      return select_base_bytes(b) + 2 * select_half_bytes(b, k, V);
     case SPEC_OP_BUILD_TREE:
       return 0;
     case SPEC_OP_VERIFY_GREEDY:  // after the attention's merge region (see spec_verify_greedy)
@@ -62,29 +67,33 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
 
 // Per workspace: whether the last call enqueued on it was a select, and the
 // half (of the select partials and counters) that select used.  A select
-// enqueued right after another select on the same workspace takes the other
-// half and runs its chunk pass before waiting on that select (programmatic
-// dependent launch); after any other call it waits first.  Every kernel lets
+// enqueued right after another select, or after a KV commit, on the same
+// workspace takes the other half and runs its chunk pass before waiting on
+// that call (programmatic dependent launch; neither touches the select's
+// area); after any other call it waits first.  Every kernel lets
 // its successor start only after its own wait, so a kernel overlaps only the
 // one kernel before it.
 struct WsState {
   bool last_select = false;
   bool last_attention = false;
+  bool last_commit = false;
   int half = 1;
 };
 std::mutex g_ws_mu;
 std::unordered_map<const void*, WsState> g_ws_state;
 
-void note_other(const void* ws, bool attention = false) {
+enum class Call { kOther, kAttention, kCommit };
+void note_other(const void* ws, Call call = Call::kOther) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
-  if (!attention) {
+  if (call == Call::kOther) {
     auto it = g_ws_state.find(ws);
-    if (it != g_ws_state.end()) it->second.last_select = it->second.last_attention = false;
+    if (it != g_ws_state.end()) it->second.last_select = it->second.last_attention = it->second.last_commit = false;
     return;
   }
   WsState& st = g_ws_state[ws];
   st.last_select = false;
-  st.last_attention = true;
+  st.last_attention = call == Call::kAttention;
+  st.last_commit = call == Call::kCommit;
 }
 
 // whether the last call enqueued on ws was the verify attention (and forget it)
@@ -93,7 +102,7 @@ bool take_after_attention(const void* ws) {
   auto it = g_ws_state.find(ws);
   if (it == g_ws_state.end()) return false;
   const bool r = it->second.last_attention;
-  it->second.last_select = it->second.last_attention = false;
+  it->second.last_select = it->second.last_attention = it->second.last_commit = false;
   return r;
 }
 
@@ -101,10 +110,10 @@ bool take_after_attention(const void* ws) {
 std::pair<bool, int> take_select(const void* ws) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   WsState& st = g_ws_state[ws];
-  const bool early = st.last_select;
+  const bool early = st.last_select || st.last_commit;
   st.half ^= 1;
   st.last_select = true;
-  st.last_attention = false;
+  st.last_attention = st.last_commit = false;
   return {early, st.half};
 }
 
@@ -239,8 +248,8 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   const std::pair<bool, int> eh = take_select(ws);
   p.early = eh.first;
   p.half = eh.second;
-  p.counters = v.counters + size_t(eh.second) * b;
-  p.partials = v.partials + size_t(eh.second) * select_half_bytes(b, k, V);
+  p.counters = v.counters + 1 + size_t(eh.second) * b;  // word 0 is the commit's
+  p.partials = v.partials + select_base_bytes(b) + size_t(eh.second) * select_half_bytes(b, k, V);
   return launch_select_topk(p, as_stream(stream));
 }
 
@@ -293,7 +302,7 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16)) return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_VERIFY_ATTENTION, b, n, 1, 1, Hq, Hkv, max_seq_len);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  note_other(ws, true);
+  note_other(ws, Call::kAttention);
   const WsView v = ws_view(ws, b);
   AttentionParams p{};
   p.b = b;
@@ -405,7 +414,7 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
     return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_COMMIT_KV, b, n, 1, 1, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  note_other(ws);
+  note_other(ws, Call::kCommit);
   const WsView v = ws_view(ws, b);
   CommitParams p{};
   p.b = b;

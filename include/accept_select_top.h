@@ -120,10 +120,10 @@ int spec_device_sm_count(void);
  * (score_ld = k + (S-1)*k*k, parent_ld = 1 + (S-1)*k).  parent_blk may be NULL
  * (the last step's parent block is not part of the parent list).  topk_p_out
  * [b*rows, k] is optional (NULL).
- * Overlap: the library remembers, per workspace pointer, whether the last call
- * enqueued on it was spec_select_topk.  If it was, this call uses the other
- * half of the select's workspace area and starts its pass over draft_logits
- * before the previous select has finished (programmatic dependent launch);
+ * Overlap: the library remembers, per workspace pointer, which call was last
+ * enqueued on it.  If it was spec_select_topk or spec_commit_kv, this call
+ * uses the other half of the select's workspace area and starts its pass over
+ * draft_logits before that call has finished (programmatic dependent launch);
  * only the step's outputs wait for it.  draft_logits must therefore be ready
  * when this call is enqueued (any producer other than this library's kernels
  * is), as for every input.  spec_workspace_init resets the record.
