@@ -7,13 +7,18 @@ spec_verify_sampling) and spec_commit_kv.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Timing: W warm-up steps, then K steps replayed from CUDA graphs (one graph per
-step, cycling over input replicas whose combined size exceeds the 129 MB L2),
-bracketed by a barrier and torch.cuda.synchronize() on both sides, CUDA events
-on the launching stream, max over ranks.  Timing events captured inside each
-graph bracket every stage, so the dominant stage's duration is measured live
-in the timed region.  Under torchrun each rank verifies its own batch (weak
-scaling, no collective on the data path).
+Timing: W warm-up steps, then K steps replayed from CUDA graphs of P
+consecutive steps each (P <= 4 divides K; consecutive steps use different
+input replicas, whose combined size exceeds the 129 MB L2), bracketed by a
+barrier and torch.cuda.synchronize() on both sides, CUDA events on the
+launching stream, max over ranks.  The timed graphs hold only the kernels, so
+consecutive kernels overlap as they do for a caller running steps back to
+back.  Stage durations (for the roofline) come from a second pass right after
+the timed region: one-step graphs with CUDA events at the stage boundaries,
+each step run alone (the events and the per-step synchronisation remove the
+overlap across stages, so these durations are upper bounds).  Under torchrun
+each rank verifies its own batch (weak scaling, no collective on the data
+path).
 """
 from __future__ import annotations
 
@@ -266,34 +271,22 @@ def run_ours(args, torch):
     accept_lens = steps[0].accept_lens.cpu().numpy()
     assert steps[0].ws.last_error() == 0, "device error word set during warm-up"
 
-    # one graph per distinct step, with timing events captured at the stage boundaries
-    G = max(1, min(args.graphs, args.steps))
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        external = True
-    except TypeError:
-        external = False
-    graphs, evs = [], []
+    # Timed graphs: P consecutive steps each (one per input replica, so every
+    # step reads inputs the previous steps did not), with nothing but the
+    # kernels inside, so that consecutive kernels overlap as they do when a
+    # caller runs steps back to back (programmatic dependent launch does not
+    # cross a graph launch or an event node).  P divides K.
+    P = min(R, 4)
+    while args.steps % P:
+        P -= 1
+    G = max(1, min(args.graphs, args.steps // P))
+    graphs = []
     for j in range(G):
-        s = steps[j % R]
-        e = [torch.cuda.Event(enable_timing=True, external=True) if external else None for _ in range(4)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            if external:
-                e[0].record()
-            s.select()
-            s.build()
-            if external:
-                e[1].record()
-            s.attention()
-            if external:
-                e[2].record()
-            s.accept()
-            s.commit()
-            if external:
-                e[3].record()
+            for t in range(P):
+                steps[(j * P + t) % R].run()
         graphs.append(g)
-        evs.append(e)
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
             graphs[i % G].replay()
@@ -309,7 +302,7 @@ def run_ours(args, torch):
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record()
-        for i in range(args.steps):
+        for i in range(args.steps // P):
             graphs[i % G].replay()
         t1.record()
     torch.cuda.synchronize()
@@ -319,11 +312,43 @@ def run_ours(args, torch):
     elapsed_ms = job_elapsed_ms(t0.elapsed_time(t1), world, device, torch)
     assert steps[0].ws.last_error() == 0, "device error word set during the timed region"
 
+    # Stage breakdown (diagnostic, after the timed region): one-step graphs
+    # with timing events captured at the stage boundaries.
     stage = None
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        external = True
+    except TypeError:
+        external = False
     if external:
-        sel = [e[0].elapsed_time(e[1]) for e in evs]
-        att = [e[1].elapsed_time(e[2]) for e in evs]
-        acc = [e[2].elapsed_time(e[3]) for e in evs]
+        evs, sgraphs = [], []
+        for j in range(R):
+            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                s = steps[j]
+                e[0].record()
+                s.select()
+                s.build()
+                e[1].record()
+                s.attention()
+                e[2].record()
+                s.accept()
+                s.commit()
+                e[3].record()
+            sgraphs.append(g)
+            evs.append(e)
+        sel, att, acc = [], [], []
+        with torch.cuda.stream(stream):
+            for i in range(max(2 * R, min(args.steps, 200))):
+                sgraphs[i % R].replay()
+                if i >= R:  # warm
+                    torch.cuda.synchronize()
+                    e = evs[i % R]
+                    sel.append(e[0].elapsed_time(e[1]))
+                    att.append(e[1].elapsed_time(e[2]))
+                    acc.append(e[2].elapsed_time(e[3]))
+        torch.cuda.synchronize()
         stage = {"select_build": statistics.mean(sel), "attention": statistics.mean(att),
                  "accept_commit": statistics.mean(acc)}
 
@@ -331,7 +356,7 @@ def run_ours(args, torch):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, mode, steps[0], lay, torch)
-    return wl, mode, lay, elapsed_ms, stage, mask_bits, accept_lens, clocks, e2e, cpu, world, G, R, external
+    return wl, mode, lay, elapsed_ms, stage, mask_bits, accept_lens, clocks, e2e, cpu, world, G, R, external, P
 
 
 def run_e2e(args, torch, wl, mode, step, stream, device):
@@ -529,7 +554,7 @@ def main(argv=None):
         return 0
 
     (wl, mode, lay, elapsed_ms, stage, mask_bits, accept_lens, clocks, e2e, cpu, world, G, R,
-     external) = run_ours(args, torch)
+     external, P) = run_ours(args, torch)
     if rank != 0:
         return 0
     from accept_select_top_gb300.pipeline import launches_per_step
@@ -572,7 +597,9 @@ def main(argv=None):
                    "vocab": wl.V, "heads": f"{wl.Hq}/{wl.Hkv}", "head_dim": wl.D, "page_size": wl.page_size,
                    "context": list(wl.ctx), "accept": mode, "parallelism": f"replicas x{world}",
                    "l2": f"{R} rotating input replicas (> 4x the 129 MB L2 per cycle)",
-                   "graphs": G, "stage_timing": "events inside the step graphs" if external else "none"},
+                   "graphs": G, "steps_per_graph": P,
+                   "stage_timing": ("separate pass after the timed region: one-step graphs, events at the stage "
+                                    "boundaries, each step alone" if external else "none")},
         "stages_us": None if stage is None else {k: v * 1e3 for k, v in stage.items()},
         "mean_accept_lens": float(np.mean(accept_lens)),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
