@@ -333,6 +333,56 @@ def test_end_to_end_step(cases, name, mode):
         np.testing.assert_array_equal(W.host(inp.k_pool), kp0)
 
 
+def test_back_to_back_calls_on_one_workspace(cases):
+    """Calls enqueued back to back on one workspace with no synchronisation
+    between them: a select right after a select of the same step (the second
+    runs its chunk pass before the first has finished, on the other half of the
+    select's area), and the whole step twice in a row (a select right after the
+    KV commit, greedy accept right after the attention).  The results are
+    bit-identical to those of calls run one at a time on a fresh workspace --
+    apart from the second step's attention output, which reads the KV rows the
+    first step's commit moved (in this layout the committed positions are the
+    tree's own slots)."""
+    from accept_select_top_gb300.pipeline import VerifyStep
+    c = cases("llama8b_greedy", "greedy")
+    wl, ops = c.wl, _ops()
+    size = ops.spec_workspace_size(ops.OP_SELECT_TOPK, wl.b, wl.n, wl.k, wl.V)
+    ws = ops.Workspace(size)
+    pairs, scores_in = [], None
+    for i in range(wl.S):
+        first = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws)
+        second = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws)
+        pairs.append((first, second))
+        scores_in = first["scores_out"]
+    torch.cuda.synchronize()
+    assert ws.last_error() == 0
+    ws_ref, scores_in = ops.Workspace(size), None
+    for i, (first, second) in enumerate(pairs):
+        ref = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws_ref)
+        torch.cuda.synchronize()
+        for k_, v in ref.items():
+            assert torch.equal(first[k_], v), (i, k_)
+            assert torch.equal(second[k_], v), (i, k_)
+        scores_in = ref["scores_out"]
+
+    def fresh():
+        inp = c.device_inputs()
+        inp.k_pool, inp.v_pool = inp.k_pool.clone(), inp.v_pool.clone()
+        return VerifyStep(wl, inp, "greedy")
+    names = ("draft_tokens", "positions", "mask_bits", "predict", "accept_index", "accept_lens",
+             "accepted_tokens", "next_root", "new_seq_lens", "free_ids", "n_free")
+    twice = fresh()
+    twice.run()
+    twice.run()
+    torch.cuda.synchronize()
+    assert twice.ws.last_error() == 0
+    once = fresh()
+    once.run()
+    torch.cuda.synchronize()
+    for k_ in names:
+        assert torch.equal(getattr(twice, k_), getattr(once, k_)), k_
+
+
 # ------------------------------------------------------------- edge cases
 
 def test_idle_batch_and_bad_workspace():
