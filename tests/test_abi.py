@@ -49,6 +49,23 @@ def test_workspace_sizes_host_only():
     assert ops.spec_workspace_size(99, 8, 16, 4, 1000) == 0
 
 
+def test_workspace_layout_keeps_overlapping_calls_apart_host_only():
+    """Greedy accept may scan while the attention before it finishes, so its
+    partials lie past the attention's merge area: its workspace need covers that
+    area plus its own partials, for any batch.  The select keeps two halves of
+    its partials (a select may overlap the previous one), past the commit's
+    area."""
+    from accept_select_top_gb300 import ops
+    for b, n in ((1, 4), (8, 16), (32, 64), (256, 4)):
+        att = ops.spec_workspace_size(ops.OP_VERIFY_ATTENTION, b, n, 1, 1, 32, 8, 4096)
+        gre = ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, b, n, 1, 128256)
+        assert gre > att, (b, n)
+    base = ops.spec_workspace_size(ops.OP_BUILD_TREE, 8, 16, 4, 128256)  # header + counters only
+    sel = ops.spec_workspace_size(ops.OP_SELECT_TOPK, 8, 16, 4, 128256)
+    # two halves of 32 rows x 19 chunks x 144-byte partials, past the commit's area
+    assert sel - base >= 2 * 32 * 19 * 144
+
+
 def test_attention_launch_count_host_only():
     """One launch for any valid sizes (split key lists are merged in the kernel)."""
     from accept_select_top_gb300 import ops
