@@ -4,13 +4,17 @@
 // [SGL-XI organize_draft_results: _select_top_k_tokens_first / _later, the
 // parent offset topk_cs_index + topk^2 (i-1) + topk], [SGL-XI draft() 主循环].
 //
-// Grid: (chunks, rows), rows = b * (step ? k : 1).  Each CTA streams one chunk
-// of one draft row once, keeping per thread an online softmax (running max and
-// sum of exp) and a sorted top-K list (K = topk rounded up to a power of two);
-// the CTA merges these into one partial (max, sum, K best logits).  The CTA
-// arriving last for a request merges the partials of the request's rows (one
-// warp per row: k-round tournament over the chunk lists), turns the k best
-// logits into probabilities, and runs the path-score step for the request.
+// Grid: (chunks, rows), rows = b * (step ? k : 1).  Each CTA reads one chunk
+// of one draft row once into registers (32 logits a thread).  Each warp takes
+// its maximum Mw and its sum of exp((x - Mw) / T); the k-th largest warp
+// maximum bounds the chunk's k best from below (k distinct elements in k
+// different warps reach it), so only the few elements at or above it are
+// ranked; the CTA writes one partial (max, sum, K best logits, K = topk
+// rounded up to a power of two).  The CTA arriving last for a request merges
+// the partials of the request's rows (one warp per row, each lane holding one
+// chunk's list: a k-round tournament), turns the k best logits into
+// probabilities, and runs the path-score step for the request.  The chunk
+// pass may overlap the call before it (see the kernel).
 #include "common.cuh"
 #include "kernels.cuh"
 
