@@ -70,20 +70,22 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
 // enqueued right after another select, or after a KV commit, on the same
 // workspace takes the other half and runs its chunk pass before waiting on
 // that call (programmatic dependent launch; neither touches the select's
-// area); after any other call it waits first.  Every kernel lets
-// its successor start only after its own wait, so a kernel overlaps only the
-// one kernel before it.
+// area); after any other call it waits first.  The workspace layout depends
+// on the batch size, so a call overlaps the one before it only when both
+// have the same b.  Every kernel lets its successor start only after its own
+// wait, so a kernel overlaps only the one kernel before it.
 struct WsState {
   bool last_select = false;
   bool last_attention = false;
   bool last_commit = false;
   int half = 1;
+  int b = -1;  // batch size of the last call
 };
 std::mutex g_ws_mu;
 std::unordered_map<const void*, WsState> g_ws_state;
 
 enum class Call { kOther, kAttention, kCommit };
-void note_other(const void* ws, Call call = Call::kOther) {
+void note_other(const void* ws, Call call = Call::kOther, int b = -1) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   if (call == Call::kOther) {
     auto it = g_ws_state.find(ws);
@@ -94,26 +96,29 @@ void note_other(const void* ws, Call call = Call::kOther) {
   st.last_select = false;
   st.last_attention = call == Call::kAttention;
   st.last_commit = call == Call::kCommit;
+  st.b = b;
 }
 
-// whether the last call enqueued on ws was the verify attention (and forget it)
-bool take_after_attention(const void* ws) {
+// whether the last call enqueued on ws was the verify attention with the
+// same batch size (and forget it)
+bool take_after_attention(const void* ws, int b) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   auto it = g_ws_state.find(ws);
   if (it == g_ws_state.end()) return false;
-  const bool r = it->second.last_attention;
+  const bool r = it->second.last_attention && it->second.b == b;
   it->second.last_select = it->second.last_attention = it->second.last_commit = false;
   return r;
 }
 
-// (early, half) for a select about to be enqueued on ws
-std::pair<bool, int> take_select(const void* ws) {
+// (early, half) for a select of batch size b about to be enqueued on ws
+std::pair<bool, int> take_select(const void* ws, int b) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   WsState& st = g_ws_state[ws];
-  const bool early = st.last_select || st.last_commit;
+  const bool early = (st.last_select || st.last_commit) && st.b == b;
   st.half ^= 1;
   st.last_select = true;
   st.last_attention = st.last_commit = false;
+  st.b = b;
   return {early, st.half};
 }
 
@@ -140,7 +145,7 @@ int greedy_call(bool compact, int b, int n, int S, int V, int dtype, const void*
   const size_t need = compact ? kHeaderBytes + counters_bytes(b) + greedy_part_bytes(b, n, V)
                               : spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  const bool early = !compact && take_after_attention(ws);
+  const bool early = !compact && take_after_attention(ws, b);
   if (compact) note_other(ws);
   const WsView v = ws_view(ws, b);
   GreedyParams p{};
@@ -245,7 +250,7 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(draft_logits, V, dtype);
   p.error = v.error;
-  const std::pair<bool, int> eh = take_select(ws);
+  const std::pair<bool, int> eh = take_select(ws, b);
   p.early = eh.first;
   p.half = eh.second;
   p.counters = v.counters + 1 + size_t(eh.second) * b;  // word 0 is the commit's
@@ -302,7 +307,7 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16)) return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_VERIFY_ATTENTION, b, n, 1, 1, Hq, Hkv, max_seq_len);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  note_other(ws, Call::kAttention);
+  note_other(ws, Call::kAttention, b);
   const WsView v = ws_view(ws, b);
   AttentionParams p{};
   p.b = b;
@@ -414,7 +419,7 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
     return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_COMMIT_KV, b, n, 1, 1, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
-  note_other(ws, Call::kCommit);
+  note_other(ws, Call::kCommit, b);
   const WsView v = ws_view(ws, b);
   CommitParams p{};
   p.b = b;
