@@ -28,10 +28,13 @@
  *     not selected).
  *
  * Parity status: every function is pinned by tests against values the pages
- * print, closed forms, library routines or brute force, except the rejection
- * sampler on trees with more than one child per node, whose multi-sibling rule
- * is pinned only by its single-candidate special case, the T=0 == greedy
- * identity and a distribution test: "parity unpinned" beyond those.
+ * print, closed forms, library routines or brute force.  The rejection sampler
+ * on trees with several children per node follows a reading of the pages (p
+ * and q fixed across siblings, one coin per child), which the pages give no
+ * numbers for; it is pinned against that reading's closed-form law for one
+ * sibling level (each sibling's acceptance probability and the residual's
+ * share, by a chi-square test), besides the single-candidate values the pages
+ * print and the T=0 == greedy identity.
  */
 #ifndef ACCEPT_SELECT_TOP_ORACLE_H
 #define ACCEPT_SELECT_TOP_ORACLE_H

@@ -253,6 +253,66 @@ def test_rejection_chi_square():
     assert abs(acc - a) < 4 * np.sqrt(a * (1 - a) / N)
 
 
+def _one_level_siblings(p, q, xs, u, uf):
+    """b requests, each a root (target p, draft q) with len(xs) leaf children
+    in sibling order carrying tokens xs; u[b, m] are the children's coins."""
+    b, m = u.shape
+    V = len(p)
+    n = m + 1
+    logits = np.zeros((b * n, V), np.float32)  # leaves: uniform p (their bonus draws)
+    logits[0::n] = np.log(np.asarray(p, np.float64)).astype(np.float32)
+    qq = np.zeros((b * n, V), np.float32)
+    qq[0::n] = np.asarray(q, np.float32)
+    draft = np.tile(np.array([0] + list(xs), np.int32), b)
+    uu = np.zeros((b, n), np.float32)
+    uu[:, 1:] = u
+    nt = np.tile(np.array([1] + [-1] * m, np.int32), b)
+    ns = np.tile(np.array([-1] + list(range(2, n)) + [-1], np.int32), b)
+    return oracle.verify_sampling(b, n, 1, logits, qq, np.ones(b, np.float32), uu.ravel(),
+                                  np.asarray(uf, np.float32), draft, np.arange(b * n), nt, ns)
+
+
+def test_rejection_siblings_closed_form():
+    """One level, three sibling leaves with distinct tokens, p and q fixed
+    across siblings, one coin per child.  With a_i = min(1, p(x_i)/q(x_i)),
+    sibling i is accepted with probability prod_{j<i}(1 - a_j) a_i, and with
+    prod_j (1 - a_j) every child is rejected and the output token follows
+    max(0, p - q)/Z.  1e5 seeded trials against that law (chi-square over the
+    outcomes: accepted sibling, or the residual token), which fixes the
+    sibling order, the per-child coin and the node the residual is taken at."""
+    rng = np.random.default_rng(11)
+    V, m, N = 12, 3, 100_000
+    p = rng.dirichlet(np.full(V, 0.7))
+    q = rng.dirichlet(np.full(V, 0.7))
+    pf = np.exp(np.log(p).astype(np.float32).astype(np.float64))
+    pf /= pf.sum()  # the oracle's p: softmax of the fp32 log-probabilities
+    qf = q.astype(np.float32).astype(np.float64)
+    # siblings on tokens with p < q, so that every one can be rejected and
+    # every outcome (each sibling, the residual) has a fair share
+    xs = [int(v) for v in rng.choice(np.flatnonzero(pf < 0.8 * qf), size=m, replace=False)]
+    a = np.minimum(1.0, pf[xs] / qf[xs])
+    reach = np.concatenate([[1.0], np.cumprod(1.0 - a)])  # reach[i]: all of the first i rejected
+    p_acc = reach[:m] * a
+    res = np.maximum(pf - qf, 0.0)
+    res /= res.sum()
+    expect = np.concatenate([p_acc, reach[m] * res])  # outcomes: sibling 0..m-1, then residual token v
+    assert p_acc.min() > 0.02 and reach[m] > 0.05  # a non-degenerate case
+    u = rng.random((N, m)).astype(np.float32)
+    uf = rng.random(N).astype(np.float32)
+    o = _one_level_siblings(p, q, xs, u, uf)
+    acc = o["accept_lens"] == 2
+    idx = o["accept_index"][:, 1] - np.arange(N) * (m + 1) - 1  # accepted sibling, -1 / -(..) if none
+    outcome = np.where(acc, idx, m + o["accepted_tokens"][:, 0])
+    counts = np.bincount(outcome, minlength=m + V)
+    keep = expect > 0
+    assert counts[~keep].sum() == 0
+    stat, pval = scipy.stats.chisquare(counts[keep], expect[keep] * N)
+    assert pval > 1e-3, (stat, pval)
+    # an accepted sibling's token is the first output; the leaf's bonus is uniform
+    first = o["accepted_tokens"][:, 0]
+    np.testing.assert_array_equal(first[acc], np.array(xs)[idx[acc]])
+
+
 def test_residual_zero_falls_back_to_p():
     """q == p at the only child's row and the child rejected: Z would be 0 only
     if p <= q everywhere; here q puts all mass on x, p does not, so the
