@@ -148,6 +148,16 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
         return str(dev_index)
 
 
+def steps_per_graph(replicas: int, steps: int) -> int:
+    """Consecutive steps captured in one timed graph: at most 4 and at most the
+    number of input replicas (consecutive steps then read different inputs),
+    and a divisor of the timed step count, so that exactly `steps` run."""
+    P = max(1, min(replicas, 4, steps))
+    while steps % P:
+        P -= 1
+    return P
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -276,9 +286,7 @@ def run_ours(args, torch):
     # kernels inside, so that consecutive kernels overlap as they do when a
     # caller runs steps back to back (programmatic dependent launch does not
     # cross a graph launch or an event node).  P divides K.
-    P = min(R, 4)
-    while args.steps % P:
-        P -= 1
+    P = steps_per_graph(R, args.steps)
     G = max(1, min(args.graphs, args.steps // P))
     graphs = []
     for j in range(G):

@@ -73,3 +73,13 @@ def test_single_rank_reference_line_without_gpu():
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference"
+
+
+def test_steps_per_graph_divides_the_timed_steps():
+    import bench
+    for R in (1, 2, 3, 4, 8):
+        for K in (1, 2, 3, 5, 7, 12, 2000, 2001):
+            P = bench.steps_per_graph(R, K)
+            assert 1 <= P <= min(R, 4, K) and K % P == 0, (R, K, P)
+    assert bench.steps_per_graph(4, 2000) == 4
+    assert bench.steps_per_graph(2, 5) == 1
