@@ -117,13 +117,13 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialisation (launch_pdl).  A kernel waits for the
 // grid before it -- its completion and its memory -- before reading anything
-// that grid may write (pdl_wait), and only then lets the grid after it be
-// scheduled (pdl_trigger).  So a kernel's work before its wait can overlap
-// only the one kernel right before it, never an earlier one.  The select's
-// chunk pass is such work when the kernel before it is the previous select
-// (the two use different halves of the select's area) or the KV commit on
-// the same workspace, and greedy accept's scan when the kernel before it is
-// the verify attention; every other kernel waits first.
+// (pdl_wait), and only then lets the grid after it be scheduled
+// (pdl_trigger).  So only a kernel's prologue overlaps the kernel before it.
+// Two kernels may do work before their wait, and only when the caller has
+// allowed overlap on the workspace: the select's chunk pass when the kernel
+// before it is the previous select (the two use different halves of the
+// select's area) or the KV commit on the same workspace, and greedy accept's
+// scan when the kernel before it is the verify attention.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -23,9 +23,10 @@ struct SelectParams {
   int rows, chunks, chunk_elems;
   bool vec_ok;
   // The chunk pass may run before the launch waits on the kernel ahead of
-  // it (early): only when that kernel is the previous select on the same
-  // workspace, which uses the other half (1 - half) of the partials and
-  // counters, or the KV commit, which uses neither.
+  // it (early): only with overlap allowed on the workspace, and only when
+  // that kernel is the previous select on it, which uses the other half
+  // (1 - half) of the partials and counters, or the KV commit, which uses
+  // neither.
   bool early;
   int half;
   uint32_t* error;
@@ -64,9 +65,9 @@ struct GreedyParams {
   int chunks, chunk_elems;
   bool vec_ok;
   // The scan may run before the launch waits on the kernel ahead of it
-  // (early): only when that kernel is the verify attention on the same
-  // workspace, whose merge slots and counters the scan's partials and
-  // counters do not share.
+  // (early): only with overlap allowed on the workspace, and only when that
+  // kernel is the verify attention on it, whose merge slots and counters the
+  // scan's partials and counters do not share.
   bool early;
   uint32_t* error;
   uint32_t* counters;
@@ -157,8 +158,8 @@ size_t sampling_partial2_bytes(int b, int chunks2);
 size_t commit_partial_bytes(int b, int n);
 
 // Geometry of the tensor-core attention: m_tiles units of 128 query rows per
-// (request, kv head); splits is the number of launches' worth of key splits
-// (always 1: units split over CTAs are merged inside the kernel).
+// (request, kv head); splits is always 1 (units split over CTAs are merged
+// inside the kernel, in the same launch).
 struct TcGeometry {
   int m_tiles, split_tiles, splits;
 };

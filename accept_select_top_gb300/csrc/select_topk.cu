@@ -13,8 +13,9 @@
 // rounded up to a power of two).  The CTA arriving last for a request merges
 // the partials of the request's rows (one warp per row, each lane holding one
 // chunk's list: a k-round tournament), turns the k best logits into
-// probabilities, and runs the path-score step for the request.  The chunk
-// pass may overlap the call before it (see the kernel).
+// probabilities, and runs the path-score step for the request.  With overlap
+// allowed by the caller, the chunk pass may overlap the call before it (see
+// the kernel).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -217,12 +218,12 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
-  // The chunk pass reads only the draft logits (which no kernel of the
-  // library writes) and this call's half of the select's workspace area.
-  // When the kernel before is the previous select (which uses the other
-  // half) or the KV commit on the same workspace, the pass runs before
-  // waiting on it; only the finalize, which reads the previous step's scores
-  // and writes this step's outputs, waits.
+  // The chunk pass reads only the draft logits and this call's half of the
+  // select's workspace area.  When the caller has allowed overlap and the
+  // kernel before is the previous select (which uses the other half) or the
+  // KV commit on the same workspace, the pass runs before waiting on it; only
+  // the finalize, which reads the previous step's scores and writes this
+  // step's outputs, waits.  Otherwise everything waits.
   if (!a.early) {
     pdl_wait();
     pdl_trigger();

@@ -65,16 +65,21 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
   }
 }
 
-// Per workspace: whether the last call enqueued on it was a select, and the
-// half (of the select partials and counters) that select used.  A select
-// enqueued right after another select, or after a KV commit, on the same
-// workspace takes the other half and runs its chunk pass before waiting on
-// that call (programmatic dependent launch; neither touches the select's
-// area); after any other call it waits first.  The workspace layout depends
-// on the batch size, so a call overlaps the one before it only when both
-// have the same b.  Every kernel lets its successor start only after its own
-// wait, so a kernel overlaps only the one kernel before it.
+// Per workspace: whether the caller has allowed overlap with the call before
+// (spec_workspace_set_overlap; off by default), whether the last call enqueued
+// on it was a select, and the half (of the select partials and counters) that
+// select used.  With overlap allowed, a select enqueued right after another
+// select, or after a KV commit, on the same workspace takes the other half and
+// runs its chunk pass before waiting on that call (programmatic dependent
+// launch; neither touches the select's area), and greedy accept right after
+// the verify attention scans its logits before waiting.  Otherwise every
+// kernel waits for the kernel before it -- whatever produced it -- before it
+// reads anything.  The workspace layout depends on the batch size, so a call
+// overlaps the one before it only when both have the same b.  Every kernel
+// lets its successor start only after its own wait, so a kernel overlaps only
+// the one kernel before it.
 struct WsState {
+  bool overlap = false;
   bool last_select = false;
   bool last_attention = false;
   bool last_commit = false;
@@ -99,13 +104,14 @@ void note_other(const void* ws, Call call = Call::kOther, int b = -1) {
   st.b = b;
 }
 
-// whether the last call enqueued on ws was the verify attention with the
-// same batch size (and forget it)
+// whether greedy accept of batch size b may scan before waiting: overlap is
+// allowed and the last call enqueued on ws was the verify attention with the
+// same batch size (the record is cleared either way)
 bool take_after_attention(const void* ws, int b) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   auto it = g_ws_state.find(ws);
   if (it == g_ws_state.end()) return false;
-  const bool r = it->second.last_attention && it->second.b == b;
+  const bool r = it->second.overlap && it->second.last_attention && it->second.b == b;
   it->second.last_select = it->second.last_attention = it->second.last_commit = false;
   return r;
 }
@@ -114,12 +120,18 @@ bool take_after_attention(const void* ws, int b) {
 std::pair<bool, int> take_select(const void* ws, int b) {
   std::lock_guard<std::mutex> lock(g_ws_mu);
   WsState& st = g_ws_state[ws];
-  const bool early = (st.last_select || st.last_commit) && st.b == b;
+  const bool early = st.overlap && (st.last_select || st.last_commit) && st.b == b;
   st.half ^= 1;
   st.last_select = true;
   st.last_attention = st.last_commit = false;
   st.b = b;
   return {early, st.half};
+}
+
+// forget everything recorded for ws (overlap back to off)
+void reset_state(const void* ws) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  g_ws_state.erase(ws);
 }
 
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -189,8 +201,16 @@ size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, 
 
 int spec_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws) return SPEC_ERR_WORKSPACE;
-  note_other(ws);
+  reset_state(ws);
   return cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_workspace_set_overlap(void* ws, int enable) {
+  if (!ws) return SPEC_ERR_WORKSPACE;
+  if (enable != 0 && enable != 1) return SPEC_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  g_ws_state[ws].overlap = enable != 0;
+  return SPEC_OK;
 }
 
 int spec_last_error(void* ws, void* stream) {
@@ -338,12 +358,6 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size, c
   p.partials = v.partials;
   return launch_attention_tc(p, geo, as_stream(stream));
 }
-
-int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len) {
-  if (b < 1 || n < 1 || n > kMaxN || Hq < 1 || Hkv < 1 || Hq % Hkv || max_seq_len < 0) return 0;
-  return attention_tc_geometry(b, n, Hq, Hkv, max_seq_len).splits;
-}
-
 
 int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
                        const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,

@@ -77,10 +77,10 @@ __device__ __forceinline__ void scan_argmax_bf16(const uint16_t* row, int begin,
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
-  // The scan reads only the target logits (which no kernel of the library
-  // writes) and greedy's own partials and counters.  When the kernel before
-  // is the verify attention on the same workspace, the scan runs before
-  // waiting on it; only the finalize waits.
+  // The scan reads only the target logits and greedy's own partials and
+  // counters.  When the caller has allowed overlap and the kernel before is
+  // the verify attention on the same workspace, the scan runs before waiting
+  // on it; only the finalize waits.  Otherwise everything waits.
   if (!a.early) {
     pdl_wait();
     pdl_trigger();

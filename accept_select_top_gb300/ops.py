@@ -25,9 +25,10 @@ DEV_INDEX, DEV_INVARIANT, DEV_LENGTH = 1, 2, 4
 _ERRORS = {-1: "bad argument", -2: "workspace too small or misaligned", -3: "CUDA launch failed",
            -4: "unsupported dtype or head size"}
 
-EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_last_error", "spec_device_sm_count",
-           "spec_select_topk", "spec_build_tree", "spec_verify_attention", "spec_verify_attention_splits", "spec_verify_greedy",
-           "spec_verify_sampling", "spec_commit_kv", "spec_verify_greedy_noalloc"]
+EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_workspace_set_overlap", "spec_last_error",
+           "spec_device_sm_count", "spec_select_topk", "spec_build_tree", "spec_verify_attention",
+           "spec_verify_greedy", "spec_verify_sampling", "spec_commit_kv", "spec_verify_greedy_noalloc",
+           "spec_noalloc_last_error"]
 
 
 class SpecError(RuntimeError):
@@ -42,16 +43,17 @@ def _load() -> ctypes.CDLL:
     sig = {
         "spec_workspace_size": (Z, [I, I, I, I, I, I, I, I]),
         "spec_workspace_init": (I, [P, Z, P]),
+        "spec_workspace_set_overlap": (I, [P, I]),
         "spec_last_error": (I, [P, P]),
         "spec_device_sm_count": (I, []),
         "spec_select_topk": (I, [I, I, I, I, I, P, F, P, P, P, I, P, I, P, P, P, P, Z, P]),
         "spec_build_tree": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_attention": (I, [I, I, I, I, I, I, P, P, P, L, P, I, I, P, P, I, P, P, F, P, P, P, Z, P]),
-        "spec_verify_attention_splits": (I, [I, I, I, I, I]),
         "spec_verify_greedy": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_sampling": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_commit_kv": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_greedy_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]),
+        "spec_noalloc_last_error": (I, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -106,6 +108,12 @@ class Workspace:
     def ptr(self):
         return ctypes.c_void_p(self.tensor.data_ptr())
 
+    def set_overlap(self, enable: bool):
+        """Allow (or forbid) a select or greedy accept on this workspace to read
+        its main input before the kernel ahead of it has finished.  Off by
+        default; see spec_workspace_set_overlap for what the caller asserts."""
+        _check(LIB.spec_workspace_set_overlap(self.ptr, 1 if enable else 0), "spec_workspace_set_overlap")
+
     def last_error(self, stream=None) -> int:
         rc = LIB.spec_last_error(self.ptr, _stream(stream))
         if rc < 0:
@@ -120,11 +128,6 @@ def spec_workspace_size(op: int, b: int, n: int, k: int, V: int, Hq: int = 0, Hk
 
 def spec_device_sm_count() -> int:
     return int(LIB.spec_device_sm_count())
-
-
-def spec_verify_attention_splits(b: int, n: int, Hq: int, Hkv: int, max_seq_len: int) -> int:
-    """Kernel launches spec_verify_attention makes for these sizes (0: invalid sizes)."""
-    return int(LIB.spec_verify_attention_splits(b, n, Hq, Hkv, max_seq_len))
 
 
 def spec_select_topk(step: int, b: int, k: int, draft_logits: torch.Tensor, temperature: float,
@@ -204,3 +207,12 @@ def spec_verify_greedy_noalloc(b: int, n: int, S: int, logits, draft_tokens, ret
                                           _ptr(retrieve_index), _ptr(next_token), _ptr(next_sibling), _ptr(predict),
                                           _ptr(accept_index), _ptr(accept_lens), _ptr(accepted_tokens),
                                           _ptr(next_root), _stream(stream)), "spec_verify_greedy_noalloc")
+
+
+def spec_noalloc_last_error(stream=None) -> int:
+    """Reads and clears the SPEC_DEV_* bits set by spec_verify_greedy_noalloc
+    calls on the current device (synchronises the stream)."""
+    rc = LIB.spec_noalloc_last_error(_stream(stream))
+    if rc < 0:
+        _check(rc, "spec_noalloc_last_error")
+    return rc

@@ -48,7 +48,7 @@ class DeviceInputs:
 
 class VerifyStep:
     def __init__(self, wl: Workload, inp: DeviceInputs, mode: str = "greedy", device="cuda",
-                 draft_temperature: float = 1.0, with_lse: bool = True):
+                 draft_temperature: float = 1.0, with_lse: bool = True, overlap: bool = False):
         assert mode in ("greedy", "sampling")
         self.wl, self.inp, self.mode = wl, inp, mode
         self.draft_temperature = draft_temperature
@@ -80,23 +80,33 @@ class VerifyStep:
         nbytes = max(ops.spec_workspace_size(op, b, n, k, wl.V, wl.Hq, wl.Hkv, inp.max_seq_len)
                      for op in range(6))
         self.ws = ops.Workspace(nbytes, device=device)
+        # overlap asserts that every draft-logits / target-logits input is
+        # complete before the previous call is enqueued (true when all inputs
+        # are resident up front, as in a benchmark; false in an EAGLE loop,
+        # where the draft forward and the target's LM head run in between)
+        self.overlap = bool(overlap)
+        self.ws.set_overlap(self.overlap)
         # select step i writes its blocks at these offsets of the score / parent spaces
         self.score_off = [0 if i == 0 else k + (i - 1) * k * k for i in range(S)]
         # parent list = [-1, 0..k-1] (step 0, k+1 entries), then k entries per later step
         self.parent_off = [0 if i == 0 else 1 + i * k for i in range(S)]
 
     # ----------------------------------------------------------- the calls
-    def select(self, stream=None):
+    def select_step(self, i: int, stream=None):
+        """Draft step i of select_top_k_tokens (one spec_select_topk call)."""
         wl, k = self.wl, self.wl.k
-        for i in range(wl.S):
-            last = i == wl.S - 1
-            pblk = _view_from(self.last_parent, 0) if last else _view_from(self.parent_space, self.parent_off[i])
-            ops.spec_select_topk(
-                i, wl.b, k, self.inp.drafts[i], self.draft_temperature,
-                None if i == 0 else self.scores[(i - 1) % 2],
-                _view_from(self.score_space, self.score_off[i]), _view_from(self.token_space, self.score_off[i]),
-                wl.C, pblk, (k + 1 if i == 0 else k) if last else wl.P,
-                self.scores[i % 2], self.next_ids, None, self.ws, stream)
+        last = i == wl.S - 1
+        pblk = _view_from(self.last_parent, 0) if last else _view_from(self.parent_space, self.parent_off[i])
+        ops.spec_select_topk(
+            i, wl.b, k, self.inp.drafts[i], self.draft_temperature,
+            None if i == 0 else self.scores[(i - 1) % 2],
+            _view_from(self.score_space, self.score_off[i]), _view_from(self.token_space, self.score_off[i]),
+            wl.C, pblk, (k + 1 if i == 0 else k) if last else wl.P,
+            self.scores[i % 2], self.next_ids, None, self.ws, stream)
+
+    def select(self, stream=None):
+        for i in range(self.wl.S):
+            self.select_step(i, stream)
 
     def build(self, stream=None):
         wl = self.wl
@@ -135,17 +145,14 @@ class VerifyStep:
         self.commit(stream)
 
     def launches_per_step(self) -> int:
-        return launches_per_step(self.wl, self.mode, self.inp.max_seq_len)
+        return launches_per_step(self.wl, self.mode)
 
 
-def launches_per_step(wl: Workload, mode: str, max_seq_len: int) -> int:
-    """Kernels one VerifyStep.run() launches: S selects, build, attention (plus
-    a merge when the key lists are split), accept (sampling: two passes),
-    commit."""
-    splits = ops.spec_verify_attention_splits(wl.b, wl.n, wl.Hq, wl.Hkv, max_seq_len)
-    if splits < 1:
-        raise ValueError("invalid attention sizes")
-    return wl.S + 1 + (1 if splits == 1 else 2) + (1 if mode == "greedy" else 2) + 1
+def launches_per_step(wl: Workload, mode: str) -> int:
+    """Kernels one VerifyStep.run() launches: S selects, the tree build, the
+    attention (one launch: split key lists are merged inside it), the accept
+    (greedy one launch, sampling two passes) and the KV commit."""
+    return wl.S + 1 + 1 + (1 if mode == "greedy" else 2) + 1
 
 
 def _view_from(t: torch.Tensor, offset: int) -> torch.Tensor:

@@ -26,9 +26,12 @@
  *     first use.  Every call leaves it zero again apart from the error word, so
  *     one workspace serves any sequence of calls on one stream.  Calls that may
  *     run concurrently (different streams) need separate workspaces.  Every
- *     kernel is launched with programmatic dependent launch and lets the next
- *     kernel start only after it has waited for the one before it, so at most
- *     two consecutive kernels overlap (see spec_select_topk).
+ *     kernel is launched with programmatic dependent launch: by default it
+ *     waits for the kernel before it on the stream -- whichever library or
+ *     framework launched that kernel -- before it reads any input, and only
+ *     then lets the next kernel start, so inputs written by any earlier work
+ *     on the stream are safe to read.  spec_workspace_set_overlap lets a
+ *     caller allow two calls to start reading earlier (see there).
  *   - Return codes: SPEC_OK, SPEC_ERR_ARG (null pointer, bad size or shape, a
  *     limit below exceeded), SPEC_ERR_WORKSPACE (ws too small or misaligned),
  *     SPEC_ERR_LAUNCH (the CUDA launch failed; cudaGetLastError is consumed),
@@ -85,8 +88,29 @@ extern "C" {
  * Returns 0 for an unknown op or invalid sizes. */
 size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len);
 
-/* Zero-fills a workspace (cudaMemsetAsync on `stream`). */
+/* Zero-fills a workspace (cudaMemsetAsync on `stream`) and forgets what the
+ * library recorded for this address (overlap back to off). */
 int spec_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Overlap with the call before (off by default; enable = 0 or 1).  The pages
+ * have no counterpart: it is a scheduling permission.  With overlap on, two
+ * calls may read their main input before the kernel ahead of them on the
+ * stream has finished (programmatic dependent launch):
+ *   - spec_select_topk reads draft_logits early when the last call enqueued
+ *     on this workspace (same batch size) was spec_select_topk or
+ *     spec_commit_kv;
+ *   - spec_verify_greedy reads logits early when the last call enqueued on
+ *     this workspace (same batch size) was spec_verify_attention.
+ * By enabling it the caller asserts that, for every call on this workspace,
+ * that input was complete before the previous library call on the stream
+ * was enqueued: no kernel that writes it sits between the two calls on the
+ * stream (in an EAGLE loop the draft forward runs between two selects and the
+ * target's MLP and LM head between the attention and the accept, so overlap
+ * must stay off there).  The library records, per workspace address and
+ * under a mutex, which call was last enqueued on it; that record is the only
+ * host state of the library.  Returns SPEC_ERR_WORKSPACE for a NULL ws and
+ * SPEC_ERR_ARG for another enable value. */
+int spec_workspace_set_overlap(void* ws, int enable);
 
 /* Synchronises `stream`, returns the device error word (SPEC_DEV_* bits, 0 if
  * clean) and clears it; a negative SPEC_ERR_* on failure. */
@@ -120,13 +144,11 @@ int spec_device_sm_count(void);
  * (score_ld = k + (S-1)*k*k, parent_ld = 1 + (S-1)*k).  parent_blk may be NULL
  * (the last step's parent block is not part of the parent list).  topk_p_out
  * [b*rows, k] is optional (NULL).
- * Overlap: the library remembers, per workspace pointer, which call was last
- * enqueued on it.  If it was spec_select_topk or spec_commit_kv, this call
- * uses the other half of the select's workspace area and starts its pass over
- * draft_logits before that call has finished (programmatic dependent launch);
- * only the step's outputs wait for it.  draft_logits must therefore be ready
- * when this call is enqueued (any producer other than this library's kernels
- * is), as for every input.  spec_workspace_init resets the record.
+ * Consecutive selects on one workspace alternate between two halves of the
+ * select's workspace area.  With overlap on (spec_workspace_set_overlap) and
+ * the last call on the workspace a select or a KV commit, the pass over
+ * draft_logits starts before that call has finished; only the step's outputs
+ * wait for it.  With overlap off (the default) the kernel waits first.
  * ------------------------------------------------------------------------- */
 int spec_select_topk(int step, int b, int k, int V, int dtype,
                      const void* draft_logits, float temperature,
@@ -191,12 +213,6 @@ int spec_verify_attention(int b, int n, int Hq, int Hkv, int D, int page_size,
                           float scale, void* out, float* lse,
                           void* ws, size_t ws_bytes, void* stream);
 
-/* Kernel launches spec_verify_attention makes for these sizes (host only, no
- * device call): 1 with the current kernel, which merges split key lists
- * itself.  0 for invalid sizes.  (An implementation detail the method itself
- * has no counterpart for: it lets a caller count launches.) */
-int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len);
-
 /* ---------------------------------------------------------------------------
  * spec_verify_greedy -- greedy accept.
  * [SGL-XI eagle_sample (路径一:贪心验证)], [ACCEPT section 3], [EAGLE2 5.3].
@@ -211,11 +227,11 @@ int spec_verify_attention_splits(int b, int n, int Hq, int Hkv, int max_seq_len)
  * (-1 padded), accept_lens [b] = accepted drafts + 1; optional (NULL):
  * accepted_tokens [b, S+1] = predict[accept_index] (-1 padded), next_root [b]
  * = the last accepted token.
- * Overlap: when the last call enqueued on the workspace was
- * spec_verify_attention, the argmax pass over logits starts before that call
- * has finished (programmatic dependent launch; logits must be ready when this
- * call is enqueued, as for every input); the walk and the outputs wait for
- * it.  The workspace keeps the attention's merge area untouched for this, so
+ * Overlap: with overlap on (spec_workspace_set_overlap) and the last call
+ * enqueued on the workspace spec_verify_attention, the argmax pass over
+ * logits starts before that call has finished; the walk and the outputs wait
+ * for it.  With overlap off (the default) the kernel waits first.  The
+ * workspace keeps the attention's merge area untouched for this, so
  * spec_workspace_size(SPEC_OP_VERIFY_GREEDY, ...) includes it (about 26 MB).
  * ------------------------------------------------------------------------- */
 int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits,
@@ -293,8 +309,12 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
  *   - The first call on a device looks the array's device address up
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - Each call zeroes the array's error word and counters on `stream`, then
- *     runs the greedy kernels with the array as their workspace.
+ *   - The first call on a device caches the address for the life of the
+ *     process; it assumes the device's primary context lives that long (do
+ *     not call this entry point after a cudaDeviceReset of that device).
+ *   - Each call checks every argument before it enqueues anything, zeroes the
+ *     array's arrival counters on `stream`, then runs the greedy kernel with
+ *     the array as its workspace.
  *   - Every call shares the one array per device: calls that overlap on the
  *     GPU (different streams, or concurrent host threads) race.  Serialise them.
  *   - Returns SPEC_ERR_WORKSPACE when b, n and V need more scratch than the
@@ -303,8 +323,10 @@ int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page
  *     call before it): 256 bytes of header, the arrival counters
  *     (4 * max(256, 2b+1) + 4b bytes, rounded up to 256) and 8 bytes per
  *     verify row and row chunk (about 9 chunks per row for 128 rows of 128K).
- *   - Device index errors go to the array's error word, which this entry point
- *     does not report; use spec_verify_greedy with a workspace to read them.
+ *   - Device index errors (a tree pointer out of range) are handled as in
+ *     spec_verify_greedy: the access is skipped and clamped, and a bit is set
+ *     in the array's error word.  The word is not cleared between calls;
+ *     spec_noalloc_last_error reads and clears it.
  * ------------------------------------------------------------------------- */
 #define SPEC_NOALLOC_SCRATCH_BYTES (1u << 20)
 
@@ -314,6 +336,12 @@ int spec_verify_greedy_noalloc(int b, int n, int S, int V, int dtype, const void
                                int32_t* predict, int32_t* accept_index,
                                int32_t* accept_lens, int32_t* accepted_tokens,
                                int32_t* next_root, void* stream);
+
+/* Synchronises `stream`, returns the SPEC_DEV_* bits that calls of
+ * spec_verify_greedy_noalloc on the current device have set since the last
+ * read (0 if clean) and clears them; a negative SPEC_ERR_* on failure.  Like
+ * the entry point it serves, it allocates nothing. */
+int spec_noalloc_last_error(void* stream);
 
 #ifdef __cplusplus
 }

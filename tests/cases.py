@@ -81,11 +81,84 @@ def certified_topk_difference(values: np.ndarray, sel_a, sel_b, k: int, rtol: fl
 
 def sampling_margin(logits_row: np.ndarray, T: float, q_row: np.ndarray, x: int, u: float) -> float:
     """Relative margin of one accept test u*q(x) < p(x) with p in fp64."""
-    z = logits_row.astype(np.float64) / T
+    p = _softmax64(logits_row, T)
+    return abs(u * float(q_row[x]) - p[x]) / max(p[x], 1e-30)
+
+
+def _softmax64(row: np.ndarray, T: float) -> np.ndarray:
+    z = row.astype(np.float64) / T
     z -= z.max()
     p = np.exp(z)
-    p /= p.sum()
-    return abs(u * float(q_row[x]) - p[x]) / max(p[x], 1e-30)
+    return p / p.sum()
+
+
+# Bounds of a near tie.  An accept test is a near tie when u*q(x) and p(x)
+# are within SAMPLING_ACCEPT_RTOL of p(x): the device's fp32 p has a relative
+# error of about 1e-6 (hardware exp2 of each term, fp32 row sum), the
+# oracle's is exact to fp32 rounding.  A terminal draw is a near tie when
+# u_final lies within SAMPLING_CDF_ATOL of the normalised cumulative mass at
+# the boundary between the two tokens and no mass above that bound lies
+# between them.
+SAMPLING_ACCEPT_RTOL = 2e-6
+SAMPLING_CDF_ATOL = 1e-6
+
+
+def sampling_divergence(lg_rows: np.ndarray, q_rows: np.ndarray, T: float, u: np.ndarray, u_final: float,
+                        tok: np.ndarray, nt: np.ndarray, ns: np.ndarray, n: int, r: int,
+                        o_idx: np.ndarray, o_len: int, o_term: int, g_idx: np.ndarray, g_len: int,
+                        g_term: int):
+    """Where the oracle's and the device's accept of request r part, and
+    whether that one decision is a near tie.
+
+    Both sides walk the same tree from the root, testing the children of the
+    current node in sibling order.  The first child that one side accepts
+    and the other rejects is the decision that parted them: it is certified
+    when its test u*q(x) < p(x) is a near tie.  When the two paths agree, the
+    terminal draw at the last node parted them: it is certified when u_final
+    sits at the boundary between the two tokens (see the bounds above).
+
+    lg_rows / q_rows: fp64 logits and fp32 q of request r's n rows; u: its n
+    coins; tok / nt / ns: its tree arrays (local node ids); *_idx: accept_index
+    rows of r (global), *_len: accept_lens, *_term: the terminal token.
+    Returns (kind, certified, margin): kind is "same", "accept" or "terminal"
+    ("greedy" for T <= 0, where every decision is exact and nothing can be
+    certified)."""
+    if T <= 0:
+        return "greedy", False, float("inf")
+    o_path = [int(x) - r * n for x in o_idx[:o_len]]
+    g_path = [int(x) - r * n for x in g_idx[:g_len]]
+    cur, d = 0, 0
+    while True:
+        oc = o_path[d + 1] if d + 1 < len(o_path) else -1
+        gc = g_path[d + 1] if d + 1 < len(g_path) else -1
+        if oc == gc:
+            if oc == -1:
+                break
+            cur, d = oc, d + 1
+            continue
+        # the first child in sibling order that one side accepted
+        c = nt[cur]
+        while c != -1 and c != oc and c != gc:
+            c = ns[c]
+        p = _softmax64(lg_rows[cur], T)
+        x = int(tok[c])
+        margin = abs(float(u[c]) * float(q_rows[cur][x]) - p[x]) / max(p[x], 1e-300)
+        return "accept", margin <= SAMPLING_ACCEPT_RTOL, margin
+    if o_term == g_term:
+        return "same", True, 0.0
+    # the terminal draw at node cur: from the residual when cur's children
+    # were all rejected, else from p
+    p = _softmax64(lg_rows[cur], T)
+    had_child = nt[cur] != -1 and len(o_path) - 1 < (len(o_idx) - 1)
+    dist = p
+    if had_child:
+        res = np.maximum(p - q_rows[cur].astype(np.float64), 0.0)
+        if res.sum() > 0:
+            dist = res
+    cdf = np.cumsum(dist) / dist.sum()
+    lo, hi = min(o_term, g_term), max(o_term, g_term)
+    margin = max(abs(float(u_final) - cdf[lo]), abs(float(u_final) - cdf[hi - 1]))
+    return "terminal", margin <= SAMPLING_CDF_ATOL, margin
 
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:

@@ -66,14 +66,27 @@ def test_workspace_layout_keeps_overlapping_calls_apart_host_only():
     assert sel - base >= 2 * 32 * 19 * 144
 
 
-def test_attention_launch_count_host_only():
-    """One launch for any valid sizes (split key lists are merged in the kernel)."""
-    from accept_select_top_gb300 import ops
-    assert ops.spec_verify_attention_splits(8, 16, 32, 8, 4096) == 1
-    assert ops.spec_verify_attention_splits(1, 4, 8, 8, 0) == 1
-    assert ops.spec_verify_attention_splits(2, 64, 64, 8, 131072) == 1
-    assert ops.spec_verify_attention_splits(8, 65, 32, 8, 4096) == 0     # n > 64
-    assert ops.spec_verify_attention_splits(8, 16, 30, 8, 4096) == 0     # Hq % Hkv
+def test_overlap_switch_host_only(lib):
+    """Overlap is a per-workspace permission: it takes 0 or 1 and a non-NULL
+    workspace, and needs no device (nothing is enqueued)."""
+    f = lib.spec_workspace_set_overlap
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: the call only records a flag
+    assert f(fake, 1) == 0
+    assert f(fake, 0) == 0
+    assert f(fake, 2) == -1
+    assert f(None, 1) == -2
+
+
+def test_launches_per_step_host_only():
+    """S selects, the tree build, one attention launch, the accept (two passes
+    when sampling) and the commit."""
+    from accept_select_top_gb300 import workloads as W
+    from accept_select_top_gb300.pipeline import launches_per_step
+    wl = W.WORKLOADS["llama8b_greedy"]
+    assert launches_per_step(wl, "greedy") == wl.S + 4
+    assert launches_per_step(wl, "sampling") == wl.S + 5
 
 
 def test_host_argument_checks_without_gpu(lib):

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from accept_select_top_gb300 import workloads as W
-from tests.cases import (bf16_to_f64, certified_topk_difference, make_case, sampling_margin)
+from tests.cases import (bf16_to_f64, certified_topk_difference, make_case, sampling_divergence)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +84,15 @@ def test_select_topk_parity(cases, name):
                 assert certified_topk_difference(o["score_blk"][r], op_ - (wl.k * wl.k * (i - 1) + wl.k),
                                                  gp - (wl.k * wl.k * (i - 1) + wl.k), wl.k), (name, i, r)
                 certified += 1
+        # chained: the oracle's path step fed the GPU's own probabilities and
+        # token ids gives the GPU's score block, selection and scores bit-exact
+        rows = wl.rows(i)
+        ids = _np(g["token_blk"]).reshape(rows, wl.k)
+        ch = oracle.path_step(i, wl.b, wl.k, _np(g["topk_p"]), ids, None if scores_in is None else _np(scores_in))
+        np.testing.assert_array_equal(_np(g["score_blk"]), ch["score_blk"])
+        np.testing.assert_array_equal(_np(g["parent_blk"]), ch["parent_blk"])
+        np.testing.assert_array_equal(_np(g["scores_out"]), ch["scores_out"])
+        np.testing.assert_array_equal(_np(g["next_ids"]).reshape(wl.b, wl.k), ch["next_ids"])
         assert ws.last_error() == 0
         # the next step consumes the GPU's own path scores
         scores_in = g["scores_out"]
@@ -142,44 +151,41 @@ def test_verify_greedy_parity(cases, name):
 
 # -------------------------------------------------------------- sampling
 
-def _certify_sampling(c, o, g_lens, g_idx, r):
-    """Some accept test on the oracle's or the GPU's path of request r, or the
-    terminal draw's CDF boundary, is within 1e-5 relative: a near tie."""
+def _sampling_certificates(c, tree, o, g):
+    """Per request: (kind, certified, margin) of the first decision where the
+    GPU's accept and the oracle's part (kind "same" when they agree)."""
     wl = c.wl
     n = wl.n
     lg = W.host(c.logits)
     lg = bf16_to_f64(lg) if lg.dtype == np.uint16 else lg.astype(np.float64)
-    q = W.host(c.q)
-    u = W.host(c.u)
-    T = float(c.temps[r])
-    if T <= 0:
-        return False
-    nt, ns, tok = c.tree["next_token"], c.tree["next_sibling"], c.tree["draft_tokens"]
-    margins = []
-    for path in (o["accept_index"][r], g_idx):
-        for row in path:
-            if row < 0:
-                break
-            ch = nt[row]                      # local node id of the first child
-            while ch != -1:
-                crow = r * n + ch             # the child's global row
-                margins.append(sampling_margin(lg[row], T, q[row], int(tok[crow]), float(u[crow])))
-                ch = ns[crow]
-    # the terminal draw: distance of u_final to the nearest normalised cumulative boundary
-    term = int(o["accept_index"][r, o["accept_lens"][r] - 1])
-    z = lg[term] / T
-    z -= z.max()
-    p = np.exp(z)
-    p /= p.sum()
-    for dist in (np.maximum(p - q[term], 0), p):
-        if dist.sum() > 0:
-            cs = np.cumsum(dist) / dist.sum()
-            margins.append(float(np.min(np.abs(cs - float(W.host(c.u_final)[r])))))
-    return min(margins) < 1e-5
+    q, u, uf = W.host(c.q), W.host(c.u), W.host(c.u_final)
+    out = []
+    for r in range(wl.b):
+        same = (g["accept_lens"][r] == o["accept_lens"][r] and np.array_equal(g["accept_index"][r], o["accept_index"][r])
+                and np.array_equal(g["accepted_tokens"][r], o["accepted_tokens"][r])
+                and np.array_equal(g["predict"][r * n:(r + 1) * n], o["predict"][r * n:(r + 1) * n]))
+        if same:
+            out.append(("same", True, 0.0))
+            continue
+        sl = slice(r * n, (r + 1) * n)
+        gl, ol = int(g["accept_lens"][r]), int(o["accept_lens"][r])
+        out.append(sampling_divergence(lg[sl], q[sl], float(c.temps[r]), u[sl], float(uf[r]),
+                                       tree["draft_tokens"][sl], tree["next_token"][sl], tree["next_sibling"][sl],
+                                       n, r, o["accept_index"][r], ol, int(o["accepted_tokens"][r, ol - 1]),
+                                       g["accept_index"][r], gl, int(g["accepted_tokens"][r, gl - 1])))
+    return out
+
+
+def _assert_certified(certs, name, record_property):
+    bad = [(r, k, m) for r, (k, ok, m) in enumerate(certs) if not ok]
+    n_cert = sum(1 for k, ok, _ in certs if k != "same" and ok)
+    record_property("certified_near_ties", n_cert)
+    print(f"{name}: {n_cert} of {len(certs)} requests differ through a certified near tie")
+    assert not bad, f"uncertified accept differences (request, kind, margin): {bad}"
 
 
 @pytest.mark.parametrize("name", ["tiny", "sampling_heavy", "mtp_chain"])
-def test_verify_sampling_parity(cases, name):
+def test_verify_sampling_parity(cases, name, record_property):
     c = cases(name, "sampling")
     wl, ops = c.wl, _ops()
     bufs = _accept_bufs(wl)
@@ -192,15 +198,7 @@ def test_verify_sampling_parity(cases, name):
                                c.tree["next_token"], c.tree["next_sibling"])
     g = {k_: _np(v) for k_, v in bufs.items()}
     assert ws.last_error() == 0
-    certified = 0
-    for r in range(wl.b):
-        same = (g["accept_lens"][r] == o["accept_lens"][r] and np.array_equal(g["accept_index"][r], o["accept_index"][r])
-                and np.array_equal(g["accepted_tokens"][r], o["accepted_tokens"][r])
-                and np.array_equal(g["predict"][r * wl.n:(r + 1) * wl.n], o["predict"][r * wl.n:(r + 1) * wl.n]))
-        if not same:
-            assert _certify_sampling(c, o, g["accept_lens"][r], g["accept_index"][r], r), (name, r)
-            certified += 1
-    assert certified <= max(1, wl.b // 50)
+    _assert_certified(_sampling_certificates(c, c.tree, o, g), name, record_property)
     np.testing.assert_array_equal(g["next_root"], [g["accepted_tokens"][r, g["accept_lens"][r] - 1] for r in range(wl.b)])
 
 
@@ -258,32 +256,37 @@ def test_verify_attention_parity(cases, name):
 
 # ----------------------------------------------------------------- commit
 
-@pytest.mark.parametrize("name", FULL)
-def test_commit_kv_parity(cases, name):
+@pytest.mark.parametrize("name,layers", [(x, 1) for x in FULL] + [("tiny", 3), ("sampling_heavy", 3)])
+def test_commit_kv_parity(cases, name, layers):
     c = cases(name, "greedy")
     wl, ops = c.wl, _ops()
     lay = c.layout
     acc = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), c.tree["draft_tokens"], c.tree["retrieve_index"],
                                c.tree["next_token"], c.tree["next_sibling"])
     t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
-    kp, vp = c.att["k_pool"].clone(), c.att["v_pool"].clone()
+    # layer l > 0 holds other values (the pools negated and shifted), so a
+    # layer copied from the wrong pool shows
+    kl = [c.att["k_pool"].clone()] + [(-c.att["k_pool"] + l).contiguous() for l in range(1, layers)]
+    vl = [c.att["v_pool"].clone()] + [(-c.att["v_pool"] - l).contiguous() for l in range(1, layers)]
+    hk = [W.host(x).copy() for x in kl]
+    hv = [W.host(x).copy() for x in vl]
     new_len = torch.zeros(wl.b, dtype=torch.int32, device="cuda")
     free_ids = torch.zeros(wl.b * wl.n, dtype=torch.int32, device="cuda")
     n_free = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = ops.Workspace(ops.spec_workspace_size(ops.OP_COMMIT_KV, wl.b, wl.n, 1, 1))
-    ops.spec_commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, [kp], [vp], t(lay["req_to_token"]),
+    ops.spec_commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, kl, vl, t(lay["req_to_token"]),
                        t(lay["req_pool_idx"]), t(lay["seq_lens"]), t(lay["verify_loc"]), t(acc["accept_index"]),
                        t(acc["accept_lens"]), new_len, free_ids, n_free, ws)
     assert ws.last_error() == 0
-    hk, hv = W.host(c.att["k_pool"]).copy(), W.host(c.att["v_pool"]).copy()
-    o = oracle.commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, [hk], [hv], lay["req_to_token"],
+    o = oracle.commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, hk, hv, lay["req_to_token"],
                          lay["req_pool_idx"], lay["seq_lens"], lay["verify_loc"], acc["accept_index"],
                          acc["accept_lens"])
     np.testing.assert_array_equal(_np(new_len), o["new_seq_lens"])
     nf = int(_np(n_free)[0])
     np.testing.assert_array_equal(_np(free_ids)[:nf], o["free_ids"])
-    np.testing.assert_array_equal(W.host(kp), hk)
-    np.testing.assert_array_equal(W.host(vp), hv)
+    for l in range(layers):
+        np.testing.assert_array_equal(W.host(kl[l]), hk[l], err_msg=f"K layer {l}")
+        np.testing.assert_array_equal(W.host(vl[l]), hv[l], err_msg=f"V layer {l}")
 
 
 # ------------------------------------------------------------- end to end
@@ -291,8 +294,13 @@ def test_commit_kv_parity(cases, name):
 @pytest.mark.parametrize("name,mode", [("tiny", "greedy"), ("tiny", "sampling"), ("llama8b_greedy", "greedy"),
                                        ("sampling_heavy", "sampling"), ("long_context", "greedy"),
                                        ("mtp_chain", "sampling")])
-def test_end_to_end_step(cases, name, mode):
-    """The whole GPU step (VerifyStep.run) against the oracle chain."""
+def test_end_to_end_step(cases, name, mode, record_property):
+    """The whole GPU step (VerifyStep.run) against the oracle.  The draft
+    tree is checked chained (the oracle's organize + build on the GPU's score,
+    token and parent spaces gives the GPU's tree bit-exact) and against the
+    oracle's own select chain (equal, or parting at its first step only
+    through a certified near tie of path scores); the accept, the commit and
+    the committed KV are then checked against the oracle on that tree."""
     from accept_select_top_gb300.pipeline import VerifyStep
     c = cases(name, mode)
     wl = c.wl
@@ -303,38 +311,105 @@ def test_end_to_end_step(cases, name, mode):
     step.run()
     torch.cuda.synchronize()
     assert step.ws.last_error() == 0
-    tr = c.tree
-    same_tree = all(np.array_equal(_np(getattr(step, k_)), tr[k_]) for k_ in
-                    ("draft_tokens", "positions", "next_token", "next_sibling"))
-    if not same_tree:
-        pytest.skip("draft tree differs through a certified near tie of path scores")  # counted by the select test
+    sp = {k_: _np(getattr(step, k_)) for k_ in ("score_space", "token_space", "parent_space")}
+    tr = oracle.build_tree(wl.b, wl.k, wl.S, wl.n, sp["score_space"], sp["token_space"], sp["parent_space"],
+                           W.host(c.bonus), c.layout["seq_lens"])
+    for k_ in ("draft_tokens", "positions", "retrieve_index", "next_token", "next_sibling"):
+        np.testing.assert_array_equal(_np(getattr(step, k_)), tr[k_], err_msg=k_)
     np.testing.assert_array_equal(_np(step.mask_bits).view(np.uint64), tr["mask_bits"])
+    ch = c.chain
+    np.testing.assert_array_equal(sp["token_space"][:, :wl.k], ch["token_space"][:, :wl.k])
+    np.testing.assert_allclose(sp["score_space"], ch["score_space"], rtol=3e-6, atol=0)
+    if not np.array_equal(sp["parent_space"], ch["parent_space"]):
+        # the first parent block that differs parts the chains: a near tie of
+        # path scores there (the blocks before it, and so its inputs, agree)
+        for i in range(1, wl.S - 1):
+            blk = slice(1 + i * wl.k, 1 + (i + 1) * wl.k)
+            if np.array_equal(sp["parent_space"][:, blk], ch["parent_space"][:, blk]):
+                continue
+            off = wl.k * wl.k * (i - 1) + wl.k
+            cols = slice(off, off + wl.k * wl.k)
+            for r in range(wl.b):
+                assert certified_topk_difference(ch["score_space"][r, cols], ch["parent_space"][r, blk] - off,
+                                                 sp["parent_space"][r, blk] - off, wl.k), (name, i, r)
+            break
+    same_tree = all(np.array_equal(tr[k_], c.tree[k_]) for k_ in ("draft_tokens", "next_token", "next_sibling"))
+    record_property("same_tree_as_oracle_chain", bool(same_tree))
+    args = (tr["draft_tokens"], tr["retrieve_index"], tr["next_token"], tr["next_sibling"])
     if mode == "greedy":
-        o = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), tr["draft_tokens"], tr["retrieve_index"],
-                                 tr["next_token"], tr["next_sibling"])
+        o = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), *args)
         for k_ in ("predict", "accept_index", "accept_lens", "accepted_tokens", "next_root"):
             np.testing.assert_array_equal(_np(getattr(step, k_)), o[k_], err_msg=k_)
+        acc = o
     else:
         o = oracle.verify_sampling(wl.b, wl.n, wl.S, W.host(c.logits), W.host(c.q), c.temps, W.host(c.u),
-                                   W.host(c.u_final), tr["draft_tokens"], tr["retrieve_index"], tr["next_token"],
-                                   tr["next_sibling"])
-        mism = int((_np(step.accept_lens) != o["accept_lens"]).sum())
-        assert mism <= max(1, wl.b // 50)
-        if mism:
-            pytest.skip(f"{mism} certified-size accept differences; exact commit check needs equal accepts")
-    # commit on the oracle side from the oracle's accept result
+                                   W.host(c.u_final), *args)
+        g = {k_: _np(getattr(step, k_)) for k_ in ("predict", "accept_index", "accept_lens", "accepted_tokens")}
+        _assert_certified(_sampling_certificates(c, tr, o, g), name, record_property)
+        acc = {"accept_index": g["accept_index"], "accept_lens": g["accept_lens"]}  # commit what the GPU accepted
+    # the commit, on the oracle side, of the accept the GPU committed
     o2 = oracle.commit_kv(wl.b, wl.n, wl.W, wl.Hkv, wl.D, wl.page_size, [kp0], [vp0], c.layout["req_to_token"],
-                          c.layout["req_pool_idx"], c.layout["seq_lens"], c.layout["verify_loc"], o["accept_index"],
-                          o["accept_lens"])
+                          c.layout["req_pool_idx"], c.layout["seq_lens"], c.layout["verify_loc"], acc["accept_index"],
+                          acc["accept_lens"])
     np.testing.assert_array_equal(_np(step.new_seq_lens), o2["new_seq_lens"])
     nf = int(_np(step.n_free)[0])
     np.testing.assert_array_equal(_np(step.free_ids)[:nf], o2["free_ids"])
-    if name != "mtp_chain":  # the largest pools: committed rows are compared through the ids above
-        np.testing.assert_array_equal(W.host(inp.k_pool), kp0)
+    np.testing.assert_array_equal(W.host(inp.k_pool), kp0)
+    np.testing.assert_array_equal(W.host(inp.v_pool), vp0)
+
+
+def test_foreign_producer_between_calls_waits_first(cases):
+    """In an EAGLE loop other kernels produce the library's inputs between its
+    calls: the draft forward writes the next draft logits between two
+    selects, the target's MLP and LM head write the logits between the verify
+    attention and the accept.  Here a torch kernel overwrites each input
+    buffer right before the call that reads it (after filling it with
+    garbage), on the same stream, with no synchronisation.  With overlap off
+    (the default) every kernel waits for that producer: the results are
+    bit-exact against the oracle."""
+    c = cases("llama8b_greedy", "greedy")
+    wl, ops = c.wl, _ops()
+    lay = c.layout
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    size = max(ops.spec_workspace_size(op, wl.b, wl.n, wl.k, wl.V, wl.Hq, wl.Hkv, int(lay["seq_lens"].max()))
+               for op in range(6))
+    ws = ops.Workspace(size)
+    buf = [torch.empty_like(d) for d in c.drafts]
+    scores_in = None
+    outs = []
+    for i in range(wl.S):
+        buf[i].fill_(float("nan"))            # garbage first ...
+        buf[i].copy_(c.drafts[i])             # ... then the producer kernel right before the call
+        g = _gpu_select_step(wl, i, buf[i], scores_in, ws)
+        outs.append(g)
+        scores_in = g["scores_out"]
+    # greedy accept right after the attention, the logits produced in between
+    out = torch.zeros(wl.b * wl.n, wl.Hq, wl.D, dtype=torch.bfloat16, device="cuda")
+    mask = t(c.tree["mask_bits"].view(np.int64))
+    ops.spec_verify_attention(wl.b, wl.n, wl.Hq, wl.Hkv, wl.D, wl.page_size, c.att["q"], c.att["k_pool"],
+                              c.att["v_pool"], t(lay["req_to_token"]), t(lay["req_pool_idx"]), t(lay["seq_lens"]),
+                              int(lay["seq_lens"].max()), t(lay["verify_loc"]), mask, 1.0 / math.sqrt(wl.D), out,
+                              None, ws)
+    logits = torch.empty_like(c.logits)
+    logits.fill_(float("nan"))
+    logits.copy_(c.logits)
+    bufs = _accept_bufs(wl)
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, logits, *_tree_dev(c), *bufs.values(), ws)
+    torch.cuda.synchronize()
+    assert ws.last_error() == 0
+    for i, g in enumerate(outs):
+        o = c.chain["steps"][i]
+        np.testing.assert_array_equal(_np(g["token_blk"]), o["token_blk"])
+        np.testing.assert_array_equal(_np(g["parent_blk"]), o["parent_blk"])
+    o = oracle.verify_greedy(wl.b, wl.n, wl.S, W.host(c.logits), c.tree["draft_tokens"], c.tree["retrieve_index"],
+                             c.tree["next_token"], c.tree["next_sibling"])
+    for k_, v in bufs.items():
+        np.testing.assert_array_equal(_np(v), o[k_], err_msg=k_)
 
 
 def test_back_to_back_calls_on_one_workspace(cases):
-    """Calls enqueued back to back on one workspace with no synchronisation
+    """Overlap allowed (every input resident before the first call).  Calls
+    enqueued back to back on one workspace with no synchronisation
     between them: a select right after a select of the same step (the second
     runs its chunk pass before the first has finished, on the other half of the
     select's area), and the whole step twice in a row (a select right after the
@@ -348,6 +423,7 @@ def test_back_to_back_calls_on_one_workspace(cases):
     wl, ops = c.wl, _ops()
     size = ops.spec_workspace_size(ops.OP_SELECT_TOPK, wl.b, wl.n, wl.k, wl.V)
     ws = ops.Workspace(size)
+    ws.set_overlap(True)  # every input is resident before the first call
     pairs, scores_in = [], None
     for i in range(wl.S):
         first = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws)
@@ -365,18 +441,18 @@ def test_back_to_back_calls_on_one_workspace(cases):
             assert torch.equal(second[k_], v), (i, k_)
         scores_in = ref["scores_out"]
 
-    def fresh():
+    def fresh(overlap):
         inp = c.device_inputs()
         inp.k_pool, inp.v_pool = inp.k_pool.clone(), inp.v_pool.clone()
-        return VerifyStep(wl, inp, "greedy")
+        return VerifyStep(wl, inp, "greedy", overlap=overlap)
     names = ("draft_tokens", "positions", "mask_bits", "predict", "accept_index", "accept_lens",
              "accepted_tokens", "next_root", "new_seq_lens", "free_ids", "n_free")
-    twice = fresh()
+    twice = fresh(True)
     twice.run()
     twice.run()
     torch.cuda.synchronize()
     assert twice.ws.last_error() == 0
-    once = fresh()
+    once = fresh(False)
     once.run()
     torch.cuda.synchronize()
     for k_ in names:
