@@ -29,7 +29,11 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Device address of g_scratch on the current device, looked up once per device
+// (with that device current) and kept for the life of the process.  The cache
+// assumes the device's primary context lives as long as the process: after a
+// cudaDeviceReset the module is reloaded and the kept address is stale, so a
+// process that resets a device must not call these entry points afterwards.
 int scratch_of_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_LAUNCH;
@@ -53,15 +57,30 @@ extern "C" int spec_verify_greedy_noalloc(int b, int n, int S, int V, int dtype,
   if (b < 0 || n < 1 || n > spec::kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (b == 0) return SPEC_OK;
+  // every check that can reject the call comes before anything is enqueued
+  if (!logits || !draft_tokens || !retrieve_index || !next_token || !next_sibling || !predict || !accept_index ||
+      !accept_lens)
+    return SPEC_ERR_ARG;
   const size_t need = spec::greedy_compact_bytes(b, n, V);
   if (need > kScratchBytes) return SPEC_ERR_WORKSPACE;  // too large for the fixed scratch
   void* ws = nullptr;
   if (int rc = scratch_of_current_device(&ws)) return rc;
-  // The array keeps the previous call's contents: the error word and the
-  // arrival counters must start at zero (the partials are always written first).
-  const size_t zero_bytes = spec::kHeaderBytes + spec::counters_bytes(b);
-  if (cudaMemsetAsync(ws, 0, zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  // The array keeps the previous call's contents.  The arrival counters must
+  // start at zero (a call that completes leaves them zero; this also clears
+  // what an interrupted call left).  The error word is not cleared: device
+  // index errors accumulate until spec_noalloc_last_error reads them.  The
+  // partials are always written before they are read.
+  unsigned char* counters = static_cast<unsigned char*>(ws) + spec::kHeaderBytes;
+  if (cudaMemsetAsync(counters, 0, spec::counters_bytes(b), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
   return spec::verify_greedy_compact(b, n, S, V, dtype, logits, draft_tokens, retrieve_index, next_token,
                                      next_sibling, predict, accept_index, accept_lens, accepted_tokens, next_root,
                                      ws, kScratchBytes, stream);
+}
+
+extern "C" int spec_noalloc_last_error(void* stream) {
+  void* ws = nullptr;
+  if (int rc = scratch_of_current_device(&ws)) return rc;
+  // the error word is the first word of the array, as in a caller workspace
+  return spec_last_error(ws, stream);
 }
