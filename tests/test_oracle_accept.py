@@ -175,8 +175,9 @@ def test_accept_invariants(mode, seed):
             assert toks[-1] == np.argmax(logits[rows[-1]])
 
 
-def _single_candidate(p, q, u, uf, x, leaf_logits=None):
-    """b single-candidate chains: root (target p, draft q) with one child x."""
+def _single_candidate(p, q, u, uf, x, leaf_logits=None, T=1.0):
+    """b single-candidate chains: root (target logits log p, draft q) with one
+    child x, every request at temperature T."""
     b = len(u)
     V = len(p)
     logits = np.empty((b * 2, V), np.float32)
@@ -191,8 +192,93 @@ def _single_candidate(p, q, u, uf, x, leaf_logits=None):
     uu[1::2] = u
     nt = np.tile(np.array([1, -1], np.int32), b)
     ns = np.full(b * 2, -1, np.int32)
-    return oracle.verify_sampling(b, 2, 1, logits, qq, np.ones(b, np.float32), uu,
+    return oracle.verify_sampling(b, 2, 1, logits, qq, np.full(b, T, np.float32), uu,
                                   np.asarray(uf, np.float32), draft, np.arange(b * 2), nt, ns)
+
+
+def _tempered(p, T):
+    """The target distribution at temperature T when the logits are the fp32
+    log-probabilities: p_T(v) = p(v)^(1/T) / sum_w p(w)^(1/T) (closed form)."""
+    lp = np.log(np.asarray(p, np.float64)).astype(np.float32).astype(np.float64)
+    w = np.power(np.exp(lp), 1.0 / T)
+    return w / w.sum()
+
+
+@pytest.mark.parametrize("T", [0.7, 2.0])
+def test_rejection_temperature_closed_form(T):
+    """The sampler's p is the softmax of logits / T.  With logits = log p the
+    tempered target is p^(1/T) normalised.  Quadrature over (x ~ q, u,
+    u_final): candidate x is accepted with probability min(1, p_T(x)/q(x)), a
+    rejected candidate's mass goes to max(0, p_T - q)/Z, and the first output
+    token is distributed as p_T.  A temperature multiplied instead of divided,
+    or left out, moves every one of these."""
+    fx = golden("rejection_example.json")
+    p, q = np.array(fx["p"]), np.array(fx["q"], np.float32).astype(np.float64)
+    pT = _tempered(p, T)
+    assert np.abs(pT - p).max() > 0.02  # the temperature matters for this p
+    G = 300
+    grid = (np.arange(G) + 0.5) / G
+    uu, ff = np.meshgrid(grid, grid, indexing="ij")
+    uu, ff = uu.ravel(), ff.ravel()
+    dist = np.zeros(3)
+    res = np.maximum(pT - q, 0.0)
+    res /= res.sum()
+    for x in range(3):
+        o = _single_candidate(p, q, uu, ff, x, T=T)
+        first = o["accepted_tokens"][:, 0]
+        acc = o["accept_lens"] == 2
+        assert abs(acc.mean() - min(1.0, pT[x] / q[x])) < 2.0 / G, (x, acc.mean())
+        if (~acc).sum() > G:
+            frac = np.bincount(first[~acc], minlength=3) / (~acc).sum()
+            np.testing.assert_allclose(frac, res, atol=2.0 / G)
+        dist += q[x] * np.bincount(first, minlength=3) / len(first)
+    np.testing.assert_allclose(dist, pT, atol=2.0 / G)
+
+
+def test_rejection_chi_square_temperature():
+    """V=16 at T=0.7, 1e5 single-candidate trials with x drawn from q: the
+    output follows p_T = softmax(log p / 0.7) and the acceptance rate is
+    sum(min(p_T, q))."""
+    rng = np.random.default_rng(17)
+    V, N, T = 16, 100_000, 0.7
+    p = rng.dirichlet(np.full(V, 0.8))
+    q = rng.dirichlet(np.full(V, 0.8))
+    pT = _tempered(p, T)
+    x = np.searchsorted(np.cumsum(q), rng.random(N), side="right").clip(0, V - 1)
+    u = rng.random(N).astype(np.float32)
+    uf = rng.random(N).astype(np.float32)
+    o = _single_candidate(p, q.astype(np.float32), u, uf, x, T=T)
+    counts = np.bincount(o["accepted_tokens"][:, 0], minlength=V)
+    stat, pval = scipy.stats.chisquare(counts, pT * N)
+    assert pval > 1e-3, (stat, pval)
+    acc = (o["accept_lens"] == 2).mean()
+    a = np.minimum(pT, q.astype(np.float32)).sum()
+    assert abs(acc - a) < 4 * np.sqrt(a * (1 - a) / N)
+
+
+def test_terminal_draw_past_the_total_mass_takes_the_last_positive_token():
+    """The draw takes the smallest v with u_final * Z < the running sum.  A
+    coin u_final = 1 (outside [0, 1): the running sum never passes u*Z = Z)
+    falls through to the last token with positive mass: C for the rejected
+    residual (0, 0.1, 0.2); with target logits -inf past token 2 of 6 (zero
+    probability there), token 2 for a draw from p itself."""
+    fx = golden("rejection_example.json")
+    o = _single_candidate(fx["p"], fx["q"], [0.9], [1.0], 0)
+    assert o["accept_lens"][0] == 1 and o["accepted_tokens"][0, 0] == 2
+    # a leaf root (no child): the bonus is drawn from p; p is zero past token 2
+    V = 6
+    logits = np.full((1, V), -np.inf, np.float32)
+    logits[0, :3] = np.log([0.2, 0.5, 0.3])
+    o = oracle.verify_sampling(1, 1, 1, logits, np.zeros((1, V), np.float32), np.ones(1, np.float32),
+                               np.zeros(1, np.float32), np.ones(1, np.float32), np.zeros(1, np.int32),
+                               np.arange(1), np.full(1, -1, np.int32), np.full(1, -1, np.int32))
+    assert o["accept_lens"][0] == 1 and o["accepted_tokens"][0, 0] == 2
+    # and just below 1 the draw is the last positive-mass token by the running sum as well
+    o = oracle.verify_sampling(1, 1, 1, logits, np.zeros((1, V), np.float32), np.ones(1, np.float32),
+                               np.zeros(1, np.float32), np.full(1, np.float32(1) - np.float32(2 ** -24)),
+                               np.zeros(1, np.int32), np.arange(1), np.full(1, -1, np.int32),
+                               np.full(1, -1, np.int32))
+    assert o["accepted_tokens"][0, 0] == 2
 
 
 def test_rejection_example_points():
