@@ -58,7 +58,7 @@ def _load():
             lib = ctypes.CDLL(build())
             for name in ("oracle_softmax_topk", "oracle_path_step", "oracle_select_topk",
                          "oracle_build_tree", "oracle_verify_attention", "oracle_verify_greedy",
-                         "oracle_verify_sampling", "oracle_commit_kv"):
+                         "oracle_verify_sampling", "oracle_verify_target_only", "oracle_commit_kv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -213,6 +213,23 @@ def verify_sampling(b, n, S, logits, draft_probs, temperatures, u, u_final, draf
         _p(_i32(retrieve_index)), _p(_i32(next_token)), _p(_i32(next_sibling)),
         _p(out["predict"]), _p(out["accept_index"]), _p(out["accept_lens"]),
         _p(out["accepted_tokens"]), _p(out["next_root"])), "verify_sampling")
+    return out
+
+
+def verify_target_only(b, n, S, logits, temperatures, u, u_final, threshold_single, threshold_acc, draft_tokens,
+                       retrieve_index, next_token, next_sibling):
+    """Target-only tree sampling: u [b*n] holds one coin per node (the coin used
+    to scan that node's children), u_final [b] the terminal draw's."""
+    x, dt = _logits(logits)
+    V = x.shape[-1]
+    out = _accept_outputs(b, n, S)
+    _check(_load().oracle_verify_target_only(
+        b, n, S, V, dt, _p(x), _p(np.ascontiguousarray(temperatures, np.float32)),
+        _p(np.ascontiguousarray(u, np.float32)), _p(np.ascontiguousarray(u_final, np.float32)),
+        ctypes.c_float(threshold_single), ctypes.c_float(threshold_acc), _p(_i32(draft_tokens)),
+        _p(_i32(retrieve_index)), _p(_i32(next_token)), _p(_i32(next_sibling)),
+        _p(out["predict"]), _p(out["accept_index"]), _p(out["accept_lens"]),
+        _p(out["accepted_tokens"]), _p(out["next_root"])), "verify_target_only")
     return out
 
 

@@ -524,6 +524,93 @@ int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* lo
   return rc;
 }
 
+/* -------------------------------------- f1 target-only tree sampling */
+
+int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void* logits,
+                              const float* temperatures, const float* u, const float* u_final,
+                              float threshold_single, float threshold_acc,
+                              const int32_t* draft_tokens, const int32_t* retrieve_index,
+                              const int32_t* next_token, const int32_t* next_sibling,
+                              int32_t* predict, int32_t* accept_index,
+                              int32_t* accept_lens, int32_t* accepted_tokens,
+                              int32_t* next_root) {
+  if (b < 0 || n <= 0 || S <= 0 || V <= 0) return ORC_EARG;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
+  if (!(threshold_single > 0.0f && threshold_single <= 1.0f)) return ORC_EARG;
+  if (!(threshold_acc > 0.0f && threshold_acc <= 1.0f)) return ORC_EARG;
+  const int W = S + 1;
+  const size_t rows = (size_t)b * n;
+  float* p = (float*)malloc(sizeof(float) * (size_t)V);
+  float* buf = (float*)malloc(sizeof(float) * (size_t)V); /* the current node's buffer row */
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  for (size_t i = 0; i < rows; ++i) predict[i] = 0;
+  for (size_t i = 0; i < (size_t)b * W; ++i) accept_index[i] = -1;
+  int rc = ORC_OK;
+  for (int q = 0; q < b && rc == ORC_OK; ++q) {
+    const size_t base = (size_t)q * n;
+    const double T = temperatures[q];
+    int cur = 0, ncd = 0;
+    float coin = u[base + 0];
+    accept_index[(size_t)q * W] = retrieve_index[base];
+    for (int d = 0; d <= S; ++d) {
+      /* the target distribution at the current node, and its empty buffer row */
+      const size_t loff = (base + cur) * (size_t)V;
+      if (T > 0.0) {
+        row_softmax(logits, dtype, loff, V, T, p);
+      } else {
+        int a = row_argmax(logits, dtype, loff, V);
+        for (int v = 0; v < V; ++v) p[v] = v == a ? 1.0f : 0.0f;
+      }
+      for (int v = 0; v < V; ++v) buf[v] = 0.0f;
+      if (d == S) break; /* depth exhausted */
+      /* siblings in order, accumulating their target mass */
+      float prob_acc = 0.0f;
+      int c = next_token[base + cur], hit = -1, guard = 0;
+      while (c != -1) {
+        if (c < 0 || c >= n || ++guard > n) { rc = ORC_EBOUNDS; break; }
+        int x = draft_tokens[base + c];
+        if (x < 0 || x >= V) { rc = ORC_EBOUNDS; break; }
+        const float px = p[x];
+        prob_acc += px; /* fp32 accumulation */
+        if (px > 0.0f && (coin < prob_acc / threshold_acc || px >= threshold_single)) {
+          hit = c;
+          break;
+        }
+        buf[x] = px; /* rejected: its mass is kept out of the terminal draw here */
+        c = next_sibling[base + c];
+      }
+      if (rc != ORC_OK || hit < 0) break;
+      predict[retrieve_index[base + cur]] = draft_tokens[base + hit];
+      accept_index[(size_t)q * W + d + 1] = retrieve_index[base + hit];
+      ++ncd;
+      cur = hit;
+      coin = u[base + hit]; /* the accepted child's own coin for the next level */
+    }
+    if (rc != ORC_OK) break;
+    /* terminal token from relu(p - buffer) at the current node */
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double rv = (double)p[v] - (double)buf[v];
+      r[v] = rv > 0.0 ? rv : 0.0;
+      Z += r[v];
+    }
+    if (!(Z > 0.0)) {
+      Z = 0.0;
+      for (int v = 0; v < V; ++v) {
+        r[v] = (double)p[v];
+        Z += r[v];
+      }
+    }
+    predict[retrieve_index[base + cur]] = sample_from(r, V, Z, u_final[q]);
+    accept_lens[q] = ncd + 1;
+  }
+  if (rc == ORC_OK) gather_outputs(b, W, predict, accept_index, accept_lens, accepted_tokens, next_root);
+  free(p);
+  free(buf);
+  free(r);
+  return rc;
+}
+
 /* ------------------------------------------------------------ c9 commit */
 
 int oracle_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers,

@@ -144,6 +144,30 @@ int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* lo
                            int32_t* accept_lens, int32_t* accepted_tokens,
                            int32_t* next_root);
 
+/* f1 -- target-only tree sampling (the second sampler of EAGLE trees).
+ * [ACCEPT section 4, "Target-only Tree Sampling"].
+ * p_cur = softmax(logits_row(cur) / T_b), rounded to fp32 (T_b <= 0: one-hot
+ * at the argmax).  The walk starts at the root with coin = u[b*n + 0]; at the
+ * current node the children are scanned in sibling order with an fp32
+ * accumulator prob_acc (zero at each node): prob_acc += p_cur(x) for child c
+ * of token x, and c is accepted iff
+ *     p_cur(x) > 0  and  (coin < prob_acc / threshold_acc  or  p_cur(x) >= threshold_single)
+ * (fp32 arithmetic).  An accepted child becomes the current node and its own
+ * coin u[b*n + c] is used for the next level; a rejected child writes p_cur(x)
+ * into the buffer row of the current node.  At most S levels.  The terminal
+ * token is drawn with u_final[b] from relu(p_cur - buffer_cur) (the current
+ * node's rejected siblings removed; from p_cur itself when that mass is 0), as
+ * the smallest v with u_final * Z < running sum (fp64, vocabulary order).
+ * Thresholds in (0, 1].  Outputs as oracle_verify_greedy. */
+int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void* logits,
+                              const float* temperatures, const float* u, const float* u_final,
+                              float threshold_single, float threshold_acc,
+                              const int32_t* draft_tokens, const int32_t* retrieve_index,
+                              const int32_t* next_token, const int32_t* next_sibling,
+                              int32_t* predict, int32_t* accept_index,
+                              int32_t* accept_lens, int32_t* accepted_tokens,
+                              int32_t* next_root);
+
 /* c9 -- KV commit.  [SGL-XI KV 回写], [ACCEPT section 3 (input/output shift)],
  * [EVOL 草稿、验证与槽位].
  * For request b with L = accept_lens[b] and k < L:
