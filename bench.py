@@ -5,20 +5,28 @@ A step is one pass of the whole hot path over one batch: spec_select_topk x S,
 spec_build_tree, spec_verify_attention, spec_verify_greedy (or
 spec_verify_sampling) and spec_commit_kv.  Prints ONE JSON line on rank 0.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--configs all|headline|a,b,..] [--impl ours|reference]
 
-Timing: W warm-up steps, then K steps replayed from CUDA graphs of P
-consecutive steps each (P <= 4 divides K; consecutive steps use different
+The headline workload is sampling_heavy (2048 verify tokens per step, the
+largest of the five, on the sampling path).  At N=1 the other four workloads
+are measured the same way and reported in the line's "configs" object.
+
+Timing, per workload: W warm-up steps, then K steps replayed from CUDA graphs
+of P consecutive steps each (P <= 4 divides K; consecutive steps use different
 input replicas, whose combined size exceeds the 129 MB L2), bracketed by a
 barrier and torch.cuda.synchronize() on both sides, CUDA events on the
-launching stream, max over ranks.  The timed graphs hold only the kernels, so
-consecutive kernels overlap as they do for a caller running steps back to
-back.  Stage durations (for the roofline) come from a second pass right after
-the timed region: one-step graphs with CUDA events at the stage boundaries,
-each step run alone (the events and the per-step synchronisation remove the
-overlap across stages, so these durations are upper bounds).  Under torchrun
-each rank verifies its own batch (weak scaling, no collective on the data
-path).
+launching stream, max over ranks.  Every kernel waits for the one before it
+(the library's default): this is the step an EAGLE loop gets, where the draft
+forward and the target's LM head run between the library's calls.  The same
+steps with overlap allowed (spec_workspace_set_overlap: a select or a greedy
+accept reads its input before the kernel ahead finishes) are timed too and
+reported as step_us_overlap.  Per-call durations (for the roofline) come from
+a separate pass right after the timed region: one-step graphs with CUDA
+events between the calls, each step on its own replica and run alone (the
+events remove the overlap of consecutive launches, so these durations are
+upper bounds).  Under torchrun each rank verifies its own batch of the
+headline workload (weak scaling, no collective on the data path).
 """
 from __future__ import annotations
 
@@ -42,20 +50,31 @@ if ROOT not in sys.path:
 METRIC = "verify-step µs and verified tree tokens/s; % of GB300 HBM/tensor roofline"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEADLINE = "sampling_heavy"
+ALL_CONFIGS = ["sampling_heavy", "llama8b_greedy", "long_context", "mtp_chain", "tiny"]
+GROUPS = ["select", "build", "attention", "accept", "commit"]
+L2_BYTES = 129e6
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="llama8b_greedy")
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, help="the headline workload")
+    ap.add_argument("--configs", default="all",
+                    help="workloads measured at N=1: all (the five), headline, or a comma list")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--replicas", type=int, default=0, help="input replicas cycled by the timed steps (0: auto)")
     ap.add_argument("--graphs", type=int, default=64, help="distinct captured step graphs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-overlap-variant", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0,
+                    help="seconds of oracle work for the headline's CPU baseline (a quarter for the others)")
+    ap.add_argument("--reference-budget-s", type=float, default=100.0,
+                    help="seconds of oracle work the reference arm spreads over its W + K steps")
     return ap.parse_args(argv)
 
 
@@ -166,22 +185,51 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def traffic_entry(kernel_key: str, sources):
-    """DRAM bytes per launch from the committed ncu summary, when it was taken
-    on the current source of the kernel; else None."""
+CSRC = "accept_select_top_gb300/csrc/"
+# the sources each group's kernels compile from (common.cuh: helpers inlined in every kernel)
+GROUP_SOURCES = {
+    "select": [CSRC + "select_topk.cu", CSRC + "common.cuh"],
+    "build": [CSRC + "build_tree.cu", CSRC + "common.cuh"],
+    "attention": [CSRC + "attention_tc.cu", CSRC + "common.cuh"],
+    "accept": [CSRC + "verify_greedy.cu", CSRC + "verify_sampling.cu", CSRC + "common.cuh"],
+    "commit": [CSRC + "commit_kv.cu", CSRC + "common.cuh"],
+}
+
+
+def traffic_entry(group: str, workload: str):
+    """DRAM bytes per step of a kernel group from the committed ncu summary,
+    when it was taken on the current source of its kernels; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             table = json.load(f)
     except (OSError, ValueError):
         return None
-    e = table.get(kernel_key)
-    if not e or e.get("source_hash") != source_hash(sources):
+    e = table.get(f"{group}:{workload}")
+    if not e or e.get("source_hash") != source_hash(GROUP_SOURCES[group]):
         return None
     return e
 
 
+def selected_configs(args, world):
+    if world > 1 or args.configs == "headline":
+        return [args.workload]
+    if args.configs == "all":
+        names = [args.workload] + [c for c in ALL_CONFIGS if c != args.workload]
+    else:
+        names = [args.workload] + [c for c in args.configs.split(",") if c and c != args.workload]
+    return names
+
+
 # ------------------------------------------------------- workload setup
+
+def accept_mode(wl):
+    return "greedy" if wl.accept == "greedy" else "sampling"
+
+
+def temps_mode(wl):
+    return {"sampling": "sampling", "mixed": "mixed", "both": "sampling"}[wl.accept]
+
 
 def prepare(wl, device, seed, torch):
     """Inputs on the device; the draft tree comes from one untimed GPU pass of
@@ -189,7 +237,7 @@ def prepare(wl, device, seed, torch):
     from accept_select_top_gb300 import workloads as W
     from accept_select_top_gb300.pipeline import DeviceInputs, VerifyStep
 
-    mode = "greedy" if wl.accept == "greedy" else "sampling"
+    mode = accept_mode(wl)
     drafts = [W.draft_logits(wl, i, device, seed) for i in range(wl.S)]
     lay = W.kv_layout(wl, seed)
     t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(device)
@@ -210,7 +258,7 @@ def prepare(wl, device, seed, torch):
         logits = W.plant_agreement(wl, logits, dt, nt, ns, seed)
     inp.target_logits = logits
     if mode == "sampling":
-        temps = W.request_temperatures(wl, {"sampling": "sampling", "mixed": "mixed", "both": "sampling"}[wl.accept])
+        temps = W.request_temperatures(wl, temps_mode(wl))
         inp.temperatures = t(temps)
         inp.draft_probs = W.draft_probs(wl, rows, all_d, temps, device)
         inp.u, inp.u_final = W.coins(wl, device, seed)
@@ -227,19 +275,29 @@ def clone_inputs(inp, torch):
                         c(inp.u_final))
 
 
-def step_bytes(wl, inp, lay, mode):
-    """Algorithmic bytes of each stage per step (what the method itself moves)."""
+def group_bytes(wl, lay, mode, accept_lens):
+    """Algorithmic bytes of each kernel group per step: what the method itself
+    must move (each input read once, each output written once)."""
     es = 4 if wl.logits_dtype == "f32" else 2
     seq = lay["seq_lens"].astype(np.int64)
-    b, n = wl.b, wl.n
-    select = sum(wl.rows(i) * wl.V * es for i in range(wl.S))
+    b, n, k = wl.b, wl.n, wl.k
     kv_row = wl.Hkv * wl.D * 2
-    attention = int((seq.sum() + b * n) * kv_row * 2 + 2 * b * n * wl.Hq * wl.D * 2 + b * n * wl.Hq * 4
-                    + (seq.sum() + b * n) * 4)
-    accept = b * n * wl.V * es
+    out = {
+        # every draft row once, plus each step's blocks
+        "select": sum(wl.rows(i) * wl.V * es for i in range(wl.S)),
+        # the score / token spaces and parent list in, the tree arrays and the mask out
+        "build": b * (wl.C * 8 + wl.P * 4 + n * (4 * 5 + 8)),
+        # the visible K/V rows once, Q in, O and LSE out, the slot ids
+        "attention": int((seq.sum() + b * n) * kv_row * 2 + 2 * b * n * wl.Hq * wl.D * 2 + b * n * wl.Hq * 4
+                         + (seq.sum() + b * n) * 4),
+        # every verify row's logits once (argmax / softmax of all b*n rows)
+        "accept": b * n * wl.V * es,
+        # accepted K and V rows read and written
+        "commit": int(np.sum(accept_lens)) * kv_row * 2 * 2,
+    }
     if mode == "sampling":
-        accept += b * n * 4 * 2 + b * wl.V * (es + 4)  # candidate q reads + one terminal row (p and q)
-    return {"select_build": select, "attention": attention, "accept_commit": accept + 4 * b * wl.W * kv_row}
+        out["accept"] += b * n * 4 + b * wl.V * (es + 4)  # candidate q reads + one terminal row (logits and q)
+    return out
 
 
 def attention_flops(wl, lay, mask_bits):
@@ -250,121 +308,136 @@ def attention_flops(wl, lay, mask_bits):
     return float(4 * wl.D * wl.Hq * keys)
 
 
-# ------------------------------------------------------------- our arm
+def roofline(group, t_us, bytes_, flops, peaks, peaks_kind):
+    """The roofline object of one kernel group: HBM-bound unless it is the
+    attention with an arithmetic intensity above the ridge."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if group == "attention" and flops / bytes_ > ridge:
+        ach = flops / (t_us * 1e-6) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "peak_kind": f"{peaks_kind} bf16 (sustained)"}
+    ach = bytes_ / (t_us * 1e-6) / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "peak_kind": f"{peaks_kind} copy bandwidth"}
 
-def run_ours(args, torch):
-    from accept_select_top_gb300 import workloads as W
-    from accept_select_top_gb300.pipeline import VerifyStep
 
-    rank, world, local = dist_env()
-    device = f"cuda:{local}"
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", init_method="env://")
-    wl = W.WORKLOADS[args.workload]
-    mode, inp, lay = prepare(wl, device, seed=rank, torch=torch)
-    per_replica = sum(d.numel() * d.element_size() for d in inp.drafts) + inp.target_logits.numel() * \
-        inp.target_logits.element_size() + 2 * inp.k_pool.numel() * 2 + inp.q.numel() * 2 + \
-        (inp.draft_probs.numel() * 4 if inp.draft_probs is not None else 0)
-    R = args.replicas or max(2, min(8, math.ceil(4 * 129e6 / per_replica)))
-    replicas = [inp] + [clone_inputs(inp, torch) for _ in range(R - 1)]
-    steps = [VerifyStep(wl, x, mode, device=device) for x in replicas]
-    stream = torch.cuda.Stream(device=device)
+# --------------------------------------------------------- one workload
 
-    # warm-up, eager
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            steps[i % R].run()
-    torch.cuda.synchronize()
-    mask_bits = steps[0].mask_bits.cpu().numpy()
-    accept_lens = steps[0].accept_lens.cpu().numpy()
-    assert steps[0].ws.last_error() == 0, "device error word set during warm-up"
+class ConfigRun:
+    """One workload on one GPU: R input replicas (each with its own KV pools),
+    one VerifyStep per replica, a private stream."""
 
-    # Timed graphs: P consecutive steps each (one per input replica, so every
-    # step reads inputs the previous steps did not), with nothing but the
-    # kernels inside, so that consecutive kernels overlap as they do when a
-    # caller runs steps back to back (programmatic dependent launch does not
-    # cross a graph launch or an event node).  P divides K.
-    P = steps_per_graph(R, args.steps)
-    G = max(1, min(args.graphs, args.steps // P))
-    graphs = []
-    for j in range(G):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for t in range(P):
-                steps[(j * P + t) % R].run()
-        graphs.append(g)
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            graphs[i % G].replay()
-    torch.cuda.synchronize()
-
-    sampler = None if args.no_clocks else ClockSampler(gpu_id_for_smi(torch, local))
-    if sampler is not None:
-        time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record()
-        for i in range(args.steps // P):
-            graphs[i % G].replay()
-        t1.record()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop() if sampler is not None else None
-    elapsed_ms = job_elapsed_ms(t0.elapsed_time(t1), world, device, torch)
-    assert steps[0].ws.last_error() == 0, "device error word set during the timed region"
-
-    # Stage breakdown (diagnostic, after the timed region): one-step graphs
-    # with timing events captured at the stage boundaries.
-    stage = None
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        external = True
-    except TypeError:
-        external = False
-    if external:
-        evs, sgraphs = [], []
-        for j in range(R):
-            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                s = steps[j]
-                e[0].record()
-                s.select()
-                s.build()
-                e[1].record()
-                s.attention()
-                e[2].record()
-                s.accept()
-                s.commit()
-                e[3].record()
-            sgraphs.append(g)
-            evs.append(e)
-        sel, att, acc = [], [], []
-        with torch.cuda.stream(stream):
-            for i in range(max(2 * R, min(args.steps, 200))):
-                sgraphs[i % R].replay()
-                if i >= R:  # warm
-                    torch.cuda.synchronize()
-                    e = evs[i % R]
-                    sel.append(e[0].elapsed_time(e[1]))
-                    att.append(e[1].elapsed_time(e[2]))
-                    acc.append(e[2].elapsed_time(e[3]))
+    def __init__(self, wl, device, seed, torch, replicas=0):
+        from accept_select_top_gb300.pipeline import VerifyStep
+        self.torch, self.wl, self.device = torch, wl, device
+        self.mode, inp, self.lay = prepare(wl, device, seed, torch)
+        nbytes = lambda x: 0 if x is None else x.numel() * x.element_size()
+        per_replica = (sum(nbytes(d) for d in inp.drafts) + nbytes(inp.target_logits) + nbytes(inp.k_pool)
+                       + nbytes(inp.v_pool) + nbytes(inp.q) + nbytes(inp.draft_probs))
+        self.R = replicas or max(2, min(8, math.ceil(4 * L2_BYTES / per_replica)))
+        self.inputs = [inp] + [clone_inputs(inp, torch) for _ in range(self.R - 1)]
+        self.steps = [VerifyStep(wl, x, self.mode, device=device) for x in self.inputs]
+        self.stream = torch.cuda.Stream(device=device)
+        # inputs, clones and workspace zero fills were enqueued on the default
+        # stream; the steps run on self.stream, which is not ordered after it
         torch.cuda.synchronize()
-        stage = {"select_build": statistics.mean(sel), "attention": statistics.mean(att),
-                 "accept_commit": statistics.mean(acc)}
 
-    e2e = None if args.no_e2e else run_e2e(args, torch, wl, mode, steps[0], stream, device)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, mode, steps[0], lay, torch)
-    return wl, mode, lay, elapsed_ms, stage, mask_bits, accept_lens, clocks, e2e, cpu, world, G, R, external, P
+    def set_overlap(self, on):
+        for s in self.steps:
+            s.ws.set_overlap(on)
+
+    def warmup(self, n):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for i in range(n):
+                self.steps[i % self.R].run()
+        torch.cuda.synchronize()
+        assert self.steps[0].ws.last_error() == 0, "device error word set during warm-up"
+
+    def capture(self, K, graphs_max):
+        """Graphs of P consecutive steps (one per replica, so every step reads
+        inputs the previous steps did not), holding only the kernels."""
+        torch = self.torch
+        P = steps_per_graph(self.R, K)
+        G = max(1, min(graphs_max, K // P))
+        graphs = []
+        for j in range(G):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for t in range(P):
+                    self.steps[(j * P + t) % self.R].run()
+            graphs.append(g)
+        return graphs, P
+
+    def replay(self, graphs, n):
+        with self.torch.cuda.stream(self.stream):
+            for i in range(n):
+                graphs[i % len(graphs)].replay()
+
+    def timed(self, graphs, P, K, world=1, barrier=None):
+        torch = self.torch
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            t0.record()
+            for i in range(K // P):
+                graphs[i % len(graphs)].replay()
+            t1.record()
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        return t0.elapsed_time(t1)
+
+    def per_call(self, M):
+        """Per-call device durations (µs), each step alone on its replica, with
+        events between the calls; averaged over M steps after one warm cycle."""
+        torch = self.torch
+        wl = self.wl
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+        names = [f"select{i}" for i in range(wl.S)] + ["build", "attention", "accept", "commit"]
+        graphs, evs = [], []
+        for j in range(self.R):
+            s = self.steps[j]
+            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                e[0].record()
+                s.select_step(0)
+                e[1].record()
+                for i in range(1, wl.S):
+                    s.select_step(i)
+                    e[i + 1].record()
+                s.build()
+                e[wl.S + 1].record()
+                s.attention()
+                e[wl.S + 2].record()
+                s.accept()
+                e[wl.S + 3].record()
+                s.commit()
+                e[wl.S + 4].record()
+            graphs.append(g)
+            evs.append(e)
+        acc = {k: [] for k in names}
+        with torch.cuda.stream(self.stream):
+            for i in range(self.R + M):
+                graphs[i % self.R].replay()
+                torch.cuda.synchronize()
+                if i >= self.R:
+                    e = evs[i % self.R]
+                    for c, k in enumerate(names):
+                        acc[k].append(e[c].elapsed_time(e[c + 1]) * 1e3)
+        per = {k: statistics.mean(v) for k, v in acc.items()}
+        groups = {"select": sum(per[f"select{i}"] for i in range(wl.S)), "build": per["build"],
+                  "attention": per["attention"], "accept": per["accept"], "commit": per["commit"]}
+        return {"calls_us": per, "groups_us": groups}
 
 
 def run_e2e(args, torch, wl, mode, step, stream, device):
@@ -387,13 +460,14 @@ def run_e2e(args, torch, wl, mode, step, stream, device):
     h2d = sum(v.numel() * v.element_size() for v in h_in.values()) + sum(d.numel() * d.element_size()
                                                                          for d in h_drafts)
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    K = min(args.steps, 200)
+    K = max(8, min(args.steps, 50))
 
     inp1 = _copy.copy(inp)  # the copied inputs get buffers of their own; the rest is shared
     for k in names:
         setattr(inp1, k, torch.empty_like(getattr(inp, k)))
     inp1.drafts = [torch.empty_like(d) for d in inp.drafts]
     sets = [(inp, step), (inp1, VerifyStep(wl, inp1, mode, device=device))]
+    torch.cuda.synchronize()  # the new step's workspace zero fill ran on the default stream
     copy_stream = torch.cuda.Stream(device)
     ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
@@ -434,44 +508,137 @@ def run_e2e(args, torch, wl, mode, step, stream, device):
                     "copies (a copy stream, two device input sets) overlap step i's compute"}
 
 
+def measure_config(name, args, torch, device, seed, world, peaks, peaks_kind, headline):
+    """Everything measured for one workload: the timed steps (and the clocks
+    around them for the headline), the same steps with overlap allowed, the
+    per-call pass, e2e and the CPU baseline."""
+    from accept_select_top_gb300 import workloads as W
+    from accept_select_top_gb300.pipeline import launches_per_step
+    rank = int(os.environ.get("RANK", 0))
+    wl = W.WORKLOADS[name]
+    run = ConfigRun(wl, device, seed, torch, args.replicas)
+    W0 = max(3, args.warmup)
+    run.warmup(W0)
+    s0 = run.steps[0]
+    mask_bits = s0.mask_bits.cpu().numpy()
+    accept_lens = s0.accept_lens.cpu().numpy()
+    K = args.steps
+    graphs, P = run.capture(K, args.graphs)
+    run.replay(graphs, W0)
+    torch.cuda.synchronize()
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else None
+    sampler = None
+    if headline and not args.no_clocks:
+        sampler = ClockSampler(gpu_id_for_smi(torch, torch.cuda.current_device()))
+        time.sleep(0.3)
+    elapsed = run.timed(graphs, P, K, world, barrier)
+    clocks = sampler.stop() if sampler is not None else None
+    elapsed = job_elapsed_ms(elapsed, world, device, torch)
+    assert s0.ws.last_error() == 0, "device error word set during the timed region"
+    del graphs
+    overlap_ms = None
+    if not args.no_overlap_variant:
+        run.set_overlap(True)
+        og, OP_ = run.capture(K, args.graphs)
+        run.replay(og, W0)
+        overlap_ms = run.timed(og, OP_, K)
+        run.set_overlap(False)
+        del og
+    calls = run.per_call(max(2 * run.R, min(K, 50)))
+    bytes_ = group_bytes(wl, run.lay, run.mode, accept_lens)
+    flops = attention_flops(wl, run.lay, mask_bits)
+    kernels = None
+    roof = None
+    if calls is not None:
+        kernels = {}
+        for g in GROUPS:
+            r = roofline(g, calls["groups_us"][g], bytes_[g], flops, peaks, peaks_kind)
+            r.update({"us": calls["groups_us"][g], "algorithmic_bytes": int(bytes_[g])})
+            kernels[g] = r
+        dom = max(GROUPS, key=lambda g: calls["groups_us"][g])
+        roof = {k: kernels[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+        tr = traffic_entry(dom, name)
+        roof.update({"traffic": None if tr is None else tr["dram_bytes_per_launch"], "kernel": dom,
+                     "kernel_us": kernels[dom]["us"], "algorithmic_bytes": kernels[dom]["algorithmic_bytes"],
+                     "peak_kind": kernels[dom]["peak_kind"],
+                     "launches": wl.S if dom == "select" else (2 if dom == "accept" and run.mode == "sampling"
+                                                               else 1)})
+        if dom == "attention":
+            roof["flops"] = flops
+    e2e = None if args.no_e2e else run_e2e(args, torch, wl, run.mode, s0, run.stream, device)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        budget = args.cpu_budget_s if headline else args.cpu_budget_s / 4
+        cpu = cpu_baseline(wl, run.mode, s0, budget)
+    ms_per_step = elapsed / K
+    out = {
+        "workload": name, "b": wl.b, "topk": wl.k, "num_steps": wl.S, "num_draft_tokens": wl.n, "vocab": wl.V,
+        "heads": f"{wl.Hq}/{wl.Hkv}", "head_dim": wl.D, "page_size": wl.page_size, "context": list(wl.ctx),
+        "accept": run.mode, "step_us": ms_per_step * 1e3,
+        "tokens_per_s": job_tokens_per_s(wl.b, wl.n, K, world, elapsed),
+        "step_us_overlap": None if overlap_ms is None else overlap_ms / K * 1e3,
+        "mean_accept_lens": float(np.mean(accept_lens)),
+        "kernels": kernels, "calls_us": None if calls is None else calls["calls_us"],
+        "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+        "gpu_launches_per_step": launches_per_step(wl, run.mode),
+        "replicas": run.R, "steps_per_graph": P, "steps": K,
+        "l2": f"{run.R} rotating input replicas, each with its own KV pools (> 4x the 129 MB L2 per cycle)",
+    }
+    del run
+    torch.cuda.empty_cache()
+    return out, elapsed, clocks
+
+
 # ------------------------------------------------- oracle (CPU baseline)
 
-def oracle_sample(wl, mode, host, r, pair_frac):
-    """Runs the oracle over requests [0, r) (attention on a fraction of their
-    (row, head) pairs) and returns per-stage seconds and the units done."""
+def oracle_sample(wl, mode, host, reqs, pair_frac, seed=0):
+    """Runs the oracle over requests `reqs` end to end, the attention on a
+    fraction of their (row, head) pairs, and returns per-stage seconds and the
+    pairs done."""
     import oracle
-    from oracle import pipeline as OP
-    sub = dict(wl.__dict__)
-    sub["b"] = r
-    from accept_select_top_gb300.workloads import Workload
-    w = Workload(**sub)
-    n = wl.n
-    times = {}
-    t = time.perf_counter()
-    chain = OP.select_chain(w, [d[: w.rows(i)] for i, d in enumerate(host["drafts"])])
-    tree = OP.tree_from_chain(w, chain, host["bonus"][:r], host["seq_lens"][:r])
-    times["select_build"] = time.perf_counter() - t
-    rows = r * n
-    npairs = max(1, int(rows * wl.Hq * pair_frac))
-    rng = np.random.default_rng(0)
-    flat = rng.choice(rows * wl.Hq, size=npairs, replace=False)
-    pairs = np.stack([flat // wl.Hq, flat % wl.Hq], 1).astype(np.int32)
-    t = time.perf_counter()
-    oracle.verify_attention(r, n, wl.Hq, wl.Hkv, wl.D, host["q"][: rows], host["k_pool"], host["v_pool"],
-                            host["req_to_token"], host["req_pool_idx"][:r], host["seq_lens"][:r],
-                            host["verify_loc"][: rows], tree["mask_bits"], 1.0 / math.sqrt(wl.D), pairs=pairs)
-    times["attention"] = time.perf_counter() - t
-    t = time.perf_counter()
-    if mode == "greedy":
-        acc = OP.accept(w, "greedy", tree, host["logits"][: rows])
-    else:
-        acc = OP.accept(w, "sampling", tree, host["logits"][: rows], host["q_probs"][: rows], host["temps"][:r],
-                        host["u"][: rows], host["u_final"][:r])
-    OP.commit(w, {"req_to_token": host["req_to_token"], "req_pool_idx": host["req_pool_idx"][:r],
-                  "seq_lens": host["seq_lens"][:r], "verify_loc": host["verify_loc"][: rows]},
-              host["k_pool"], host["v_pool"], acc)
-    times["accept_commit"] = time.perf_counter() - t
-    return times, npairs
+    from accept_select_top_gb300.workloads import scaled
+    n, V = wl.n, wl.V
+    times = {"select_build": 0.0, "attention": 0.0, "accept_commit": 0.0}
+    npairs_total = 0
+    w1 = scaled(wl, b=1)
+    rng = np.random.default_rng(seed)
+    for r in reqs:
+        rows = slice(r * n, (r + 1) * n)
+        t = time.perf_counter()
+        chain_steps, scores = [], None
+        for i in range(wl.S):
+            rr = slice(r * w1.rows(i), (r + 1) * w1.rows(i))
+            o = oracle.select_topk(i, 1, wl.k, host["drafts"][i][rr], 1.0, scores)
+            chain_steps.append(o)
+            scores = o["scores_out"]
+        score_space = np.ascontiguousarray(np.concatenate([s["score_blk"] for s in chain_steps], axis=1))
+        token_space = np.ascontiguousarray(np.concatenate([s["token_blk"] for s in chain_steps], axis=1))
+        parent_space = (np.ascontiguousarray(np.concatenate([s["parent_blk"] for s in chain_steps[:-1]], axis=1))
+                        if wl.S > 1 else np.full((1, 1), -1, np.int32))
+        tree = oracle.build_tree(1, wl.k, wl.S, n, score_space, token_space, parent_space,
+                                 host["bonus"][r:r + 1], host["seq_lens"][r:r + 1])
+        times["select_build"] += time.perf_counter() - t
+        npairs = max(1, int(round(n * wl.Hq * pair_frac)))
+        flat = rng.choice(n * wl.Hq, size=npairs, replace=False)
+        pairs = np.stack([flat // wl.Hq, flat % wl.Hq], 1).astype(np.int32)
+        t = time.perf_counter()
+        oracle.verify_attention(1, n, wl.Hq, wl.Hkv, wl.D, host["q"][rows], host["k_pool"], host["v_pool"],
+                                host["req_to_token"], host["req_pool_idx"][r:r + 1], host["seq_lens"][r:r + 1],
+                                host["verify_loc"][rows], tree["mask_bits"], 1.0 / math.sqrt(wl.D), pairs=pairs)
+        times["attention"] += time.perf_counter() - t
+        npairs_total += npairs
+        t = time.perf_counter()
+        args = (tree["draft_tokens"], np.arange(n, dtype=np.int32), tree["next_token"], tree["next_sibling"])
+        if mode == "greedy":
+            acc = oracle.verify_greedy(1, n, wl.S, host["logits"][rows], *args)
+        else:
+            acc = oracle.verify_sampling(1, n, wl.S, host["logits"][rows], host["q_probs"][rows],
+                                         host["temps"][r:r + 1], host["u"][rows], host["u_final"][r:r + 1], *args)
+        oracle.commit_kv(1, n, wl.W, wl.Hkv, wl.D, wl.page_size, [host["k_pool"]], [host["v_pool"]],
+                         host["req_to_token"], host["req_pool_idx"][r:r + 1], host["seq_lens"][r:r + 1],
+                         host["verify_loc"][rows], acc["accept_index"], acc["accept_lens"])
+        times["accept_commit"] += time.perf_counter() - t
+    return times, npairs_total
 
 
 def host_inputs(step, mode):
@@ -487,131 +654,159 @@ def host_inputs(step, mode):
     return h
 
 
-def sample_plan(wl):
-    """(requests, attention pair fraction) of the bounded oracle sample."""
+def pair_seconds(wl):
+    """A rough cost of one (row, head) pair of the oracle's fp64 attention."""
     ctx = wl.ctx[1] if wl.ctx[0] == "fixed" else (wl.ctx[2] if wl.ctx[0] == "uniform" else max(wl.ctx[1]))
-    per_pair = 4.0 * wl.D * (ctx + wl.n) * 2.5e-9  # ~ seconds of fp64 work per (row, head) pair
-    r = max(1, min(wl.b, 2))
-    frac = min(1.0, 6.0 / max(1e-9, per_pair * r * wl.n * wl.Hq))
-    return r, frac
+    return 4.0 * wl.D * (ctx + wl.n) * 2.5e-9
 
 
-def cpu_baseline(wl, mode, step, lay, torch):
+def pair_fraction(wl, budget_s, reqs):
+    """The fraction of a request's (row, head) pairs whose attention fits in
+    about half the budget for `reqs` requests."""
+    return min(1.0, 0.5 * budget_s / max(1e-9, pair_seconds(wl) * reqs * wl.n * wl.Hq))
+
+
+def scale_to_request(wl, times, nreq, npairs):
+    """Seconds one full request costs the oracle: select/build and
+    accept/commit per request, attention per (row, head) pair."""
+    return ((times["select_build"] + times["accept_commit"]) / nreq
+            + times["attention"] / npairs * wl.n * wl.Hq)
+
+
+def cpu_baseline(wl, mode, step, budget_s):
     host = host_inputs(step, mode)
-    r, frac = sample_plan(wl)
-    times, npairs = oracle_sample(wl, mode, host, r, frac)
-    # scale each stage to the whole batch: select/build and accept/commit by
-    # requests, attention by (row, head) pairs
-    full = (times["select_build"] + times["accept_commit"]) * (wl.b / r) + \
-        times["attention"] * (wl.b * wl.n * wl.Hq / npairs)
-    return {"value": wl.b * wl.n / full, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{r} of {wl.b} requests end to end, attention on {npairs} of {r * wl.n * wl.Hq} "
-                      f"(row, head) pairs; stages scaled to the full batch",
-            "sample_seconds": round(sum(times.values()), 2), "full_step_seconds_est": round(full, 3)}
+    reqs = list(range(min(wl.b, 2)))
+    frac = pair_fraction(wl, budget_s, len(reqs))
+    times, npairs = oracle_sample(wl, mode, host, reqs, frac)
+    per_req = scale_to_request(wl, times, len(reqs), npairs)
+    return {"value": wl.n / per_req, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"requests {reqs} of {wl.b} end to end, attention on {npairs} of "
+                      f"{len(reqs) * wl.n * wl.Hq} (row, head) pairs; scaled by request and by pair",
+            "sample_seconds": round(sum(times.values()), 2), "full_step_seconds_est": round(per_req * wl.b, 3)}
 
 
 # ---------------------------------------------------------- reference arm
 
-def run_reference(args, torch):
-    """The oracle, as it stands, timed on the host cores for the same workload,
-    metric and unit; each step is a bounded sample (one request, a fraction of
-    the attention pairs) scaled to the full batch."""
+def host_prepare(wl, seed=0):
+    """The workload's inputs drawn on the host, the draft tree and the target
+    agreement from the oracle's own select chain: no GPU and no CUDA library."""
+    import torch
     from accept_select_top_gb300 import workloads as W
-    from accept_select_top_gb300.pipeline import VerifyStep
-    wl = W.WORKLOADS[args.workload]
-    device = "cuda:0" if torch.cuda.is_available() else "cpu"
-    if device == "cpu":
-        return None
-    mode, inp, lay = prepare(wl, device, 0, torch)
-    step = VerifyStep(wl, inp, mode, device=device)
-    host = host_inputs(step, mode)
-    del step
-    r, frac = 1, sample_plan(wl)[1] / 2
-    tot = []
-    for i in range(max(3, args.warmup) + args.steps):
-        times, npairs = oracle_sample(wl, mode, host, r, frac)
-        if i >= max(3, args.warmup):
-            tot.append((times["select_build"] + times["accept_commit"]) * wl.b / r +
-                       times["attention"] * (wl.b * wl.n * wl.Hq / npairs))
-    sec = sum(tot) / len(tot)
-    return wl, sec, f"1 of {wl.b} requests per step, attention on {npairs} (row, head) pairs; scaled to the batch"
+    from oracle import pipeline as OP
+    mode = accept_mode(wl)
+    drafts_t = [W.draft_logits(wl, i, "cpu", seed) for i in range(wl.S)]
+    drafts = [W.host(d) for d in drafts_t]
+    lay = W.kv_layout(wl, seed)
+    bonus = W.host(W.bonus_tokens(wl, "cpu", seed))
+    chain = OP.select_chain(wl, drafts)
+    tree = OP.tree_from_chain(wl, chain, bonus, lay["seq_lens"])
+    rows = W.draft_rows_of_nodes(wl, tree["draft_tokens"], tree["next_token"], tree["next_sibling"],
+                                 chain["token_space"], chain["parent_space"])
+    all_d = torch.cat(drafts_t, 0)
+    logits = W.target_logits(wl, rows, all_d, "cpu", seed)
+    if wl.agreement == "planted":
+        logits = W.plant_agreement(wl, logits, tree["draft_tokens"], tree["next_token"], tree["next_sibling"], seed)
+    att = W.attention_tensors(wl, int(lay["num_slots"]), "cpu", seed)
+    host = {"drafts": drafts, "bonus": bonus, "seq_lens": lay["seq_lens"], "req_pool_idx": lay["req_pool_idx"],
+            "req_to_token": lay["req_to_token"], "verify_loc": lay["verify_loc"], "q": W.host(att["q"]),
+            "k_pool": W.host(att["k_pool"]).copy(), "v_pool": W.host(att["v_pool"]).copy(),
+            "logits": W.host(logits)}
+    if mode == "sampling":
+        temps = W.request_temperatures(wl, temps_mode(wl))
+        u, uf = W.coins(wl, "cpu", seed)
+        host.update(q_probs=W.host(W.draft_probs(wl, rows, all_d, temps, "cpu")), temps=temps, u=W.host(u),
+                    u_final=W.host(uf))
+    return mode, host
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores (one thread) for the same
+    workload, metric and unit.  Each of the W + K steps is one request of the
+    batch (cycling through a few) end to end, with the attention on a fraction
+    of its (row, head) pairs sized so that the whole run spends about
+    --reference-budget-s seconds; every step's wall time is measured.  The
+    value scales each step's stages to one full request (select/build and
+    accept/commit per request, attention per pair) and counts its n tokens."""
+    from accept_select_top_gb300 import workloads as W
+    wl_full = W.WORKLOADS[args.workload]
+    nreq = min(wl_full.b, 4)
+    wl = W.scaled(wl_full, b=nreq)  # a few requests of the same recipe, drawn on the host
+    t_setup = time.perf_counter()
+    mode, host = host_prepare(wl, 0)
+    setup_s = time.perf_counter() - t_setup
+    Wn, K = max(3, args.warmup), args.steps
+    per_step = args.reference_budget_s / (Wn + K)
+    frac = pair_fraction(wl, per_step, 1)
+    walls, per_req = [], []
+    for i in range(Wn + K):
+        t = time.perf_counter()
+        times, npairs = oracle_sample(wl, mode, host, [i % nreq], frac, seed=i)
+        wall = time.perf_counter() - t
+        if i >= Wn:
+            walls.append(wall)
+            per_req.append(scale_to_request(wl, times, 1, npairs))
+    sec_per_req = sum(per_req) / len(per_req)
+    sample = (f"each step one request (of {nreq} drawn on the host with the {args.workload} recipe) end to end, "
+              f"attention on {npairs} of {wl.n * wl.Hq} (row, head) pairs; value scales each step to one full "
+              f"request ({wl.n} tokens)")
+    return wl_full, sec_per_req, sum(walls) / len(walls), sample, setup_s
 
 
 def main(argv=None):
     args = parse_args(argv)
-    import torch
-    rank, world, _ = dist_env()
+    rank, world, local = dist_env()
     peaks, peaks_kind = load_peaks()
     if args.impl == "reference":
         if rank != 0:
             return 0
-        res = run_reference(args, torch)
-        if res is None:
-            print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to prepare the inputs"}))
-            return 0
-        wl, sec, sample = res
-        val = wl.b * wl.n / sec
+        wl, sec_req, wall, sample, setup_s = run_reference(args)
+        val = wl.n / sec_req
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": max(3, args.warmup), "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "warmup": max(3, args.warmup), "ms_per_step": wall * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (drawn on the host)",
             "config": {"workload": args.workload, "b": wl.b, "topk": wl.k, "num_steps": wl.S,
                        "num_draft_tokens": wl.n, "vocab": wl.V},
+            "full_batch_step_s_est": sec_req * wl.b, "setup_s": round(setup_s, 2),
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return 0
 
-    (wl, mode, lay, elapsed_ms, stage, mask_bits, accept_lens, clocks, e2e, cpu, world, G, R,
-     external, P) = run_ours(args, torch)
+    import torch
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    names = selected_configs(args, world)
+    results, head_elapsed, head_clocks = {}, None, None
+    for name in names:
+        headline = name == names[0]
+        out, elapsed, clocks = measure_config(name, args, torch, device, rank, world, peaks, peaks_kind, headline)
+        results[name] = out
+        if headline:
+            head_elapsed, head_clocks = elapsed, clocks
     if rank != 0:
         return 0
-    from accept_select_top_gb300.pipeline import launches_per_step
-    ms_per_step = elapsed_ms / args.steps
-    value = job_tokens_per_s(wl.b, wl.n, args.steps, world, elapsed_ms)
-    bytes_ = step_bytes(wl, None, lay, mode)
-    roof = None
-    if stage is not None:
-        dom = max(stage, key=stage.get)
-        common = "accept_select_top_gb300/csrc/common.cuh"  # helpers compiled into every kernel
-        sources = {"attention": ["accept_select_top_gb300/csrc/attention_tc.cu", common],
-                   "select_build": ["accept_select_top_gb300/csrc/select_topk.cu",
-                                    "accept_select_top_gb300/csrc/build_tree.cu", common],
-                   "accept_commit": ["accept_select_top_gb300/csrc/verify_greedy.cu",
-                                     "accept_select_top_gb300/csrc/verify_sampling.cu",
-                                     "accept_select_top_gb300/csrc/commit_kv.cu", common]}[dom]
-        flops = attention_flops(wl, lay, mask_bits)
-        tensor_bound = dom == "attention" and flops / bytes_["attention"] > \
-            peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        ms = stage[dom]
-        if tensor_bound:
-            ach = flops / (ms / 1e3) / 1e12
-            peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-            roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak}
-        else:
-            ach = bytes_[dom] / (ms / 1e3) / 1e9
-            peak = peaks["hbm_gbs"]
-            roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak}
-        tr = traffic_entry(f"{dom}:{args.workload}", sources)
-        roof.update({"traffic": None if tr is None else tr["dram_bytes_per_launch"], "stage": dom,
-                     "stage_us": ms * 1e3, "algorithmic_bytes": bytes_[dom],
-                     "peak_kind": f"{peaks_kind} ({'sustained' if tensor_bound else 'copy'})"})
-    launches = launches_per_step(wl, mode, int(lay["seq_lens"].max()))
+    h = results[names[0]]
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "step_us": ms_per_step * 1e3,
+        "metric": METRIC, "value": h["tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": head_elapsed / args.steps, "step_us": h["step_us"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded draws; target agreement planted / correlated per the workload recipe)",
-        "config": {"workload": args.workload, "b": wl.b, "topk": wl.k, "num_steps": wl.S, "num_draft_tokens": wl.n,
-                   "vocab": wl.V, "heads": f"{wl.Hq}/{wl.Hkv}", "head_dim": wl.D, "page_size": wl.page_size,
-                   "context": list(wl.ctx), "accept": mode, "parallelism": f"replicas x{world}",
-                   "l2": f"{R} rotating input replicas (> 4x the 129 MB L2 per cycle)",
-                   "graphs": G, "steps_per_graph": P,
-                   "stage_timing": ("separate pass after the timed region: one-step graphs, events at the stage "
-                                    "boundaries, each step alone" if external else "none")},
-        "stages_us": None if stage is None else {k: v * 1e3 for k, v in stage.items()},
-        "mean_accept_lens": float(np.mean(accept_lens)),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches * args.steps, "clocks": clocks,
+        "config": {"workload": names[0], "b": h["b"], "topk": h["topk"], "num_steps": h["num_steps"],
+                   "num_draft_tokens": h["num_draft_tokens"], "vocab": h["vocab"], "heads": h["heads"],
+                   "head_dim": h["head_dim"], "page_size": h["page_size"], "context": h["context"],
+                   "accept": h["accept"], "parallelism": f"replicas x{world}", "l2": h["l2"],
+                   "steps_per_graph": h["steps_per_graph"],
+                   "timing": "every kernel waits for the one before it (no overlap: the EAGLE-loop step); "
+                             "step_us_overlap: the same steps with overlap allowed",
+                   "kernel_timing": "separate pass after the timed region: one-step graphs with events between "
+                                    "the calls, each step alone on its replica"},
+        "step_us_overlap": h["step_us_overlap"], "mean_accept_lens": h["mean_accept_lens"],
+        "roofline": h["roofline"], "kernels": h["kernels"], "cpu_baseline": h["cpu_baseline"], "e2e": h["e2e"],
+        "gpu_launches": h["gpu_launches_per_step"] * args.steps, "clocks": head_clocks,
+        "configs": {k: v for k, v in results.items() if k != names[0]},
     }
     print(json.dumps(line))
     return 0
