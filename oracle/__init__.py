@@ -58,7 +58,9 @@ def _load():
             lib = ctypes.CDLL(build())
             for name in ("oracle_softmax_topk", "oracle_path_step", "oracle_select_topk",
                          "oracle_build_tree", "oracle_verify_attention", "oracle_verify_greedy",
-                         "oracle_verify_sampling", "oracle_verify_target_only", "oracle_commit_kv"):
+                         "oracle_verify_sampling", "oracle_verify_target_only", "oracle_build_chain_tree",
+                         "oracle_chain_accept_greedy", "oracle_assign_draft_locs", "oracle_duplicate_prefix_tail",
+                         "oracle_full_mask", "oracle_commit_kv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -231,6 +233,72 @@ def verify_target_only(b, n, S, logits, temperatures, u, u_final, threshold_sing
         _p(out["predict"]), _p(out["accept_index"]), _p(out["accept_lens"]),
         _p(out["accepted_tokens"]), _p(out["next_root"])), "verify_target_only")
     return out
+
+
+def build_chain_tree(b, S, bonus, draft_tokens, seq_lens):
+    """Tree arrays of b chains; draft_tokens [b, S] (row stride = its width)."""
+    dt = _i32(draft_tokens)
+    dt = dt.reshape(b, -1)
+    n = S + 1
+    out = {name: np.empty(b * n, np.int32) for name in
+           ("draft_tokens", "positions", "retrieve_index", "next_token", "next_sibling")}
+    out["mask_bits"] = np.empty(b * n, np.uint64)
+    _check(_load().oracle_build_chain_tree(b, S, _p(_i32(bonus, (b,))), _p(dt), dt.shape[1],
+                                           _p(_i32(seq_lens, (b,))), _p(out["draft_tokens"]), _p(out["positions"]),
+                                           _p(out["retrieve_index"]), _p(out["next_token"]),
+                                           _p(out["next_sibling"]), _p(out["mask_bits"])), "build_chain_tree")
+    return out
+
+
+def chain_accept_greedy(b, S, logits, draft_tokens, prefix_lens):
+    x, dt = _logits(logits)
+    V = x.shape[-1]
+    d = _i32(draft_tokens).reshape(b, -1)
+    n = S + 1
+    out = {"correct_len": np.empty(b, np.int32), "bonus": np.empty(b, np.int32),
+           "out_tokens": np.empty((b, n), np.int32), "commit_lens": np.empty(b, np.int32),
+           "new_seq_lens": np.empty(b, np.int32), "accept_index": np.empty((b, n), np.int32)}
+    _check(_load().oracle_chain_accept_greedy(
+        b, S, V, dt, _p(x), _p(d), d.shape[1], _p(_i32(prefix_lens, (b,))), _p(out["correct_len"]),
+        _p(out["bonus"]), _p(out["out_tokens"]), _p(out["commit_lens"]), _p(out["new_seq_lens"]),
+        _p(out["accept_index"])), "chain_accept_greedy")
+    return out
+
+
+def assign_draft_locs(b, topk, S, page_size, req_to_token, req_pool_idx, seq_lens, num_slots):
+    r2t = _i32(req_to_token)
+    out = np.empty(b * topk * S, np.int32)
+    pos = np.empty(b, np.int32)
+    _check(_load().oracle_assign_draft_locs(b, topk, S, page_size, _p(r2t), r2t.shape[-1], _p(_i32(req_pool_idx)),
+                                            _p(_i32(seq_lens)), ctypes.c_int64(num_slots), _p(out), _p(pos)),
+           "assign_draft_locs")
+    return {"out_cache_loc": out, "positions": pos if topk == 1 else None}
+
+
+def duplicate_prefix_tail(b, topk, S, page_size, Hkv, D, k_layers, v_layers, req_to_token, req_pool_idx, seq_lens):
+    """Copies in place into the uint16 pool arrays of k_layers / v_layers."""
+    L = len(k_layers)
+    for a in list(k_layers) + list(v_layers):
+        assert a.dtype == np.uint16 and a.flags["C_CONTIGUOUS"]
+    num_slots = k_layers[0].size // (Hkv * D)
+    kp = (ctypes.c_void_p * L)(*[a.ctypes.data for a in k_layers])
+    vp = (ctypes.c_void_p * L)(*[a.ctypes.data for a in v_layers])
+    r2t = _i32(req_to_token)
+    _check(_load().oracle_duplicate_prefix_tail(b, topk, S, page_size, Hkv, D, L, kp, vp, ctypes.c_int64(num_slots),
+                                                _p(r2t), r2t.shape[-1], _p(_i32(req_pool_idx)), _p(_i32(seq_lens))),
+           "duplicate_prefix_tail")
+
+
+def full_mask(b, n, seq_lens, mask_bits, fill_prefix=True, out=None):
+    """The FULL_MASK verify mask (uint8, one [n, L_b + n] block per request);
+    with fill_prefix False the prefix columns keep the values of ``out``."""
+    sl = _i32(seq_lens, (b,))
+    total = int(np.sum(n * (sl.astype(np.int64) + n)))
+    m = np.zeros(total, np.uint8) if out is None else np.ascontiguousarray(out, np.uint8).copy()
+    assert m.size == total
+    _check(_load().oracle_full_mask(b, n, _p(sl), _p(np.ascontiguousarray(mask_bits, np.uint64)),
+                                    1 if fill_prefix else 0, _p(m)), "full_mask")
+    return m
 
 
 def commit_kv(b, n, W, Hkv, D, page_size, k_layers, v_layers, req_to_token, req_pool_idx, seq_lens,

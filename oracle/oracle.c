@@ -611,6 +611,143 @@ int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void*
   return rc;
 }
 
+/* ------------------------------------------------------ f2 chain fast path */
+
+int oracle_build_chain_tree(int b, int S, const int32_t* bonus, const int32_t* draft_tokens,
+                            int draft_ld, const int32_t* seq_lens,
+                            int32_t* tree_tokens, int32_t* positions, int32_t* retrieve_index,
+                            int32_t* next_token, int32_t* next_sibling, uint64_t* mask_bits) {
+  if (b < 0 || S < 1 || S + 1 > 64 || draft_ld < S) return ORC_EARG;
+  const int n = S + 1;
+  for (int q = 0; q < b; ++q) {
+    const size_t base = (size_t)q * n;
+    for (int i = 0; i < n; ++i) {
+      /* a chain: node i hangs below node i-1 and sees nodes 0..i */
+      tree_tokens[base + i] = i == 0 ? bonus[q] : draft_tokens[(size_t)q * draft_ld + i - 1];
+      positions[base + i] = seq_lens[q] + i;
+      retrieve_index[base + i] = (int32_t)(base + i);
+      next_token[base + i] = i + 1 < n ? i + 1 : -1;
+      next_sibling[base + i] = -1;
+      uint64_t m = 0;
+      for (int j = 0; j <= i; ++j) m |= (uint64_t)1 << j;
+      mask_bits[base + i] = m;
+    }
+  }
+  return ORC_OK;
+}
+
+int oracle_chain_accept_greedy(int b, int S, int V, int dtype, const void* logits,
+                               const int32_t* draft_tokens, int draft_ld, const int32_t* prefix_lens,
+                               int32_t* correct_len, int32_t* bonus, int32_t* out_tokens,
+                               int32_t* commit_lens, int32_t* new_seq_lens, int32_t* accept_index) {
+  if (b < 0 || S < 1 || V <= 0 || draft_ld < S) return ORC_EARG;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
+  const int n = S + 1;
+  for (int q = 0; q < b; ++q) {
+    /* compute_dflash_correct_drafts_and_bonus: leading matches of the chain */
+    int c = 0;
+    while (c < S) {
+      int tp = row_argmax(logits, dtype, ((size_t)q * n + c) * (size_t)V, V);
+      if (draft_tokens[(size_t)q * draft_ld + c] != tp) break;
+      ++c;
+    }
+    correct_len[q] = c;
+    bonus[q] = row_argmax(logits, dtype, ((size_t)q * n + c) * (size_t)V, V);
+    /* BuildOutTokens: the draft tokens, then the bonus scattered at correct_len */
+    for (int j = 0; j < n; ++j) out_tokens[(size_t)q * n + j] = j < S ? draft_tokens[(size_t)q * draft_ld + j] : -1;
+    out_tokens[(size_t)q * n + c] = bonus[q];
+    /* FinalizeAcceptLens */
+    commit_lens[q] = c + 1;
+    new_seq_lens[q] = prefix_lens[q] + c + 1;
+    if (accept_index)
+      for (int j = 0; j < n; ++j) accept_index[(size_t)q * n + j] = j <= c ? (int32_t)((size_t)q * n + j) : -1;
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------- f4 the draft side of the KV */
+
+/* The region geometry of paged branches: hole count, page-aligned base and
+ * the positions one branch region spans. */
+static void branch_region(int L, int S, int page_size, int* last_page, int* prefix_base, int* R) {
+  *last_page = L % page_size;
+  *prefix_base = L - *last_page;
+  *R = (*last_page + S + page_size - 1) / page_size * page_size;
+}
+
+int oracle_assign_draft_locs(int b, int topk, int S, int page_size, const int32_t* req_to_token,
+                             int row_w, const int32_t* req_pool_idx, const int32_t* seq_lens,
+                             int64_t num_slots, int32_t* out_cache_loc, int32_t* positions) {
+  if (b < 0 || topk < 1 || S < 1 || page_size < 1 || row_w < 1) return ORC_EARG;
+  for (int q = 0; q < b; ++q) {
+    const int L = seq_lens[q];
+    const int32_t* row = req_to_token + (size_t)req_pool_idx[q] * row_w;
+    for (int t = 0; t < topk; ++t) {
+      for (int s = 0; s < S; ++s) {
+        long pos;
+        if (page_size == 1 || topk == 1) {
+          pos = (long)L + (long)t * S + s; /* contiguous after the prefix */
+        } else {
+          int last_page, prefix_base, R;
+          branch_region(L, S, page_size, &last_page, &prefix_base, &R);
+          pos = (long)prefix_base + (long)t * R + last_page + s;
+        }
+        if (L < 0 || pos >= row_w) return ORC_EBOUNDS;
+        const int32_t slot = row[pos];
+        if (slot < 0 || slot >= num_slots) return ORC_EBOUNDS;
+        out_cache_loc[((size_t)q * topk + t) * S + s] = slot;
+      }
+    }
+    if (positions && topk == 1) positions[q] = L;
+  }
+  return ORC_OK;
+}
+
+int oracle_duplicate_prefix_tail(int b, int topk, int S, int page_size, int Hkv, int D, int num_layers,
+                                 uint16_t* const* k_layers, uint16_t* const* v_layers, int64_t num_slots,
+                                 const int32_t* req_to_token, int row_w, const int32_t* req_pool_idx,
+                                 const int32_t* seq_lens) {
+  if (b < 0 || topk < 1 || S < 1 || page_size < 1 || Hkv < 1 || D < 1 || num_layers < 1) return ORC_EARG;
+  if (page_size == 1 || topk == 1) return ORC_OK;
+  const size_t rowlen = (size_t)Hkv * D;
+  for (int q = 0; q < b; ++q) {
+    int last_page, prefix_base, R;
+    branch_region(seq_lens[q], S, page_size, &last_page, &prefix_base, &R);
+    const int32_t* row = req_to_token + (size_t)req_pool_idx[q] * row_w;
+    for (int t = 1; t < topk; ++t) {
+      for (int j = 0; j < last_page; ++j) {
+        const long sp = (long)prefix_base + j, dp = (long)prefix_base + (long)t * R + j;
+        if (dp >= row_w) return ORC_EBOUNDS;
+        const int64_t src = row[sp], dst = row[dp];
+        if (src < 0 || src >= num_slots || dst < 0 || dst >= num_slots) return ORC_EBOUNDS;
+        for (int l = 0; l < num_layers; ++l) {
+          memcpy(k_layers[l] + (size_t)dst * rowlen, k_layers[l] + (size_t)src * rowlen, rowlen * 2);
+          memcpy(v_layers[l] + (size_t)dst * rowlen, v_layers[l] + (size_t)src * rowlen, rowlen * 2);
+        }
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+int oracle_full_mask(int b, int n, const int32_t* seq_lens, const uint64_t* mask_bits, int fill_prefix,
+                     uint8_t* mask) {
+  if (b < 0 || n < 1 || n > 64) return ORC_EARG;
+  size_t off = 0;
+  for (int q = 0; q < b; ++q) {
+    const int L = seq_lens[q];
+    if (L < 0) return ORC_EBOUNDS;
+    for (int i = 0; i < n; ++i) {
+      uint8_t* row = mask + off + (size_t)i * (L + n);
+      if (fill_prefix)
+        for (int j = 0; j < L; ++j) row[j] = 1; /* every verify row sees the whole prefix */
+      for (int j = 0; j < n; ++j) row[L + j] = (uint8_t)((mask_bits[(size_t)q * n + i] >> j) & 1u);
+    }
+    off += (size_t)n * (L + n);
+  }
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------ c9 commit */
 
 int oracle_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers,

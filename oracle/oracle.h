@@ -168,6 +168,77 @@ int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void*
                               int32_t* accept_lens, int32_t* accepted_tokens,
                               int32_t* next_root);
 
+/* f2 -- the chain fast path for topk == 1 (num_draft_tokens = num_steps + 1).
+ * [SGL-XI 平台分派与 chain 特化 (build_chain_tree)], [ACCEPT section 5 (DSpark
+ * correct_len)].
+ *
+ * oracle_build_chain_tree: the tree of a chain of S draft tokens per request,
+ * n = S + 1 nodes: node 0 = bonus[b], node i = draft_tokens[b*draft_ld + i-1];
+ * the parent of node i is node i-1; positions = seq_len + i; mask row i =
+ * nodes 0..i (lower triangular); next_token[i] = i + 1 (-1 for the last);
+ * next_sibling = -1; retrieve_index = b*n + i.  Outputs [b*n]. */
+int oracle_build_chain_tree(int b, int S, const int32_t* bonus, const int32_t* draft_tokens,
+                            int draft_ld, const int32_t* seq_lens,
+                            int32_t* tree_tokens, int32_t* positions, int32_t* retrieve_index,
+                            int32_t* next_token, int32_t* next_sibling, uint64_t* mask_bits);
+
+/* oracle_chain_accept_greedy: the chain's greedy accept in the counts DSpark
+ * uses.  logits: [b*(S+1), V], row b*(S+1)+j = the target at chain position
+ * j (the root is position 0).  target_predict[j] = argmax (lowest index on
+ * ties).  correct_len = the number of leading positions j < S with
+ * draft_tokens[b, j] == target_predict[j] (the first mismatch ends it);
+ * bonus = target_predict[correct_len]; out_tokens [b, S+1] = the draft tokens
+ * then -1, with the bonus written at position correct_len (only the first
+ * commit_lens entries are output); commit_lens = correct_len + 1;
+ * new_seq_lens = prefix_lens + commit_lens; accept_index [b, S+1] (nullable)
+ * = b*(S+1) + j for j < commit_lens, -1 after. */
+int oracle_chain_accept_greedy(int b, int S, int V, int dtype, const void* logits,
+                               const int32_t* draft_tokens, int draft_ld, const int32_t* prefix_lens,
+                               int32_t* correct_len, int32_t* bonus, int32_t* out_tokens,
+                               int32_t* commit_lens, int32_t* new_seq_lens, int32_t* accept_index);
+
+/* f4 -- the draft side of the KV: slots for the draft writes, the prefix-tail
+ * copy of paged branches, and the materialised verify mask.
+ * [SGL-XI draft 前向的输入准备:prepare_for_draft], [EVOL 草稿、验证与槽位 (the
+ * last partial page is duplicated)], [SGL-XI 三种 mask 形态 (FULL_MASK,
+ * fill_prefix_mask)].
+ *
+ * oracle_assign_draft_locs: out_cache_loc [b, topk, S] (flattened) = the slots
+ * the S draft steps of each of the topk branches write.  With L = seq_lens[b]
+ * and row = req_to_token row req_pool_idx[b]:
+ *   page_size == 1 or topk == 1: branch t, step s -> row[L + t*S + s] (each
+ *     branch writes contiguous positions after the prefix);
+ *   page_size > 1 and topk > 1: last_page = L % page_size, prefix_base = L -
+ *     last_page, R = ceil((last_page + S) / page_size) * page_size; branch t's
+ *     page-aligned region is positions [prefix_base + t*R, prefix_base +
+ *     (t+1)*R), its first last_page positions are holes (branch 0's are the
+ *     real prefix tail) and step s -> row[prefix_base + t*R + last_page + s].
+ * positions [b] (nullable; topk == 1 only) = L, the position of the first
+ * draft row.  ORC_EBOUNDS when a position passes row_w or a slot is out of
+ * [0, num_slots). */
+int oracle_assign_draft_locs(int b, int topk, int S, int page_size, const int32_t* req_to_token,
+                             int row_w, const int32_t* req_pool_idx, const int32_t* seq_lens,
+                             int64_t num_slots, int32_t* out_cache_loc, int32_t* positions);
+
+/* oracle_duplicate_prefix_tail: for page_size > 1 and topk > 1, copies the KV
+ * of the real prefix tail (row[prefix_base + j], j < last_page) into the hole
+ * slots of branches 1..topk-1 (row[prefix_base + t*R + j]), every layer, K and
+ * V, so that a kernel reading whole pages sees the prefix tail in every
+ * branch.  Does nothing for page_size == 1 or topk == 1. */
+int oracle_duplicate_prefix_tail(int b, int topk, int S, int page_size, int Hkv, int D, int num_layers,
+                                 uint16_t* const* k_layers, uint16_t* const* v_layers, int64_t num_slots,
+                                 const int32_t* req_to_token, int row_w, const int32_t* req_pool_idx,
+                                 const int32_t* seq_lens);
+
+/* oracle_full_mask: the FULL_MASK verify mask, one block per request, blocks
+ * concatenated in request order: request b's block is n rows of L_b + n bytes
+ * (L_b = seq_lens[b]), row i = L_b prefix columns (1, visible; written only
+ * when fill_prefix, else left as they are) then n tree columns, column j = 1
+ * iff bit j of mask_bits[b*n + i] is set.  mask: uint8, sum_b n*(L_b + n)
+ * bytes. */
+int oracle_full_mask(int b, int n, const int32_t* seq_lens, const uint64_t* mask_bits, int fill_prefix,
+                     uint8_t* mask);
+
 /* c9 -- KV commit.  [SGL-XI KV 回写], [ACCEPT section 3 (input/output shift)],
  * [EVOL 草稿、验证与槽位].
  * For request b with L = accept_lens[b] and k < L:
