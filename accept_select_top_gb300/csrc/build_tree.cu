@@ -152,7 +152,35 @@ __global__ void __launch_bounds__(kBuildThreads) build_tree_kernel(BuildParams a
   }
 }
 
+// build_chain_tree [SGL-XI 平台分派与 chain 特化]: with topk = 1 and
+// num_draft_tokens = num_steps + 1 the tree is a chain whose structure is
+// constant (node i hangs below node i - 1, the mask is lower triangular); one
+// thread per node writes it, reading only its own token and the request's
+// prefix length.
+__global__ void __launch_bounds__(256) build_chain_kernel(ChainParams a) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = a.S + 1;
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= a.b * n) return;
+  const int req = g / n, i = g - req * n;
+  const int tok = i == 0 ? a.bonus[req] : a.draft_tokens[size_t(req) * a.draft_ld + i - 1];
+  a.tree_tokens[g] = tok;
+  a.positions[g] = a.seq_lens[req] + i;
+  a.retrieve_index[g] = g;
+  a.next_token[g] = i + 1 < n ? i + 1 : -1;
+  a.next_sibling[g] = -1;
+  a.mask_bits[g] = i == 63 ? ~uint64_t(0) : (uint64_t(1) << (i + 1)) - 1;  // nodes 0..i
+}
+
 }  // namespace
+
+int launch_build_chain_tree(const ChainParams& p, cudaStream_t stream) {
+  const int total = p.b * (p.S + 1);
+  if (launch_pdl(build_chain_kernel, dim3((total + 255) / 256), dim3(256), 0, stream, p) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
 
 size_t build_tree_smem_bytes(int k, int S) {
   const size_t C = size_t(k) + size_t(S - 1) * k * k;

@@ -34,6 +34,19 @@ struct SelectParams {
   unsigned char* partials;  // this call's half
 };
 
+struct ChainParams {
+  int b, S, draft_ld;
+  const int32_t* bonus;
+  const int32_t* draft_tokens;
+  const int32_t* seq_lens;
+  int32_t* tree_tokens;
+  int32_t* positions;
+  int32_t* retrieve_index;
+  int32_t* next_token;
+  int32_t* next_sibling;
+  uint64_t* mask_bits;
+};
+
 struct BuildParams {
   int b, k, S, n;
   const float* score_space;
@@ -53,6 +66,19 @@ struct BuildParams {
 struct GreedyParams {
   int b, n, S, V, dtype;
   const void* logits;
+  // chain: the DSpark counts of a topk = 1 chain (n = S + 1; no tree arrays):
+  // draft tokens [b, S] with row stride draft_ld, prefix_lens in, and
+  // correct_len / bonus / out_tokens [b, n] / commit_lens / new_seq_lens out;
+  // accept_index [b, n] is written too (nullable in this mode)
+  int chain;
+  int draft_ld;
+  const int32_t* chain_drafts;
+  const int32_t* prefix_lens;
+  int32_t* correct_len;
+  int32_t* bonus;
+  int32_t* out_tokens;
+  int32_t* commit_lens;
+  int32_t* new_seq_lens;
   const int32_t* draft_tokens;
   const int32_t* retrieve_index;
   const int32_t* next_token;
@@ -77,6 +103,10 @@ struct GreedyParams {
 struct SamplingParams {
   int b, n, S, V, dtype;
   const void* logits;
+  // target_only: the target-only tree sampler (coin of the scanned node,
+  // sibling mass against the thresholds; draft_probs unused, may be null)
+  int target_only;
+  float thr_single, thr_acc;
   const float* draft_probs;
   const float* temperatures;
   const float* u;
@@ -146,6 +176,7 @@ struct CommitParams {
 
 int launch_select_topk(const SelectParams& p, cudaStream_t stream);
 int launch_build_tree(const BuildParams& p, cudaStream_t stream);
+int launch_build_chain_tree(const ChainParams& p, cudaStream_t stream);
 int launch_verify_greedy(const GreedyParams& p, cudaStream_t stream);
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream);
 int launch_commit_kv(const CommitParams& p, cudaStream_t stream);

@@ -54,6 +54,7 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
     case SPEC_OP_VERIFY_GREEDY:  // after the attention's merge region (see spec_verify_greedy)
       return attention_partial_bytes() + greedy_part_bytes(b, n, V);
     case SPEC_OP_VERIFY_SAMPLING:
+    case SPEC_OP_VERIFY_TARGET_ONLY:
       return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
              sampling_partial2_bytes(b, terminal_split(V).chunks);
     case SPEC_OP_VERIFY_ATTENTION:
@@ -187,12 +188,89 @@ int greedy_call(bool compact, int b, int n, int S, int V, int dtype, const void*
   return launch_verify_greedy(p, as_stream(stream));
 }
 
+// The chain's greedy accept (DSpark counts), on greedy accept's workspace
+// layout and overlap rule.
+int chain_call(int b, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens, int draft_ld,
+               const int32_t* prefix_lens, int32_t* correct_len, int32_t* bonus, int32_t* out_tokens,
+               int32_t* commit_lens, int32_t* new_seq_lens, int32_t* accept_index, void* ws, size_t ws_bytes,
+               void* stream) {
+  const int n = S + 1;
+  if (b < 0 || S < 1 || n > kMaxN || V < 1 || draft_ld < S) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (b == 0) return SPEC_OK;
+  if (!logits || !draft_tokens || !prefix_lens || !correct_len || !bonus || !out_tokens || !commit_lens ||
+      !new_seq_lens)
+    return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_GREEDY, b, n, 1, V, 0, 0, 0);
+  if (int rc = check_ws(ws, ws_bytes, need)) return rc;
+  const bool early = take_after_attention(ws, b);
+  const WsView v = ws_view(ws, b);
+  GreedyParams p{};
+  p.b = b;
+  p.n = n;
+  p.S = S;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = logits;
+  p.chain = 1;
+  p.draft_ld = draft_ld;
+  p.chain_drafts = draft_tokens;
+  p.prefix_lens = prefix_lens;
+  p.correct_len = correct_len;
+  p.bonus = bonus;
+  p.out_tokens = out_tokens;
+  p.commit_lens = commit_lens;
+  p.new_seq_lens = new_seq_lens;
+  p.accept_index = accept_index;
+  const RowSplit sp = greedy_split(long(b) * n, V, vec_elems(dtype));
+  p.chunks = sp.chunks;
+  p.chunk_elems = sp.chunk_elems;
+  p.vec_ok = vec_ok(logits, V, dtype);
+  p.early = early;
+  p.error = v.error;
+  p.counters = v.counters + greedy_counter_base(b);
+  p.partials = v.partials + attention_partial_bytes();
+  return launch_verify_greedy(p, as_stream(stream));
+}
+
 }  // namespace
 
 extern "C" {
 
+int spec_build_chain_tree(int b, int S, const int32_t* bonus, const int32_t* draft_tokens, int draft_ld,
+                          const int32_t* seq_lens, int32_t* tree_tokens, int32_t* positions, int32_t* retrieve_index,
+                          int32_t* next_token, int32_t* next_sibling, uint64_t* mask_bits, void* stream) {
+  if (b < 0 || S < 1 || S + 1 > kMaxN || draft_ld < S) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!bonus || !draft_tokens || !seq_lens || !tree_tokens || !positions || !retrieve_index || !next_token ||
+      !next_sibling || !mask_bits)
+    return SPEC_ERR_ARG;
+  ChainParams p{};
+  p.b = b;
+  p.S = S;
+  p.draft_ld = draft_ld;
+  p.bonus = bonus;
+  p.draft_tokens = draft_tokens;
+  p.seq_lens = seq_lens;
+  p.tree_tokens = tree_tokens;
+  p.positions = positions;
+  p.retrieve_index = retrieve_index;
+  p.next_token = next_token;
+  p.next_sibling = next_sibling;
+  p.mask_bits = mask_bits;
+  return launch_build_chain_tree(p, as_stream(stream));
+}
+
+int spec_verify_chain_greedy(int b, int S, int V, int dtype, const void* logits, const int32_t* draft_tokens,
+                             int draft_ld, const int32_t* prefix_lens, int32_t* correct_len, int32_t* bonus,
+                             int32_t* out_tokens, int32_t* commit_lens, int32_t* new_seq_lens,
+                             int32_t* accept_index, void* ws, size_t ws_bytes, void* stream) {
+  return chain_call(b, S, V, dtype, logits, draft_tokens, draft_ld, prefix_lens, correct_len, bonus, out_tokens,
+                    commit_lens, new_seq_lens, accept_index, ws, ws_bytes, stream);
+}
+
 size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
-  if (b < 0 || op < 0 || op > SPEC_OP_COMMIT_KV) return 0;
+  if (b < 0 || op < 0 || op > SPEC_OP_LAST) return 0;
   if (b == 0) return kHeaderBytes + counters_bytes(0);
   if (n < 1 || n > kMaxN || k < 1 || k > kMaxK || V < 1) return 0;
   if (op == SPEC_OP_VERIFY_ATTENTION && (Hq < 1 || Hkv < 1 || Hq % Hkv || max_seq_len < 0)) return 0;
@@ -367,19 +445,28 @@ int spec_verify_greedy(int b, int n, int S, int V, int dtype, const void* logits
                      predict, accept_index, accept_lens, accepted_tokens, next_root, ws, ws_bytes, stream);
 }
 
-int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits, const float* draft_probs,
-                         const float* temperatures, const float* u, const float* u_final,
-                         const int32_t* draft_tokens, const int32_t* retrieve_index, const int32_t* next_token,
-                         const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
-                         int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws,
-                         size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Both samplers: the classic p/q rejection sampler (draft_probs given) or the
+// target-only tree sampler (thresholds given, draft_probs unused).
+int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const void* logits,
+                  const float* draft_probs, const float* temperatures, const float* u, const float* u_final,
+                  float thr_single, float thr_acc, const int32_t* draft_tokens, const int32_t* retrieve_index,
+                  const int32_t* next_token, const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
+                  int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws, size_t ws_bytes,
+                  void* stream) {
   if (b < 0 || n < 1 || n > kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
+  if (target_only && !(thr_single > 0.f && thr_single <= 1.f && thr_acc > 0.f && thr_acc <= 1.f))
+    return SPEC_ERR_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (b == 0) return SPEC_OK;
-  if (!logits || !draft_probs || !temperatures || !u || !u_final || !draft_tokens || !retrieve_index ||
-      !next_token || !next_sibling || !predict || !accept_index || !accept_lens)
+  if (!logits || (!target_only && !draft_probs) || !temperatures || !u || !u_final || !draft_tokens ||
+      !retrieve_index || !next_token || !next_sibling || !predict || !accept_index || !accept_lens)
     return SPEC_ERR_ARG;
-  const size_t need = spec_workspace_size(SPEC_OP_VERIFY_SAMPLING, b, n, 1, V, 0, 0, 0);
+  const size_t need = spec_workspace_size(target_only ? SPEC_OP_VERIFY_TARGET_ONLY : SPEC_OP_VERIFY_SAMPLING, b,
+                                          n, 1, V, 0, 0, 0);
   if (int rc = check_ws(ws, ws_bytes, need)) return rc;
   note_other(ws);
   const WsView v = ws_view(ws, b);
@@ -390,7 +477,10 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
   p.V = V;
   p.dtype = dtype;
   p.logits = logits;
-  p.draft_probs = draft_probs;
+  p.target_only = target_only ? 1 : 0;
+  p.thr_single = thr_single;
+  p.thr_acc = thr_acc;
+  p.draft_probs = target_only ? nullptr : draft_probs;
   p.temperatures = temperatures;
   p.u = u;
   p.u_final = u_final;
@@ -417,6 +507,32 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
   p.state = v.partials + sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V));
   p.partials2 = p.state + sampling_state_bytes(b);
   return launch_verify_sampling(p, as_stream(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits, const float* draft_probs,
+                         const float* temperatures, const float* u, const float* u_final,
+                         const int32_t* draft_tokens, const int32_t* retrieve_index, const int32_t* next_token,
+                         const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
+                         int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return sampling_call(false, b, n, S, V, dtype, logits, draft_probs, temperatures, u, u_final, 1.f, 1.f,
+                       draft_tokens, retrieve_index, next_token, next_sibling, predict, accept_index, accept_lens,
+                       accepted_tokens, next_root, ws, ws_bytes, stream);
+}
+
+int spec_verify_target_only(int b, int n, int S, int V, int dtype, const void* logits, const float* temperatures,
+                            const float* coins, const float* u_final, float threshold_single, float threshold_acc,
+                            const int32_t* draft_tokens, const int32_t* retrieve_index, const int32_t* next_token,
+                            const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
+                            int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return sampling_call(true, b, n, S, V, dtype, logits, nullptr, temperatures, coins, u_final, threshold_single,
+                       threshold_acc, draft_tokens, retrieve_index, next_token, next_sibling, predict, accept_index,
+                       accept_lens, accepted_tokens, next_root, ws, ws_bytes, stream);
 }
 
 int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page_size, void* const* k_layers,

@@ -120,17 +120,62 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(GreedyParams a) {
   __shared__ int tp[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
   __shared__ int2 stage[kMaxN * kMaxChunks];
   __shared__ int s_len;
-  // the request's tree arrays and every (row, chunk) partial in one round
-  // of loads; partials of other CTAs are read through L2 (__ldcg), not a
-  // stale L1 line
+  // the request's tree arrays (or chain tokens) and every (row, chunk)
+  // partial in one round of loads; partials of other CTAs are read through L2
+  // (__ldcg), not a stale L1 line
   const int tt = threadIdx.x;
-  const int tok0 = tt < n ? a.draft_tokens[base + tt] : 0;
-  const int x0 = tt < n ? a.next_token[base + tt] : -1;
-  const int y0 = tt < n ? a.next_sibling[base + tt] : -1;
-  const int r0 = tt < n ? a.retrieve_index[base + tt] : base;
+  int tok0 = 0, x0 = -1, y0 = -1, r0 = base, pre = 0;
+  if (a.chain) {
+    tok0 = tt < a.S ? a.chain_drafts[size_t(req) * a.draft_ld + tt] : 0;
+    if (tt == 0) pre = a.prefix_lens[req];
+  } else {
+    tok0 = tt < n ? a.draft_tokens[base + tt] : 0;
+    x0 = tt < n ? a.next_token[base + tt] : -1;
+    y0 = tt < n ? a.next_sibling[base + tt] : -1;
+    r0 = tt < n ? a.retrieve_index[base + tt] : base;
+  }
   for (int t = threadIdx.x; t < n * a.chunks; t += blockDim.x)
     stage[t] = __ldcg(reinterpret_cast<const int2*>(part + size_t(base) * a.chunks) + t);
   __syncthreads();
+  if (a.chain) {
+    // compute_dflash_correct_drafts_and_bonus [ACCEPT section 5]: the number
+    // of leading chain positions whose draft token is the target's argmax
+    // (the first mismatch ends it), the bonus at that position, the
+    // fixed-width out tokens with the bonus scattered there, commit_lens =
+    // correct_len + 1, new_seq_lens = prefix_lens + commit_lens
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      float v = -INFINITY;
+      int i = INT_MAX;
+      for (int c = 0; c < a.chunks; ++c) {
+        const int2 q = stage[t * a.chunks + c];
+        const float qv = __int_as_float(q.x);
+        if (better(qv, q.y, v, i)) {
+          v = qv;
+          i = q.y;
+        }
+      }
+      tp[t] = i;
+      tok[t] = tok0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int c = 0;
+      while (c < a.S && tok[c] == tp[c]) ++c;
+      s_len = c;
+      a.correct_len[req] = c;
+      a.bonus[req] = tp[c];
+      a.commit_lens[req] = c + 1;
+      a.new_seq_lens[req] = pre + c + 1;
+    }
+    __syncthreads();
+    const int c = s_len;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+      a.out_tokens[size_t(req) * n + j] = j == c ? tp[c] : (j < a.S ? tok[j] : -1);
+      if (a.accept_index) a.accept_index[size_t(req) * n + j] = j <= c ? base + j : -1;
+    }
+    counter_reset(a.counters + req);
+    return;
+  }
   for (int t = threadIdx.x; t < n; t += blockDim.x) {
     float v = -INFINITY;
     int i = INT_MAX;

@@ -7,13 +7,18 @@
 // rejected child passes to the next sibling, all rejected -> residual],
 // [SGL-XI eagle_sample, 路径三:拒绝采样].
 //
+// The same two passes serve the target-only tree sampler [ACCEPT section 4,
+// Target-only Tree Sampling]: only the walk and the terminal mass differ.
+//
 // Pass 1, grid (chunks, b*n): every verify row is reduced to (max, argmax,
 // sum of exp((x - max)/T)) by chunk; the CTA arriving last for a request merges
 // the request's rows and walks the tree with p(x) = exp((l_x - max)/T)/sum
 // (fp32) read at the children's tokens only.  It writes everything but the
 // terminal token, and leaves the request's state (terminal node, mode) in the
 // workspace: mode 0 = done (greedy request, terminal = argmax), 1 = sample the
-// terminal from p, 2 = sample it from the residual max(0, p - q).
+// terminal from p, 2 = sample it from the residual max(0, p - q), 3 = sample
+// it from p without the terminal node's rejected children (target-only:
+// relu(p - buffer), the buffer holding those children's p).
 // Pass 2, grid (chunks, b): for requests of mode 1 or 2 each CTA sums, in fp64,
 // the residual and p over one chunk of the terminal row; the last CTA finds the
 // chunk where u_final * Z falls and the token inside it by an in-order scan.
@@ -33,7 +38,7 @@ struct StatPart {
 
 struct ReqState {
   int cur;    // terminal node
-  int mode;   // 0 done, 1 from p, 2 from residual
+  int mode;   // 0 done, 1 from p, 2 from residual, 3 from p without the rejected children
   int ncd;    // accepted drafts
   int row;    // verify row of the terminal node (logits / q row)
   float M;    // max logit of that row
@@ -150,11 +155,15 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
     const T* L = static_cast<const T*>(a.logits);
     int cur = 0, ncd = 0, all_rejected = 0;
     path[0] = 0;
+    // target-only: the coin of the node whose children are scanned (the
+    // root's first, then each accepted child's own)
+    float coin = a.target_only ? a.u[base] : 0.f;
     for (int d = 0; d < a.S && ncd < n - 1; ++d) {  // bounded by the tree depth
       const size_t vrow = size_t(base + cur);
-      const float* q = a.draft_probs + vrow * a.V;
+      const float* q = a.target_only ? nullptr : a.draft_probs + vrow * a.V;
       int c2 = nt[cur], hit = -1, guard = 0;
       const int had_child = c2 != -1;
+      float prob_acc = 0.f;  // target-only: the scanned siblings' mass, fp32
       while (c2 != -1 && guard++ < n) {
         const int x = tok[c2];
         if (x < 0 || x >= a.V) {
@@ -165,7 +174,14 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
         float px;
         if (soft) px = p_of(Tr::load(L, vrow * a.V + x), rM[cur], temp, rS[cur]);
         else px = x == rA[cur] ? 1.f : 0.f;
-        if (__fmul_rn(a.u[base + c2], __ldg(q + x)) < px) {
+        bool accept;
+        if (a.target_only) {
+          prob_acc = __fadd_rn(prob_acc, px);
+          accept = px > 0.f && (coin < __fdiv_rn(prob_acc, a.thr_acc) || px >= a.thr_single);
+        } else {
+          accept = __fmul_rn(a.u[base + c2], __ldg(q + x)) < px;
+        }
+        if (accept) {
           hit = c2;
           break;
         }
@@ -178,8 +194,9 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
       pred[cur] = tok[hit];
       path[++ncd] = hit;
       cur = hit;
+      if (a.target_only) coin = a.u[base + hit];
     }
-    int mode = soft ? (all_rejected ? 2 : 1) : 0;
+    int mode = soft ? (all_rejected ? (a.target_only ? 3 : 2) : 1) : 0;
     if (mode == 0) pred[cur] = rA[cur];
     ReqState* st = reinterpret_cast<ReqState*>(a.state) + req;
     *st = ReqState{cur, mode, ncd, base + cur, rM[cur], rS[cur], temp, ri[cur]};
@@ -223,23 +240,52 @@ struct TermP {
   __device__ __forceinline__ float p(float l) const { return fast_exp2((l - M) * c) * invS; }
 };
 
-// Residual max(0, p - q) (mode 2) or p of a token given its logit l and q.
-__device__ __forceinline__ float term_mass(const TermP& tp, bool use_res, float l, float qv) {
+// Target-only terminal draws leave out the terminal node's rejected children:
+// their tokens, listed once per CTA, marked in a bitmap over one chunk of the
+// row (a chunk holds at most 4096 tokens).
+constexpr int kExclWords = 4096 / 32;
+
+struct Excluded {
+  int n;             // listed tokens
+  const int* tok;    // [n] in shared memory
+  uint32_t* bits;    // [kExclWords] in shared memory
+  // Marks the listed tokens inside [lo, lo + 4096) (every thread of the CTA).
+  __device__ __forceinline__ void mark(int lo) const {
+    for (int i = threadIdx.x; i < kExclWords; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int x = tok[i] - lo;
+      if (x >= 0 && x < kExclWords * 32) atomicOr(&bits[x >> 5], 1u << (x & 31));
+    }
+    __syncthreads();
+  }
+  __device__ __forceinline__ bool has(int v, int lo) const {
+    const int x = v - lo;
+    return (bits[x >> 5] >> (x & 31)) & 1u;
+  }
+};
+
+// Mass of a token of the terminal row given its logit l and q: the residual
+// max(0, p - q) (mode 2), p unless the token is excluded (mode 3), or p.
+__device__ __forceinline__ float term_mass(const TermP& tp, int mode, bool excluded, float l, float qv) {
   const float p = tp.p(l);
-  if (!use_res) return p;
+  if (mode == 3) return excluded ? 0.f : p;
+  if (mode != 2) return p;
   return p > qv ? p - qv : 0.f;  // the fp32 difference of the two values
 }
 
 constexpr int kTermPer = 16;  // terminal tokens a thread holds at once
 
-// Sums of the residual and of p over row[begin, end) of the terminal row,
-// each thread loading kTermPer tokens (logit and q) before using any.
+// Sums of the rule's mass (residual, or p without the excluded tokens) and of
+// p over row[begin, end) of the terminal row, each thread loading kTermPer
+// tokens (logit and q) before using any.
 template <typename T>
-__device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqState& st, int begin, int end,
-                                           double& res, double& ps, int& last_res, int& last_p) {
+__device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqState& st, const Excluded& ex,
+                                           int begin, int end, double& res, double& ps, int& last_res,
+                                           int& last_p) {
   using Tr = LogitTraits<T>;
   const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
-  const float* q = a.draft_probs + size_t(st.row) * a.V;
+  const float* q = st.mode == 2 ? a.draft_probs + size_t(st.row) * a.V : nullptr;
   const TermP tp(st);
   const int nt = blockDim.x;
   Kahan kr, kp;
@@ -249,13 +295,15 @@ __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqSta
     for (int u = 0; u < kTermPer; ++u) {
       const int v = b0 + u * nt;
       lv[u] = v < end ? Tr::load(L, v) : -INFINITY;
-      qv[u] = (st.mode == 2 && v < end) ? __ldg(q + v) : 0.f;
+      qv[u] = (q && v < end) ? __ldg(q + v) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kTermPer; ++u) {
       const int v = b0 + u * nt;
       const float p = v < end ? tp.p(lv[u]) : 0.f;
-      const float r = (st.mode == 2 && p > qv[u]) ? p - qv[u] : 0.f;
+      float r = 0.f;
+      if (st.mode == 2) r = p > qv[u] ? p - qv[u] : 0.f;
+      else if (st.mode == 3 && v < end) r = ex.has(v, begin) ? 0.f : p;
       kr.add(r);
       kp.add(p);
       if (r > 0.f) last_res = v;
@@ -275,11 +323,52 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   const int chunk = blockIdx.x;
   const ReqState st = reinterpret_cast<const ReqState*>(a.state)[req];
   if (st.mode == 0) return;  // every CTA of this request agrees: nothing to sample
+  // The state comes from the workspace.  One the stats pass did not write (a
+  // workspace used before its zero fill completed) must not steer an access:
+  // every field that addresses memory is checked, and the request is skipped
+  // with SPEC_DEV_INVARIANT (all CTAs of the request see the same state).
+  {
+    const int base = req * a.n;
+    const bool ok = st.mode >= 1 && st.mode <= 3 && st.cur >= 0 && st.cur < a.n && st.row == base + st.cur &&
+                    st.out_row >= base && st.out_row < base + a.n && st.ncd >= 0 && st.ncd <= a.S &&
+                    st.S > 0.f && st.T > 0.f;
+    if (!ok) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(a.error, SPEC_DEV_INVARIANT);
+      return;
+    }
+  }
   const int begin = chunk * a.chunk2_elems;
   const int end = min(a.V, begin + a.chunk2_elems);
+  // mode 3: the tokens of the terminal node's children (all rejected), read
+  // from the tree arrays in one round of loads and walked in shared memory
+  __shared__ int s_tok[kMaxN], s_ns[kMaxN], s_excl[kMaxN];
+  __shared__ int s_nexcl, s_first;
+  __shared__ uint32_t s_bits[kExclWords];
+  Excluded ex{0, s_excl, s_bits};
+  if (st.mode == 3) {
+    const int base = req * a.n, t = threadIdx.x;
+    if (t < a.n) {
+      s_tok[t] = a.draft_tokens[base + t];
+      s_ns[t] = a.next_sibling[base + t];
+    }
+    if (t == kMaxN) s_first = a.next_token[base + st.cur];
+    __syncthreads();
+    if (t == 0) {
+      int k = 0, c = s_first, guard = 0;
+      while (c >= 0 && c < a.n && guard++ < a.n) {  // an index out of range ends the list
+        const int x = s_tok[c];
+        if (x >= 0 && x < a.V) s_excl[k++] = x;
+        c = s_ns[c];
+      }
+      s_nexcl = k;
+    }
+    __syncthreads();
+    ex.n = s_nexcl;
+    ex.mark(begin);
+  }
   double res = 0.0, ps = 0.0;
   int last_res = -1, last_p = -1;
-  chunk_mass<T>(a, st, begin, end, res, ps, last_res, last_p);
+  chunk_mass<T>(a, st, ex, begin, end, res, ps, last_res, last_p);
   __shared__ double sres[kThreads / 32], sps[kThreads / 32];
   __shared__ int slr[kThreads / 32], slp[kThreads / 32];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -333,7 +422,7 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
       lr = max(lr, s_lr[ch]);
       lp = max(lp, s_lp[ch]);
     }
-    const int use_res = st.mode == 2 && zr > 0.0;
+    const int use_res = (st.mode == 2 || st.mode == 3) && zr > 0.0;
     const double Z = use_res ? zr : zp;
     const double target = double(a.u_final[req]) * Z;
     double acc = 0.0;
@@ -365,9 +454,11 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
     const int cb = s_chunk * a.chunk2_elems;
     const int ce = min(a.V, cb + a.chunk2_elems);
     const bool use_res = s_use_res != 0;
+    const int rule = use_res ? st.mode : 1;  // Z == 0 under the rule: draw from p
+    if (rule == 3) ex.mark(cb);              // the bitmap of the searched chunk
     const TermP tp(st);
     const T* Lr = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
-    const float* qr = a.draft_probs + size_t(st.row) * a.V;
+    const float* qr = rule == 2 ? a.draft_probs + size_t(st.row) * a.V : nullptr;
     __shared__ float wtot[kThreads / 32];
     __shared__ int s_hit;
     if (threadIdx.x == 0) s_hit = INT_MAX;
@@ -380,13 +471,14 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
       const int v = t0 + u;
       const bool in = u < per && v < ce;
       lv[u] = in ? Tr::load(Lr, v) : -INFINITY;
-      qv[u] = (in && use_res) ? __ldg(qr + v) : 0.f;
+      qv[u] = (in && qr) ? __ldg(qr + v) : 0.f;
     }
     float tot = 0.f;
 #pragma unroll
     for (int u = 0; u < kTermPer; ++u) {
       const int v = t0 + u;
-      mv[u] = (u < per && v < ce) ? term_mass(tp, use_res, lv[u], qv[u]) : 0.f;
+      const bool in = u < per && v < ce;
+      mv[u] = in ? term_mass(tp, rule, rule == 3 && ex.has(v, cb), lv[u], qv[u]) : 0.f;
       tot += mv[u];
     }
     float incl = tot;

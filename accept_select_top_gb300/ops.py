@@ -20,14 +20,16 @@ LIB_PATH = os.path.join(_HERE, "_build", "libspecdec.so")
 
 SPEC_OK = 0
 SPEC_F32, SPEC_BF16 = 0, 1
-OP_SELECT_TOPK, OP_BUILD_TREE, OP_VERIFY_ATTENTION, OP_VERIFY_GREEDY, OP_VERIFY_SAMPLING, OP_COMMIT_KV = range(6)
+(OP_SELECT_TOPK, OP_BUILD_TREE, OP_VERIFY_ATTENTION, OP_VERIFY_GREEDY, OP_VERIFY_SAMPLING, OP_COMMIT_KV,
+ OP_VERIFY_TARGET_ONLY) = range(7)
 DEV_INDEX, DEV_INVARIANT, DEV_LENGTH = 1, 2, 4
 _ERRORS = {-1: "bad argument", -2: "workspace too small or misaligned", -3: "CUDA launch failed",
            -4: "unsupported dtype or head size"}
 
 EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_workspace_set_overlap", "spec_last_error",
            "spec_device_sm_count", "spec_select_topk", "spec_build_tree", "spec_verify_attention",
-           "spec_verify_greedy", "spec_verify_sampling", "spec_commit_kv", "spec_verify_greedy_noalloc",
+           "spec_verify_greedy", "spec_verify_sampling", "spec_verify_target_only", "spec_build_chain_tree",
+           "spec_verify_chain_greedy", "spec_commit_kv", "spec_verify_greedy_noalloc",
            "spec_noalloc_last_error"]
 
 
@@ -51,6 +53,9 @@ def _load() -> ctypes.CDLL:
         "spec_verify_attention": (I, [I, I, I, I, I, I, P, P, P, L, P, I, I, P, P, I, P, P, F, P, P, P, Z, P]),
         "spec_verify_greedy": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_sampling": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
+        "spec_verify_target_only": (I, [I, I, I, I, I, P, P, P, P, F, F, P, P, P, P, P, P, P, P, P, P, Z, P]),
+        "spec_build_chain_tree": (I, [I, I, P, P, I, P, P, P, P, P, P, P, P]),
+        "spec_verify_chain_greedy": (I, [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, Z, P]),
         "spec_commit_kv": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_greedy_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]),
         "spec_noalloc_last_error": (I, [P]),
@@ -180,6 +185,34 @@ def spec_verify_sampling(b: int, n: int, S: int, logits, draft_probs, temperatur
                                     _ptr(retrieve_index), _ptr(next_token), _ptr(next_sibling), _ptr(predict),
                                     _ptr(accept_index), _ptr(accept_lens), _ptr(accepted_tokens), _ptr(next_root),
                                     ws.ptr, ws.nbytes, _stream(stream)), "spec_verify_sampling")
+
+
+def spec_verify_target_only(b: int, n: int, S: int, logits, temperatures, coins, u_final, threshold_single: float,
+                            threshold_acc: float, draft_tokens, retrieve_index, next_token, next_sibling, predict,
+                            accept_index, accept_lens, accepted_tokens, next_root, ws: Workspace, stream=None):
+    V = logits.shape[-1]
+    _check(LIB.spec_verify_target_only(b, n, S, V, _dtype_code(logits), _ptr(logits), _ptr(temperatures),
+                                       _ptr(coins), _ptr(u_final), float(threshold_single), float(threshold_acc),
+                                       _ptr(draft_tokens), _ptr(retrieve_index), _ptr(next_token),
+                                       _ptr(next_sibling), _ptr(predict), _ptr(accept_index), _ptr(accept_lens),
+                                       _ptr(accepted_tokens), _ptr(next_root), ws.ptr, ws.nbytes, _stream(stream)),
+           "spec_verify_target_only")
+
+
+def spec_build_chain_tree(b: int, S: int, bonus, draft_tokens, draft_ld: int, seq_lens, tree_tokens, positions,
+                          retrieve_index, next_token, next_sibling, mask_bits, stream=None):
+    _check(LIB.spec_build_chain_tree(b, S, _ptr(bonus), _ptr(draft_tokens), int(draft_ld), _ptr(seq_lens),
+                                     _ptr(tree_tokens), _ptr(positions), _ptr(retrieve_index), _ptr(next_token),
+                                     _ptr(next_sibling), _ptr(mask_bits), _stream(stream)), "spec_build_chain_tree")
+
+
+def spec_verify_chain_greedy(b: int, S: int, logits, draft_tokens, draft_ld: int, prefix_lens, correct_len, bonus,
+                             out_tokens, commit_lens, new_seq_lens, accept_index, ws: Workspace, stream=None):
+    V = logits.shape[-1]
+    _check(LIB.spec_verify_chain_greedy(b, S, V, _dtype_code(logits), _ptr(logits), _ptr(draft_tokens),
+                                        int(draft_ld), _ptr(prefix_lens), _ptr(correct_len), _ptr(bonus),
+                                        _ptr(out_tokens), _ptr(commit_lens), _ptr(new_seq_lens), _ptr(accept_index),
+                                        ws.ptr, ws.nbytes, _stream(stream)), "spec_verify_chain_greedy")
 
 
 def spec_commit_kv(b: int, n: int, W: int, Hkv: int, D: int, page_size: int, k_layers: Sequence[torch.Tensor],

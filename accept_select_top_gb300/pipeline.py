@@ -48,9 +48,16 @@ class DeviceInputs:
 
 class VerifyStep:
     def __init__(self, wl: Workload, inp: DeviceInputs, mode: str = "greedy", device="cuda",
-                 draft_temperature: float = 1.0, with_lse: bool = True, overlap: bool = False):
+                 draft_temperature: float = 1.0, with_lse: bool = True, overlap: bool = False,
+                 chain: Optional[bool] = None):
         assert mode in ("greedy", "sampling")
         self.wl, self.inp, self.mode = wl, inp, mode
+        # the chain fast path: topk = 1 with num_draft_tokens = num_steps + 1
+        # (the tree is the chain of the S selected tokens)
+        is_chain = wl.k == 1 and wl.n == wl.S + 1
+        self.chain = is_chain if chain is None else bool(chain)
+        if self.chain and not is_chain:
+            raise ValueError("the chain fast path needs topk = 1 and num_draft_tokens = num_steps + 1")
         self.draft_temperature = draft_temperature
         b, k, S, n, W = wl.b, wl.k, wl.S, wl.n, wl.W
         i32, f32 = torch.int32, torch.float32
@@ -75,6 +82,7 @@ class VerifyStep:
         self.accepted_tokens = z((b, W), i32)
         self.next_root = z((b,), i32)
         self.new_seq_lens = z((b,), i32)
+        self.correct_len = z((b,), i32)  # chain greedy accept: leading matches
         self.free_ids = z((max(1, b * n),), i32)
         self.n_free = z((1,), i32)
         nbytes = max(ops.spec_workspace_size(op, b, n, k, wl.V, wl.Hq, wl.Hkv, inp.max_seq_len)
@@ -110,6 +118,12 @@ class VerifyStep:
 
     def build(self, stream=None):
         wl = self.wl
+        if self.chain:
+            # for topk = 1 the token space holds the S chain tokens, in order
+            ops.spec_build_chain_tree(wl.b, wl.S, self.inp.bonus, self.token_space, wl.C, self.inp.seq_lens,
+                                      self.draft_tokens, self.positions, self.retrieve_index, self.next_token,
+                                      self.next_sibling, self.mask_bits, stream)
+            return
         ops.spec_build_tree(wl.b, wl.k, wl.S, wl.n, self.score_space, self.token_space, self.parent_space,
                             self.inp.bonus, self.inp.seq_lens, self.draft_tokens, self.positions,
                             self.retrieve_index, self.next_token, self.next_sibling, self.mask_bits, self.ws, stream)
@@ -125,7 +139,13 @@ class VerifyStep:
         wl, inp = self.wl, self.inp
         tree = (self.draft_tokens, self.retrieve_index, self.next_token, self.next_sibling)
         outs = (self.predict, self.accept_index, self.accept_lens, self.accepted_tokens, self.next_root)
-        if self.mode == "greedy":
+        if self.mode == "greedy" and self.chain:
+            # DSpark counts: commit_lens is accept_lens, the out tokens are the
+            # accepted tokens, the bonus is the next root
+            ops.spec_verify_chain_greedy(wl.b, wl.S, inp.target_logits, self.token_space, wl.C, inp.seq_lens,
+                                         self.correct_len, self.next_root, self.accepted_tokens, self.accept_lens,
+                                         self.new_seq_lens, self.accept_index, self.ws, stream)
+        elif self.mode == "greedy":
             ops.spec_verify_greedy(wl.b, wl.n, wl.S, inp.target_logits, *tree, *outs, self.ws, stream)
         else:
             ops.spec_verify_sampling(wl.b, wl.n, wl.S, inp.target_logits, inp.draft_probs, inp.temperatures,
@@ -149,9 +169,10 @@ class VerifyStep:
 
 
 def launches_per_step(wl: Workload, mode: str) -> int:
-    """Kernels one VerifyStep.run() launches: S selects, the tree build, the
-    attention (one launch: split key lists are merged inside it), the accept
-    (greedy one launch, sampling two passes) and the KV commit."""
+    """Kernels one VerifyStep.run() launches: S selects, the tree build (the
+    generic or the chain kernel), the attention (one launch: split key lists
+    are merged inside it), the accept (greedy one launch, sampling two passes)
+    and the KV commit."""
     return wl.S + 1 + 1 + (1 if mode == "greedy" else 2) + 1
 
 

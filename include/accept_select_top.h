@@ -81,6 +81,8 @@ extern "C" {
 #define SPEC_OP_VERIFY_GREEDY 3
 #define SPEC_OP_VERIFY_SAMPLING 4
 #define SPEC_OP_COMMIT_KV 5
+#define SPEC_OP_VERIFY_TARGET_ONLY 6
+#define SPEC_OP_LAST SPEC_OP_VERIFY_TARGET_ONLY
 
 /* Bytes of workspace the operation needs for these sizes (b requests, n tree
  * nodes, k = topk, V vocabulary, Hq query heads, Hkv kv heads, max_seq_len an
@@ -265,6 +267,77 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
                          int32_t* accept_lens, int32_t* accepted_tokens,
                          int32_t* next_root,
                          void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_verify_target_only -- target-only tree sampling, the second sampler of
+ * EAGLE trees (it uses the target distribution alone, no draft proposal q).
+ * [ACCEPT section 4, "Target-only Tree Sampling"].
+ *
+ * p = softmax(logits_row / T_b) (T_b <= 0: one-hot at the argmax).  coins:
+ * [b*n] fp32 in [0, 1), one per node: the coin used when that node's
+ * children are scanned (the root's first).  At the current node the children
+ * are scanned in sibling order with prob_acc = 0 (fp32): prob_acc += p(x), and
+ * child c of token x is accepted iff
+ *     p(x) > 0 and (coin < prob_acc / threshold_acc or p(x) >= threshold_single);
+ * the accepted child becomes the current node and its own coin is used next.
+ * At most S levels.  The terminal token is the smallest v with
+ * u_final[b] * Z < sum_{w<=v} r_w, r = p with the tokens of the current
+ * node's children removed when they were all rejected (relu(p - buffer), the
+ * buffer holding the rejected children's p), else r = p; from p when Z == 0.
+ * Thresholds in (0, 1] (else SPEC_ERR_ARG).  Outputs as spec_verify_greedy;
+ * workspace: spec_workspace_size(SPEC_OP_VERIFY_TARGET_ONLY, ...).
+ * ------------------------------------------------------------------------- */
+int spec_verify_target_only(int b, int n, int S, int V, int dtype, const void* logits,
+                            const float* temperatures, const float* coins, const float* u_final,
+                            float threshold_single, float threshold_acc,
+                            const int32_t* draft_tokens, const int32_t* retrieve_index,
+                            const int32_t* next_token, const int32_t* next_sibling,
+                            int32_t* predict, int32_t* accept_index,
+                            int32_t* accept_lens, int32_t* accepted_tokens,
+                            int32_t* next_root,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The chain fast path: topk == 1 with num_draft_tokens == num_steps + 1.
+ * [SGL-XI 平台分派与 chain 特化 (build_chain_tree)], [ACCEPT section 5 (DSpark
+ * correct_len, commit_lens, BuildOutTokens)].
+ *
+ * spec_build_chain_tree -- the tree of b chains of S draft tokens without the
+ * generic ranking (its structure is constant): n = S + 1 nodes per request,
+ * node 0 = bonus[b], node i = draft_tokens[b*draft_ld + i - 1] (for topk = 1
+ * the concatenated token space of the select steps, draft_ld = S); parent of
+ * node i = node i - 1; positions = seq_lens[b] + i; mask row i = nodes 0..i
+ * (lower triangular); next_token[i] = i + 1 (-1 for the last); next_sibling
+ * = -1; retrieve_index = b*n + i.  Outputs [b*n] as spec_build_tree's.  No
+ * workspace; waits for the kernel before it like every call.
+ * ------------------------------------------------------------------------- */
+int spec_build_chain_tree(int b, int S, const int32_t* bonus, const int32_t* draft_tokens, int draft_ld,
+                          const int32_t* seq_lens, int32_t* tree_tokens, int32_t* positions,
+                          int32_t* retrieve_index, int32_t* next_token, int32_t* next_sibling,
+                          uint64_t* mask_bits, void* stream);
+
+/* spec_verify_chain_greedy -- the greedy accept of b chains in DSpark's
+ * counts.  logits: [b*(S+1), V] (row b*(S+1)+j = chain position j, the root
+ * first); target_predict = per-row argmax (lowest index on ties).
+ *   correct_len[b] = number of leading positions j < S with draft_tokens[b, j]
+ *                    == target_predict[j] (the first mismatch ends it);
+ *   bonus[b]       = target_predict[correct_len];
+ *   out_tokens     [b, S+1] = the draft tokens then -1, with the bonus written
+ *                    at position correct_len (only the first commit_lens are
+ *                    output);
+ *   commit_lens[b] = correct_len + 1;  new_seq_lens[b] = prefix_lens[b] +
+ *                    commit_lens (the accepted drafts and the root get KV;
+ *                    the bonus gets its KV next step);
+ *   accept_index   [b, S+1] (nullable) = b*(S+1) + j for j < commit_lens,
+ *                    -1 after: with commit_lens as accept_lens it feeds
+ *                    spec_commit_kv.
+ * Workspace and overlap as spec_verify_greedy (n = S + 1).
+ * ------------------------------------------------------------------------- */
+int spec_verify_chain_greedy(int b, int S, int V, int dtype, const void* logits,
+                             const int32_t* draft_tokens, int draft_ld, const int32_t* prefix_lens,
+                             int32_t* correct_len, int32_t* bonus, int32_t* out_tokens,
+                             int32_t* commit_lens, int32_t* new_seq_lens, int32_t* accept_index,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * spec_commit_kv -- move the accepted rows' KV into the sequence, release the rest.

@@ -163,3 +163,57 @@ def sampling_divergence(lg_rows: np.ndarray, q_rows: np.ndarray, T: float, u: np
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def target_only_divergence(lg_rows: np.ndarray, T: float, coins: np.ndarray, u_final: float, t_single: float,
+                           t_acc: float, tok: np.ndarray, nt: np.ndarray, ns: np.ndarray, S: int, n: int, r: int,
+                           o_idx: np.ndarray, o_len: int, o_term: int, g_idx: np.ndarray, g_len: int,
+                           g_term: int):
+    """As sampling_divergence, for the target-only sampler: the first child
+    one side accepts and the other rejects is certified when either of its
+    tests is a near tie (the coin against prob_acc / threshold_acc, or p(x)
+    against threshold_single, within SAMPLING_ACCEPT_RTOL), the terminal draw
+    as in sampling_divergence with the rejected children's tokens removed."""
+    if T <= 0:
+        return "greedy", False, float("inf")
+    o_path = [int(x) - r * n for x in o_idx[:o_len]]
+    g_path = [int(x) - r * n for x in g_idx[:g_len]]
+    cur, d = 0, 0
+    while True:
+        oc = o_path[d + 1] if d + 1 < len(o_path) else -1
+        gc = g_path[d + 1] if d + 1 < len(g_path) else -1
+        if oc == gc:
+            if oc == -1:
+                break
+            cur, d = oc, d + 1
+            continue
+        p = _softmax64(lg_rows[cur], T)
+        coin = float(coins[cur])
+        acc = 0.0
+        c = nt[cur]
+        while c != -1:
+            acc += p[int(tok[c])]
+            if c == oc or c == gc:
+                break
+            c = ns[c]
+        x = int(tok[c])
+        m1 = abs(coin - acc / t_acc) / max(acc / t_acc, 1e-300)
+        m2 = abs(p[x] - t_single) / t_single
+        margin = min(m1, m2)
+        return "accept", margin <= SAMPLING_ACCEPT_RTOL, margin
+    if o_term == g_term:
+        return "same", True, 0.0
+    p = _softmax64(lg_rows[cur], T)
+    dist = p
+    if nt[cur] != -1 and len(o_path) - 1 < S:  # every child of cur was rejected
+        dist = p.copy()
+        c = nt[cur]
+        while c != -1:
+            dist[int(tok[c])] = 0.0
+            c = ns[c]
+        if dist.sum() <= 0:
+            dist = p
+    cdf = np.cumsum(dist) / dist.sum()
+    lo, hi = min(o_term, g_term), max(o_term, g_term)
+    margin = max(abs(float(u_final) - cdf[lo]), abs(float(u_final) - cdf[hi - 1]))
+    return "terminal", margin <= SAMPLING_CDF_ATOL, margin

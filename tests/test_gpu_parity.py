@@ -12,7 +12,8 @@ import torch
 
 import oracle
 from accept_select_top_gb300 import workloads as W
-from tests.cases import (bf16_to_f64, certified_topk_difference, make_case, sampling_divergence)
+from tests.cases import (bf16_to_f64, certified_topk_difference, make_case, sampling_divergence,
+                         target_only_divergence)
 
 pytestmark = pytest.mark.gpu
 
@@ -202,6 +203,60 @@ def test_verify_sampling_parity(cases, name, record_property):
     np.testing.assert_array_equal(g["next_root"], [g["accepted_tokens"][r, g["accept_lens"][r] - 1] for r in range(wl.b)])
 
 
+@pytest.mark.parametrize("t_single,t_acc", [(1.0, 1.0), (0.3, 0.5)])
+@pytest.mark.parametrize("name", ["tiny", "sampling_heavy", "mtp_chain"])
+def test_verify_target_only_parity(cases, name, t_single, t_acc, record_property):
+    """Target-only tree sampling against the oracle: the case's b*n uniforms
+    serve as the per-node coins.  Every difference must be certified at the
+    one decision where the walks part."""
+    c = cases(name, "sampling")
+    wl, ops = c.wl, _ops()
+    bufs = _accept_bufs(wl)
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_TARGET_ONLY, wl.b, wl.n, 1, wl.V))
+    temps = torch.as_tensor(c.temps).cuda()
+    ops.spec_verify_target_only(wl.b, wl.n, wl.S, c.logits, temps, c.u, c.u_final, t_single, t_acc, *_tree_dev(c),
+                                *bufs.values(), ws)
+    o = oracle.verify_target_only(wl.b, wl.n, wl.S, W.host(c.logits), c.temps, W.host(c.u), W.host(c.u_final),
+                                  t_single, t_acc, c.tree["draft_tokens"], c.tree["retrieve_index"],
+                                  c.tree["next_token"], c.tree["next_sibling"])
+    g = {k_: _np(v) for k_, v in bufs.items()}
+    assert ws.last_error() == 0
+    n = wl.n
+    lg = W.host(c.logits)
+    lg = bf16_to_f64(lg) if lg.dtype == np.uint16 else lg.astype(np.float64)
+    u, uf = W.host(c.u), W.host(c.u_final)
+    certs = []
+    for r in range(wl.b):
+        sl = slice(r * n, (r + 1) * n)
+        same = all(np.array_equal(g[k_][r] if k_ != "predict" else g[k_][sl], o[k_][r] if k_ != "predict" else o[k_][sl])
+                   for k_ in ("accept_lens", "accept_index", "accepted_tokens", "predict"))
+        if same:
+            certs.append(("same", True, 0.0))
+            continue
+        gl, ol = int(g["accept_lens"][r]), int(o["accept_lens"][r])
+        certs.append(target_only_divergence(lg[sl], float(c.temps[r]), u[sl], float(uf[r]), t_single, t_acc,
+                                            c.tree["draft_tokens"][sl], c.tree["next_token"][sl],
+                                            c.tree["next_sibling"][sl], wl.S, n, r, o["accept_index"][r], ol,
+                                            int(o["accepted_tokens"][r, ol - 1]), g["accept_index"][r], gl,
+                                            int(g["accepted_tokens"][r, gl - 1])))
+    _assert_certified(certs, f"{name} target-only ({t_single}, {t_acc})", record_property)
+    np.testing.assert_array_equal(g["next_root"], [g["accepted_tokens"][r, g["accept_lens"][r] - 1] for r in range(wl.b)])
+
+
+def test_target_only_t0_equals_greedy_on_gpu(cases):
+    c = cases("mtp_chain", "sampling")
+    wl, ops = c.wl, _ops()
+    a, b_ = _accept_bufs(wl), _accept_bufs(wl)
+    ws = ops.Workspace(max(ops.spec_workspace_size(op, wl.b, wl.n, 1, wl.V)
+                           for op in (ops.OP_VERIFY_TARGET_ONLY, ops.OP_VERIFY_GREEDY)))
+    zeros = torch.zeros(wl.b, device="cuda")
+    ops.spec_verify_target_only(wl.b, wl.n, wl.S, c.logits, zeros, c.u, c.u_final, 0.7, 0.4, *_tree_dev(c),
+                                *a.values(), ws)
+    ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *b_.values(), ws)
+    for k_ in a:
+        assert torch.equal(a[k_], b_[k_]), k_
+
+
 def test_sampling_t0_equals_greedy_on_gpu(cases):
     c = cases("mtp_chain", "sampling")
     wl, ops = c.wl, _ops()
@@ -213,6 +268,83 @@ def test_sampling_t0_equals_greedy_on_gpu(cases):
     ops.spec_verify_greedy(wl.b, wl.n, wl.S, c.logits, *_tree_dev(c), *b_.values(), ws)
     for k_ in a:
         assert torch.equal(a[k_], b_[k_]), k_
+
+
+# ---------------------------------------------------------- chain fast path
+
+def _chain_tree_gpu(wl, bonus, drafts, ld, seq_lens):
+    ops = _ops()
+    z = lambda: torch.zeros(wl.b * wl.n, dtype=torch.int32, device="cuda")
+    out = {k_: z() for k_ in ("draft_tokens", "positions", "retrieve_index", "next_token", "next_sibling")}
+    mask = torch.zeros(wl.b * wl.n, dtype=torch.int64, device="cuda")
+    ops.spec_build_chain_tree(wl.b, wl.S, bonus, drafts, ld, seq_lens, out["draft_tokens"], out["positions"],
+                              out["retrieve_index"], out["next_token"], out["next_sibling"], mask)
+    torch.cuda.synchronize()
+    out = {k_: _np(v) for k_, v in out.items()}
+    out["mask_bits"] = _np(mask).view(np.uint64)
+    return out
+
+
+@pytest.mark.parametrize("name", ["mtp_chain", "chain_ragged"])
+def test_chain_build_parity(cases, name):
+    """spec_build_chain_tree on the topk = 1 token space: bit-exact against the
+    oracle's chain tree and against the generic organize + build."""
+    wl = _chain_workload(name)
+    c = cases(wl, "greedy")
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    g = _chain_tree_gpu(wl, c.bonus, t(c.chain["token_space"]), wl.C, t(c.layout["seq_lens"]))
+    o = oracle.build_chain_tree(wl.b, wl.S, W.host(c.bonus), c.chain["token_space"], c.layout["seq_lens"])
+    for k_ in o:
+        np.testing.assert_array_equal(g[k_], o[k_], err_msg=k_)
+        np.testing.assert_array_equal(g[k_], c.tree[k_], err_msg=k_)
+
+
+def _chain_workload(name):
+    if name == "chain_ragged":  # a vocabulary off the 16-byte vector: the scalar scan
+        return W.scaled(W.WORKLOADS["mtp_chain"], name="chain_ragged", b=9, V=1001, ctx=("uniform", 50, 90))
+    return W.WORKLOADS[name]
+
+
+@pytest.mark.parametrize("name", ["mtp_chain", "chain_ragged"])
+def test_chain_greedy_parity(cases, name):
+    """The DSpark counts of every chain, all requests greedy: bit-exact."""
+    wl = _chain_workload(name)
+    c = cases(wl, "greedy")
+    ops = _ops()
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    b, n = wl.b, wl.n
+    z = lambda *s_: torch.full(s_, 7, dtype=torch.int32, device="cuda")
+    out = {"correct_len": z(b), "bonus": z(b), "out_tokens": z(b, n), "commit_lens": z(b), "new_seq_lens": z(b),
+           "accept_index": z(b, n)}
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, b, n, 1, wl.V))
+    ops.spec_verify_chain_greedy(b, wl.S, c.logits, t(c.chain["token_space"]), wl.C, t(c.layout["seq_lens"]),
+                                 *out.values(), ws)
+    o = oracle.chain_accept_greedy(b, wl.S, W.host(c.logits), c.chain["token_space"], c.layout["seq_lens"])
+    assert ws.last_error() == 0
+    for k_, v in out.items():
+        np.testing.assert_array_equal(_np(v), o[k_], err_msg=k_)
+    assert (o["correct_len"] > 0).any()  # some chains accept drafts
+
+
+def test_chain_dspark_example_on_gpu():
+    """Draft A -> B -> C, target A -> B -> X, prefix 10: correct_len 2, bonus X,
+    out tokens A, B, X, commit_lens 3, new_seq_lens 13."""
+    from tests.helpers import golden, onehot_logits
+    ops = _ops()
+    fx = golden("chain_commit.json")
+    tok = fx["tokens"]
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a)).cuda()
+    logits = t(onehot_logits([tok[x] for x in fx["target_argmax"]], 8))
+    drafts = t(np.array([[tok[x] for x in fx["nodes"][1:]]], np.int32))
+    z = lambda *s_: torch.zeros(s_, dtype=torch.int32, device="cuda")
+    out = [z(1), z(1), z(1, 4), z(1), z(1), z(1, 4)]
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_VERIFY_GREEDY, 1, 4, 1, 8))
+    ops.spec_verify_chain_greedy(1, 3, logits, drafts, 3, t(np.array([fx["prefix"]], np.int32)), *out, ws)
+    cl, bo, ot, cm, ns, ai = (_np(x) for x in out)
+    ex = fx["expect"]
+    assert cl[0] == ex["correct_len"] and cm[0] == ex["commit_lens"] and ns[0] == ex["new_seq_len"]
+    assert bo[0] == tok["X"] and ot[0, :3].tolist() == [tok[x] for x in ex["accepted_tokens"]]
+    assert [fx["nodes"][r] for r in ai[0, :3]] == ex["committed_rows"]
 
 
 # -------------------------------------------------------------- attention
