@@ -7,6 +7,8 @@
 
 namespace spec {
 
+constexpr int kMaxLayers = 128;
+
 struct SelectParams {
   int step, b, k, V, dtype;
   const void* logits;
@@ -152,8 +154,6 @@ struct AttentionParams {
   unsigned char* partials;
 };
 
-constexpr int kMaxLayers = 128;
-
 struct CommitParams {
   int b, n, W, Hkv, D, num_layers, page_size;
   void* k_layers[kMaxLayers];
@@ -174,6 +174,43 @@ struct CommitParams {
   unsigned char* partials;
 };
 
+struct DraftLocParams {
+  int b, topk, S, page_size;
+  const int32_t* req_to_token;
+  int req_rows, row_w;
+  const int32_t* req_pool_idx;
+  const int32_t* seq_lens;
+  long long num_slots;
+  int32_t* out_cache_loc;
+  int32_t* positions;
+  uint32_t* error;
+};
+
+struct DupTailParams {
+  int b, topk, S, page_size, Hkv, D, num_layers;
+  void* k_layers[kMaxLayers];
+  void* v_layers[kMaxLayers];
+  long long num_slots;
+  const int32_t* req_to_token;
+  int req_rows, row_w;
+  const int32_t* req_pool_idx;
+  const int32_t* seq_lens;
+  uint32_t* error;
+};
+
+struct FullMaskParams {
+  int b, n, fill_prefix;
+  const int32_t* seq_lens;
+  const uint64_t* mask_bits;
+  uint8_t* mask;
+  size_t mask_bytes;
+  uint32_t* error;
+};
+
+int launch_assign_draft_locs(const DraftLocParams& p, cudaStream_t stream);
+int launch_duplicate_prefix_tail(const DupTailParams& p, cudaStream_t stream);
+int launch_full_mask(const FullMaskParams& p, cudaStream_t stream);
+
 int launch_select_topk(const SelectParams& p, cudaStream_t stream);
 int launch_build_tree(const BuildParams& p, cudaStream_t stream);
 int launch_build_chain_tree(const ChainParams& p, cudaStream_t stream);
@@ -182,6 +219,7 @@ int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream);
 int launch_commit_kv(const CommitParams& p, cudaStream_t stream);
 
 size_t select_partial_bytes(int rows, int chunks);
+
 size_t build_tree_smem_bytes(int k, int S);
 size_t sampling_partial_bytes(int rows, int chunks);
 size_t sampling_state_bytes(int b);

@@ -269,6 +269,87 @@ int spec_verify_chain_greedy(int b, int S, int V, int dtype, const void* logits,
                     commit_lens, new_seq_lens, accept_index, ws, ws_bytes, stream);
 }
 
+int spec_assign_draft_locs(int b, int topk, int S, int page_size, const int32_t* req_to_token, int req_rows,
+                           int row_w, const int32_t* req_pool_idx, const int32_t* seq_lens, int64_t num_slots,
+                           int32_t* out_cache_loc, int32_t* positions, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || topk < 1 || topk > kMaxK || S < 1 || page_size < 1 || req_rows < 1 || row_w < 1 || num_slots < 1)
+    return SPEC_ERR_ARG;
+  if (int64_t(b) * topk * S >= (int64_t(1) << 31)) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!req_to_token || !req_pool_idx || !seq_lens || !out_cache_loc) return SPEC_ERR_ARG;
+  if (int rc = check_ws(ws, ws_bytes, kHeaderBytes)) return rc;
+  note_other(ws);
+  DraftLocParams p{};
+  p.b = b;
+  p.topk = topk;
+  p.S = S;
+  p.page_size = page_size;
+  p.req_to_token = req_to_token;
+  p.req_rows = req_rows;
+  p.row_w = row_w;
+  p.req_pool_idx = req_pool_idx;
+  p.seq_lens = seq_lens;
+  p.num_slots = num_slots;
+  p.out_cache_loc = out_cache_loc;
+  p.positions = topk == 1 ? positions : nullptr;
+  p.error = ws_view(ws, b).error;
+  return launch_assign_draft_locs(p, as_stream(stream));
+}
+
+int spec_duplicate_prefix_tail(int b, int topk, int S, int page_size, int Hkv, int D, int num_layers,
+                               void* const* k_layers, void* const* v_layers, int64_t num_slots,
+                               const int32_t* req_to_token, int req_rows, int row_w, const int32_t* req_pool_idx,
+                               const int32_t* seq_lens, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || topk < 1 || topk > kMaxK || S < 1 || page_size < 1 || Hkv < 1) return SPEC_ERR_ARG;
+  if (page_size > 64) return SPEC_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (num_layers < 1 || num_layers > kMaxLayers || num_slots < 1 || req_rows < 1 || row_w < 1) return SPEC_ERR_ARG;
+  if (b == 0 || topk == 1 || page_size == 1) return SPEC_OK;  // no holes to fill
+  if (!k_layers || !v_layers || !req_to_token || !req_pool_idx || !seq_lens) return SPEC_ERR_ARG;
+  if (int rc = check_ws(ws, ws_bytes, kHeaderBytes)) return rc;
+  DupTailParams p{};
+  p.b = b;
+  p.topk = topk;
+  p.S = S;
+  p.page_size = page_size;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.num_layers = num_layers;
+  for (int i = 0; i < num_layers; ++i) {
+    if (!k_layers[i] || !v_layers[i] || !aligned(k_layers[i], 16) || !aligned(v_layers[i], 16)) return SPEC_ERR_ARG;
+    p.k_layers[i] = k_layers[i];
+    p.v_layers[i] = v_layers[i];
+  }
+  note_other(ws);
+  p.num_slots = num_slots;
+  p.req_to_token = req_to_token;
+  p.req_rows = req_rows;
+  p.row_w = row_w;
+  p.req_pool_idx = req_pool_idx;
+  p.seq_lens = seq_lens;
+  p.error = ws_view(ws, b).error;
+  return launch_duplicate_prefix_tail(p, as_stream(stream));
+}
+
+int spec_build_full_mask(int b, int n, const int32_t* seq_lens, const uint64_t* mask_bits, int fill_prefix,
+                         uint8_t* mask, size_t mask_bytes, void* ws, size_t ws_bytes, void* stream) {
+  if (b < 0 || b > 16384 || n < 1 || n > kMaxN || (fill_prefix != 0 && fill_prefix != 1)) return SPEC_ERR_ARG;
+  if (b == 0) return SPEC_OK;
+  if (!seq_lens || !mask_bits || !mask) return SPEC_ERR_ARG;
+  if (int rc = check_ws(ws, ws_bytes, kHeaderBytes)) return rc;
+  note_other(ws);
+  FullMaskParams p{};
+  p.b = b;
+  p.n = n;
+  p.fill_prefix = fill_prefix;
+  p.seq_lens = seq_lens;
+  p.mask_bits = mask_bits;
+  p.mask = mask;
+  p.mask_bytes = mask_bytes;
+  p.error = ws_view(ws, b).error;
+  return launch_full_mask(p, as_stream(stream));
+}
+
 size_t spec_workspace_size(int op, int b, int n, int k, int V, int Hq, int Hkv, int max_seq_len) {
   if (b < 0 || op < 0 || op > SPEC_OP_LAST) return 0;
   if (b == 0) return kHeaderBytes + counters_bytes(0);

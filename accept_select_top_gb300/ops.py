@@ -29,7 +29,8 @@ _ERRORS = {-1: "bad argument", -2: "workspace too small or misaligned", -3: "CUD
 EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_workspace_set_overlap", "spec_last_error",
            "spec_device_sm_count", "spec_select_topk", "spec_build_tree", "spec_verify_attention",
            "spec_verify_greedy", "spec_verify_sampling", "spec_verify_target_only", "spec_build_chain_tree",
-           "spec_verify_chain_greedy", "spec_commit_kv", "spec_verify_greedy_noalloc",
+           "spec_verify_chain_greedy", "spec_assign_draft_locs", "spec_duplicate_prefix_tail",
+           "spec_build_full_mask", "spec_commit_kv", "spec_verify_greedy_noalloc",
            "spec_noalloc_last_error"]
 
 
@@ -56,6 +57,9 @@ def _load() -> ctypes.CDLL:
         "spec_verify_target_only": (I, [I, I, I, I, I, P, P, P, P, F, F, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_build_chain_tree": (I, [I, I, P, P, I, P, P, P, P, P, P, P, P]),
         "spec_verify_chain_greedy": (I, [I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, Z, P]),
+        "spec_assign_draft_locs": (I, [I, I, I, I, P, I, I, P, P, L, P, P, P, Z, P]),
+        "spec_duplicate_prefix_tail": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, Z, P]),
+        "spec_build_full_mask": (I, [I, I, P, P, I, P, Z, P, Z, P]),
         "spec_commit_kv": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_greedy_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]),
         "spec_noalloc_last_error": (I, [P]),
@@ -213,6 +217,37 @@ def spec_verify_chain_greedy(b: int, S: int, logits, draft_tokens, draft_ld: int
                                         int(draft_ld), _ptr(prefix_lens), _ptr(correct_len), _ptr(bonus),
                                         _ptr(out_tokens), _ptr(commit_lens), _ptr(new_seq_lens), _ptr(accept_index),
                                         ws.ptr, ws.nbytes, _stream(stream)), "spec_verify_chain_greedy")
+
+
+def spec_assign_draft_locs(b: int, topk: int, S: int, page_size: int, req_to_token, req_pool_idx, seq_lens,
+                           num_slots: int, out_cache_loc, positions, ws: Workspace, stream=None):
+    _check(LIB.spec_assign_draft_locs(b, topk, S, page_size, _ptr(req_to_token), req_to_token.shape[0],
+                                      req_to_token.shape[1], _ptr(req_pool_idx), _ptr(seq_lens), int(num_slots),
+                                      _ptr(out_cache_loc), _ptr(positions), ws.ptr, ws.nbytes, _stream(stream)),
+           "spec_assign_draft_locs")
+
+
+def spec_duplicate_prefix_tail(b: int, topk: int, S: int, page_size: int, Hkv: int, D: int,
+                               k_layers: Sequence[torch.Tensor], v_layers: Sequence[torch.Tensor], req_to_token,
+                               req_pool_idx, seq_lens, ws: Workspace, stream=None):
+    L = len(k_layers)
+    for t in list(k_layers) + list(v_layers):
+        _ptr(t)
+    kp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_layers])
+    vp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_layers])
+    _check(LIB.spec_duplicate_prefix_tail(b, topk, S, page_size, Hkv, D, L, ctypes.cast(kp, ctypes.c_void_p),
+                                          ctypes.cast(vp, ctypes.c_void_p), k_layers[0].shape[0],
+                                          _ptr(req_to_token), req_to_token.shape[0], req_to_token.shape[1],
+                                          _ptr(req_pool_idx), _ptr(seq_lens), ws.ptr, ws.nbytes, _stream(stream)),
+           "spec_duplicate_prefix_tail")
+
+
+def spec_build_full_mask(b: int, n: int, seq_lens, mask_bits, fill_prefix: bool, mask, ws: Workspace,
+                         stream=None):
+    """mask: a uint8 tensor of at least sum_b n*(L_b + n) bytes."""
+    _check(LIB.spec_build_full_mask(b, n, _ptr(seq_lens), _ptr(mask_bits), 1 if fill_prefix else 0, _ptr(mask),
+                                    ctypes.c_size_t(mask.numel()), ws.ptr, ws.nbytes, _stream(stream)),
+           "spec_build_full_mask")
 
 
 def spec_commit_kv(b: int, n: int, W: int, Hkv: int, D: int, page_size: int, k_layers: Sequence[torch.Tensor],

@@ -340,6 +340,55 @@ int spec_verify_chain_greedy(int b, int S, int V, int dtype, const void* logits,
                              void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The draft side of the KV, and the materialised verify mask.
+ * [SGL-XI draft 前向的输入准备:prepare_for_draft], [EVOL 草稿、验证与槽位 (the
+ * last partial page is duplicated)], [SGL-XI 三种 mask 形态].
+ * Each takes a workspace for its error word only (spec_workspace_size of any
+ * op is enough; SPEC_DEV_INDEX / SPEC_DEV_LENGTH as for the other calls).
+ *
+ * spec_assign_draft_locs -- out_cache_loc [b, topk, S] (flattened): the slots
+ * the S draft steps of each of the topk branches write.  With L = seq_lens[b]
+ * and row = req_to_token[req_pool_idx[b]] (req_rows rows of row_w entries):
+ *   page_size == 1 or topk == 1: branch t, step s -> row[L + t*S + s] (each
+ *     branch's steps are contiguous positions after the prefix);
+ *   page_size > 1 and topk > 1: last_page = L % page_size, prefix_base =
+ *     L - last_page, R = ceil((last_page + S) / page_size) * page_size; branch
+ *     t's region is the page-aligned positions [prefix_base + t*R, +R); its
+ *     first last_page positions are holes over the prefix tail (branch 0's
+ *     are the real tail) and step s -> row[prefix_base + t*R + last_page + s].
+ * The caller has allocated those positions in req_to_token.  positions [b]
+ * (nullable, topk == 1 only) receives L, the first draft row's position.  A
+ * position past row_w or a slot outside [0, num_slots) writes -1 and sets
+ * SPEC_DEV_INDEX.
+ * ------------------------------------------------------------------------- */
+int spec_assign_draft_locs(int b, int topk, int S, int page_size, const int32_t* req_to_token, int req_rows,
+                           int row_w, const int32_t* req_pool_idx, const int32_t* seq_lens, int64_t num_slots,
+                           int32_t* out_cache_loc, int32_t* positions, void* ws, size_t ws_bytes, void* stream);
+
+/* spec_duplicate_prefix_tail -- for page_size > 1 and topk > 1, copies the KV of
+ * the real prefix tail (row[prefix_base + j], j < last_page) into the hole
+ * slots of branches 1..topk-1 (row[prefix_base + t*R + j]), every layer, K and
+ * V [Hkv, D] bf16, so that a kernel reading whole pages sees the prefix tail
+ * in every branch.  A no-op for page_size == 1 or topk == 1.  page_size <= 64;
+ * k_layers / v_layers: HOST arrays of num_layers (<= 128) device pointers,
+ * 16-byte aligned. */
+int spec_duplicate_prefix_tail(int b, int topk, int S, int page_size, int Hkv, int D, int num_layers,
+                               void* const* k_layers, void* const* v_layers, int64_t num_slots,
+                               const int32_t* req_to_token, int req_rows, int row_w, const int32_t* req_pool_idx,
+                               const int32_t* seq_lens, void* ws, size_t ws_bytes, void* stream);
+
+/* spec_build_full_mask -- the FULL_MASK verify mask: one block per request in
+ * request order, request b's block = n rows of L_b + n bytes (L_b =
+ * seq_lens[b]); row i = L_b prefix bytes (1: every verify row sees the whole
+ * prefix), then n tree bytes (byte j = bit j of mask_bits[b*n + i]).
+ * fill_prefix (0/1, the pages' fill_prefix_mask): 0 writes the tree bytes only
+ * and leaves the prefix bytes as the reused buffer holds them.  mask_bytes is
+ * the buffer's size, at least sum_b n*(L_b + n) (else nothing is written and
+ * SPEC_DEV_LENGTH is set); b <= 16384.  HBM-bound: 16-byte stores. */
+int spec_build_full_mask(int b, int n, const int32_t* seq_lens, const uint64_t* mask_bits, int fill_prefix,
+                         uint8_t* mask, size_t mask_bytes, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * spec_commit_kv -- move the accepted rows' KV into the sequence, release the rest.
  * [SGL-XI KV 回写 (move_accept_tokens_to_target_kvcache)], [ACCEPT section 3
  * (input/output shift)], [EVOL 草稿、验证与槽位].
