@@ -60,7 +60,8 @@ def _load():
                          "oracle_build_tree", "oracle_verify_attention", "oracle_verify_greedy",
                          "oracle_verify_sampling", "oracle_verify_target_only", "oracle_build_chain_tree",
                          "oracle_chain_accept_greedy", "oracle_assign_draft_locs", "oracle_duplicate_prefix_tail",
-                         "oracle_full_mask", "oracle_commit_kv"):
+                         "oracle_full_mask", "oracle_add_penalties", "oracle_renorm_probs",
+                         "oracle_verify_sampling_probs", "oracle_verify_target_only_probs", "oracle_commit_kv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -299,6 +300,55 @@ def full_mask(b, n, seq_lens, mask_bits, fill_prefix=True, out=None):
     _check(_load().oracle_full_mask(b, n, _p(sl), _p(np.ascontiguousarray(mask_bits, np.uint64)),
                                     1 if fill_prefix else 0, _p(m)), "full_mask")
     return m
+
+
+def add_penalties(b, n, logits, penalties):
+    """A copy of the logits (fp32, or bf16 bits as uint16) with each request's
+    penalty row [b, V] fp32 added to its n verify rows."""
+    x, dt = _logits(logits)
+    out = x.copy()
+    V = out.shape[-1]
+    _check(_load().oracle_add_penalties(b, n, V, dt, _p(out), _p(np.ascontiguousarray(penalties, np.float32))),
+           "add_penalties")
+    return out
+
+
+def renorm_probs(b, n, logits, temperatures, top_k, top_p):
+    x, dt = _logits(logits)
+    V = x.shape[-1]
+    out = np.empty((b * n, V), np.float32)
+    _check(_load().oracle_renorm_probs(b, n, V, dt, _p(x), _p(np.ascontiguousarray(temperatures, np.float32)),
+                                       _p(_i32(top_k, (b,))), _p(np.ascontiguousarray(top_p, np.float32)),
+                                       _p(out)), "renorm_probs")
+    return out
+
+
+def verify_sampling_probs(b, n, S, probs, draft_probs, u, u_final, draft_tokens, retrieve_index, next_token,
+                          next_sibling):
+    pr = np.ascontiguousarray(probs, np.float32)
+    V = pr.shape[-1]
+    out = _accept_outputs(b, n, S)
+    _check(_load().oracle_verify_sampling_probs(
+        b, n, S, V, _p(pr), _p(np.ascontiguousarray(draft_probs, np.float32)),
+        _p(np.ascontiguousarray(u, np.float32)), _p(np.ascontiguousarray(u_final, np.float32)),
+        _p(_i32(draft_tokens)), _p(_i32(retrieve_index)), _p(_i32(next_token)), _p(_i32(next_sibling)),
+        _p(out["predict"]), _p(out["accept_index"]), _p(out["accept_lens"]), _p(out["accepted_tokens"]),
+        _p(out["next_root"])), "verify_sampling_probs")
+    return out
+
+
+def verify_target_only_probs(b, n, S, probs, u, u_final, threshold_single, threshold_acc, draft_tokens,
+                             retrieve_index, next_token, next_sibling):
+    pr = np.ascontiguousarray(probs, np.float32)
+    V = pr.shape[-1]
+    out = _accept_outputs(b, n, S)
+    _check(_load().oracle_verify_target_only_probs(
+        b, n, S, V, _p(pr), _p(np.ascontiguousarray(u, np.float32)), _p(np.ascontiguousarray(u_final, np.float32)),
+        ctypes.c_float(threshold_single), ctypes.c_float(threshold_acc), _p(_i32(draft_tokens)),
+        _p(_i32(retrieve_index)), _p(_i32(next_token)), _p(_i32(next_sibling)), _p(out["predict"]),
+        _p(out["accept_index"]), _p(out["accept_lens"]), _p(out["accepted_tokens"]), _p(out["next_root"])),
+        "verify_target_only_probs")
+    return out
 
 
 def commit_kv(b, n, W, Hkv, D, page_size, k_layers, v_layers, req_to_token, req_pool_idx, seq_lens,

@@ -441,16 +441,30 @@ static int sample_from(const double* r, int V, double Z, float u) {
   return last;
 }
 
-int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits,
-                           const float* draft_probs, const float* temperatures,
-                           const float* u, const float* u_final,
-                           const int32_t* draft_tokens, const int32_t* retrieve_index,
-                           const int32_t* next_token, const int32_t* next_sibling,
-                           int32_t* predict, int32_t* accept_index,
-                           int32_t* accept_lens, int32_t* accepted_tokens,
-                           int32_t* next_root) {
+/* The target distribution at a verify row: given (probs, the renormalised
+ * distribution), or softmax(logits / T) (one-hot at the argmax for T <= 0). */
+static void target_p(const float* probs, const void* logits, int dtype, size_t row, int V, double T, float* p) {
+  const size_t loff = row * (size_t)V;
+  if (probs) {
+    memcpy(p, probs + loff, sizeof(float) * (size_t)V);
+  } else if (T > 0.0) {
+    row_softmax(logits, dtype, loff, V, T, p);
+  } else {
+    int a = row_argmax(logits, dtype, loff, V);
+    for (int v = 0; v < V; ++v) p[v] = v == a ? 1.0f : 0.0f;
+  }
+}
+
+static int sampling_walk(int b, int n, int S, int V, int dtype, const void* logits, const float* probs,
+                         const float* draft_probs, const float* temperatures,
+                         const float* u, const float* u_final,
+                         const int32_t* draft_tokens, const int32_t* retrieve_index,
+                         const int32_t* next_token, const int32_t* next_sibling,
+                         int32_t* predict, int32_t* accept_index,
+                         int32_t* accept_lens, int32_t* accepted_tokens,
+                         int32_t* next_root) {
   if (b < 0 || n <= 0 || S <= 0 || V <= 0) return ORC_EARG;
-  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
+  if (!probs && dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
   const int W = S + 1;
   const size_t rows = (size_t)b * n;
   float* p = (float*)malloc(sizeof(float) * (size_t)V);
@@ -460,19 +474,13 @@ int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* lo
   int rc = ORC_OK;
   for (int r = 0; r < b && rc == ORC_OK; ++r) {
     const size_t base = (size_t)r * n;
-    const double T = temperatures[r];
+    const double T = probs ? 1.0 : temperatures[r];
     int cur = 0, ncd = 0, all_rejected = 0;
     accept_index[(size_t)r * W] = retrieve_index[base];
     for (int d = 0; d <= S; ++d) {
       /* p = the target distribution at the current node: softmax(logits / T),
-       * or the one-hot argmax when T <= 0 (greedy) */
-      const size_t loff = (base + cur) * (size_t)V;
-      if (T > 0.0) {
-        row_softmax(logits, dtype, loff, V, T, p);
-      } else {
-        int a = row_argmax(logits, dtype, loff, V);
-        for (int v = 0; v < V; ++v) p[v] = v == a ? 1.0f : 0.0f;
-      }
+       * or the one-hot argmax when T <= 0 (greedy), or the given one */
+      target_p(probs, logits, dtype, base + cur, V, T, p);
       if (d == S) break; /* depth exhausted: bonus from p */
       const float* q = draft_probs + (base + cur) * (size_t)V;
       /* try the children in sibling order; accept x when u*q(x) < p(x), i.e.
@@ -524,18 +532,44 @@ int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* lo
   return rc;
 }
 
+int oracle_verify_sampling(int b, int n, int S, int V, int dtype, const void* logits,
+                           const float* draft_probs, const float* temperatures,
+                           const float* u, const float* u_final,
+                           const int32_t* draft_tokens, const int32_t* retrieve_index,
+                           const int32_t* next_token, const int32_t* next_sibling,
+                           int32_t* predict, int32_t* accept_index,
+                           int32_t* accept_lens, int32_t* accepted_tokens,
+                           int32_t* next_root) {
+  return sampling_walk(b, n, S, V, dtype, logits, NULL, draft_probs, temperatures, u, u_final, draft_tokens,
+                       retrieve_index, next_token, next_sibling, predict, accept_index, accept_lens,
+                       accepted_tokens, next_root);
+}
+
+int oracle_verify_sampling_probs(int b, int n, int S, int V, const float* probs, const float* draft_probs,
+                                 const float* u, const float* u_final,
+                                 const int32_t* draft_tokens, const int32_t* retrieve_index,
+                                 const int32_t* next_token, const int32_t* next_sibling,
+                                 int32_t* predict, int32_t* accept_index,
+                                 int32_t* accept_lens, int32_t* accepted_tokens,
+                                 int32_t* next_root) {
+  if (!probs) return ORC_EARG;
+  return sampling_walk(b, n, S, V, ORC_F32, NULL, probs, draft_probs, NULL, u, u_final, draft_tokens,
+                       retrieve_index, next_token, next_sibling, predict, accept_index, accept_lens,
+                       accepted_tokens, next_root);
+}
+
 /* -------------------------------------- f1 target-only tree sampling */
 
-int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void* logits,
-                              const float* temperatures, const float* u, const float* u_final,
-                              float threshold_single, float threshold_acc,
-                              const int32_t* draft_tokens, const int32_t* retrieve_index,
-                              const int32_t* next_token, const int32_t* next_sibling,
-                              int32_t* predict, int32_t* accept_index,
-                              int32_t* accept_lens, int32_t* accepted_tokens,
-                              int32_t* next_root) {
+static int target_only_walk(int b, int n, int S, int V, int dtype, const void* logits, const float* probs,
+                            const float* temperatures, const float* u, const float* u_final,
+                            float threshold_single, float threshold_acc,
+                            const int32_t* draft_tokens, const int32_t* retrieve_index,
+                            const int32_t* next_token, const int32_t* next_sibling,
+                            int32_t* predict, int32_t* accept_index,
+                            int32_t* accept_lens, int32_t* accepted_tokens,
+                            int32_t* next_root) {
   if (b < 0 || n <= 0 || S <= 0 || V <= 0) return ORC_EARG;
-  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
+  if (!probs && dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
   if (!(threshold_single > 0.0f && threshold_single <= 1.0f)) return ORC_EARG;
   if (!(threshold_acc > 0.0f && threshold_acc <= 1.0f)) return ORC_EARG;
   const int W = S + 1;
@@ -548,19 +582,13 @@ int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void*
   int rc = ORC_OK;
   for (int q = 0; q < b && rc == ORC_OK; ++q) {
     const size_t base = (size_t)q * n;
-    const double T = temperatures[q];
+    const double T = probs ? 1.0 : temperatures[q];
     int cur = 0, ncd = 0;
     float coin = u[base + 0];
     accept_index[(size_t)q * W] = retrieve_index[base];
     for (int d = 0; d <= S; ++d) {
       /* the target distribution at the current node, and its empty buffer row */
-      const size_t loff = (base + cur) * (size_t)V;
-      if (T > 0.0) {
-        row_softmax(logits, dtype, loff, V, T, p);
-      } else {
-        int a = row_argmax(logits, dtype, loff, V);
-        for (int v = 0; v < V; ++v) p[v] = v == a ? 1.0f : 0.0f;
-      }
+      target_p(probs, logits, dtype, base + cur, V, T, p);
       for (int v = 0; v < V; ++v) buf[v] = 0.0f;
       if (d == S) break; /* depth exhausted */
       /* siblings in order, accumulating their target mass */
@@ -609,6 +637,32 @@ int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void*
   free(buf);
   free(r);
   return rc;
+}
+
+int oracle_verify_target_only(int b, int n, int S, int V, int dtype, const void* logits,
+                              const float* temperatures, const float* u, const float* u_final,
+                              float threshold_single, float threshold_acc,
+                              const int32_t* draft_tokens, const int32_t* retrieve_index,
+                              const int32_t* next_token, const int32_t* next_sibling,
+                              int32_t* predict, int32_t* accept_index,
+                              int32_t* accept_lens, int32_t* accepted_tokens,
+                              int32_t* next_root) {
+  return target_only_walk(b, n, S, V, dtype, logits, NULL, temperatures, u, u_final, threshold_single,
+                          threshold_acc, draft_tokens, retrieve_index, next_token, next_sibling, predict,
+                          accept_index, accept_lens, accepted_tokens, next_root);
+}
+
+int oracle_verify_target_only_probs(int b, int n, int S, int V, const float* probs, const float* u,
+                                    const float* u_final, float threshold_single, float threshold_acc,
+                                    const int32_t* draft_tokens, const int32_t* retrieve_index,
+                                    const int32_t* next_token, const int32_t* next_sibling,
+                                    int32_t* predict, int32_t* accept_index,
+                                    int32_t* accept_lens, int32_t* accepted_tokens,
+                                    int32_t* next_root) {
+  if (!probs) return ORC_EARG;
+  return target_only_walk(b, n, S, V, ORC_F32, NULL, probs, NULL, u, u_final, threshold_single, threshold_acc,
+                          draft_tokens, retrieve_index, next_token, next_sibling, predict, accept_index,
+                          accept_lens, accepted_tokens, next_root);
 }
 
 /* ------------------------------------------------------ f2 chain fast path */
@@ -745,6 +799,110 @@ int oracle_full_mask(int b, int n, const int32_t* seq_lens, const uint64_t* mask
     }
     off += (size_t)n * (L + n);
   }
+  return ORC_OK;
+}
+
+/* ------------------------- f3 relaxed penalties, top-k / top-p renorm */
+
+/* fp32 -> bf16 bits, round to nearest with ties to even (NaN kept quiet). */
+static uint16_t to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+int oracle_add_penalties(int b, int n, int V, int dtype, void* logits, const float* penalties) {
+  if (b < 0 || n <= 0 || V <= 0) return ORC_EARG;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
+  for (int q = 0; q < b; ++q)
+    for (int i = 0; i < n; ++i)
+      for (int v = 0; v < V; ++v) {
+        const size_t e = ((size_t)q * n + i) * (size_t)V + v;
+        /* the same penalty row for every verify row of the request, added in fp32 */
+        const float sum = (float)logit_at(logits, dtype, e) + penalties[(size_t)q * V + v];
+        if (dtype == ORC_F32) ((float*)logits)[e] = sum;
+        else ((uint16_t*)logits)[e] = to_bf16(sum);
+      }
+  return ORC_OK;
+}
+
+typedef struct {
+  double l;
+  int v;
+} LogitAt;
+
+/* descending logit, ascending index among equals */
+static int by_logit_desc(const void* pa, const void* pb) {
+  const LogitAt* a = (const LogitAt*)pa;
+  const LogitAt* b = (const LogitAt*)pb;
+  if (a->l != b->l) return a->l > b->l ? -1 : 1;
+  return a->v < b->v ? -1 : (a->v > b->v);
+}
+
+int oracle_renorm_probs(int b, int n, int V, int dtype, const void* logits, const float* temperatures,
+                        const int32_t* top_k, const float* top_p, float* probs) {
+  if (b < 0 || n <= 0 || V <= 0) return ORC_EARG;
+  if (dtype != ORC_F32 && dtype != ORC_BF16) return ORC_EARG;
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  char* keep = (char*)malloc((size_t)V);
+  LogitAt* order = (LogitAt*)malloc(sizeof(LogitAt) * (size_t)V);
+  for (int q = 0; q < b; ++q) {
+    const double T = temperatures[q];
+    for (int i = 0; i < n; ++i) {
+      const size_t off = ((size_t)q * n + i) * (size_t)V;
+      /* the temperature softmax (one-hot at the argmax for T <= 0) */
+      if (T > 0.0) {
+        double m = -INFINITY, s = 0.0;
+        for (int v = 0; v < V; ++v) {
+          double x = logit_at(logits, dtype, off + v);
+          if (x > m) m = x;
+        }
+        for (int v = 0; v < V; ++v) s += (p[v] = exp((logit_at(logits, dtype, off + v) - m) / T));
+        for (int v = 0; v < V; ++v) p[v] /= s;
+      } else {
+        int a = row_argmax(logits, dtype, off, V);
+        for (int v = 0; v < V; ++v) p[v] = v == a ? 1.0 : 0.0;
+      }
+      for (int v = 0; v < V; ++v) {
+        keep[v] = 1;
+        order[v].l = logit_at(logits, dtype, off + v);
+        order[v].v = v;
+      }
+      qsort(order, (size_t)V, sizeof(LogitAt), by_logit_desc);
+      /* top-k: every token at or above the k-th largest logit */
+      const int k = top_k[q];
+      if (k > 0 && k < V) {
+        const double cut = order[k - 1].l;
+        for (int v = 0; v < V; ++v) keep[v] = logit_at(logits, dtype, off + v) >= cut;
+      }
+      double z = 0.0;
+      for (int v = 0; v < V; ++v) z += keep[v] ? p[v] : 0.0;
+      for (int v = 0; v < V; ++v) p[v] = keep[v] ? p[v] / z : 0.0;
+      /* top-p on the renormalised distribution: the shortest prefix (in
+       * descending order) whose mass reaches top_p, widened to ties */
+      const double tp = top_p[q];
+      if (tp < 1.0) {
+        double acc = 0.0, cut = order[0].l;
+        for (int r = 0; r < V; ++r) {
+          const int v = order[r].v;
+          if (!keep[v]) continue;
+          acc += p[v];
+          cut = order[r].l;
+          if (acc >= tp) break;
+        }
+        for (int v = 0; v < V; ++v) keep[v] = keep[v] && logit_at(logits, dtype, off + v) >= cut;
+        z = 0.0;
+        for (int v = 0; v < V; ++v) z += keep[v] ? p[v] : 0.0;
+        for (int v = 0; v < V; ++v) p[v] = keep[v] ? p[v] / z : 0.0;
+      }
+      for (int v = 0; v < V; ++v) probs[off + v] = (float)p[v];
+    }
+  }
+  free(p);
+  free(keep);
+  free(order);
   return ORC_OK;
 }
 

@@ -239,6 +239,46 @@ int oracle_duplicate_prefix_tail(int b, int topk, int S, int page_size, int Hkv,
 int oracle_full_mask(int b, int n, const int32_t* seq_lens, const uint64_t* mask_bits, int fill_prefix,
                      uint8_t* mask);
 
+/* f3 -- relaxed penalties and top-k / top-p renormalisation before the accept.
+ * [SGL-XI eagle_sample 的骨架 (acc_additive_penalties, repeat_interleave over
+ * draft_token_num: the relaxed penalties)], [SGL-XI 路径三 and ACCEPT section 4
+ * (temperature softmax, then top-k, then top-p, then renormalisation; p is the
+ * distribution the accept consumes)].
+ *
+ * oracle_add_penalties: logits[b*n + i][v] += penalties[b][v] for every verify
+ * row i of request b, the sum formed in fp32 and stored in the logits' type
+ * (bf16: rounded to nearest, ties to even). */
+int oracle_add_penalties(int b, int n, int V, int dtype, void* logits, const float* penalties);
+
+/* oracle_renorm_probs: probs [b*n, V] fp32 = the target distribution of every
+ * verify row: p = softmax(l / T_b) in fp64 (T_b <= 0: one-hot at the argmax);
+ * top-k (0 < top_k[b] < V): the tokens whose logit is at least the k-th
+ * largest logit (ties at the cut all kept), renormalised; top-p (top_p[b] <
+ * 1): in descending order of p (index ascending among equals) the shortest
+ * prefix whose mass reaches top_p, widened to every token whose logit equals
+ * the last one kept, renormalised; each probability rounded to fp32. */
+int oracle_renorm_probs(int b, int n, int V, int dtype, const void* logits, const float* temperatures,
+                        const int32_t* top_k, const float* top_p, float* probs);
+
+/* The two samplers on a given target distribution (probs [b*n, V] fp32, the
+ * output of oracle_renorm_probs): p at a verify row is that row, no softmax
+ * and no temperature; everything else as oracle_verify_sampling and
+ * oracle_verify_target_only. */
+int oracle_verify_sampling_probs(int b, int n, int S, int V, const float* probs, const float* draft_probs,
+                                 const float* u, const float* u_final,
+                                 const int32_t* draft_tokens, const int32_t* retrieve_index,
+                                 const int32_t* next_token, const int32_t* next_sibling,
+                                 int32_t* predict, int32_t* accept_index,
+                                 int32_t* accept_lens, int32_t* accepted_tokens,
+                                 int32_t* next_root);
+int oracle_verify_target_only_probs(int b, int n, int S, int V, const float* probs, const float* u,
+                                    const float* u_final, float threshold_single, float threshold_acc,
+                                    const int32_t* draft_tokens, const int32_t* retrieve_index,
+                                    const int32_t* next_token, const int32_t* next_sibling,
+                                    int32_t* predict, int32_t* accept_index,
+                                    int32_t* accept_lens, int32_t* accepted_tokens,
+                                    int32_t* next_root);
+
 /* c9 -- KV commit.  [SGL-XI KV 回写], [ACCEPT section 3 (input/output shift)],
  * [EVOL 草稿、验证与槽位].
  * For request b with L = accept_lens[b] and k < L:
