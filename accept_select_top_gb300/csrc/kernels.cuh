@@ -31,6 +31,9 @@ struct SelectParams {
   // neither.
   bool early;
   int half;
+  // streaming kernel (rows 16-byte aligned): stream_ctas persistent CTAs,
+  // partials [rows][stream_pmax]; 0 selects the chunked kernel
+  int stream_ctas, stream_pmax;
   uint32_t* error;
   uint32_t* counters;    // this call's half: b counters
   unsigned char* partials;  // this call's half
@@ -105,6 +108,9 @@ struct GreedyParams {
 struct SamplingParams {
   int b, n, S, V, dtype;
   const void* logits;
+  // probabilities mode: probs [b*n, V] fp32 is the target distribution of
+  // every verify row (no softmax, no temperature; logits unused)
+  const float* probs;
   // target_only: the target-only tree sampler (coin of the scanned node,
   // sibling mass against the thresholds; draft_probs unused, may be null)
   int target_only;
@@ -207,6 +213,24 @@ struct FullMaskParams {
   uint32_t* error;
 };
 
+struct PenaltyParams {
+  int b, n, V, dtype;
+  void* logits;
+  const float* penalties;
+};
+
+struct RenormParams {
+  int b, n, V, dtype;
+  const void* logits;
+  const float* temperatures;
+  const int32_t* top_k;
+  const float* top_p;
+  float* probs;
+};
+
+int launch_add_penalties(const PenaltyParams& p, cudaStream_t stream);
+int launch_renorm(const RenormParams& p, cudaStream_t stream);
+
 int launch_assign_draft_locs(const DraftLocParams& p, cudaStream_t stream);
 int launch_duplicate_prefix_tail(const DupTailParams& p, cudaStream_t stream);
 int launch_full_mask(const FullMaskParams& p, cudaStream_t stream);
@@ -219,7 +243,12 @@ int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream);
 int launch_commit_kv(const CommitParams& p, cudaStream_t stream);
 
 size_t select_partial_bytes(int rows, int chunks);
-
+struct StreamGeometry {
+  int ctas, pmax;
+};
+// CTAs and pieces a row can have for the streaming select of `rows` rows of V
+// logits, vec per 16-byte vector, on a device of `sms` SMs
+StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms);
 size_t build_tree_smem_bytes(int k, int S);
 size_t sampling_partial_bytes(int rows, int chunks);
 size_t sampling_state_bytes(int b);

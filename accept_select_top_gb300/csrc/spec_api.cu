@@ -37,11 +37,37 @@ size_t greedy_part_bytes(int b, int n, int V) { return align256(size_t(b) * n * 
 // a select may also overlap a commit before it.
 size_t select_base_bytes(int b) { return align256(size_t(b) * (kMaxN + 1) * 4); }
 
+// SMs of the current device (152, a GB300's, when no device answers: the
+// workspace size is then computed for that part).
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    cudaGetLastError();  // leave no sticky error behind
+    return 152;
+  }
+  return sms;
+}
+
+// Partials of one select launch of `rows` rows: the chunked layout, or the
+// streaming layout (rows x pieces) when the rows are 16-byte vectors.
+size_t select_launch_bytes(long rows, int V) {
+  const size_t chunked = select_partial_bytes(int(rows), select_split(rows, V, 1).chunks);
+  size_t streamed = 0;
+  for (int vec : {4, 8}) {  // fp32 and bf16 rows
+    if (V % vec) continue;
+    const StreamGeometry g = select_stream_geometry(rows, V, vec, device_sms());
+    const size_t s = select_partial_bytes(int(rows), g.pmax);
+    if (s > streamed) streamed = s;
+  }
+  return chunked > streamed ? chunked : streamed;
+}
+
 // One half of the select partials: the larger of step 0 (b rows) and a
 // later step (b*k rows).
 size_t select_half_bytes(int b, int k, int V) {
-  const size_t a = select_partial_bytes(b, select_split(b, V, 1).chunks);
-  const size_t c = select_partial_bytes(b * k, select_split(long(b) * k, V, 1).chunks);
+  const size_t a = select_launch_bytes(b, V);
+  const size_t c = select_launch_bytes(long(b) * k, V);
   return a > c ? a : c;
 }
 
@@ -269,6 +295,42 @@ int spec_verify_chain_greedy(int b, int S, int V, int dtype, const void* logits,
                     commit_lens, new_seq_lens, accept_index, ws, ws_bytes, stream);
 }
 
+int spec_add_penalties(int b, int n, int V, int dtype, void* logits, const float* penalties, void* stream) {
+  if (b < 0 || n < 1 || V < 1) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (b == 0) return SPEC_OK;
+  if (!logits || !penalties) return SPEC_ERR_ARG;
+  // 16-byte vectors of logits and of penalties
+  if (!vec_ok(logits, V, dtype) || !aligned(penalties, 16) || V % 8) return SPEC_ERR_UNSUPPORTED;
+  PenaltyParams p{};
+  p.b = b;
+  p.n = n;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = logits;
+  p.penalties = penalties;
+  return launch_add_penalties(p, as_stream(stream));
+}
+
+int spec_renorm_probs(int b, int n, int V, int dtype, const void* logits, const float* temperatures,
+                      const int32_t* top_k, const float* top_p, float* probs, void* stream) {
+  if (b < 0 || n < 1 || V < 1 || int64_t(b) * n >= (int64_t(1) << 31)) return SPEC_ERR_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (b == 0) return SPEC_OK;
+  if (!logits || !temperatures || !top_k || !top_p || !probs) return SPEC_ERR_ARG;
+  RenormParams p{};
+  p.b = b;
+  p.n = n;
+  p.V = V;
+  p.dtype = dtype;
+  p.logits = logits;
+  p.temperatures = temperatures;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.probs = probs;
+  return launch_renorm(p, as_stream(stream));
+}
+
 int spec_assign_draft_locs(int b, int topk, int S, int page_size, const int32_t* req_to_token, int req_rows,
                            int row_w, const int32_t* req_pool_idx, const int32_t* seq_lens, int64_t num_slots,
                            int32_t* out_cache_loc, int32_t* positions, void* ws, size_t ws_bytes, void* stream) {
@@ -428,6 +490,11 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   p.chunks = sp.chunks;
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(draft_logits, V, dtype);
+  if (p.vec_ok) {  // rows of whole 16-byte vectors: the streaming kernel
+    const StreamGeometry g = select_stream_geometry(p.rows, V, vec_elems(dtype), device_sms());
+    p.stream_ctas = g.ctas;
+    p.stream_pmax = g.pmax;
+  }
   p.error = v.error;
   const std::pair<bool, int> eh = take_select(ws, b);
   p.early = eh.first;
@@ -532,7 +599,7 @@ namespace {
 
 // Both samplers: the classic p/q rejection sampler (draft_probs given) or the
 // target-only tree sampler (thresholds given, draft_probs unused).
-int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const void* logits,
+int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const void* logits, const float* probs,
                   const float* draft_probs, const float* temperatures, const float* u, const float* u_final,
                   float thr_single, float thr_acc, const int32_t* draft_tokens, const int32_t* retrieve_index,
                   const int32_t* next_token, const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
@@ -541,10 +608,11 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
   if (b < 0 || n < 1 || n > kMaxN || S < 1 || V < 1) return SPEC_ERR_ARG;
   if (target_only && !(thr_single > 0.f && thr_single <= 1.f && thr_acc > 0.f && thr_acc <= 1.f))
     return SPEC_ERR_ARG;
+  if (probs) dtype = SPEC_F32;  // the probabilities mode reads fp32 probabilities, no logits
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (b == 0) return SPEC_OK;
-  if (!logits || (!target_only && !draft_probs) || !temperatures || !u || !u_final || !draft_tokens ||
-      !retrieve_index || !next_token || !next_sibling || !predict || !accept_index || !accept_lens)
+  if ((!logits && !probs) || (!target_only && !draft_probs) || (!probs && !temperatures) || !u || !u_final ||
+      !draft_tokens || !retrieve_index || !next_token || !next_sibling || !predict || !accept_index || !accept_lens)
     return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(target_only ? SPEC_OP_VERIFY_TARGET_ONLY : SPEC_OP_VERIFY_SAMPLING, b,
                                           n, 1, V, 0, 0, 0);
@@ -557,7 +625,8 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
   p.S = S;
   p.V = V;
   p.dtype = dtype;
-  p.logits = logits;
+  p.logits = probs ? static_cast<const void*>(probs) : logits;  // (not read in the probabilities mode)
+  p.probs = probs;
   p.target_only = target_only ? 1 : 0;
   p.thr_single = thr_single;
   p.thr_acc = thr_acc;
@@ -574,7 +643,8 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
   p.accept_lens = accept_lens;
   p.accepted_tokens = accepted_tokens;
   p.next_root = next_root;
-  const RowSplit s1 = pick_split(long(b) * n, V, vec_elems(dtype));
+  // the probabilities mode has no row statistics to gather: one CTA a row
+  const RowSplit s1 = probs ? RowSplit{1, V} : pick_split(long(b) * n, V, vec_elems(dtype));
   const RowSplit s2 = terminal_split(V);
   if (s2.chunks > kMaxChunks2) return SPEC_ERR_UNSUPPORTED;
   p.chunks = s1.chunks;
@@ -600,7 +670,7 @@ int spec_verify_sampling(int b, int n, int S, int V, int dtype, const void* logi
                          const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
                          int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws,
                          size_t ws_bytes, void* stream) {
-  return sampling_call(false, b, n, S, V, dtype, logits, draft_probs, temperatures, u, u_final, 1.f, 1.f,
+  return sampling_call(false, b, n, S, V, dtype, logits, nullptr, draft_probs, temperatures, u, u_final, 1.f, 1.f,
                        draft_tokens, retrieve_index, next_token, next_sibling, predict, accept_index, accept_lens,
                        accepted_tokens, next_root, ws, ws_bytes, stream);
 }
@@ -611,10 +681,35 @@ int spec_verify_target_only(int b, int n, int S, int V, int dtype, const void* l
                             const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
                             int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root, void* ws,
                             size_t ws_bytes, void* stream) {
-  return sampling_call(true, b, n, S, V, dtype, logits, nullptr, temperatures, coins, u_final, threshold_single,
+  return sampling_call(true, b, n, S, V, dtype, logits, nullptr, nullptr, temperatures, coins, u_final, threshold_single,
                        threshold_acc, draft_tokens, retrieve_index, next_token, next_sibling, predict, accept_index,
                        accept_lens, accepted_tokens, next_root, ws, ws_bytes, stream);
 }
+
+int spec_verify_sampling_probs(int b, int n, int S, int V, const float* probs, const float* draft_probs,
+                               const float* u, const float* u_final, const int32_t* draft_tokens,
+                               const int32_t* retrieve_index, const int32_t* next_token, const int32_t* next_sibling,
+                               int32_t* predict, int32_t* accept_index, int32_t* accept_lens,
+                               int32_t* accepted_tokens, int32_t* next_root, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (!probs && b > 0) return SPEC_ERR_ARG;
+  return sampling_call(false, b, n, S, V, SPEC_F32, nullptr, probs, draft_probs, nullptr, u, u_final, 1.f, 1.f,
+                       draft_tokens, retrieve_index, next_token, next_sibling, predict, accept_index, accept_lens,
+                       accepted_tokens, next_root, ws, ws_bytes, stream);
+}
+
+int spec_verify_target_only_probs(int b, int n, int S, int V, const float* probs, const float* coins,
+                                  const float* u_final, float threshold_single, float threshold_acc,
+                                  const int32_t* draft_tokens, const int32_t* retrieve_index,
+                                  const int32_t* next_token, const int32_t* next_sibling, int32_t* predict,
+                                  int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
+                                  int32_t* next_root, void* ws, size_t ws_bytes, void* stream) {
+  if (!probs && b > 0) return SPEC_ERR_ARG;
+  return sampling_call(true, b, n, S, V, SPEC_F32, nullptr, probs, nullptr, nullptr, coins, u_final,
+                       threshold_single, threshold_acc, draft_tokens, retrieve_index, next_token, next_sibling,
+                       predict, accept_index, accept_lens, accepted_tokens, next_root, ws, ws_bytes, stream);
+}
+
 
 int spec_commit_kv(int b, int n, int W, int Hkv, int D, int num_layers, int page_size, void* const* k_layers,
                    void* const* v_layers, int64_t num_slots, const int32_t* req_to_token, int req_rows, int row_w,

@@ -58,7 +58,9 @@ struct MassPart {
 // p of one token given the row statistics (T > 0).
 __device__ __forceinline__ float p_of(float l, float M, float T, float S) { return expf((l - M) / T) / S; }
 
-template <typename T>
+// PROBS: the probabilities mode (a.probs given), a separate instantiation so
+// that the logit path carries none of its branches.
+template <typename T, bool PROBS>
 __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams a) {
   pdl_wait();
   pdl_trigger();
@@ -69,13 +71,13 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
   const int begin = chunk * a.chunk_elems;
   const int end = min(a.V, begin + a.chunk_elems);
   const T* lrow = static_cast<const T*>(a.logits) + size_t(row) * a.V;
-  const float temp = a.temperatures[req];
+  const float temp = PROBS ? 1.f : a.temperatures[req];  // the probabilities mode has no temperature
   const bool soft = temp > 0.f;
   const float c = soft ? 1.4426950408889634f / temp : 0.f;
 
   float m = -3.0e38f, s = 0.f, bv = -INFINITY;
   int bi = INT_MAX;
-  scan_row_stats<T>(lrow, begin, end, a.vec_ok, soft, c, bv, bi, m, s);
+  if (!PROBS) scan_row_stats<T>(lrow, begin, end, a.vec_ok, soft, c, bv, bi, m, s);
   // CTA reduction
   __shared__ float sm_[kThreads / 32], ss_[kThreads / 32], sv_[kThreads / 32];
   __shared__ int si_[kThreads / 32];
@@ -172,7 +174,8 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
           continue;
         }
         float px;
-        if (soft) px = p_of(Tr::load(L, vrow * a.V + x), rM[cur], temp, rS[cur]);
+        if (PROBS) px = __ldg(a.probs + vrow * a.V + x);  // the given distribution
+        else if (soft) px = p_of(Tr::load(L, vrow * a.V + x), rM[cur], temp, rS[cur]);
         else px = x == rA[cur] ? 1.f : 0.f;
         bool accept;
         if (a.target_only) {
@@ -196,10 +199,11 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
       cur = hit;
       if (a.target_only) coin = a.u[base + hit];
     }
-    int mode = soft ? (all_rejected ? (a.target_only ? 3 : 2) : 1) : 0;
+    int mode = (soft || PROBS) ? (all_rejected ? (a.target_only ? 3 : 2) : 1) : 0;
     if (mode == 0) pred[cur] = rA[cur];
     ReqState* st = reinterpret_cast<ReqState*>(a.state) + req;
-    *st = ReqState{cur, mode, ncd, base + cur, rM[cur], rS[cur], temp, ri[cur]};
+    if (PROBS) *st = ReqState{cur, mode, ncd, base + cur, 0.f, 1.f, 1.f, ri[cur]};
+    else *st = ReqState{cur, mode, ncd, base + cur, rM[cur], rS[cur], temp, ri[cur]};
     a.accept_lens[req] = ncd + 1;
     if (mode == 0 && a.next_root) a.next_root[req] = pred[cur];
     s_len = ncd + 1;
@@ -235,10 +239,19 @@ struct Kahan {
 // multiply.  The chunk sums and the in-chunk search use the same p.
 struct TermP {
   float M, c, invS;
-  __device__ __forceinline__ explicit TermP(const ReqState& st)
-      : M(st.M), c(1.4426950408889634f / st.T), invS(1.f / st.S) {}
-  __device__ __forceinline__ float p(float l) const { return fast_exp2((l - M) * c) * invS; }
+  bool given;  // probabilities mode: the loaded value is p itself
+  __device__ __forceinline__ TermP(const ReqState& st, bool probs)
+      : M(st.M), c(1.4426950408889634f / st.T), invS(1.f / st.S), given(probs) {}
+  __device__ __forceinline__ float p(float l) const { return given ? l : fast_exp2((l - M) * c) * invS; }
 };
+
+// The value the terminal pass loads for token v of a row: its logit, or its
+// probability in the probabilities mode.
+template <typename T, bool PROBS>
+__device__ __forceinline__ float term_load(const SamplingParams& a, size_t row, int v) {
+  if (PROBS) return __ldg(a.probs + row * a.V + v);
+  return LogitTraits<T>::load(static_cast<const T*>(a.logits) + row * a.V, size_t(v));
+}
 
 // Target-only terminal draws leave out the terminal node's rejected children:
 // their tokens, listed once per CTA, marked in a bitmap over one chunk of the
@@ -279,14 +292,12 @@ constexpr int kTermPer = 16;  // terminal tokens a thread holds at once
 // Sums of the rule's mass (residual, or p without the excluded tokens) and of
 // p over row[begin, end) of the terminal row, each thread loading kTermPer
 // tokens (logit and q) before using any.
-template <typename T>
+template <typename T, bool PROBS>
 __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqState& st, const Excluded& ex,
                                            int begin, int end, double& res, double& ps, int& last_res,
                                            int& last_p) {
-  using Tr = LogitTraits<T>;
-  const T* L = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
   const float* q = st.mode == 2 ? a.draft_probs + size_t(st.row) * a.V : nullptr;
-  const TermP tp(st);
+  const TermP tp(st, PROBS);
   const int nt = blockDim.x;
   Kahan kr, kp;
   for (int b0 = begin + int(threadIdx.x); b0 < end; b0 += kTermPer * nt) {
@@ -294,7 +305,7 @@ __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqSta
 #pragma unroll
     for (int u = 0; u < kTermPer; ++u) {
       const int v = b0 + u * nt;
-      lv[u] = v < end ? Tr::load(L, v) : -INFINITY;
+      lv[u] = v < end ? term_load<T, PROBS>(a, size_t(st.row), v) : (PROBS ? 0.f : -INFINITY);
       qv[u] = (q && v < end) ? __ldg(q + v) : 0.f;
     }
 #pragma unroll
@@ -314,7 +325,7 @@ __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqSta
   ps = double(kp.sum) - double(kp.comp);
 }
 
-template <typename T>
+template <typename T, bool PROBS>
 __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams a) {
   pdl_wait();
   pdl_trigger();
@@ -368,7 +379,7 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   }
   double res = 0.0, ps = 0.0;
   int last_res = -1, last_p = -1;
-  chunk_mass<T>(a, st, ex, begin, end, res, ps, last_res, last_p);
+  chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
   __shared__ double sres[kThreads / 32], sps[kThreads / 32];
   __shared__ int slr[kThreads / 32], slp[kThreads / 32];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -456,8 +467,7 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
     const bool use_res = s_use_res != 0;
     const int rule = use_res ? st.mode : 1;  // Z == 0 under the rule: draw from p
     if (rule == 3) ex.mark(cb);              // the bitmap of the searched chunk
-    const TermP tp(st);
-    const T* Lr = static_cast<const T*>(a.logits) + size_t(st.row) * a.V;
+    const TermP tp(st, PROBS);
     const float* qr = rule == 2 ? a.draft_probs + size_t(st.row) * a.V : nullptr;
     __shared__ float wtot[kThreads / 32];
     __shared__ int s_hit;
@@ -470,7 +480,7 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
     for (int u = 0; u < kTermPer; ++u) {
       const int v = t0 + u;
       const bool in = u < per && v < ce;
-      lv[u] = in ? Tr::load(Lr, v) : -INFINITY;
+      lv[u] = in ? term_load<T, PROBS>(a, size_t(st.row), v) : (PROBS ? 0.f : -INFINITY);
       qv[u] = (in && qr) ? __ldg(qr + v) : 0.f;
     }
     float tot = 0.f;
@@ -524,12 +534,15 @@ size_t sampling_partial2_bytes(int b, int chunks2) { return align256(size_t(b) *
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
   dim3 g1(p.chunks, p.b * p.n), g2(p.chunks2, p.b);
   cudaError_t e;
-  if (p.dtype == SPEC_F32) {
-    e = launch_pdl(sampling_stats_kernel<float>, g1, dim3(kThreads), 0, stream, p);
-    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float>, g2, dim3(kThreads), 0, stream, p);
+  if (p.probs) {  // fp32 probabilities
+    e = launch_pdl(sampling_stats_kernel<float, true>, g1, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, true>, g2, dim3(kThreads), 0, stream, p);
+  } else if (p.dtype == SPEC_F32) {
+    e = launch_pdl(sampling_stats_kernel<float, false>, g1, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, false>, g2, dim3(kThreads), 0, stream, p);
   } else {
-    e = launch_pdl(sampling_stats_kernel<uint16_t>, g1, dim3(kThreads), 0, stream, p);
-    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t>, g2, dim3(kThreads), 0, stream, p);
+    e = launch_pdl(sampling_stats_kernel<uint16_t, false>, g1, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t, false>, g2, dim3(kThreads), 0, stream, p);
   }
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }

@@ -30,7 +30,8 @@ EXPORTS = ["spec_workspace_size", "spec_workspace_init", "spec_workspace_set_ove
            "spec_device_sm_count", "spec_select_topk", "spec_build_tree", "spec_verify_attention",
            "spec_verify_greedy", "spec_verify_sampling", "spec_verify_target_only", "spec_build_chain_tree",
            "spec_verify_chain_greedy", "spec_assign_draft_locs", "spec_duplicate_prefix_tail",
-           "spec_build_full_mask", "spec_commit_kv", "spec_verify_greedy_noalloc",
+           "spec_build_full_mask", "spec_add_penalties", "spec_renorm_probs", "spec_verify_sampling_probs",
+           "spec_verify_target_only_probs", "spec_commit_kv", "spec_verify_greedy_noalloc",
            "spec_noalloc_last_error"]
 
 
@@ -60,6 +61,10 @@ def _load() -> ctypes.CDLL:
         "spec_assign_draft_locs": (I, [I, I, I, I, P, I, I, P, P, L, P, P, P, Z, P]),
         "spec_duplicate_prefix_tail": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, Z, P]),
         "spec_build_full_mask": (I, [I, I, P, P, I, P, Z, P, Z, P]),
+        "spec_add_penalties": (I, [I, I, I, I, P, P, P]),
+        "spec_renorm_probs": (I, [I, I, I, I, P, P, P, P, P, P]),
+        "spec_verify_sampling_probs": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]),
+        "spec_verify_target_only_probs": (I, [I, I, I, I, P, P, P, F, F, P, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_commit_kv": (I, [I, I, I, I, I, I, I, P, P, L, P, I, I, P, P, P, P, P, P, P, P, P, Z, P]),
         "spec_verify_greedy_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]),
         "spec_noalloc_last_error": (I, [P]),
@@ -248,6 +253,43 @@ def spec_build_full_mask(b: int, n: int, seq_lens, mask_bits, fill_prefix: bool,
     _check(LIB.spec_build_full_mask(b, n, _ptr(seq_lens), _ptr(mask_bits), 1 if fill_prefix else 0, _ptr(mask),
                                     ctypes.c_size_t(mask.numel()), ws.ptr, ws.nbytes, _stream(stream)),
            "spec_build_full_mask")
+
+
+def spec_add_penalties(b: int, n: int, logits, penalties, stream=None):
+    """In place: each request's penalty row [b, V] fp32 added to its n verify rows."""
+    V = logits.shape[-1]
+    _check(LIB.spec_add_penalties(b, n, V, _dtype_code(logits), _ptr(logits), _ptr(penalties), _stream(stream)),
+           "spec_add_penalties")
+
+
+def spec_renorm_probs(b: int, n: int, logits, temperatures, top_k, top_p, probs, stream=None):
+    V = logits.shape[-1]
+    _check(LIB.spec_renorm_probs(b, n, V, _dtype_code(logits), _ptr(logits), _ptr(temperatures), _ptr(top_k),
+                                 _ptr(top_p), _ptr(probs), _stream(stream)), "spec_renorm_probs")
+
+
+def spec_verify_sampling_probs(b: int, n: int, S: int, probs, draft_probs, u, u_final, draft_tokens, retrieve_index,
+                               next_token, next_sibling, predict, accept_index, accept_lens, accepted_tokens,
+                               next_root, ws: Workspace, stream=None):
+    V = probs.shape[-1]
+    _check(LIB.spec_verify_sampling_probs(b, n, S, V, _ptr(probs), _ptr(draft_probs), _ptr(u), _ptr(u_final),
+                                          _ptr(draft_tokens), _ptr(retrieve_index), _ptr(next_token),
+                                          _ptr(next_sibling), _ptr(predict), _ptr(accept_index), _ptr(accept_lens),
+                                          _ptr(accepted_tokens), _ptr(next_root), ws.ptr, ws.nbytes,
+                                          _stream(stream)), "spec_verify_sampling_probs")
+
+
+def spec_verify_target_only_probs(b: int, n: int, S: int, probs, coins, u_final, threshold_single: float,
+                                  threshold_acc: float, draft_tokens, retrieve_index, next_token, next_sibling,
+                                  predict, accept_index, accept_lens, accepted_tokens, next_root, ws: Workspace,
+                                  stream=None):
+    V = probs.shape[-1]
+    _check(LIB.spec_verify_target_only_probs(b, n, S, V, _ptr(probs), _ptr(coins), _ptr(u_final),
+                                             float(threshold_single), float(threshold_acc), _ptr(draft_tokens),
+                                             _ptr(retrieve_index), _ptr(next_token), _ptr(next_sibling),
+                                             _ptr(predict), _ptr(accept_index), _ptr(accept_lens),
+                                             _ptr(accepted_tokens), _ptr(next_root), ws.ptr, ws.nbytes,
+                                             _stream(stream)), "spec_verify_target_only_probs")
 
 
 def spec_commit_kv(b: int, n: int, W: int, Hkv: int, D: int, page_size: int, k_layers: Sequence[torch.Tensor],

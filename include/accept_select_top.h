@@ -298,6 +298,47 @@ int spec_verify_target_only(int b, int n, int S, int V, int dtype, const void* l
                             void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Relaxed penalties and the top-k / top-p renormalisation before the accept.
+ * [SGL-XI eagle_sample 的骨架 (acc_additive_penalties repeated over
+ * draft_token_num: the relaxed penalties)], [SGL-XI 路径三, ACCEPT section 4
+ * (temperature softmax, then top-k, then top-p, then renormalisation: the p
+ * the accept consumes)].
+ *
+ * spec_add_penalties -- in place: logits[b*n + i][v] += penalties[b][v] for
+ * each of request b's n verify rows (fp32 sum; bf16 logits store it rounded
+ * to nearest even).  logits [b*n, V] and penalties [b, V] fp32 16-byte
+ * aligned with V a multiple of 8 (else SPEC_ERR_UNSUPPORTED).  HBM-bound.
+ *
+ * spec_renorm_probs -- probs [b*n, V] fp32, the target distribution of every
+ * verify row: softmax(logits / T_b) (T_b <= 0: one-hot at the argmax); with
+ * 0 < top_k[b] < V the tokens whose logit is at least the k-th largest logit
+ * (ties at the cut all kept), renormalised; with top_p[b] < 1, in descending
+ * order, the shortest prefix whose mass reaches top_p of the kept mass,
+ * widened to the last kept logit's ties, renormalised.  No workspace.
+ *
+ * spec_verify_sampling_probs / spec_verify_target_only_probs -- the two
+ * samplers with the target distribution given (probs from spec_renorm_probs):
+ * p at a verify row is that row; no softmax, no temperature.  Otherwise as
+ * spec_verify_sampling / spec_verify_target_only, with workspaces of
+ * SPEC_OP_VERIFY_SAMPLING / SPEC_OP_VERIFY_TARGET_ONLY.
+ * ------------------------------------------------------------------------- */
+int spec_add_penalties(int b, int n, int V, int dtype, void* logits, const float* penalties, void* stream);
+int spec_renorm_probs(int b, int n, int V, int dtype, const void* logits, const float* temperatures,
+                      const int32_t* top_k, const float* top_p, float* probs, void* stream);
+int spec_verify_sampling_probs(int b, int n, int S, int V, const float* probs, const float* draft_probs,
+                               const float* u, const float* u_final, const int32_t* draft_tokens,
+                               const int32_t* retrieve_index, const int32_t* next_token,
+                               const int32_t* next_sibling, int32_t* predict, int32_t* accept_index,
+                               int32_t* accept_lens, int32_t* accepted_tokens, int32_t* next_root,
+                               void* ws, size_t ws_bytes, void* stream);
+int spec_verify_target_only_probs(int b, int n, int S, int V, const float* probs, const float* coins,
+                                  const float* u_final, float threshold_single, float threshold_acc,
+                                  const int32_t* draft_tokens, const int32_t* retrieve_index,
+                                  const int32_t* next_token, const int32_t* next_sibling, int32_t* predict,
+                                  int32_t* accept_index, int32_t* accept_lens, int32_t* accepted_tokens,
+                                  int32_t* next_root, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * The chain fast path: topk == 1 with num_draft_tokens == num_steps + 1.
  * [SGL-XI 平台分派与 chain 特化 (build_chain_tree)], [ACCEPT section 5 (DSpark
  * correct_len, commit_lens, BuildOutTokens)].
