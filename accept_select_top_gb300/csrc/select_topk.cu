@@ -152,11 +152,41 @@ __device__ __forceinline__ void warp_merge(TopList<K>& top, float* out_v, int* o
   }
 }
 
+// Warp 0 merges the warps' sorted lists lv/li[0, nw) (K entries each, best
+// first) into the partial's k best, slots k..K-1 left empty: k rounds of a
+// warp argmax over the lists' heads, lane l < nw reading list l.  Element
+// indices are unique, so only the winner's lane advances.
+template <int K>
+__device__ __forceinline__ void merge_warp_lists(const float (*lv)[K], const int (*li)[K], int nw, int k,
+                                                 SelPart* part) {
+  const int lane = threadIdx.x & 31;
+  const bool mine = lane < nw;
+  int pos = 0;
+  float ov = -INFINITY;
+  int oi = INT_MAX;
+  for (int j = 0; j < k; ++j) {
+    float hv = mine && pos < K ? lv[lane][pos] : -INFINITY;
+    int hi = mine && pos < K ? li[lane][pos] : INT_MAX;
+    const int own = hi;
+    warp_argmax(hv, hi);
+    if (own == hi && hi != INT_MAX) ++pos;
+    if (lane == j) {
+      ov = hv;
+      oi = hi;
+    }
+  }
+  if (lane < K) {
+    part->v[lane] = ov;
+    part->i[lane] = oi;
+  }
+}
+
 // Outputs of request req once p_s / id_s hold its rows' k probabilities and
 // tokens (best first): topk_p_out, and for step 0 the first score block, else
 // the path-score expansion scores_in[r] * p[r][j] (one fp32 multiply) and its
 // top-k with parent offsets.  Called by every thread of the CTA after a
-// __syncthreads; sc_in is scores_in[req*k + lane/k] prefetched by warp 0.
+// __syncthreads (it may hold one more); sc_in is scores_in[req*k + lane/k]
+// prefetched by warp 0 (read where k*k <= 32).
 __device__ __forceinline__ void write_request(const SelectParams& a, int req, int rows_per_req,
                                               const float (*p_s)[kMaxK], const int (*id_s)[kMaxK], float sc_in) {
   const int k = a.k, kk = k * k, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -195,16 +225,16 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
       a.scores_out[size_t(req) * k + rank] = ex;
       a.next_ids[size_t(req) * k + rank] = id;
     }
-  } else if (w == 0) {
+  } else {
+    // more than 32 expansions: one a thread of the CTA (k*k <= 256)
     __shared__ float ex[kMaxK * kMaxK];
-    for (int f = lane; f < kk; f += 32) {
-      const float sin = f < 32 ? sc_in : a.scores_in[size_t(req) * k + f / k];
-      ex[f] = __fmul_rn(sin, p_s[f / k][f % k]);
+    for (int f = threadIdx.x; f < kk; f += blockDim.x) {
+      ex[f] = __fmul_rn(a.scores_in[size_t(req) * k + f / k], p_s[f / k][f % k]);
       a.score_blk[sb + f] = ex[f];
       a.token_blk[sb + f] = id_s[f / k][f % k];
     }
-    __syncwarp();
-    for (int f = lane; f < kk; f += 32) {
+    __syncthreads();
+    for (int f = threadIdx.x; f < kk; f += blockDim.x) {
       int rank = 0;
       for (int g = 0; g < kk; ++g) rank += better(ex[g], g, ex[f], f);
       if (rank < k) {
@@ -368,19 +398,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
     __shared__ int li[kThreads / 32][K];
     warp_merge<K>(top, lv[w], li[w]);
     __syncthreads();
-    if (w == 0) {
-      // rank each of the nw*K candidates among all of them (lowest-index ties)
-      for (int t = lane; t < nw * K; t += 32) {
-        const float v = lv[t / K][t % K];
-        const int ix = li[t / K][t % K];
-        int rank = 0;
-        for (int u = 0; u < nw * K; ++u) rank += better(lv[u / K][u % K], li[u / K][u % K], v, ix);
-        if (rank < K) {
-          part->v[rank] = v;
-          part->i[rank] = ix;
-        }
-      }
-    }
+    if (w == 0) merge_warp_lists<K>(lv, li, nw, a.k, part);
   }
 
   if (!arrive_last(a.counters + req, uint32_t(rows_per_req * a.chunks))) return;
@@ -466,47 +484,51 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
 
 
 // ---------------------------------------------------------------------------
-// The streaming select: one persistent pass over the step's logits at HBM
-// rate.  The flattened [rows, V] logits (16-byte vectors, rows contiguous) are
-// cut into G equal contiguous ranges, one per CTA (G = a few CTAs per SM).  A
-// CTA streams its range in 16 KB tiles through a ring of kStreamStages shared
-// buffers filled by bulk asynchronous copies (cp.async.bulk, completion on an
-// mbarrier), so several tiles are in flight while one is reduced.  Each
-// thread keeps an online (max, sum of exp) of its elements; the CTA keeps the
-// running k best of the row piece and its k-th value theta: only elements at
-// or above theta are ranked (the first tile of a piece seeds theta from the
-// k-th largest warp maximum).  A row piece (the part of one row inside one
-// CTA's range) ends with one partial (max, sum, k best); the CTA whose piece
+// The streaming select: one persistent pass over the step's logits.  The
+// flattened [rows, V] logits (16-byte vectors, rows contiguous) are cut into G
+// equal contiguous ranges, one per CTA (three CTAs a SM).  Thread t of a CTA
+// takes the range's vectors t, t + 256, t + 512, ... through a private ring of
+// 16-byte cp.async copies, kStreamStages batches of kStreamVpt vectors deep,
+// and waits for its own copies with cp.async.wait_group: no barrier and no
+// polling while streaming.  Each thread keeps an online (max, sum of exp) of
+// the row piece (the part of one row inside the CTA's range), rescaled once a
+// batch.
+//
+// The k best are kept a warp at a time, behind a bound that only rises:
+//   - every batch, the warp's lanes' running maxima give one: split the 32
+//     lanes into k' groups (k' = k rounded up to a power of two); the smallest
+//     group maximum is at most the k-th largest of k' distinct elements, so at
+//     most the piece's k-th value (two shuffle trees);
+//   - the warp's own k-th value once its list holds k;
+//   - theta, the CTA's: the largest bound any warp has published (atomicMax
+//     on an order key).
+// An element below the bound cannot be among the piece's k best.  Elements
+// that reach it are appended to the warp's candidate buffer (one ballot a
+// batch finds the rare batch that has any; then one element a lane a round,
+// positions by prefix counts of the ballot).  A full buffer is merged into the
+// list (lane j < k holds entry j) by k rounds of a warp argmax.
+//
+// Only where a row piece ends does the CTA meet: warp 0 merges the warps'
+// lists into the piece's partial (max, sum, k best), and the CTA whose piece
 // is the last of a request to arrive merges the request's pieces and runs the
 // path step, as the chunked kernel does.
 
 constexpr int kStreamThreads = 256;
-constexpr int kStreamStages = 4;
-constexpr int kStreamTileBytes = 16384;
-constexpr int kStreamTileVecs = kStreamTileBytes / 16;           // 1024 vectors a tile
-constexpr int kStreamVpt = kStreamTileVecs / kStreamThreads;      // 4 vectors a thread a tile
-constexpr int kStreamCap = kStreamThreads - kMaxK;                // ranked candidates + the running list <= 256
-constexpr long long kStreamWaitCycles = 4000000000ll;              // ~2 s: bound of every mbarrier wait
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamPerSm = 2;                   // CTAs a SM (the ring and the registers allow two)
+constexpr int kStreamStages = 3;                  // batches in flight a thread
+constexpr int kStreamVpt = 8;                     // 16-byte vectors a batch
+constexpr int kStreamBatchVecs = kStreamVpt * kStreamThreads;  // vectors a CTA batch
+constexpr int kStreamCand = 32;                   // candidate elements a warp buffers (one a lane)
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return uint32_t(__cvta_generic_to_shared(p)); }
-
-__device__ __forceinline__ bool stream_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(20000u)
-      : "memory");
-  return ok != 0;
+// 16-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing.
+__device__ __forceinline__ void stream_cp16(void* dst, const void* src, uint32_t src_bytes) {
+  const uint32_t d = uint32_t(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
 }
-// false once the bound passes (the copy never landed)
-__device__ __forceinline__ bool stream_wait(uint32_t bar, uint32_t parity) {
-  if (stream_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (clock64() - t0 < kStreamWaitCycles)
-    if (stream_try_wait(bar, parity)) return true;
-  return false;
-}
+__device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void stream_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // The owner CTA of vector u when U vectors are cut into G ranges
 // [c*U/G, (c+1)*U/G).
@@ -564,32 +586,152 @@ __device__ __forceinline__ void merge_row(const SelPart* pr, int count, int k, f
   }
 }
 
+// Element q (0 <= q < E, a runtime value) of a 16-byte vector, by selects.
+template <typename T>
+__device__ __forceinline__ float vec_elem(const uint4& x, int q) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w = q < 4 ? (q < 2 ? x.x : x.y) : (q < 6 ? x.z : x.w);
+    return (q & 1) ? bf16_hi(w) : bf16_lo(w);
+  } else {
+    return __uint_as_float(q < 2 ? (q == 0 ? x.x : x.y) : (q == 2 ? x.z : x.w));
+  }
+}
+
+// A warp's k best so far (lane j < k holds entry j, best first; the other
+// lanes hold nothing) merged with the buffered candidates (lane l < ncand
+// holds buffer entry l): k rounds of a warp argmax over each lane's two
+// entries.  Element indices are unique within a row, so a winner is removed
+// by its index.
+__device__ __forceinline__ void stream_merge_candidates(const float* bv_s, const int* bi_s, int ncand, int k,
+                                                        float& lv_r, int& li_r) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();  // the lanes' appends are visible
+  float cv = lane < ncand ? bv_s[lane] : -INFINITY;
+  int ci = lane < ncand ? bi_s[lane] : INT_MAX;
+  float ev = lv_r;
+  int ei = li_r;
+  float nv = -INFINITY;
+  int ni = INT_MAX;
+  for (int j = 0; j < k; ++j) {
+    const bool c_first = better(cv, ci, ev, ei);
+    float bv = c_first ? cv : ev;
+    int bi = c_first ? ci : ei;
+    warp_argmax(bv, bi);
+    if (ci == bi) {
+      cv = -INFINITY;
+      ci = INT_MAX;
+    }
+    if (ei == bi) {
+      ev = -INFINITY;
+      ei = INT_MAX;
+    }
+    if (lane == j) {
+      nv = bv;
+      ni = bi;
+    }
+  }
+  lv_r = nv;
+  li_r = ni;
+  __syncwarp();  // every lane has read the buffer before it is refilled
+}
+
+// Two fp32 lanes in one 64-bit register: the packed FMA and add of sm_100
+// and later (each lane rounded as the scalar instruction rounds it).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Per-vector maxima kept packed where the type allows it (bf16x2: both halves
+// of a vector's maximum), combined into the batch maximum; value() gives the
+// fp32 maximum.
+template <typename T>
+struct VecMax;
+template <>
+struct VecMax<uint16_t> {
+  using type = __nv_bfloat162;
+  __device__ static type of(const uint4& x) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+    return __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+  }
+  __device__ static type comb(type a, type b) { return __hmax2(a, b); }
+  __device__ static float value(type a) { return fmaxf(__low2float(a), __high2float(a)); }
+};
+template <>
+struct VecMax<float> {
+  using type = float;
+  __device__ static type of(const uint4& x) {
+    return fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)), fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)));
+  }
+  __device__ static type comb(type a, type b) { return fmaxf(a, b); }
+  __device__ static float value(type a) { return a; }
+};
+
+// Sum over the batch of 2^(x c - mc), two lanes at a time (packed FMA and
+// add, one ex2 an element).
+template <typename T>
+__device__ __forceinline__ float batch_exp_sum(const uint4 (&x)[kStreamVpt], float c, float mc) {
+  const unsigned long long c2 = f2_pack(c, c), nm2 = f2_pack(-mc, -mc);
+  unsigned long long acc = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < kStreamVpt; ++u) {
+    const uint32_t wd[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 t = f2_unpack(f2_fma(f2_pack(bf16_lo(wd[j]), bf16_hi(wd[j])), c2, nm2));
+        acc = f2_add(acc, f2_pack(fast_exp2(t.x), fast_exp2(t.y)));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; j += 2) {
+        const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(wd[j]), __uint_as_float(wd[j + 1])), c2, nm2));
+        acc = f2_add(acc, f2_pack(fast_exp2(t.x), fast_exp2(t.y)));
+      }
+    }
+  }
+  const float2 s = f2_unpack(acc);
+  return s.x + s.y;
+}
+
 template <typename T, int K>
-__global__ void __launch_bounds__(kStreamThreads, K > 8 ? 2 : 3) select_stream_kernel(SelectParams a) {
+__global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) select_stream_kernel(SelectParams a) {
   constexpr int E = LogitTraits<T>::kVec;  // elements per 16-byte vector
-  extern __shared__ __align__(128) unsigned char ring[];  // kStreamStages tiles
-  __shared__ __align__(8) uint64_t full[kStreamStages];
-  __shared__ float cand_v[kStreamThreads];
-  __shared__ int cand_i[kStreamThreads];
-  __shared__ int cand_n[1];  // buffered candidates since the last merge
-  __shared__ float best_v[K];
-  __shared__ int best_i[K];
-  __shared__ int best_n;
-  __shared__ float s_theta;
-  __shared__ float wmax[kStreamThreads / 32], tau_w[kStreamThreads / 32], ws2[kStreamThreads / 32];
-  __shared__ float lv[kStreamThreads / 32][K];
-  __shared__ int li[kStreamThreads / 32][K];
-  __shared__ float p_s[kMaxK][kMaxK];
-  __shared__ int id_s[kMaxK][kMaxK];
-  __shared__ int s_abort;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, nw = kStreamThreads / 32;
+  // ring: vector u of batch slot s of thread t at [(s * kStreamVpt + u) * 256 + t]
+  extern __shared__ __align__(16) uint4 ring[];
+  __shared__ float cand_v[kStreamWarps][kStreamCand];  // a warp's candidate elements
+  __shared__ int cand_i[kStreamWarps][kStreamCand];    // their element indices in the row
+  __shared__ uint32_t s_theta;  // order key of the CTA's lower bound on the piece's k-th value
+  __shared__ float wmax[kStreamWarps], ws2[kStreamWarps];
+  __shared__ float lv[kStreamWarps][K];
+  __shared__ int li[kStreamWarps][K];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, nw = kStreamWarps;
   const int G = gridDim.x;
   const long long rowU = a.V / E;
   const long long U = (long long)a.rows * rowU;
   const long long u_lo = (long long)blockIdx.x * U / G, u_hi = (long long)(blockIdx.x + 1) * U / G;
-  const int rows_per_req = a.step ? a.k : 1;
+  const int n_vec = int(u_hi - u_lo);  // vectors of this CTA (a range is far below 2^31 vectors)
   const float c = 1.4426950408889634f / a.temperature;
-  const unsigned char* src = static_cast<const unsigned char*>(a.logits);
+  const uint4* src = static_cast<const uint4*>(a.logits) + u_lo;  // this CTA's first vector
+  const unsigned lanes_below = (1u << lane) - 1u;
+  // the lane-maxima bound uses K groups of 32 / K lanes (K, a power of two, is at least k)
+  constexpr int kGroupLanes = 32 / K;
 
   bool waited = false;
   if (!a.early) {
@@ -597,325 +739,222 @@ __global__ void __launch_bounds__(kStreamThreads, K > 8 ? 2 : 3) select_stream_k
     pdl_trigger();
     waited = true;
   }
-  if (tid == 0) {
-    for (int s = 0; s < kStreamStages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full[s])) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    cand_n[0] = 0;
-    best_n = 0;
-    s_theta = -INFINITY;
-    s_abort = 0;
-  }
+  if (tid == 0) s_theta = 0u;  // the smallest key: no bound yet
   __syncthreads();
 
-  // Tiles of this CTA, in order: [u, min(u + tile, row end, u_hi)).  The
-  // producer (thread 0) runs kStreamStages tiles ahead of the consumers; both
-  // track the end of their current row instead of dividing.
-  const long long first_row_end = (u_lo / rowU + 1) * rowU;
-  auto tile_end = [&](long long u, long long re) {
-    long long e = u + kStreamTileVecs;
-    if (e > re) e = re;
-    if (e > u_hi) e = u_hi;
-    return e;
+  // batch bb of this thread: offsets (bb * Vpt + u) * 256 + t of the range
+  auto issue = [&](int bb) {
+    uint4* slot = ring + (unsigned(bb) % kStreamStages) * (kStreamVpt * kStreamThreads) + tid;
+    const int o0 = bb * kStreamBatchVecs + tid;
+    if (o0 + (kStreamVpt - 1) * kStreamThreads < n_vec) {  // the whole batch lies in the range
+#pragma unroll
+      for (int u = 0; u < kStreamVpt; ++u) stream_cp16(slot + u * kStreamThreads, src + o0 + u * kStreamThreads, 16u);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kStreamVpt; ++u) {
+        const int o = o0 + u * kStreamThreads;
+        const bool ok = o < n_vec;
+        stream_cp16(slot + u * kStreamThreads, ok ? src + o : src, ok ? 16u : 0u);
+      }
+    }
+    stream_commit();
   };
-  long long pu = u_lo, p_re = first_row_end;  // producer cursor and its row's end
-  int issued = 0;
-  auto issue = [&]() {  // thread 0: the next tile into stage issued % stages
-    if (pu >= u_hi) return;
-    const long long e = tile_end(pu, p_re);
-    const uint32_t bytes = uint32_t((e - pu) * 16);
-    const int s = issued % kStreamStages;
-    const uint32_t bar = smem_addr(&full[s]);
-    const uint32_t dst = smem_addr(ring + size_t(s) * kStreamTileBytes);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src + pu * 16), "r"(bytes), "r"(bar)
-                 : "memory");
-    pu = e;
-    if (pu == p_re) p_re += rowU;
-    ++issued;
-  };
-  if (tid == 0)
-    for (int s = 0; s < kStreamStages; ++s) issue();
+  const int nbatch = (n_vec + kStreamBatchVecs - 1) / kStreamBatchVecs;
+#pragma unroll
+  for (int q = 0; q < kStreamStages - 1; ++q) issue(q);
 
   float m = -3.0e38f, ssum = 0.f;  // this thread's online softmax of the current row piece
-  long long cu = u_lo, c_re = first_row_end;  // consumer cursor and its row's end
-  int row = int(first_row_end / rowU) - 1;
-  int j = 0;                                   // tile number
-  while (cu < u_hi) {
-    const long long e = tile_end(cu, c_re);
-    const int nvec = int(e - cu);
-    const bool piece_end = e == c_re || e >= u_hi;
-    const int s = j % kStreamStages;
-    const bool ok = stream_wait(smem_addr(&full[s]), uint32_t((j / kStreamStages) & 1));
-    // this thread's vectors of the tile (a tile that never landed is read as is:
-    // in bounds, and the CTA stops below)
-    const uint4* tv = reinterpret_cast<const uint4*>(ring + size_t(s) * kStreamTileBytes);
-    uint4 x[kStreamVpt];
-    float vm[kStreamVpt];
+  float lv_r = -INFINITY;          // lane j < k: entry j of the warp's k best of the piece
+  int li_r = INT_MAX;
+  float thr_w = -INFINITY;         // the warp's bound (lane maxima, own list); warp-uniform
+  float thr_pub = -INFINITY;       // the last bound this warp published
+  int ncand = 0;                   // candidates in the warp's buffer (warp-uniform)
+  int row = int(u_lo / rowU);
+  int re = int((long long)(row + 1) * rowU - u_lo);  // end of the current row, as an offset of the range
+  for (int bb = 0; bb < nbatch; ++bb) {
+    issue(bb + kStreamStages - 1);  // (past the range: an empty group, so the count stays exact)
+    stream_wait_group<kStreamStages - 1>();  // this thread's copies of batch bb have landed
+    const uint4* slot = ring + (unsigned(bb) % kStreamStages) * (kStreamVpt * kStreamThreads);
+    const int b0 = bb * kStreamBatchVecs;
+    const int b1 = b0 + kStreamBatchVecs < n_vec ? b0 + kStreamBatchVecs : n_vec;
+    int cur = b0;
+    while (cur < b1) {  // the batch's vectors, one row piece at a time (uniform over the CTA)
+      const int seg = b1 < re ? b1 : re;
+      uint4 x[kStreamVpt];
+      uint32_t vin;  // bit u: vector u lies in the segment (the others read as -inf)
+      if (cur == b0 && seg == b0 + kStreamBatchVecs) {  // the common case: the whole batch
+        vin = (1u << kStreamVpt) - 1u;
 #pragma unroll
-    for (int i = 0; i < kStreamVpt; ++i) {
-      const int v = tid + i * kStreamThreads;
-      x[i] = v < nvec ? tv[v] : VecOps<T>::neg_inf();
-      vm[i] = VecOps<T>::vmax(x[i]);
-    }
-    float tm = vm[0];
-#pragma unroll
-    for (int i = 1; i < kStreamVpt; ++i) tm = fmaxf(tm, vm[i]);
-    if (tm > m) {
-      ssum *= fast_exp2((m - tm) * c);
-      m = tm;
-    }
-    // m * c of a thread that has seen only padding (m still the sentinel)
-    // would overflow: its elements are -inf, any finite offset gives 0
-    const float mc = m > -1.0e30f ? m * c : 0.f;
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < kStreamVpt; ++i)
-#pragma unroll
-      for (int q = 0; q < E; ++q) acc += fast_exp2(fmaf(VecOps<T>::at(x[i], q), c, -mc));
-    ssum += acc;
-    // Candidates gather across tiles against the theta of the last merge:
-    // elements above it (an element equal to theta comes after theta's own
-    // element in the row, so it cannot rank before it), or, while the piece
-    // has fewer than k best (theta = -inf), at or above the tile's k-th
-    // largest warp maximum.  Only the vectors whose maximum passes are
-    // scanned.
-    float thr = s_theta;
-    const bool seed = thr == -INFINITY;
-    if (seed) {
-      const float Mw = warp_max(tm);
-      if (lane == 0) wmax[w] = Mw;
-      if (a.k > nw) {
-        const float kth = warp_kth_largest(tm, a.k);
-        if (lane == 0) tau_w[w] = kth;
-      }
-      __syncthreads();
-      if (a.k <= nw) {
-        const float v = lane < nw ? wmax[lane] : -INFINITY;
-        int rank = 0;
-        for (int q = 0; q < nw; ++q) {
-          const float o = __shfl_sync(0xffffffffu, v, q);
-          rank += (o > v || (o == v && q < lane)) ? 1 : 0;
-        }
-        const unsigned at = __ballot_sync(0xffffffffu, lane < nw && rank == a.k - 1);
-        thr = at ? __shfl_sync(0xffffffffu, v, __ffs(at) - 1) : -INFINITY;
+        for (int u = 0; u < kStreamVpt; ++u) x[u] = slot[u * kStreamThreads + tid];
       } else {
-        thr = -INFINITY;
-        for (int q = 0; q < nw; ++q) thr = fmaxf(thr, tau_w[q]);
+        vin = 0u;
+#pragma unroll
+        for (int u = 0; u < kStreamVpt; ++u) {
+          const int o = b0 + u * kStreamThreads + tid;
+          x[u] = VecOps<T>::neg_inf();
+          if (o >= cur && o < seg) {
+            vin |= 1u << u;
+            x[u] = slot[u * kStreamThreads + tid];
+          }
+        }
       }
-    }
-    const int ebase = int((cu - (c_re - rowU)) * E);  // element index (in its row) of the tile's first element
+      typename VecMax<T>::type vm[kStreamVpt];  // each vector's maximum
 #pragma unroll
-    for (int i = 0; i < kStreamVpt; ++i) {
-      const int v = tid + i * kStreamThreads;
-      if (v < nvec && (seed ? vm[i] >= thr : vm[i] > thr)) {
+      for (int u = 0; u < kStreamVpt; ++u) vm[u] = VecMax<T>::of(x[u]);
+      typename VecMax<T>::type bmv = vm[0];
 #pragma unroll
-        for (int q = 0; q < E; ++q) {
-          const float f = VecOps<T>::at(x[i], q);
-          if (seed ? f >= thr : f > thr) {
-            const int pos = atomicAdd(&cand_n[0], 1);
-            if (pos < kStreamCap) {
-              cand_v[pos] = f;
-              cand_i[pos] = ebase + v * E + q;
+      for (int u = 1; u < kStreamVpt; ++u) bmv = VecMax<T>::comb(bmv, vm[u]);
+      const float bm = VecMax<T>::value(bmv);
+      if (bm > m) {
+        ssum *= fast_exp2((m - bm) * c);
+        m = bm;
+      }
+      // (m still the sentinel: every term is 0 anyway; -inf entries give 0)
+      ssum += batch_exp_sum<T>(x, c, m > -1.0e30f ? m * c : 0.f);
+      // the lane-maxima bound: max within groups of 32 / K lanes, min across the K groups
+      float gb = m > -1.0e30f ? m : -INFINITY;
+#pragma unroll
+      for (int o = 1; o < kGroupLanes; o <<= 1) gb = fmaxf(gb, __shfl_xor_sync(0xffffffffu, gb, o));
+#pragma unroll
+      for (int o = kGroupLanes; o < 32; o <<= 1) gb = fminf(gb, __shfl_xor_sync(0xffffffffu, gb, o));
+      thr_w = fmaxf(thr_w, gb);
+      if (thr_w > thr_pub) {  // warp-uniform
+        if (lane == 0) atomicMax(&s_theta, order_key(thr_w));
+        thr_pub = thr_w;
+      }
+      // a stale (lower) theta only lets more through; key 0 reads as NaN, which fmaxf drops
+      const float thr = fmaxf(key_value(*reinterpret_cast<volatile uint32_t*>(&s_theta)), thr_w);
+      if (__ballot_sync(0xffffffffu, vin != 0u && bm >= thr)) {  // the rare batch with a candidate
+        uint32_t vmask = 0;  // bit u: vector u holds an element that reaches the bound
+        if (bm >= thr) {
+#pragma unroll
+          for (int u = 0; u < kStreamVpt; ++u)
+            if ((vin & (1u << u)) && VecMax<T>::value(vm[u]) >= thr) vmask |= 1u << u;
+        }
+        const int rbase = int(u_lo - ((long long)row * rowU));  // vector o of the range is vector o + rbase of the row
+        while (__any_sync(0xffffffffu, vmask != 0u)) {  // one candidate vector a lane a round
+          uint32_t bits = 0;  // bit q: element q of vector u reaches the bound
+          int u = 0;
+          if (vmask) {
+            u = __ffs(vmask) - 1;
+            vmask &= vmask - 1u;
+            const uint4 xv = slot[u * kStreamThreads + tid];  // (the batch is still in its slot)
+#pragma unroll
+            for (int q = 0; q < E; ++q) bits |= (VecOps<T>::at(xv, q) >= thr ? 1u : 0u) << q;
+          }
+          for (;;) {  // one element a lane a round
+            const unsigned mask = __ballot_sync(0xffffffffu, bits != 0u);
+            if (!mask) break;
+            const int nnew = __popc(mask);
+            if (ncand + nnew > kStreamCand) {
+              stream_merge_candidates(cand_v[w], cand_i[w], ncand, a.k, lv_r, li_r);
+              ncand = 0;
+              if (__shfl_sync(0xffffffffu, li_r, a.k - 1) != INT_MAX) {  // the list holds k: its k-th
+                thr_w = fmaxf(thr_w, __shfl_sync(0xffffffffu, lv_r, a.k - 1));
+                if (thr_w > thr_pub) {
+                  if (lane == 0) atomicMax(&s_theta, order_key(thr_w));
+                  thr_pub = thr_w;
+                }
+              }
             }
-          }
-        }
-      }
-    }
-    if (__syncthreads_or(!ok)) {  // (A) a copy never landed: stop cleanly
-      if (tid == 0) {
-        raise_error(a.error, SPEC_DEV_TIMEOUT);
-        for (int q = j; q < issued; ++q)  // wait (bounded) for this CTA's copies in flight
-          stream_wait(smem_addr(&full[q % kStreamStages]), uint32_t((q / kStreamStages) & 1));
-      }
-      __syncthreads();
-      return;
-    }
-    // Merge the gathered candidates into the running list after a seed tile
-    // (to set theta), when the buffer is half full, and at the end of the
-    // piece.  The count is cleared after the merge's first barrier (every
-    // thread has read it by then) and the next pushes follow barrier (B).
-    const int n = cand_n[0];
-    if (n > 0 && (seed || piece_end || n > kStreamCap / 2)) {
-      const int nb = best_n;
-      if (n <= kStreamCap) {
-        // rank the candidates with the running list: one entry a thread
-        if (tid < nb) {
-          cand_v[n + tid] = best_v[tid];
-          cand_i[n + tid] = best_i[tid];
-        }
-        __syncthreads();
-        if (tid == 0) cand_n[0] = 0;
-        const int total = n + nb;
-        if (tid < total) {
-          const float v = cand_v[tid];
-          const int ix = cand_i[tid];
-          int rank = 0;
-          for (int u = 0; u < total; ++u) rank += better(cand_v[u], cand_i[u], v, ix);
-          if (rank < a.k) {
-            best_v[rank] = v;
-            best_i[rank] = ix;
-            if (rank == a.k - 1) s_theta = v;
-          }
-        }
-        if (tid == 0) {
-          best_n = total < a.k ? total : a.k;
-          if (total < a.k) s_theta = -INFINITY;
-        }
-      } else {
-        // The buffer overflowed (heavy ties).  Rank together: the running
-        // list, the buffered entries of earlier tiles (index below this
-        // tile's), and the k best of this tile's elements that pass, kept by
-        // every thread and merged by every warp.
-        TopList<K> top;
-        top.init();
-#pragma unroll
-        for (int i = 0; i < kStreamVpt; ++i) {
-          const int v = tid + i * kStreamThreads;
-#pragma unroll
-          for (int q = 0; q < E; ++q) {
-            const float f = VecOps<T>::at(x[i], q);
-            if (v < nvec && (seed ? f >= thr : f > thr)) top.push(f, ebase + v * E + q);
-          }
-        }
-        warp_merge<K>(top, lv[w], li[w]);
-        __syncthreads();
-        if (tid == 0) cand_n[0] = 0;
-        auto entry = [&](int u, float& v, int& ix) -> bool {
-          if (u < nb) {
-            v = best_v[u];
-            ix = best_i[u];
-            return true;
-          }
-          u -= nb;
-          if (u < kStreamCap) {
-            v = cand_v[u];
-            ix = cand_i[u];
-            return ix < ebase;
-          }
-          u -= kStreamCap;
-          v = lv[u / K][u % K];
-          ix = li[u / K][u % K];
-          return ix != INT_MAX;
-        };
-        const int total = nb + kStreamCap + nw * K;  // <= 16 + 240 + 128
-        float rv[2];
-        int ri[2], rr[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int t0 = tid + q * kStreamThreads;
-          rr[q] = INT_MAX;
-          float v;
-          int ix;
-          if (t0 < total && entry(t0, v, ix)) {
-            int rank = 0;
-            for (int u = 0; u < total; ++u) {
-              float uv;
-              int ui;
-              if (entry(u, uv, ui)) rank += better(uv, ui, v, ix);
+            if (bits) {
+              const int q = __ffs(bits) - 1;
+              bits &= bits - 1u;
+              const int pos = ncand + __popc(mask & lanes_below);
+              cand_v[w][pos] = vec_elem<T>(slot[u * kStreamThreads + tid], q);
+              cand_i[w][pos] = (b0 + u * kStreamThreads + tid + rbase) * E + q;
             }
-            rv[q] = v;
-            ri[q] = ix;
-            rr[q] = rank;
+            ncand += nnew;
           }
         }
-        __syncthreads();  // every read of the list is done
-        int real = 0;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          if (rr[q] != INT_MAX) ++real;
-          if (rr[q] < a.k) {
-            best_v[rr[q]] = rv[q];
-            best_i[rr[q]] = ri[q];
-          }
-        }
-        real = __syncthreads_count(real > 0 ? 1 : 0) + __syncthreads_count(real > 1 ? 1 : 0);
-        if (tid == 0) {
-          const int kept = real < a.k ? real : a.k;
-          best_n = kept;
-          s_theta = kept == a.k ? best_v[a.k - 1] : -INFINITY;
-        }
       }
-      __syncthreads();  // (B)
-    }
-    if (tid == 0) {  // the stage of tile j is free again: every thread has read it (barrier above)
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue();
-    }
-    cu = e;
-    ++j;
-
-    // ---- end of a row piece: its partial, and the request's finalize ----
-    if (piece_end) {
-      const float Mw = warp_max(m);
-      const float Sw = warp_sum(ssum * exp2f((m - Mw) * c));
-      if (lane == 0) {
-        wmax[w] = Mw;
-        ws2[w] = Sw;
-      }
-      __syncthreads();
-      const int r0 = int(stream_owner((long long)row * rowU, U, G));
-      SelPart* part = reinterpret_cast<SelPart*>(a.partials) + size_t(row) * a.stream_pmax + (blockIdx.x - r0);
-      if (w == 0) {
-        const float wm = lane < nw ? wmax[lane] : -3.0e38f;
-        const float Mc = warp_max(wm);
-        const float Sc = warp_sum(lane < nw ? ws2[lane] * exp2f((wm - Mc) * c) : 0.f);
+      cur = seg;
+      if (seg == re || seg == n_vec) {
+        // ---- end of a row piece: its partial ----
+        if (ncand) stream_merge_candidates(cand_v[w], cand_i[w], ncand, a.k, lv_r, li_r);
+        const float Mw = warp_max(m);
+        const float Sw = warp_sum(ssum * exp2f((m - Mw) * c));
         if (lane == 0) {
-          part->m = Mc;
-          part->s = Sc;
+          wmax[w] = Mw;
+          ws2[w] = Sw;
         }
-        if (lane < K) {
-          const bool has = lane < best_n;
-          part->v[lane] = has ? best_v[lane] : -INFINITY;
-          part->i[lane] = has ? best_i[lane] : INT_MAX;
-        }
-      }
-      const int req = row / rows_per_req;
-      uint32_t target = 0;
-      for (int r = req * rows_per_req; r < (req + 1) * rows_per_req; ++r)
-        target += uint32_t(stream_pieces(r, rowU, U, G));
-      const bool last = arrive_last(a.counters + req, target);  // (syncs: the partial is written before)
-      if (tid == 0) {
-        best_n = 0;
-        s_theta = -INFINITY;
-      }
-      m = -3.0e38f;
-      ssum = 0.f;
-      if (last) {
-        if (!waited) {
-          pdl_wait();
-          pdl_trigger();
-          waited = true;
-        }
-        const int k = a.k, kk = k * k;
-        const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
-        for (int r = w; r < rows_per_req; r += nw) {
-          const int grow = req * rows_per_req + r;
-          const SelPart* pr = reinterpret_cast<const SelPart*>(a.partials) + size_t(grow) * a.stream_pmax;
-          float myv, M, S;
-          int myi;
-          merge_row<K>(pr, stream_pieces(grow, rowU, U, G), k, c, myv, myi, M, S);
-          const float invS = 1.f / S;
-          if (lane < k) {
-            p_s[r][lane] = expf((myv - M) / a.temperature) * invS;
-            id_s[r][lane] = myi;
-          }
+        if (lane < K) {  // lanes k..K-1 hold no entry
+          lv[w][lane] = lv_r;
+          li[w][lane] = li_r;
         }
         __syncthreads();
-        write_request(a, req, rows_per_req, p_s, id_s, sc_in);
-        counter_reset(a.counters + req);
-      }
-      __syncthreads();  // the piece state is reset before the next tile
-      if (cu == c_re) {
-        c_re += rowU;
+        if (w == 0) {
+          if (!waited) {  // overlap: the partials are written only once the grid before is done
+            pdl_wait();
+            pdl_trigger();
+            waited = true;
+          }
+          const int r0 = stream_owner((long long)row * rowU, U, G);
+          SelPart* part = reinterpret_cast<SelPart*>(a.partials) + size_t(row) * a.stream_pmax + (blockIdx.x - r0);
+          const float wm = lane < nw ? wmax[lane] : -3.0e38f;
+          const float Mc = warp_max(wm);
+          const float Sc = warp_sum(lane < nw ? ws2[lane] * exp2f((wm - Mc) * c) : 0.f);
+          if (lane == 0) {
+            part->m = Mc;
+            part->s = Sc;
+          }
+          merge_warp_lists<K>(lv, li, nw, a.k, part);
+        }
+        m = -3.0e38f;
+        ssum = 0.f;
+        lv_r = -INFINITY;
+        li_r = INT_MAX;
+        thr_w = -INFINITY;
+        thr_pub = -INFINITY;
+        ncand = 0;
+        if (tid == 0) s_theta = 0u;
+        __syncthreads();  // lv / li are read and the bound is reset before the next piece
+        re += int(rowU);
         ++row;
       }
     }
   }
+  stream_wait_group<0>();  // no copy of this CTA is left in flight (the last groups are empty)
 }
 
-// The split the streaming select uses: G CTAs (at most 3 a SM, at least 64
+// The request step after the streaming select: one CTA a request, one warp a
+// row of it merging the row's pieces (merge_row), then the path step
+// (write_request).  Launched after the streaming kernel; it waits for that
+// grid before it reads a partial.
+constexpr int kFinalizeThreads = 32 * kMaxK;
+
+template <int K>
+__global__ void __launch_bounds__(kFinalizeThreads) select_finalize_kernel(SelectParams a) {
+  __shared__ float p_s[kMaxK][kMaxK];
+  __shared__ int id_s[kMaxK][kMaxK];
+  pdl_wait();
+  pdl_trigger();
+  const int req = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = a.k, kk = k * k;
+  const int rows_per_req = a.step ? k : 1;
+  const int vec = a.dtype == SPEC_F32 ? 4 : 8;
+  const long long rowU = a.V / vec;
+  const long long U = (long long)a.rows * rowU;
+  const int G = a.stream_ctas;
+  const float c = 1.4426950408889634f / a.temperature;
+  const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
+  if (w < rows_per_req) {
+    const int grow = req * rows_per_req + w;
+    const SelPart* pr = reinterpret_cast<const SelPart*>(a.partials) + size_t(grow) * a.stream_pmax;
+    float myv, M, S;
+    int myi;
+    merge_row<K>(pr, stream_pieces(grow, rowU, U, G), k, c, myv, myi, M, S);
+    const float invS = 1.f / S;
+    if (lane < k) {
+      p_s[w][lane] = expf((myv - M) / a.temperature) * invS;
+      id_s[w][lane] = myi;
+    }
+  }
+  __syncthreads();
+  write_request(a, req, rows_per_req, p_s, id_s, sc_in);
+}
+
+// The split the streaming select uses: G CTAs (kStreamPerSm a SM, at least 64
 // vectors each) and the pieces a row can have.
 struct StreamSplit {
   int ctas, pmax;
@@ -923,7 +962,7 @@ struct StreamSplit {
 inline StreamSplit stream_split(long rows, int V, int vec, int sms) {
   const long long rowU = V / vec;
   const long long U = rows * rowU;
-  long long G = 3LL * sms;
+  long long G = (long long)kStreamPerSm * sms;
   if (G > U / 64) G = U / 64;
   if (G < 1) G = 1;
   auto pmax_of = [&](long long g) {
@@ -946,11 +985,14 @@ inline StreamSplit stream_split(long rows, int V, int vec, int sms) {
 
 template <typename T, int K>
 cudaError_t launch_stream(const SelectParams& p, cudaStream_t stream) {
-  constexpr size_t smem = size_t(kStreamStages) * kStreamTileBytes;
-  const cudaError_t e =
+  constexpr size_t smem = size_t(kStreamStages) * kStreamVpt * kStreamThreads * 16;
+  cudaError_t e =
       cudaFuncSetAttribute(select_stream_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(select_stream_kernel<T, K>, dim3(p.stream_ctas), dim3(kStreamThreads), smem, stream, p);
+  e = launch_pdl(select_stream_kernel<T, K>, dim3(p.stream_ctas), dim3(kStreamThreads), smem, stream, p);
+  if (e != cudaSuccess) return e;
+  const int requests = p.step ? p.rows / p.k : p.rows;
+  return launch_pdl(select_finalize_kernel<K>, dim3(requests), dim3(kFinalizeThreads), 0, stream, p);
 }
 
 template <typename T>

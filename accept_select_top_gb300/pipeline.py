@@ -168,12 +168,20 @@ class VerifyStep:
         return launches_per_step(self.wl, self.mode)
 
 
+def select_launches(wl: Workload) -> int:
+    """Kernels one spec_select_topk call launches: rows of whole 16-byte
+    vectors (the buffers here are aligned) take the streaming kernel and its
+    request step, other rows the chunked kernel alone."""
+    elem = 4 if wl.logits_dtype == "f32" else 2
+    return 2 if (wl.V * elem) % 16 == 0 else 1
+
+
 def launches_per_step(wl: Workload, mode: str) -> int:
     """Kernels one VerifyStep.run() launches: S selects, the tree build (the
     generic or the chain kernel), the attention (one launch: split key lists
     are merged inside it), the accept (greedy one launch, sampling two passes)
     and the KV commit."""
-    return wl.S + 1 + 1 + (1 if mode == "greedy" else 2) + 1
+    return wl.S * select_launches(wl) + 1 + 1 + (1 if mode == "greedy" else 2) + 1
 
 
 def _view_from(t: torch.Tensor, offset: int) -> torch.Tensor:
