@@ -31,11 +31,15 @@ struct SelectParams {
   // neither.
   bool early;
   int half;
-  // streaming kernel (rows 16-byte aligned): stream_ctas persistent CTAs,
-  // partials [rows][stream_pmax]; 0 selects the chunked kernel
-  int stream_ctas, stream_pmax;
+  // streaming kernel (rows 16-byte aligned, at least one batch of vectors
+  // long): stream_ctas persistent CTAs taking the stream_nb batches from a
+  // queue, group records [stream_nb][2 row parities][256 threads] in the
+  // partials, then each row's k best [rows][kMaxK]; 0 selects the chunked
+  // kernel
+  int stream_ctas, stream_nb;
   uint32_t* error;
   uint32_t* counters;    // this call's half: b counters
+  uint32_t* queue;       // this call's half: the streaming kernel's batch queue
   unsigned char* partials;  // this call's half
 };
 
@@ -244,10 +248,11 @@ int launch_commit_kv(const CommitParams& p, cudaStream_t stream);
 
 size_t select_partial_bytes(int rows, int chunks);
 struct StreamGeometry {
-  int ctas, pmax;
+  int ctas, nb;    // CTAs (0: the streaming kernel does not apply) and batches
+  size_t bytes;    // its group records and the rows' k best
 };
-// CTAs and pieces a row can have for the streaming select of `rows` rows of V
-// logits, vec per 16-byte vector, on a device of `sms` SMs
+// The streaming select's split of `rows` rows of V logits (vec per 16-byte
+// vector) on a device of `sms` SMs.
 StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms);
 size_t build_tree_smem_bytes(int k, int S);
 size_t sampling_partial_bytes(int rows, int chunks);

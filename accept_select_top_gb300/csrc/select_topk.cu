@@ -484,41 +484,41 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
 
 
 // ---------------------------------------------------------------------------
-// The streaming select: one persistent pass over the step's logits.  The
-// flattened [rows, V] logits (16-byte vectors, rows contiguous) are cut into G
-// equal contiguous ranges, one per CTA (three CTAs a SM).  Thread t of a CTA
-// takes the range's vectors t, t + 256, t + 512, ... through a private ring of
-// 16-byte cp.async copies, kStreamStages batches of kStreamVpt vectors deep,
-// and waits for its own copies with cp.async.wait_group: no barrier and no
-// polling while streaming.  Each thread keeps an online (max, sum of exp) of
-// the row piece (the part of one row inside the CTA's range), rescaled once a
-// batch.
+// The streaming select: two kernels.
 //
-// The k best are kept a warp at a time, behind a bound that only rises:
-//   - every batch, the warp's lanes' running maxima give one: split the 32
-//     lanes into k' groups (k' = k rounded up to a power of two); the smallest
-//     group maximum is at most the k-th largest of k' distinct elements, so at
-//     most the piece's k-th value (two shuffle trees);
-//   - the warp's own k-th value once its list holds k;
-//   - theta, the CTA's: the largest bound any warp has published (atomicMax
-//     on an order key).
-// An element below the bound cannot be among the piece's k best.  Elements
-// that reach it are appended to the warp's candidate buffer (one ballot a
-// batch finds the rare batch that has any; then one element a lane a round,
-// positions by prefix counts of the ballot).  A full buffer is merged into the
-// list (lane j < k holds entry j) by k rounds of a warp argmax.
+// select_stream_kernel reads the step's logits once.  The flattened [rows, V]
+// logits (16-byte vectors, rows contiguous) are cut into units of 256 vectors
+// (4 KB).  Every warp of the persistent grid (two CTAs a SM) works on its own:
+// it takes units in pairs, the first two pairs fixed by its index, the rest
+// from a queue (an atomic counter, asked two pairs ahead so that its latency
+// stays hidden), so that warps the memory serves faster take more.  Lane l
+// holds vectors l, l + 32, ..., l + 224 of a unit in a private ring of 16-byte
+// cp.async copies, three units deep, and waits for its own copies with
+// cp.async.wait_group: no barrier and no wait on another warp anywhere.  A
+// lane's vectors of one unit inside one row form a group; for each group it
+// writes one record: the group's maximum g and s = sum over the group of
+// 2^((x - g) c) (s = -1 where the lane has no vector in that row of the unit).
+// A unit spans at most two rows, so the record slot is (unit, row parity,
+// lane).
 //
-// Only where a row piece ends does the CTA meet: warp 0 merges the warps'
-// lists into the piece's partial (max, sum, k best), and the CTA whose piece
-// is the last of a request to arrive merges the request's pieces and runs the
-// path step, as the chunked kernel does.
+// select_finalize_kernel (one CTA a row) reads a row's records: the row
+// maximum M is the largest g, the denominator S = sum of s 2^((g - M) c) (fp64
+// accumulation).  The row's k best elements lie in its k best groups by
+// (maximum desc, index of the maximum asc): were an element among the k best
+// in a group outside them, the k groups ahead of its group would each hold an
+// element that ranks before it.  So theta = the largest over warps of the
+// warp's k-th largest group maximum (k distinct groups reach it); the groups
+// whose maximum reaches theta are gathered, and their elements that reach it
+// merged into the k best by warp 0 (k rounds of a warp argmax).  The row's k
+// probabilities and tokens are stored; the CTA whose row is the last of its
+// request to arrive runs the path step of the request.
 
 constexpr int kStreamThreads = 256;
 constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kStreamPerSm = 2;                   // CTAs a SM (the ring and the registers allow two)
-constexpr int kStreamStages = 3;                  // batches in flight a thread
-constexpr int kStreamVpt = 8;                     // 16-byte vectors a batch
-constexpr int kStreamBatchVecs = kStreamVpt * kStreamThreads;  // vectors a CTA batch
+constexpr int kStreamStages = 3;                  // units in flight a lane
+constexpr int kStreamVpt = 8;                     // 16-byte vectors a lane holds of a unit
+constexpr int kUnitVecs = kStreamVpt * 32;        // vectors a unit
 constexpr int kStreamCand = 32;                   // candidate elements a warp buffers (one a lane)
 
 // 16-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing.
@@ -529,62 +529,6 @@ __device__ __forceinline__ void stream_cp16(void* dst, const void* src, uint32_t
 __device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void stream_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// The owner CTA of vector u when U vectors are cut into G ranges
-// [c*U/G, (c+1)*U/G).
-__device__ __forceinline__ int stream_owner(long long u, long long U, int G) {
-  return int(((u + 1) * G - 1) / U);
-}
-
-// Number of row pieces (ranges touching the row) of row r.
-__device__ __forceinline__ int stream_pieces(int r, long long rowU, long long U, int G) {
-  return stream_owner((r + 1) * rowU - 1, U, G) - stream_owner(r * rowU, U, G) + 1;
-}
-
-// Merge of one row's pieces by one warp (at most 32 pieces, one a lane: the
-// host caps the grid so): lane q reads piece q's (m, s) and sorted list.  Lane
-// j < k ends with the row's j-th best (value desc, index asc); every lane with
-// the row's max M and sum S (of exp2((x - M) c)).
-template <int K>
-__device__ __forceinline__ void merge_row(const SelPart* pr, int count, int k, float c, float& myv, int& myi,
-                                          float& M, float& S) {
-  const int lane = threadIdx.x & 31;
-  const bool has = lane < count;
-  float hv[K], pm = -3.0e38f, psum = 0.f;
-  int hi[K];
-#pragma unroll
-  for (int q = 0; q < K; ++q) {
-    hv[q] = has ? __ldcg(&pr[lane].v[q]) : -INFINITY;
-    hi[q] = has ? __ldcg(&pr[lane].i[q]) : INT_MAX;
-  }
-  if (has) {
-    const float2 ms = __ldcg(reinterpret_cast<const float2*>(&pr[lane].m));
-    pm = ms.x;
-    psum = ms.y;
-  }
-  M = warp_max(pm);
-  S = warp_sum(psum * exp2f((pm - M) * c));
-  myv = -INFINITY;
-  myi = INT_MAX;
-  for (int j = 0; j < k; ++j) {
-    float bv = hv[0];
-    int bi = hi[0];
-    warp_argmax(bv, bi);
-    if (hi[0] == bi && bi != INT_MAX) {
-#pragma unroll
-      for (int q = 0; q + 1 < K; ++q) {
-        hv[q] = hv[q + 1];
-        hi[q] = hi[q + 1];
-      }
-      hv[K - 1] = -INFINITY;
-      hi[K - 1] = INT_MAX;
-    }
-    if (lane == j) {
-      myv = bv;
-      myi = bi;
-    }
-  }
-}
 
 // Element q (0 <= q < E, a runtime value) of a 16-byte vector, by selects.
 template <typename T>
@@ -710,289 +654,426 @@ __device__ __forceinline__ float batch_exp_sum(const uint4 (&x)[kStreamVpt], flo
   return s.x + s.y;
 }
 
-template <typename T, int K>
+// The record slot of (unit, row parity, lane).
+__device__ __forceinline__ int stream_slot(int unit, int parity, int lane) { return (unit * 2 + parity) * 32 + lane; }
+
+template <typename T>
 __global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) select_stream_kernel(SelectParams a) {
   constexpr int E = LogitTraits<T>::kVec;  // elements per 16-byte vector
-  // ring: vector u of batch slot s of thread t at [(s * kStreamVpt + u) * 256 + t]
+  // ring: vector u of stage s of lane l of warp w at [((w * stages + s) * Vpt + u) * 32 + l]
   extern __shared__ __align__(16) uint4 ring[];
-  __shared__ float cand_v[kStreamWarps][kStreamCand];  // a warp's candidate elements
-  __shared__ int cand_i[kStreamWarps][kStreamCand];    // their element indices in the row
-  __shared__ uint32_t s_theta;  // order key of the CTA's lower bound on the piece's k-th value
-  __shared__ float wmax[kStreamWarps], ws2[kStreamWarps];
-  __shared__ float lv[kStreamWarps][K];
-  __shared__ int li[kStreamWarps][K];
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, nw = kStreamWarps;
-  const int G = gridDim.x;
-  const long long rowU = a.V / E;
-  const long long U = (long long)a.rows * rowU;
-  const long long u_lo = (long long)blockIdx.x * U / G, u_hi = (long long)(blockIdx.x + 1) * U / G;
-  const int n_vec = int(u_hi - u_lo);  // vectors of this CTA (a range is far below 2^31 vectors)
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned rowU = unsigned(a.V / E);
+  const unsigned U = unsigned(a.rows) * rowU;  // (the host keeps it below 2^31)
+  const int nu = a.stream_nb;                  // units in all
   const float c = 1.4426950408889634f / a.temperature;
-  const uint4* src = static_cast<const uint4*>(a.logits) + u_lo;  // this CTA's first vector
-  const unsigned lanes_below = (1u << lane) - 1u;
-  // the lane-maxima bound uses K groups of 32 / K lanes (K, a power of two, is at least k)
-  constexpr int kGroupLanes = 32 / K;
+  const uint4* src = static_cast<const uint4*>(a.logits);
+  float2* rec = reinterpret_cast<float2*>(a.partials);
+  uint4* wring = ring + w * (kStreamStages * kUnitVecs) + lane;
 
-  bool waited = false;
-  if (!a.early) {
-    pdl_wait();
-    pdl_trigger();
-    waited = true;
-  }
-  if (tid == 0) s_theta = 0u;  // the smallest key: no bound yet
-  __syncthreads();
+  // Without overlap: wait for the grid before, then let the request step
+  // launch (it waits for this grid to finish before it reads a record).  With
+  // overlap the reads start at once and a lane waits before its first record
+  // write.
+  bool waited = !a.early;
+  if (waited) pdl_wait();
+  pdl_trigger();
 
-  // batch bb of this thread: offsets (bb * Vpt + u) * 256 + t of the range
-  auto issue = [&](int bb) {
-    uint4* slot = ring + (unsigned(bb) % kStreamStages) * (kStreamVpt * kStreamThreads) + tid;
-    const int o0 = bb * kStreamBatchVecs + tid;
-    if (o0 + (kStreamVpt - 1) * kStreamThreads < n_vec) {  // the whole batch lies in the range
+  // iteration j works on unit 2 * pair(j / 2) + (j & 1); pc = pair(j / 2), pn
+  // = pair(j / 2 + 1); lane 0 holds the queue's answer for pair(j / 2 + 2)
+  const int NW = gridDim.x * kStreamWarps, gw = blockIdx.x * kStreamWarps + w;
+  int pc = gw, pn = gw + NW, pending = 0;
+  if (lane == 0) pending = 2 * NW + int(atomicAdd(a.queue, 1u));
+  auto issue = [&](int j, int unit) {  // stage j % 3 <- unit (an empty group past the last unit)
+    if (unit < nu) {
+      uint4* st = wring + (unsigned(j) % kStreamStages) * kUnitVecs;
+      const unsigned o0 = unsigned(unit) * kUnitVecs + lane;
+      if (o0 + (kStreamVpt - 1) * 32 < U) {  // the whole unit exists
 #pragma unroll
-      for (int u = 0; u < kStreamVpt; ++u) stream_cp16(slot + u * kStreamThreads, src + o0 + u * kStreamThreads, 16u);
-    } else {
+        for (int u = 0; u < kStreamVpt; ++u) stream_cp16(st + u * 32, src + o0 + u * 32, 16u);
+      } else {
 #pragma unroll
-      for (int u = 0; u < kStreamVpt; ++u) {
-        const int o = o0 + u * kStreamThreads;
-        const bool ok = o < n_vec;
-        stream_cp16(slot + u * kStreamThreads, ok ? src + o : src, ok ? 16u : 0u);
+        for (int u = 0; u < kStreamVpt; ++u) {
+          const unsigned o = o0 + u * 32;
+          const bool ok = o < U;
+          stream_cp16(st + u * 32, ok ? src + o : src, ok ? 16u : 0u);
+        }
       }
     }
     stream_commit();
   };
-  const int nbatch = (n_vec + kStreamBatchVecs - 1) / kStreamBatchVecs;
-#pragma unroll
-  for (int q = 0; q < kStreamStages - 1; ++q) issue(q);
-
-  float m = -3.0e38f, ssum = 0.f;  // this thread's online softmax of the current row piece
-  float lv_r = -INFINITY;          // lane j < k: entry j of the warp's k best of the piece
-  int li_r = INT_MAX;
-  float thr_w = -INFINITY;         // the warp's bound (lane maxima, own list); warp-uniform
-  float thr_pub = -INFINITY;       // the last bound this warp published
-  int ncand = 0;                   // candidates in the warp's buffer (warp-uniform)
-  int row = int(u_lo / rowU);
-  int re = int((long long)(row + 1) * rowU - u_lo);  // end of the current row, as an offset of the range
-  for (int bb = 0; bb < nbatch; ++bb) {
-    issue(bb + kStreamStages - 1);  // (past the range: an empty group, so the count stays exact)
-    stream_wait_group<kStreamStages - 1>();  // this thread's copies of batch bb have landed
-    const uint4* slot = ring + (unsigned(bb) % kStreamStages) * (kStreamVpt * kStreamThreads);
-    const int b0 = bb * kStreamBatchVecs;
-    const int b1 = b0 + kStreamBatchVecs < n_vec ? b0 + kStreamBatchVecs : n_vec;
-    int cur = b0;
-    while (cur < b1) {  // the batch's vectors, one row piece at a time (uniform over the CTA)
-      const int seg = b1 < re ? b1 : re;
+  issue(0, 2 * pc);
+  issue(1, 2 * pc + 1);
+  for (int j = 0;; ++j) {
+    if (j >= 2 && !(j & 1)) {  // a new pair
+      pc = pn;
+      pn = __shfl_sync(0xffffffffu, pending, 0);
+      if (lane == 0) pending = 2 * NW + int(atomicAdd(a.queue, 1u));
+    }
+    const int unit = 2 * pc + (j & 1);
+    if (unit >= nu) break;  // (a warp's units only grow: every later one is past the end too)
+    issue(j + 2, 2 * pn + (j & 1));
+    stream_wait_group<kStreamStages - 1>();  // this lane's copies of unit j have landed
+    const uint4* st = wring + (unsigned(j) % kStreamStages) * kUnitVecs;
+    const unsigned b0 = unsigned(unit) * kUnitVecs;
+    const unsigned b1 = b0 + kUnitVecs < U ? b0 + kUnitVecs : U;
+    unsigned row = b0 / rowU;
+    unsigned cur = b0;
+    while (cur < b1) {  // the unit's vectors, one row at a time (at most two rows)
+      const unsigned re = (row + 1) * rowU;
+      const unsigned seg = b1 < re ? b1 : re;
       uint4 x[kStreamVpt];
-      uint32_t vin;  // bit u: vector u lies in the segment (the others read as -inf)
-      if (cur == b0 && seg == b0 + kStreamBatchVecs) {  // the common case: the whole batch
-        vin = (1u << kStreamVpt) - 1u;
+      bool any = true;  // the group holds at least one vector
+      if (cur == b0 && seg == b0 + kUnitVecs) {  // the common case: the whole unit
 #pragma unroll
-        for (int u = 0; u < kStreamVpt; ++u) x[u] = slot[u * kStreamThreads + tid];
-      } else {
-        vin = 0u;
+        for (int u = 0; u < kStreamVpt; ++u) x[u] = st[u * 32];
+      } else {  // vectors outside the segment read as -inf
+        any = false;
 #pragma unroll
         for (int u = 0; u < kStreamVpt; ++u) {
-          const int o = b0 + u * kStreamThreads + tid;
-          x[u] = VecOps<T>::neg_inf();
-          if (o >= cur && o < seg) {
-            vin |= 1u << u;
-            x[u] = slot[u * kStreamThreads + tid];
+          const unsigned o = b0 + u * 32 + lane;
+          const bool in = o >= cur && o < seg;
+          any = any || in;
+          x[u] = in ? st[u * 32] : VecOps<T>::neg_inf();
+        }
+      }
+      typename VecMax<T>::type gm = VecMax<T>::of(x[0]);
+#pragma unroll
+      for (int u = 1; u < kStreamVpt; ++u) gm = VecMax<T>::comb(gm, VecMax<T>::of(x[u]));
+      const float g = VecMax<T>::value(gm);
+      // (g = -inf: no element, or all -inf: every term is 0)
+      const float s = batch_exp_sum<T>(x, c, g > -INFINITY ? g * c : 0.f);
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
+      __stcg(&rec[stream_slot(unit, row & 1, lane)], make_float2(g, any ? s : -1.f));
+      cur = seg;
+      ++row;
+    }
+  }
+  stream_wait_group<0>();  // no copy of this lane is left in flight (the last groups are empty)
+}
+
+// The request step after the streaming kernel: one CTA a row.
+constexpr int kFinalizeThreads = 256;
+constexpr int kFinalizeWarps = kFinalizeThreads / 32;
+constexpr int kFinalizeMaxPer = 32;  // records a thread of the request step takes at most
+constexpr int kElemCap = 32 * 32;    // gathered elements the request step ranks directly
+
+// Maximum / sum over the CTA (scratch: a slot a warp); every thread gets the
+// result.  Both end with a barrier, so the scratch may be reused.
+__device__ __forceinline__ float block_max_f(float v, float* scratch) {
+  v = warp_max(v);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = scratch[0];
+  for (int i = 1; i < kFinalizeWarps; ++i) r = fmaxf(r, scratch[i]);
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ float block_sum_f(float v, float* scratch) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int i = 0; i < kFinalizeWarps; ++i) r += scratch[i];
+  __syncthreads();
+  return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(SelectParams a) {
+  constexpr int E = LogitTraits<T>::kVec;
+  // the row's group maxima by flat record index f (an empty group as NaN,
+  // which no comparison takes), then the gathered groups' indices
+  extern __shared__ float gval[];
+  __shared__ float p_s[kMaxK][kMaxK];
+  __shared__ int id_s[kMaxK][kMaxK];
+  __shared__ float el_v[kElemCap];               // the gathered elements (value, index in the row)
+  __shared__ int el_i[kElemCap];
+  __shared__ float cand_v[kStreamCand];
+  __shared__ int cand_i[kStreamCand];
+  __shared__ float s_f[kFinalizeWarps];
+  __shared__ int s_n, s_ne;
+  __shared__ float s_vk;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int k = a.k, kk = k * k;
+  const int rows_per_req = a.step ? k : 1;
+  const int req = row / rows_per_req;
+  const long long rowU = a.V / E;
+  const float c = 1.4426950408889634f / a.temperature;
+  const float2* rec = reinterpret_cast<const float2*>(a.partials);
+  const uint4* logits = static_cast<const uint4*>(a.logits);
+  float2* best = reinterpret_cast<float2*>(a.partials + align256(size_t(a.stream_nb) * 2 * 32 * sizeof(float2)));
+  const unsigned lanes_below = (1u << lane) - 1u;
+  if (row == 0 && tid == 0) *a.queue = 0u;  // the streaming grid is done with the queue: ready for the next call
+  const long long rs = (long long)row * rowU, rend = rs + rowU;  // the row's vectors
+  const int uf = int(rs / kUnitVecs), ul = int((rend - 1) / kUnitVecs);
+  const int F = (ul - uf + 1) * 32;  // the row's records: f = (unit - uf) * 32 + lane'
+  const int par = row & 1;
+  int* gsel = reinterpret_cast<int*>(gval + F);
+  if (tid == 0) {
+    s_n = 0;
+    s_ne = 0;
+  }
+
+  // one pass over the records (thread tid: f = tid + 256 m, eight loads in
+  // flight): the maxima to shared memory, this thread's maximum and its sum
+  // relative to it (fp32: a chain of at most 32 additions here, 8 across the CTA)
+  float tm = -INFINITY, ts = 0.f;
+  for (int f0 = 0; f0 < F; f0 += 8 * kFinalizeThreads) {
+    float2 r[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int f = f0 + q * kFinalizeThreads + tid;
+      r[q] = f < F ? __ldcg(&rec[stream_slot(uf + f / 32, par, f % 32)]) : make_float2(NAN, -1.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int f = f0 + q * kFinalizeThreads + tid;
+      if (f < F) gval[f] = r[q].y >= 0.f ? r[q].x : NAN;
+      if (r[q].y > 0.f) {  // (s = 0: the group is all -inf)
+        if (r[q].x > tm) {
+          ts = ts * fast_exp2((tm - r[q].x) * c) + r[q].y;
+          tm = r[q].x;
+        } else {
+          ts += r[q].y * fast_exp2((r[q].x - tm) * c);
+        }
+      }
+    }
+  }
+  const float M = block_max_f(tm, s_f);
+  const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f);
+  // theta: the largest over warps of the k-th largest of the lanes' best group
+  // maxima (k distinct groups reach it)
+  {
+    float bv = -INFINITY;
+    for (int m = tid; m < F; m += kFinalizeThreads) bv = fmaxf(bv, gval[m]);
+    float wk = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      float wv = bv;
+      int wi = lane;
+      warp_argmax(wv, wi);
+      if (lane == wi) bv = -INFINITY;
+      wk = wv;
+    }
+    if (lane == 0) s_f[w] = wk;
+  }
+  __syncthreads();
+  float theta = -INFINITY;
+  for (int i = 0; i < kFinalizeWarps; ++i) theta = fmaxf(theta, s_f[i]);
+  // the groups that reach theta
+  for (int m = 0; m < (F + kFinalizeThreads - 1) / kFinalizeThreads; ++m) {
+    const int f = tid + m * kFinalizeThreads;
+    const bool take = f < F && gval[f] >= theta;
+    const unsigned mask = __ballot_sync(0xffffffffu, take);
+    if (mask) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_n, __popc(mask));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (take) gsel[base + __popc(mask & lanes_below)] = f;
+    }
+  }
+  __syncthreads();
+  // v_k, the row's k-th largest group maximum, among the gathered (warp 0: k
+  // rounds of a warp argmax; lane l takes gathered entries l, l + 32, ...)
+  if (w == 0) {
+    const int n0 = s_n;
+    const int per = (n0 - lane + 31) / 32;
+    uint64_t taken = 0;
+    float vk = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = INT_MAX, bm = -1;
+      for (int m = 0; m < per && m < 64; ++m) {
+        const int f = gsel[lane + 32 * m];
+        if (!(taken & (1ull << m)) && better(gval[f], f, bv, bi)) {
+          bv = gval[f];
+          bi = f;
+          bm = m;
+        }
+      }
+      const int own = bi;
+      warp_argmax(bv, bi);
+      if (own == bi && bi != INT_MAX) taken |= 1ull << bm;
+      vk = bv;
+    }
+    if (lane == 0) {
+      // more than 2048 gathered (values tied at theta): theta itself stays the cut
+      s_vk = n0 <= 32 * 64 ? vk : theta;
+      s_n = 0;
+    }
+  }
+  __syncthreads();
+  const float vk = s_vk;  // k distinct groups reach it: the k best elements all do
+  // the groups that reach v_k (every group with that maximum: a tie keeps them all)
+  for (int m = 0; m < (F + kFinalizeThreads - 1) / kFinalizeThreads; ++m) {
+    const int f = tid + m * kFinalizeThreads;
+    const bool take = f < F && gval[f] >= vk;
+    const unsigned mask = __ballot_sync(0xffffffffu, take);
+    if (mask) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_n, __popc(mask));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (take) gsel[base + __popc(mask & lanes_below)] = f;
+    }
+  }
+  __syncthreads();
+  const int ng = s_n;
+  // their elements that reach v_k: a vector a thread
+  for (int i = tid; i < ng * kStreamVpt; i += kFinalizeThreads) {
+    const int f = gsel[i / kStreamVpt], u = i % kStreamVpt;
+    const long long gv = (long long)(uf + f / 32) * kUnitVecs + f % 32 + u * 32;
+    if (gv >= rs && gv < rend) {
+      const uint4 x = __ldcg(logits + gv);
+#pragma unroll
+      for (int q = 0; q < E; ++q) {
+        const float v = VecOps<T>::at(x, q);
+        if (v >= vk) {
+          const int pos = atomicAdd(&s_ne, 1);
+          if (pos < kElemCap) {
+            el_v[pos] = v;
+            el_i[pos] = int((gv - rs) * E) + q;
           }
         }
       }
-      typename VecMax<T>::type vm[kStreamVpt];  // each vector's maximum
-#pragma unroll
-      for (int u = 0; u < kStreamVpt; ++u) vm[u] = VecMax<T>::of(x[u]);
-      typename VecMax<T>::type bmv = vm[0];
-#pragma unroll
-      for (int u = 1; u < kStreamVpt; ++u) bmv = VecMax<T>::comb(bmv, vm[u]);
-      const float bm = VecMax<T>::value(bmv);
-      if (bm > m) {
-        ssum *= fast_exp2((m - bm) * c);
-        m = bm;
-      }
-      // (m still the sentinel: every term is 0 anyway; -inf entries give 0)
-      ssum += batch_exp_sum<T>(x, c, m > -1.0e30f ? m * c : 0.f);
-      // the lane-maxima bound: max within groups of 32 / K lanes, min across the K groups
-      float gb = m > -1.0e30f ? m : -INFINITY;
-#pragma unroll
-      for (int o = 1; o < kGroupLanes; o <<= 1) gb = fmaxf(gb, __shfl_xor_sync(0xffffffffu, gb, o));
-#pragma unroll
-      for (int o = kGroupLanes; o < 32; o <<= 1) gb = fminf(gb, __shfl_xor_sync(0xffffffffu, gb, o));
-      thr_w = fmaxf(thr_w, gb);
-      if (thr_w > thr_pub) {  // warp-uniform
-        if (lane == 0) atomicMax(&s_theta, order_key(thr_w));
-        thr_pub = thr_w;
-      }
-      // a stale (lower) theta only lets more through; key 0 reads as NaN, which fmaxf drops
-      const float thr = fmaxf(key_value(*reinterpret_cast<volatile uint32_t*>(&s_theta)), thr_w);
-      if (__ballot_sync(0xffffffffu, vin != 0u && bm >= thr)) {  // the rare batch with a candidate
-        uint32_t vmask = 0;  // bit u: vector u holds an element that reaches the bound
-        if (bm >= thr) {
-#pragma unroll
-          for (int u = 0; u < kStreamVpt; ++u)
-            if ((vin & (1u << u)) && VecMax<T>::value(vm[u]) >= thr) vmask |= 1u << u;
+    }
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int ne = s_ne;
+    float lv_r = -INFINITY;  // lane j < k: entry j of the row's k best
+    int li_r = INT_MAX;
+    if (ne <= kElemCap) {
+      // k rounds of a warp argmax over the gathered elements (lane l: entries l, l + 32, ...)
+      uint32_t taken = 0;
+      const int per = (ne - lane + 31) / 32;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = INT_MAX, bm = -1;
+        for (int m = 0; m < per; ++m) {
+          const int e2 = lane + 32 * m;
+          if (!(taken & (1u << m)) && better(el_v[e2], el_i[e2], bv, bi)) {
+            bv = el_v[e2];
+            bi = el_i[e2];
+            bm = m;
+          }
         }
-        const int rbase = int(u_lo - ((long long)row * rowU));  // vector o of the range is vector o + rbase of the row
-        while (__any_sync(0xffffffffu, vmask != 0u)) {  // one candidate vector a lane a round
-          uint32_t bits = 0;  // bit q: element q of vector u reaches the bound
-          int u = 0;
-          if (vmask) {
-            u = __ffs(vmask) - 1;
-            vmask &= vmask - 1u;
-            const uint4 xv = slot[u * kStreamThreads + tid];  // (the batch is still in its slot)
+        const int own = bi;
+        warp_argmax(bv, bi);
+        if (own == bi && bi != INT_MAX) taken |= 1u << bm;
+        if (lane == j) {
+          lv_r = bv;
+          li_r = bi;
+        }
+      }
+    } else {
+      // more than kElemCap elements reach v_k (values tied at the cut): the
+      // groups again, through the candidate buffer, 32 at a time
+      float theta = vk;
+      int ncand = 0;
+      for (int g0 = 0; g0 < ng; g0 += 32) {
+        const int gi = g0 + lane;
+        uint4 xv[kStreamVpt];
+        uint32_t vin = 0;
+        long long gv0 = 0;
+        if (gi < ng) {
+          const int f = gsel[gi];
+          gv0 = (long long)(uf + f / 32) * kUnitVecs + f % 32;
 #pragma unroll
-            for (int q = 0; q < E; ++q) bits |= (VecOps<T>::at(xv, q) >= thr ? 1u : 0u) << q;
+          for (int u = 0; u < kStreamVpt; ++u) {
+            const long long gv = gv0 + u * 32;
+            if (gv >= rs && gv < rend) {
+              vin |= 1u << u;
+              xv[u] = __ldcg(logits + gv);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kStreamVpt; ++u) {
+          uint32_t bits = 0;
+          if (vin & (1u << u)) {
+#pragma unroll
+            for (int q = 0; q < E; ++q) bits |= (VecOps<T>::at(xv[u], q) >= theta ? 1u : 0u) << q;
           }
           for (;;) {  // one element a lane a round
             const unsigned mask = __ballot_sync(0xffffffffu, bits != 0u);
             if (!mask) break;
             const int nnew = __popc(mask);
             if (ncand + nnew > kStreamCand) {
-              stream_merge_candidates(cand_v[w], cand_i[w], ncand, a.k, lv_r, li_r);
+              stream_merge_candidates(cand_v, cand_i, ncand, k, lv_r, li_r);
               ncand = 0;
-              if (__shfl_sync(0xffffffffu, li_r, a.k - 1) != INT_MAX) {  // the list holds k: its k-th
-                thr_w = fmaxf(thr_w, __shfl_sync(0xffffffffu, lv_r, a.k - 1));
-                if (thr_w > thr_pub) {
-                  if (lane == 0) atomicMax(&s_theta, order_key(thr_w));
-                  thr_pub = thr_w;
-                }
-              }
+              if (__shfl_sync(0xffffffffu, li_r, k - 1) != INT_MAX)  // the list holds k: a tighter bound
+                theta = fmaxf(theta, __shfl_sync(0xffffffffu, lv_r, k - 1));
             }
             if (bits) {
               const int q = __ffs(bits) - 1;
               bits &= bits - 1u;
               const int pos = ncand + __popc(mask & lanes_below);
-              cand_v[w][pos] = vec_elem<T>(slot[u * kStreamThreads + tid], q);
-              cand_i[w][pos] = (b0 + u * kStreamThreads + tid + rbase) * E + q;
+              cand_v[pos] = vec_elem<T>(xv[u], q);
+              cand_i[pos] = int((gv0 + u * 32 - rs) * E) + q;
             }
             ncand += nnew;
           }
         }
       }
-      cur = seg;
-      if (seg == re || seg == n_vec) {
-        // ---- end of a row piece: its partial ----
-        if (ncand) stream_merge_candidates(cand_v[w], cand_i[w], ncand, a.k, lv_r, li_r);
-        const float Mw = warp_max(m);
-        const float Sw = warp_sum(ssum * exp2f((m - Mw) * c));
-        if (lane == 0) {
-          wmax[w] = Mw;
-          ws2[w] = Sw;
-        }
-        if (lane < K) {  // lanes k..K-1 hold no entry
-          lv[w][lane] = lv_r;
-          li[w][lane] = li_r;
-        }
-        __syncthreads();
-        if (w == 0) {
-          if (!waited) {  // overlap: the partials are written only once the grid before is done
-            pdl_wait();
-            pdl_trigger();
-            waited = true;
-          }
-          const int r0 = stream_owner((long long)row * rowU, U, G);
-          SelPart* part = reinterpret_cast<SelPart*>(a.partials) + size_t(row) * a.stream_pmax + (blockIdx.x - r0);
-          const float wm = lane < nw ? wmax[lane] : -3.0e38f;
-          const float Mc = warp_max(wm);
-          const float Sc = warp_sum(lane < nw ? ws2[lane] * exp2f((wm - Mc) * c) : 0.f);
-          if (lane == 0) {
-            part->m = Mc;
-            part->s = Sc;
-          }
-          merge_warp_lists<K>(lv, li, nw, a.k, part);
-        }
-        m = -3.0e38f;
-        ssum = 0.f;
-        lv_r = -INFINITY;
-        li_r = INT_MAX;
-        thr_w = -INFINITY;
-        thr_pub = -INFINITY;
-        ncand = 0;
-        if (tid == 0) s_theta = 0u;
-        __syncthreads();  // lv / li are read and the bound is reset before the next piece
-        re += int(rowU);
-        ++row;
-      }
+      if (ncand) stream_merge_candidates(cand_v, cand_i, ncand, k, lv_r, li_r);
     }
-  }
-  stream_wait_group<0>();  // no copy of this CTA is left in flight (the last groups are empty)
-}
-
-// The request step after the streaming select: one CTA a request, one warp a
-// row of it merging the row's pieces (merge_row), then the path step
-// (write_request).  Launched after the streaming kernel; it waits for that
-// grid before it reads a partial.
-constexpr int kFinalizeThreads = 32 * kMaxK;
-
-template <int K>
-__global__ void __launch_bounds__(kFinalizeThreads) select_finalize_kernel(SelectParams a) {
-  __shared__ float p_s[kMaxK][kMaxK];
-  __shared__ int id_s[kMaxK][kMaxK];
-  pdl_wait();
-  pdl_trigger();
-  const int req = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k = a.k, kk = k * k;
-  const int rows_per_req = a.step ? k : 1;
-  const int vec = a.dtype == SPEC_F32 ? 4 : 8;
-  const long long rowU = a.V / vec;
-  const long long U = (long long)a.rows * rowU;
-  const int G = a.stream_ctas;
-  const float c = 1.4426950408889634f / a.temperature;
-  const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
-  if (w < rows_per_req) {
-    const int grow = req * rows_per_req + w;
-    const SelPart* pr = reinterpret_cast<const SelPart*>(a.partials) + size_t(grow) * a.stream_pmax;
-    float myv, M, S;
-    int myi;
-    merge_row<K>(pr, stream_pieces(grow, rowU, U, G), k, c, myv, myi, M, S);
     const float invS = 1.f / S;
-    if (lane < k) {
-      p_s[w][lane] = expf((myv - M) / a.temperature) * invS;
-      id_s[w][lane] = myi;
-    }
+    if (lane < k) best[size_t(row) * kMaxK + lane] = make_float2(expf((lv_r - M) / a.temperature) * invS, __int_as_float(li_r));
+  }
+  // the last row of the request to arrive runs the path step
+  if (!arrive_last(a.counters + req, uint32_t(rows_per_req))) return;
+  const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
+  for (int i = tid; i < rows_per_req * k; i += kFinalizeThreads) {
+    const float2 v = __ldcg(&best[(size_t(req) * rows_per_req + i / k) * kMaxK + i % k]);
+    p_s[i / k][i % k] = v.x;
+    id_s[i / k][i % k] = __float_as_int(v.y);
   }
   __syncthreads();
   write_request(a, req, rows_per_req, p_s, id_s, sc_in);
+  counter_reset(a.counters + req);
 }
 
-// The split the streaming select uses: G CTAs (kStreamPerSm a SM, at least 64
-// vectors each) and the pieces a row can have.
-struct StreamSplit {
-  int ctas, pmax;
-};
-inline StreamSplit stream_split(long rows, int V, int vec, int sms) {
+// The streaming split: G CTAs (kStreamPerSm a SM) over the units.  None where
+// a row is shorter than a unit (a unit then could span more than two rows),
+// where the request step's threads would take more than kFinalizeMaxPer
+// records, or where the vector count reaches 2^31.
+StreamGeometry stream_geometry(long rows, int V, int vec, int sms) {
   const long long rowU = V / vec;
+  if (rows < 1 || rowU < kUnitVecs) return StreamGeometry{0, 0, 0};
+  if ((rowU / kUnitVecs + 2) * 32 > (long long)kFinalizeMaxPer * kFinalizeThreads) return StreamGeometry{0, 0, 0};
   const long long U = rows * rowU;
+  if (U >= (1LL << 31) - kUnitVecs) return StreamGeometry{0, 0, 0};
+  const long long nu = (U + kUnitVecs - 1) / kUnitVecs;
   long long G = (long long)kStreamPerSm * sms;
-  if (G > U / 64) G = U / 64;
+  const long long need = (nu + 2 * kStreamWarps - 1) / (2 * kStreamWarps);  // CTAs whose warps get a pair each
+  if (G > need) G = need;
   if (G < 1) G = 1;
-  auto pmax_of = [&](long long g) {
-    auto owner = [&](long long u) { return ((u + 1) * g - 1) / U; };
-    long long pm = 1;
-    for (long r = 0; r < rows; ++r) {
-      const long long p = owner((r + 1) * rowU - 1) - owner(r * rowU) + 1;
-      if (p > pm) pm = p;
-    }
-    return pm;
-  };
-  // at most 32 pieces a row, so that a warp merges a row one piece a lane
-  long long pmax = pmax_of(G);
-  while (pmax > 32 && G > 1) {
-    G = G * 31 / 32;
-    pmax = pmax_of(G);
-  }
-  return StreamSplit{int(G), int(pmax)};
+  const size_t bytes = align256(size_t(nu) * 2 * 32 * sizeof(float2)) + align256(size_t(rows) * kMaxK * sizeof(float2));
+  return StreamGeometry{int(G), int(nu), bytes};
 }
 
-template <typename T, int K>
+// Dynamic shared memory of the request step: a row's record maxima and indices.
+inline size_t finalize_smem(int V, int vec) {
+  const long long rowU = V / vec;
+  return 2 * size_t(rowU / kUnitVecs + 2) * 32 * sizeof(float);
+}
+
+template <typename T>
 cudaError_t launch_stream(const SelectParams& p, cudaStream_t stream) {
-  constexpr size_t smem = size_t(kStreamStages) * kStreamVpt * kStreamThreads * 16;
-  cudaError_t e =
-      cudaFuncSetAttribute(select_stream_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  constexpr size_t smem = size_t(kStreamWarps) * kStreamStages * kUnitVecs * 16;
+  cudaError_t e = cudaFuncSetAttribute(select_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(select_stream_kernel<T, K>, dim3(p.stream_ctas), dim3(kStreamThreads), smem, stream, p);
+  e = launch_pdl(select_stream_kernel<T>, dim3(p.stream_ctas), dim3(kStreamThreads), smem, stream, p);
   if (e != cudaSuccess) return e;
-  const int requests = p.step ? p.rows / p.k : p.rows;
-  return launch_pdl(select_finalize_kernel<K>, dim3(requests), dim3(kFinalizeThreads), 0, stream, p);
+  const size_t fsmem = finalize_smem(p.V, LogitTraits<T>::kVec);
+  e = cudaFuncSetAttribute(select_finalize_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fsmem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(select_finalize_kernel<T>, dim3(p.rows), dim3(kFinalizeThreads), fsmem, stream, p);
 }
 
 template <typename T>
@@ -1001,13 +1082,7 @@ int launch_t(const SelectParams& p, cudaStream_t stream) {
   const int K = p.k <= 1 ? 1 : p.k <= 2 ? 2 : p.k <= 4 ? 4 : p.k <= 8 ? 8 : 16;
   cudaError_t e = cudaSuccess;
   if (p.stream_ctas > 0) {
-    switch (K) {
-      case 1: e = launch_stream<T, 1>(p, stream); break;
-      case 2: e = launch_stream<T, 2>(p, stream); break;
-      case 4: e = launch_stream<T, 4>(p, stream); break;
-      case 8: e = launch_stream<T, 8>(p, stream); break;
-      default: e = launch_stream<T, 16>(p, stream); break;
-    }
+    e = launch_stream<T>(p, stream);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
   }
   switch (K) {
@@ -1024,10 +1099,7 @@ int launch_t(const SelectParams& p, cudaStream_t stream) {
 
 size_t select_partial_bytes(int rows, int chunks) { return align256(size_t(rows) * chunks * sizeof(SelPart)); }
 
-StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms) {
-  const StreamSplit s = stream_split(rows, V, vec, sms);
-  return StreamGeometry{s.ctas, s.pmax};
-}
+StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms) { return stream_geometry(rows, V, vec, sms); }
 
 int launch_select_topk(const SelectParams& p, cudaStream_t stream) {
   return p.dtype == SPEC_F32 ? launch_t<float>(p, stream) : launch_t<uint16_t>(p, stream);

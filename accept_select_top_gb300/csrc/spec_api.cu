@@ -57,8 +57,7 @@ size_t select_launch_bytes(long rows, int V) {
   for (int vec : {4, 8}) {  // fp32 and bf16 rows
     if (V % vec) continue;
     const StreamGeometry g = select_stream_geometry(rows, V, vec, device_sms());
-    const size_t s = select_partial_bytes(int(rows), g.pmax);
-    if (s > streamed) streamed = s;
+    if (g.bytes > streamed) streamed = g.bytes;
   }
   return chunked > streamed ? chunked : streamed;
 }
@@ -490,16 +489,17 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   p.chunks = sp.chunks;
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(draft_logits, V, dtype);
-  if (p.vec_ok) {  // rows of whole 16-byte vectors: the streaming kernel
+  if (p.vec_ok) {  // rows of whole 16-byte vectors: the streaming kernel, where a row is a batch or longer
     const StreamGeometry g = select_stream_geometry(p.rows, V, vec_elems(dtype), device_sms());
     p.stream_ctas = g.ctas;
-    p.stream_pmax = g.pmax;
+    p.stream_nb = g.nb;
   }
   p.error = v.error;
   const std::pair<bool, int> eh = take_select(ws, b);
   p.early = eh.first;
   p.half = eh.second;
   p.counters = v.counters + 1 + size_t(eh.second) * b;  // word 0 is the commit's
+  p.queue = v.counters + 1 + 2 * size_t(b) + eh.second;
   p.partials = v.partials + select_base_bytes(b) + size_t(eh.second) * select_half_bytes(b, k, V);
   return launch_select_topk(p, as_stream(stream));
 }

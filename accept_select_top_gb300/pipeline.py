@@ -170,10 +170,12 @@ class VerifyStep:
 
 def select_launches(wl: Workload) -> int:
     """Kernels one spec_select_topk call launches: rows of whole 16-byte
-    vectors (the buffers here are aligned) take the streaming kernel and its
-    request step, other rows the chunked kernel alone."""
+    vectors, at least one streaming unit (256 vectors) and at most 254 units
+    long (the buffers here are aligned), take the streaming kernel and its
+    request step; other rows the chunked kernel alone."""
     elem = 4 if wl.logits_dtype == "f32" else 2
-    return 2 if (wl.V * elem) % 16 == 0 else 1
+    vecs = wl.V * elem // 16
+    return 2 if (wl.V * elem) % 16 == 0 and 256 <= vecs and (vecs // 256 + 2) <= 256 else 1
 
 
 def launches_per_step(wl: Workload, mode: str) -> int:
