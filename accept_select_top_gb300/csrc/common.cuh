@@ -34,11 +34,13 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 // at least 256 words: the attention merge counts arrivals per CTA (<= 192)
 // Arrival counters: words [0, max(256, 2b+3)) serve every call (the
 // attention's merge counters take up to 256; the select's two halves take 2b
-// request counters from word 1 and one batch queue each at 2b+1 and 2b+2);
+// request counters from word 1 and one unit queue each at 2b+1 and 2b+2);
 // greedy accept counts at greedy_counter_base(b) + request, a range no other
-// call uses, so that its scan may overlap the attention before it.
+// call uses, so that its scan may overlap the attention before it; the word
+// after them is the sampling accept's unit queue.
 __host__ __device__ inline size_t greedy_counter_base(int b) { return size_t(2 * b + 3 > 256 ? 2 * b + 3 : 256); }
-__host__ __device__ inline size_t counters_bytes(int b) { return align256((greedy_counter_base(b) + size_t(b)) * 4); }
+__host__ __device__ inline size_t sampling_queue_word(int b) { return greedy_counter_base(b) + size_t(b); }
+__host__ __device__ inline size_t counters_bytes(int b) { return align256((sampling_queue_word(b) + 1) * 4); }
 
 struct WsView {
   uint32_t* error;

@@ -135,9 +135,14 @@ struct SamplingParams {
   int chunks, chunk_elems;    // pass 1 split of a verify row
   int chunks2, chunk2_elems;  // pass 2 split of the terminal row
   bool vec_ok;
+  // the streaming pass (logit rows of whole 16-byte vectors): stream_ctas
+  // CTAs over stream_nu units, records rec; 0: the chunked pass 1
+  int stream_ctas, stream_nu;
+  float2* rec;
+  uint32_t* queue;
   uint32_t* error;
   uint32_t* counters;
-  unsigned char* partials;   // pass 1 partials
+  unsigned char* partials;   // pass 1 partials (a row's statistics after the streaming pass)
   unsigned char* state;      // per-request state handed from pass 1 to pass 2
   unsigned char* partials2;  // pass 2 partials
 };
@@ -247,12 +252,32 @@ int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream);
 int launch_commit_kv(const CommitParams& p, cudaStream_t stream);
 
 size_t select_partial_bytes(int rows, int chunks);
-struct StreamGeometry {
-  int ctas, nb;    // CTAs (0: the streaming kernel does not apply) and batches
-  size_t bytes;    // its group records and the rows' k best
+// The logits streaming pass (stream_records.cu): per group of a lane's 8
+// vectors of a 4 KB unit inside one row, the group maximum and the sum of
+// 2^((x - max) c), c = log2(e) / T of the row.
+struct StreamRecParams {
+  const void* logits;
+  int rows, V;
+  float temperature;          // one temperature for every row, or
+  const float* temperatures;  // one a request of rows_per_temp rows (0: greedy)
+  int rows_per_temp;
+  int nu;                     // units
+  int cu;                     // units a queue answer hands out (set by launch_stream_records)
+  float2* rec;                // records [nu][2 row parities][32 lanes]
+  uint32_t* queue;            // the unit queue (0 at launch)
+  bool early;                 // reads may start before the grid before is done
 };
-// The streaming select's split of `rows` rows of V logits (vec per 16-byte
-// vector) on a device of `sms` SMs.
+struct StreamGeometry {
+  int ctas, nb;    // CTAs (0: the streaming pass does not apply) and units
+  size_t bytes;    // the records
+};
+// Records of a row that a request step holds at most (shared memory).
+constexpr int kRowRecordsMax = 8192;
+// The streaming split of `rows` rows of V logits (vec per 16-byte vector) on a
+// device of `sms` SMs.
+StreamGeometry stream_geometry(long rows, int V, int vec, int sms);
+int launch_stream_records(const StreamRecParams& p, int ctas, int dtype, cudaStream_t stream);
+// The select's streaming layout: the records and then the rows' k best.
 StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms);
 size_t build_tree_smem_bytes(int k, int S);
 size_t sampling_partial_bytes(int rows, int chunks);

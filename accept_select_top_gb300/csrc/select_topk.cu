@@ -18,6 +18,7 @@
 // the kernel).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "stream_records.cuh"
 
 namespace spec {
 
@@ -484,303 +485,21 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
 
 
 // ---------------------------------------------------------------------------
-// The streaming select: two kernels.
-//
-// select_stream_kernel reads the step's logits once.  The flattened [rows, V]
-// logits (16-byte vectors, rows contiguous) are cut into units of 256 vectors
-// (4 KB).  Every warp of the persistent grid (two CTAs a SM) works on its own:
-// it takes units in pairs, the first two pairs fixed by its index, the rest
-// from a queue (an atomic counter, asked two pairs ahead so that its latency
-// stays hidden), so that warps the memory serves faster take more.  Lane l
-// holds vectors l, l + 32, ..., l + 224 of a unit in a private ring of 16-byte
-// cp.async copies, three units deep, and waits for its own copies with
-// cp.async.wait_group: no barrier and no wait on another warp anywhere.  A
-// lane's vectors of one unit inside one row form a group; for each group it
-// writes one record: the group's maximum g and s = sum over the group of
-// 2^((x - g) c) (s = -1 where the lane has no vector in that row of the unit).
-// A unit spans at most two rows, so the record slot is (unit, row parity,
-// lane).
-//
-// select_finalize_kernel (one CTA a row) reads a row's records: the row
-// maximum M is the largest g, the denominator S = sum of s 2^((g - M) c) (fp64
-// accumulation).  The row's k best elements lie in its k best groups by
-// (maximum desc, index of the maximum asc): were an element among the k best
-// in a group outside them, the k groups ahead of its group would each hold an
-// element that ranks before it.  So theta = the largest over warps of the
-// warp's k-th largest group maximum (k distinct groups reach it); the groups
-// whose maximum reaches theta are gathered, and their elements that reach it
-// merged into the k best by warp 0 (k rounds of a warp argmax).  The row's k
-// probabilities and tokens are stored; the CTA whose row is the last of its
-// request to arrive runs the path step of the request.
-
-constexpr int kStreamThreads = 256;
-constexpr int kStreamWarps = kStreamThreads / 32;
-constexpr int kStreamPerSm = 2;                   // CTAs a SM (the ring and the registers allow two)
-constexpr int kStreamStages = 3;                  // units in flight a lane
-constexpr int kStreamVpt = 8;                     // 16-byte vectors a lane holds of a unit
-constexpr int kUnitVecs = kStreamVpt * 32;        // vectors a unit
-constexpr int kStreamCand = 32;                   // candidate elements a warp buffers (one a lane)
-
-// 16-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing.
-__device__ __forceinline__ void stream_cp16(void* dst, const void* src, uint32_t src_bytes) {
-  const uint32_t d = uint32_t(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void stream_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Element q (0 <= q < E, a runtime value) of a 16-byte vector, by selects.
-template <typename T>
-__device__ __forceinline__ float vec_elem(const uint4& x, int q) {
-  if constexpr (sizeof(T) == 2) {
-    const uint32_t w = q < 4 ? (q < 2 ? x.x : x.y) : (q < 6 ? x.z : x.w);
-    return (q & 1) ? bf16_hi(w) : bf16_lo(w);
-  } else {
-    return __uint_as_float(q < 2 ? (q == 0 ? x.x : x.y) : (q == 2 ? x.z : x.w));
-  }
-}
-
-// A warp's k best so far (lane j < k holds entry j, best first; the other
-// lanes hold nothing) merged with the buffered candidates (lane l < ncand
-// holds buffer entry l): k rounds of a warp argmax over each lane's two
-// entries.  Element indices are unique within a row, so a winner is removed
-// by its index.
-__device__ __forceinline__ void stream_merge_candidates(const float* bv_s, const int* bi_s, int ncand, int k,
-                                                        float& lv_r, int& li_r) {
-  const int lane = threadIdx.x & 31;
-  __syncwarp();  // the lanes' appends are visible
-  float cv = lane < ncand ? bv_s[lane] : -INFINITY;
-  int ci = lane < ncand ? bi_s[lane] : INT_MAX;
-  float ev = lv_r;
-  int ei = li_r;
-  float nv = -INFINITY;
-  int ni = INT_MAX;
-  for (int j = 0; j < k; ++j) {
-    const bool c_first = better(cv, ci, ev, ei);
-    float bv = c_first ? cv : ev;
-    int bi = c_first ? ci : ei;
-    warp_argmax(bv, bi);
-    if (ci == bi) {
-      cv = -INFINITY;
-      ci = INT_MAX;
-    }
-    if (ei == bi) {
-      ev = -INFINITY;
-      ei = INT_MAX;
-    }
-    if (lane == j) {
-      nv = bv;
-      ni = bi;
-    }
-  }
-  lv_r = nv;
-  li_r = ni;
-  __syncwarp();  // every lane has read the buffer before it is refilled
-}
-
-// Two fp32 lanes in one 64-bit register: the packed FMA and add of sm_100
-// and later (each lane rounded as the scalar instruction rounds it).
-__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
-  float2 v;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-  return v;
-}
-__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// Per-vector maxima kept packed where the type allows it (bf16x2: both halves
-// of a vector's maximum), combined into the batch maximum; value() gives the
-// fp32 maximum.
-template <typename T>
-struct VecMax;
-template <>
-struct VecMax<uint16_t> {
-  using type = __nv_bfloat162;
-  __device__ static type of(const uint4& x) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
-    return __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
-  }
-  __device__ static type comb(type a, type b) { return __hmax2(a, b); }
-  __device__ static float value(type a) { return fmaxf(__low2float(a), __high2float(a)); }
-};
-template <>
-struct VecMax<float> {
-  using type = float;
-  __device__ static type of(const uint4& x) {
-    return fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)), fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)));
-  }
-  __device__ static type comb(type a, type b) { return fmaxf(a, b); }
-  __device__ static float value(type a) { return a; }
-};
-
-// Sum over the batch of 2^(x c - mc), two lanes at a time (packed FMA and
-// add, one ex2 an element).
-template <typename T>
-__device__ __forceinline__ float batch_exp_sum(const uint4 (&x)[kStreamVpt], float c, float mc) {
-  const unsigned long long c2 = f2_pack(c, c), nm2 = f2_pack(-mc, -mc);
-  unsigned long long acc = f2_pack(0.f, 0.f);
-#pragma unroll
-  for (int u = 0; u < kStreamVpt; ++u) {
-    const uint32_t wd[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-    if constexpr (sizeof(T) == 2) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 t = f2_unpack(f2_fma(f2_pack(bf16_lo(wd[j]), bf16_hi(wd[j])), c2, nm2));
-        acc = f2_add(acc, f2_pack(fast_exp2(t.x), fast_exp2(t.y)));
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; j += 2) {
-        const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(wd[j]), __uint_as_float(wd[j + 1])), c2, nm2));
-        acc = f2_add(acc, f2_pack(fast_exp2(t.x), fast_exp2(t.y)));
-      }
-    }
-  }
-  const float2 s = f2_unpack(acc);
-  return s.x + s.y;
-}
-
-// The record slot of (unit, row parity, lane).
-__device__ __forceinline__ int stream_slot(int unit, int parity, int lane) { return (unit * 2 + parity) * 32 + lane; }
-
-template <typename T>
-__global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) select_stream_kernel(SelectParams a) {
-  constexpr int E = LogitTraits<T>::kVec;  // elements per 16-byte vector
-  // ring: vector u of stage s of lane l of warp w at [((w * stages + s) * Vpt + u) * 32 + l]
-  extern __shared__ __align__(16) uint4 ring[];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const unsigned rowU = unsigned(a.V / E);
-  const unsigned U = unsigned(a.rows) * rowU;  // (the host keeps it below 2^31)
-  const int nu = a.stream_nb;                  // units in all
-  const float c = 1.4426950408889634f / a.temperature;
-  const uint4* src = static_cast<const uint4*>(a.logits);
-  float2* rec = reinterpret_cast<float2*>(a.partials);
-  uint4* wring = ring + w * (kStreamStages * kUnitVecs) + lane;
-
-  // Without overlap: wait for the grid before, then let the request step
-  // launch (it waits for this grid to finish before it reads a record).  With
-  // overlap the reads start at once and a lane waits before its first record
-  // write.
-  bool waited = !a.early;
-  if (waited) pdl_wait();
-  pdl_trigger();
-
-  // iteration j works on unit 2 * pair(j / 2) + (j & 1); pc = pair(j / 2), pn
-  // = pair(j / 2 + 1); lane 0 holds the queue's answer for pair(j / 2 + 2)
-  const int NW = gridDim.x * kStreamWarps, gw = blockIdx.x * kStreamWarps + w;
-  int pc = gw, pn = gw + NW, pending = 0;
-  if (lane == 0) pending = 2 * NW + int(atomicAdd(a.queue, 1u));
-  auto issue = [&](int j, int unit) {  // stage j % 3 <- unit (an empty group past the last unit)
-    if (unit < nu) {
-      uint4* st = wring + (unsigned(j) % kStreamStages) * kUnitVecs;
-      const unsigned o0 = unsigned(unit) * kUnitVecs + lane;
-      if (o0 + (kStreamVpt - 1) * 32 < U) {  // the whole unit exists
-#pragma unroll
-        for (int u = 0; u < kStreamVpt; ++u) stream_cp16(st + u * 32, src + o0 + u * 32, 16u);
-      } else {
-#pragma unroll
-        for (int u = 0; u < kStreamVpt; ++u) {
-          const unsigned o = o0 + u * 32;
-          const bool ok = o < U;
-          stream_cp16(st + u * 32, ok ? src + o : src, ok ? 16u : 0u);
-        }
-      }
-    }
-    stream_commit();
-  };
-  issue(0, 2 * pc);
-  issue(1, 2 * pc + 1);
-  for (int j = 0;; ++j) {
-    if (j >= 2 && !(j & 1)) {  // a new pair
-      pc = pn;
-      pn = __shfl_sync(0xffffffffu, pending, 0);
-      if (lane == 0) pending = 2 * NW + int(atomicAdd(a.queue, 1u));
-    }
-    const int unit = 2 * pc + (j & 1);
-    if (unit >= nu) break;  // (a warp's units only grow: every later one is past the end too)
-    issue(j + 2, 2 * pn + (j & 1));
-    stream_wait_group<kStreamStages - 1>();  // this lane's copies of unit j have landed
-    const uint4* st = wring + (unsigned(j) % kStreamStages) * kUnitVecs;
-    const unsigned b0 = unsigned(unit) * kUnitVecs;
-    const unsigned b1 = b0 + kUnitVecs < U ? b0 + kUnitVecs : U;
-    unsigned row = b0 / rowU;
-    unsigned cur = b0;
-    while (cur < b1) {  // the unit's vectors, one row at a time (at most two rows)
-      const unsigned re = (row + 1) * rowU;
-      const unsigned seg = b1 < re ? b1 : re;
-      uint4 x[kStreamVpt];
-      bool any = true;  // the group holds at least one vector
-      if (cur == b0 && seg == b0 + kUnitVecs) {  // the common case: the whole unit
-#pragma unroll
-        for (int u = 0; u < kStreamVpt; ++u) x[u] = st[u * 32];
-      } else {  // vectors outside the segment read as -inf
-        any = false;
-#pragma unroll
-        for (int u = 0; u < kStreamVpt; ++u) {
-          const unsigned o = b0 + u * 32 + lane;
-          const bool in = o >= cur && o < seg;
-          any = any || in;
-          x[u] = in ? st[u * 32] : VecOps<T>::neg_inf();
-        }
-      }
-      typename VecMax<T>::type gm = VecMax<T>::of(x[0]);
-#pragma unroll
-      for (int u = 1; u < kStreamVpt; ++u) gm = VecMax<T>::comb(gm, VecMax<T>::of(x[u]));
-      const float g = VecMax<T>::value(gm);
-      // (g = -inf: no element, or all -inf: every term is 0)
-      const float s = batch_exp_sum<T>(x, c, g > -INFINITY ? g * c : 0.f);
-      if (!waited) {
-        pdl_wait();
-        waited = true;
-      }
-      __stcg(&rec[stream_slot(unit, row & 1, lane)], make_float2(g, any ? s : -1.f));
-      cur = seg;
-      ++row;
-    }
-  }
-  stream_wait_group<0>();  // no copy of this lane is left in flight (the last groups are empty)
-}
+// The streaming select: the logits streaming pass (stream_records.cu: one
+// record, maximum and exp sum, a group of a lane's 8 vectors of a unit), then
+// select_finalize_kernel, one CTA a row.  From the row's records: the row
+// maximum M, the denominator S = sum of s 2^((g - M) c); theta = the largest
+// over warps of the k-th largest of the lanes' best group maxima (k distinct
+// groups reach it); among the groups that reach theta, v_k = the k-th largest
+// group maximum; the groups that reach v_k (ties kept) are reloaded and their
+// elements that reach it ranked (the k best elements lie in the k best groups).
+// The row's k probabilities and tokens are stored; the CTA whose row is the
+// last of its request to arrive runs the path step of the request.
 
 // The request step after the streaming kernel: one CTA a row.
 constexpr int kFinalizeThreads = 256;
 constexpr int kFinalizeWarps = kFinalizeThreads / 32;
-constexpr int kFinalizeMaxPer = 32;  // records a thread of the request step takes at most
 constexpr int kElemCap = 32 * 32;    // gathered elements the request step ranks directly
-
-// Maximum / sum over the CTA (scratch: a slot a warp); every thread gets the
-// result.  Both end with a barrier, so the scratch may be reused.
-__device__ __forceinline__ float block_max_f(float v, float* scratch) {
-  v = warp_max(v);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = scratch[0];
-  for (int i = 1; i < kFinalizeWarps; ++i) r = fmaxf(r, scratch[i]);
-  __syncthreads();
-  return r;
-}
-__device__ __forceinline__ float block_sum_f(float v, float* scratch) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = 0.f;
-  for (int i = 0; i < kFinalizeWarps; ++i) r += scratch[i];
-  __syncthreads();
-  return r;
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(SelectParams a) {
@@ -845,8 +564,8 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
       }
     }
   }
-  const float M = block_max_f(tm, s_f);
-  const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f);
+  const float M = block_max_f(tm, s_f, kFinalizeWarps);
+  const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f, kFinalizeWarps);
   // theta: the largest over warps of the k-th largest of the lanes' best group
   // maxima (k distinct groups reach it)
   {
@@ -1038,25 +757,6 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   counter_reset(a.counters + req);
 }
 
-// The streaming split: G CTAs (kStreamPerSm a SM) over the units.  None where
-// a row is shorter than a unit (a unit then could span more than two rows),
-// where the request step's threads would take more than kFinalizeMaxPer
-// records, or where the vector count reaches 2^31.
-StreamGeometry stream_geometry(long rows, int V, int vec, int sms) {
-  const long long rowU = V / vec;
-  if (rows < 1 || rowU < kUnitVecs) return StreamGeometry{0, 0, 0};
-  if ((rowU / kUnitVecs + 2) * 32 > (long long)kFinalizeMaxPer * kFinalizeThreads) return StreamGeometry{0, 0, 0};
-  const long long U = rows * rowU;
-  if (U >= (1LL << 31) - kUnitVecs) return StreamGeometry{0, 0, 0};
-  const long long nu = (U + kUnitVecs - 1) / kUnitVecs;
-  long long G = (long long)kStreamPerSm * sms;
-  const long long need = (nu + 2 * kStreamWarps - 1) / (2 * kStreamWarps);  // CTAs whose warps get a pair each
-  if (G > need) G = need;
-  if (G < 1) G = 1;
-  const size_t bytes = align256(size_t(nu) * 2 * 32 * sizeof(float2)) + align256(size_t(rows) * kMaxK * sizeof(float2));
-  return StreamGeometry{int(G), int(nu), bytes};
-}
-
 // Dynamic shared memory of the request step: a row's record maxima and indices.
 inline size_t finalize_smem(int V, int vec) {
   const long long rowU = V / vec;
@@ -1065,13 +765,20 @@ inline size_t finalize_smem(int V, int vec) {
 
 template <typename T>
 cudaError_t launch_stream(const SelectParams& p, cudaStream_t stream) {
-  constexpr size_t smem = size_t(kStreamWarps) * kStreamStages * kUnitVecs * 16;
-  cudaError_t e = cudaFuncSetAttribute(select_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(select_stream_kernel<T>, dim3(p.stream_ctas), dim3(kStreamThreads), smem, stream, p);
-  if (e != cudaSuccess) return e;
+  StreamRecParams r{};
+  r.logits = p.logits;
+  r.rows = p.rows;
+  r.V = p.V;
+  r.temperature = p.temperature;
+  r.temperatures = nullptr;
+  r.rows_per_temp = 1;
+  r.nu = p.stream_nb;
+  r.rec = reinterpret_cast<float2*>(p.partials);
+  r.queue = p.queue;
+  r.early = p.early;
+  if (launch_stream_records(r, p.stream_ctas, p.dtype, stream) != SPEC_OK) return cudaErrorLaunchFailure;
   const size_t fsmem = finalize_smem(p.V, LogitTraits<T>::kVec);
-  e = cudaFuncSetAttribute(select_finalize_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fsmem));
+  cudaError_t e = cudaFuncSetAttribute(select_finalize_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(fsmem));
   if (e != cudaSuccess) return e;
   return launch_pdl(select_finalize_kernel<T>, dim3(p.rows), dim3(kFinalizeThreads), fsmem, stream, p);
 }
@@ -1099,7 +806,11 @@ int launch_t(const SelectParams& p, cudaStream_t stream) {
 
 size_t select_partial_bytes(int rows, int chunks) { return align256(size_t(rows) * chunks * sizeof(SelPart)); }
 
-StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms) { return stream_geometry(rows, V, vec, sms); }
+StreamGeometry select_stream_geometry(long rows, int V, int vec, int sms) {
+  StreamGeometry g = stream_geometry(rows, V, vec, sms);
+  if (g.ctas > 0) g.bytes += align256(size_t(rows) * kMaxK * sizeof(float2));  // the rows' k best
+  return g;
+}
 
 int launch_select_topk(const SelectParams& p, cudaStream_t stream) {
   return p.dtype == SPEC_F32 ? launch_t<float>(p, stream) : launch_t<uint16_t>(p, stream);

@@ -29,6 +29,19 @@ inline bool vec_ok(const void* logits, int V, int dtype) {
   return aligned(logits, 16) && (size_t(V) * elem_bytes(dtype)) % 16 == 0;
 }
 
+// Pass 1 partials of the sampling accept over `rows` rows: the chunked
+// partials, or a row's statistics and the streaming pass's records.
+size_t sampling_pass1_bytes(long rows, int V) {
+  size_t bytes = sampling_partial_bytes(int(rows), chunk_bound(rows, V));
+  for (int vec : {4, 8}) {  // fp32 and bf16 rows
+    if (V % vec) continue;
+    const StreamGeometry g = stream_geometry(rows, V, vec, 152);  // (the records do not depend on the SM count)
+    const size_t s = g.ctas > 0 ? sampling_partial_bytes(int(rows), 1) + g.bytes : 0;
+    if (s > bytes) bytes = s;
+  }
+  return bytes;
+}
+
 // Greedy accept's per-chunk argmax partials.
 size_t greedy_part_bytes(int b, int n, int V) { return align256(size_t(b) * n * greedy_split(long(b) * n, V, 1).chunks * 8); }
 
@@ -80,7 +93,7 @@ size_t partial_bytes(int op, int b, int n, int k, int V, int Hq, int Hkv, int ma
       return attention_partial_bytes() + greedy_part_bytes(b, n, V);
     case SPEC_OP_VERIFY_SAMPLING:
     case SPEC_OP_VERIFY_TARGET_ONLY:
-      return sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V)) + sampling_state_bytes(b) +
+      return sampling_pass1_bytes(long(b) * n, V) + sampling_state_bytes(b) +
              sampling_partial2_bytes(b, terminal_split(V).chunks);
     case SPEC_OP_VERIFY_ATTENTION:
       return attention_partial_bytes();
@@ -652,10 +665,19 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
   p.chunks2 = s2.chunks;
   p.chunk2_elems = s2.chunk_elems;
   p.vec_ok = vec_ok(logits, V, dtype);
+  if (!probs && p.vec_ok) {  // logit rows of whole 16-byte vectors: the streaming pass, where it applies
+    const StreamGeometry g = stream_geometry(long(b) * n, V, vec_elems(dtype), device_sms());
+    if (g.ctas > 0) {
+      p.stream_ctas = g.ctas;
+      p.stream_nu = g.nb;
+      p.rec = reinterpret_cast<float2*>(v.partials + sampling_partial_bytes(b * n, 1));
+      p.queue = v.counters + sampling_queue_word(b);
+    }
+  }
   p.error = v.error;
   p.counters = v.counters;
   p.partials = v.partials;
-  p.state = v.partials + sampling_partial_bytes(b * n, chunk_bound(long(b) * n, V));
+  p.state = v.partials + sampling_pass1_bytes(long(b) * n, V);
   p.partials2 = p.state + sampling_state_bytes(b);
   return launch_verify_sampling(p, as_stream(stream));
 }

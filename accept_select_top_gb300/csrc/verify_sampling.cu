@@ -24,6 +24,7 @@
 // chunk where u_final * Z falls and the token inside it by an in-order scan.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "stream_records.cuh"
 
 namespace spec {
 
@@ -57,6 +58,9 @@ struct MassPart {
 
 // p of one token given the row statistics (T > 0).
 __device__ __forceinline__ float p_of(float l, float M, float T, float S) { return expf((l - M) / T) / S; }
+
+template <typename T, bool PROBS>
+__device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, float temp, bool soft, float c);
 
 // PROBS: the probabilities mode (a.probs given), a separate instantiation so
 // that the logit path carries none of its branches.
@@ -106,8 +110,15 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
   }
 
   if (!arrive_last(a.counters + req, uint32_t(a.n * a.chunks))) return;
+  sampling_walk<T, PROBS>(a, req, temp, soft, c);
+}
 
-  // ---- finalize request `req`: merge the row statistics, then walk ----
+// ---- the walk of request `req` (the CTA whose statistics arrived last) ----
+// Merges the request's row statistics (a.chunks partials a row), then walks
+// the tree; every thread of the CTA calls it.
+template <typename T, bool PROBS>
+__device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, float temp, bool soft, float c) {
+  using Tr = LogitTraits<T>;
   const int n = a.n, base = req * n, W = a.S + 1;
   __shared__ float rM[kMaxN], rS[kMaxN];
   __shared__ int rA[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
@@ -220,6 +231,79 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
     }
   }
   counter_reset(a.counters + req);
+}
+
+// Pass 1 on the streaming pass's records (stream_records.cu), one CTA a verify
+// row: the row maximum M, the softmax denominator S (soft rows) and the
+// argmax (the lowest index holding M, found by reloading the groups whose
+// maximum is M) as one chunk's statistics; the CTA whose row is the last of
+// its request to arrive walks the request.
+constexpr int kRowThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(SamplingParams a) {
+  constexpr int E = LogitTraits<T>::kVec;
+  __shared__ float s_f[kRowThreads / 32];
+  __shared__ int s_arg;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const int req = row / a.n;
+  const float temp = a.temperatures[req];
+  const bool soft = temp > 0.f;
+  const float c = soft ? 1.4426950408889634f / temp : 0.f;
+  if (row == 0 && tid == 0) *a.queue = 0u;  // the streaming grid is done with the queue: ready for the next call
+  if (tid == 0) s_arg = INT_MAX;
+  const RowRecords rr(row, a.V / E);
+  // this thread's records f = tid + 256 m, eight loads in flight: its maximum
+  // and its sum relative to it
+  float tm = -INFINITY, ts = 0.f;
+  for (int f0 = 0; f0 < rr.F; f0 += 8 * kRowThreads) {
+    float2 r[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int f = f0 + q * kRowThreads + tid;
+      r[q] = f < rr.F ? __ldcg(&a.rec[rr.slot(f)]) : make_float2(NAN, -1.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (r[q].y > 0.f) {  // (s = 0: the group is all -inf; s < 0: empty)
+        if (r[q].x > tm) {
+          ts = ts * fast_exp2((tm - r[q].x) * c) + r[q].y;
+          tm = r[q].x;
+        } else {
+          ts += r[q].y * fast_exp2((r[q].x - tm) * c);
+        }
+      }
+    }
+  }
+  const float M = block_max_f(tm, s_f, kRowThreads / 32);
+  const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f, kRowThreads / 32);
+  // the argmax: the first element equal to M in the groups whose maximum is M
+  const uint4* L = static_cast<const uint4*>(a.logits);
+  for (int f = tid; f < rr.F; f += kRowThreads) {
+    const float2 r = __ldcg(&a.rec[rr.slot(f)]);
+    if (r.y >= 0.f && r.x == M) {
+      const long long gv0 = rr.first_vec(f);
+      for (int u = 0; u < kStreamVpt; ++u) {
+        const long long gv = gv0 + u * 32;
+        if (gv < rr.rs || gv >= rr.rend) continue;
+        const uint4 x = __ldcg(L + gv);
+        int q = 0;
+        while (q < E && VecOps<T>::at(x, q) != M) ++q;
+        if (q < E) {
+          atomicMin(&s_arg, int((gv - rr.rs) * E) + q);
+          break;  // (later vectors of the group hold higher indices)
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) reinterpret_cast<StatPart*>(a.partials)[row] = StatPart{M, s_arg, S, 0.f};
+  if (!arrive_last(a.counters + req, uint32_t(a.n))) return;
+  SamplingParams a1 = a;
+  a1.chunks = 1;  // a row's statistics are one chunk's
+  sampling_walk<T, false>(a1, req, temp, soft, c);
 }
 
 // Compensated (Kahan) fp32 accumulation: the per-element work stays off the
@@ -534,6 +618,27 @@ size_t sampling_partial2_bytes(int b, int chunks2) { return align256(size_t(b) *
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
   dim3 g1(p.chunks, p.b * p.n), g2(p.chunks2, p.b);
   cudaError_t e;
+  if (!p.probs && p.stream_ctas > 0) {  // the streaming pass, then the row statistics and the walk
+    StreamRecParams r{};
+    r.logits = p.logits;
+    r.rows = p.b * p.n;
+    r.V = p.V;
+    r.temperatures = p.temperatures;
+    r.rows_per_temp = p.n;
+    r.nu = p.stream_nu;
+    r.rec = p.rec;
+    r.queue = p.queue;
+    r.early = false;
+    if (launch_stream_records(r, p.stream_ctas, p.dtype, stream) != SPEC_OK) return SPEC_ERR_LAUNCH;
+    if (p.dtype == SPEC_F32) {
+      e = launch_pdl(sampling_rowstats_kernel<float>, dim3(p.b * p.n), dim3(kRowThreads), 0, stream, p);
+      if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, false>, g2, dim3(kThreads), 0, stream, p);
+    } else {
+      e = launch_pdl(sampling_rowstats_kernel<uint16_t>, dim3(p.b * p.n), dim3(kRowThreads), 0, stream, p);
+      if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t, false>, g2, dim3(kThreads), 0, stream, p);
+    }
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  }
   if (p.probs) {  // fp32 probabilities
     e = launch_pdl(sampling_stats_kernel<float, true>, g1, dim3(kThreads), 0, stream, p);
     if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, true>, g2, dim3(kThreads), 0, stream, p);
