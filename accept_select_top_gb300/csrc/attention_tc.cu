@@ -259,9 +259,12 @@ __device__ __forceinline__ ReqInfo req_info(const AttentionParams& a, int r, boo
 }
 
 // Stream-K partition.  The units (request, kv head, 128-row tile) are laid
-// end to end in tile space, request by request; unit (r, j) has the tiles of
-// request r.  CTA c takes tiles [c*T/G, (c+1)*T/G) and cuts them into pieces,
-// one per unit it touches.
+// end to end in tile space, row tile outermost, then request, then kv head;
+// unit (mt, r, g) has the tiles of request r.  CTA c takes tiles [c*T/G,
+// (c+1)*T/G) and cuts them into pieces, one per unit it touches.  With the row
+// tile outermost, the units that read the same keys (same request and kv head,
+// other row tiles) sit T / m_tiles tiles apart, so CTAs that far apart read
+// those keys at about the same time and the second read finds them in L2.
 __host__ __device__ __forceinline__ long long cta_start(long long c, long long T, long long G) { return c * T / G; }
 // the CTA whose range holds tile x
 __host__ __device__ __forceinline__ int cta_of(long long x, long long T, long long G) {
@@ -275,19 +278,18 @@ struct Piece {
 };
 
 struct PieceIter {
-  int r, j, t0, idx;
+  int r, j, mt, t0, idx;  // j: the kv head
   long long cur, end;
   int nr, nlen, nrq;  // request nr's raw seq_len and pool row, loaded one piece ahead
   __device__ __forceinline__ bool next(const AttentionParams& a, int m_tiles, Piece& p, bool report) {
     if (cur >= end) return false;
-    const int upr = a.Hkv * m_tiles;
     const ReqInfo q = nr == r ? req_check(a, nlen, nrq, report && j == 0 && t0 == 0)
                               : req_info(a, r, report && j == 0 && t0 == 0);
     const long long left = end - cur;
     const int take = int(left < (long long)(q.tiles - t0) ? left : (long long)(q.tiles - t0));
     p.req = r;
-    p.g = j / m_tiles;
-    p.mt = j % m_tiles;
+    p.g = j;
+    p.mt = mt;
     p.t0 = t0;
     p.T = take;
     p.Tr = q.tiles;
@@ -302,9 +304,12 @@ struct PieceIter {
     t0 += take;
     if (t0 == q.tiles) {
       t0 = 0;
-      if (++j == upr) {
+      if (++j == a.Hkv) {
         j = 0;
-        ++r;
+        if (++r == a.b) {
+          r = 0;
+          ++mt;
+        }
       }
     }
     if (r != nr && cur < end) {  // the next piece's request: loads in flight meanwhile
@@ -403,16 +408,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncthreads();
     const long long T = scratch[16];
+    const long long TB = T / args.m_tiles;  // the tiles of one row tile over every request and kv head
     // Ge = min(grid, T) CTAs share the tiles, so every one of them has at
     // least one (a unit's pieces are then in consecutive CTAs); the others idle
     const long long Ge = T < gridDim.x ? T : gridDim.x;
     const bool part = blockIdx.x < Ge;
     const long long S = part ? cta_start(blockIdx.x, T, Ge) : 0, E = part ? cta_start(blockIdx.x + 1, T, Ge) : 0;
-    // the request holding tile S: chunks of blockDim requests, a block scan each
+    // the request holding tile S (at S' = S mod TB inside row tile S / TB):
+    // chunks of blockDim requests, a block scan each
+    const long long Sr = TB > 0 ? S % TB : 0;
     long long run = 0;
     for (int rb = 0; rb < a.b; rb += blockDim.x) {
       const int r = rb + threadIdx.x;
-      const long long v = r < a.b ? (long long)req_info(a, r, false).tiles * upr : 0;
+      const long long v = r < a.b ? (long long)req_info(a, r, false).tiles * a.Hkv : 0;
       long long incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -425,12 +433,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       long long before = run;
       for (int w = 0; w < warp; ++w) before += scratch[w];
       const long long excl = before + incl - v;
-      if (r < a.b && v > 0 && excl <= S && S < excl + v) {
-        const long long o = S - excl;  // offset inside request r
+      if (r < a.b && v > 0 && excl <= Sr && Sr < excl + v) {
+        const long long o = Sr - excl;  // offset inside request r
         const ReqInfo q = req_info(a, r, false);
         scratch[17] = r;
-        scratch[18] = o / q.tiles;  // unit within the request
+        scratch[18] = o / q.tiles;  // kv head
         scratch[19] = o % q.tiles;  // tile within the unit
+        scratch[23] = TB > 0 ? S / TB : 0;  // row tile
       }
       for (int w = 0; w < nwarps; ++w) run += scratch[w];
     }
@@ -451,6 +460,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     it.end = scratch[21];
     it.r = it.cur < it.end ? int(scratch[17]) : 0;
     it.j = it.cur < it.end ? int(scratch[18]) : 0;
+    it.mt = it.cur < it.end ? int(scratch[23]) : 0;
     it.t0 = it.cur < it.end ? int(scratch[19]) : 0;
     it.idx = 0;
     it.nr = -1;

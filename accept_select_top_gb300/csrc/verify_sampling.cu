@@ -59,7 +59,7 @@ struct MassPart {
 // p of one token given the row statistics (T > 0).
 __device__ __forceinline__ float p_of(float l, float M, float T, float S) { return expf((l - M) / T) / S; }
 
-template <typename T, bool PROBS>
+template <typename T, bool PROBS, int MAXCH = kMaxChunks>
 __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, float temp, bool soft, float c);
 
 // PROBS: the probabilities mode (a.probs given), a separate instantiation so
@@ -114,16 +114,17 @@ __global__ void __launch_bounds__(kThreads) sampling_stats_kernel(SamplingParams
 }
 
 // ---- the walk of request `req` (the CTA whose statistics arrived last) ----
-// Merges the request's row statistics (a.chunks partials a row), then walks
-// the tree; every thread of the CTA calls it.
-template <typename T, bool PROBS>
+// Merges the request's row statistics (a.chunks <= MAXCH partials a row),
+// then walks the tree; every thread of the CTA calls it.
+template <typename T, bool PROBS, int MAXCH>
 __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, float temp, bool soft, float c) {
   using Tr = LogitTraits<T>;
   const int n = a.n, base = req * n, W = a.S + 1;
   __shared__ float rM[kMaxN], rS[kMaxN];
-  __shared__ int rA[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1];
+  __shared__ int rA[kMaxN], tok[kMaxN], nt[kMaxN], ns[kMaxN], ri[kMaxN], pred[kMaxN], path[kMaxN + 1], par[kMaxN];
+  __shared__ float lgs[kMaxN], qxs[kMaxN], us[kMaxN];
   __shared__ int s_len, s_mode;
-  __shared__ float4 stage[kMaxN * kMaxChunks];
+  __shared__ float4 stage[kMaxN * MAXCH];  // (MAXCH: the most chunks a row of this caller has)
   // every (row, chunk) partial in one round of loads, through L2 (__ldcg)
   for (int t = threadIdx.x; t < n * a.chunks; t += blockDim.x)
     stage[t] = __ldcg(reinterpret_cast<const float4*>(
@@ -162,15 +163,42 @@ __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, 
     ns[t] = y;
     ri[t] = r;
     pred[t] = 0;
+    par[t] = -1;
+  }
+  __syncthreads();
+  // Every value the walk reads, loaded by all threads at once: node i's
+  // logit (or probability) and q at its parent's row and its token, and its
+  // coin.  The parent is taken from the children lists; the walk falls back to
+  // a direct load wherever it reaches a node from another parent (a malformed
+  // tree).
+  const T* L = static_cast<const T*>(a.logits);
+  for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    int ch = nt[t], guard = 0;
+    while (ch != -1 && guard++ < n) {
+      par[ch] = t;
+      ch = ns[ch];
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    const int pa = par[t], x = tok[t];
+    us[t] = a.u[base + t];
+    lgs[t] = 0.f;
+    qxs[t] = 0.f;
+    if (pa >= 0 && x >= 0 && x < a.V) {
+      const size_t prow = size_t(base + pa);
+      if (PROBS) lgs[t] = __ldg(a.probs + prow * a.V + x);
+      else if (soft) lgs[t] = Tr::load(L, prow * a.V + x);
+      if (!a.target_only) qxs[t] = __ldg(a.draft_probs + prow * a.V + x);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const T* L = static_cast<const T*>(a.logits);
     int cur = 0, ncd = 0, all_rejected = 0;
     path[0] = 0;
     // target-only: the coin of the node whose children are scanned (the
     // root's first, then each accepted child's own)
-    float coin = a.target_only ? a.u[base] : 0.f;
+    float coin = a.target_only ? us[0] : 0.f;
     for (int d = 0; d < a.S && ncd < n - 1; ++d) {  // bounded by the tree depth
       const size_t vrow = size_t(base + cur);
       const float* q = a.target_only ? nullptr : a.draft_probs + vrow * a.V;
@@ -184,16 +212,17 @@ __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, 
           c2 = ns[c2];
           continue;
         }
+        const bool pre = par[c2] == cur;  // the values loaded above are this node's at this row
         float px;
-        if (PROBS) px = __ldg(a.probs + vrow * a.V + x);  // the given distribution
-        else if (soft) px = p_of(Tr::load(L, vrow * a.V + x), rM[cur], temp, rS[cur]);
+        if (PROBS) px = pre ? lgs[c2] : __ldg(a.probs + vrow * a.V + x);  // the given distribution
+        else if (soft) px = p_of(pre ? lgs[c2] : Tr::load(L, vrow * a.V + x), rM[cur], temp, rS[cur]);
         else px = x == rA[cur] ? 1.f : 0.f;
         bool accept;
         if (a.target_only) {
           prob_acc = __fadd_rn(prob_acc, px);
           accept = px > 0.f && (coin < __fdiv_rn(prob_acc, a.thr_acc) || px >= a.thr_single);
         } else {
-          accept = __fmul_rn(a.u[base + c2], __ldg(q + x)) < px;
+          accept = __fmul_rn(us[c2], pre ? qxs[c2] : __ldg(q + x)) < px;
         }
         if (accept) {
           hit = c2;
@@ -208,7 +237,7 @@ __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, 
       pred[cur] = tok[hit];
       path[++ncd] = hit;
       cur = hit;
-      if (a.target_only) coin = a.u[base + hit];
+      if (a.target_only) coin = us[hit];
     }
     int mode = (soft || PROBS) ? (all_rejected ? (a.target_only ? 3 : 2) : 1) : 0;
     if (mode == 0) pred[cur] = rA[cur];
@@ -303,7 +332,7 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
   if (!arrive_last(a.counters + req, uint32_t(a.n))) return;
   SamplingParams a1 = a;
   a1.chunks = 1;  // a row's statistics are one chunk's
-  sampling_walk<T, false>(a1, req, temp, soft, c);
+  sampling_walk<T, false, 1>(a1, req, temp, soft, c);
 }
 
 // Compensated (Kahan) fp32 accumulation: the per-element work stays off the

@@ -188,10 +188,11 @@ def source_hash(paths):
 CSRC = "accept_select_top_gb300/csrc/"
 # the sources each group's kernels compile from (common.cuh: helpers inlined in every kernel)
 GROUP_SOURCES = {
-    "select": [CSRC + "select_topk.cu", CSRC + "common.cuh"],
+    "select": [CSRC + "select_topk.cu", CSRC + "stream_records.cu", CSRC + "stream_records.cuh", CSRC + "common.cuh"],
     "build": [CSRC + "build_tree.cu", CSRC + "common.cuh"],
     "attention": [CSRC + "attention_tc.cu", CSRC + "common.cuh"],
-    "accept": [CSRC + "verify_greedy.cu", CSRC + "verify_sampling.cu", CSRC + "common.cuh"],
+    "accept": [CSRC + "verify_greedy.cu", CSRC + "verify_sampling.cu", CSRC + "stream_records.cu",
+               CSRC + "stream_records.cuh", CSRC + "common.cuh"],
     "commit": [CSRC + "commit_kv.cu", CSRC + "common.cuh"],
 }
 
