@@ -273,6 +273,9 @@ struct StreamGeometry {
 };
 // Records of a row that a request step holds at most (shared memory).
 constexpr int kRowRecordsMax = 8192;
+// The select takes the streaming pass from this many bytes of logits a call
+// (measured crossover with the chunked kernel: about 30 MB on GB300).
+constexpr size_t kStreamMinBytes = size_t(32) << 20;
 // The streaming split of `rows` rows of V logits (vec per 16-byte vector) on a
 // device of `sms` SMs.
 StreamGeometry stream_geometry(long rows, int V, int vec, int sms);

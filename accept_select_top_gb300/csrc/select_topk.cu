@@ -490,9 +490,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
 // select_finalize_kernel, one CTA a row.  From the row's records: the row
 // maximum M, the denominator S = sum of s 2^((g - M) c); theta = the largest
 // over warps of the k-th largest of the lanes' best group maxima (k distinct
-// groups reach it); among the groups that reach theta, v_k = the k-th largest
-// group maximum; the groups that reach v_k (ties kept) are reloaded and their
-// elements that reach it ranked (the k best elements lie in the k best groups).
+// groups reach it, so the k best elements all do); the groups that reach
+// theta are reloaded, a vector a thread, and their elements that reach it
+// ranked by warp 0 (the k best elements lie in the k best groups).
 // The row's k probabilities and tokens are stored; the CTA whose row is the
 // last of its request to arrive runs the path step of the request.
 
@@ -515,7 +515,6 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   __shared__ int cand_i[kStreamCand];
   __shared__ float s_f[kFinalizeWarps];
   __shared__ int s_n, s_ne;
-  __shared__ float s_vk;
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -597,52 +596,8 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
     }
   }
   __syncthreads();
-  // v_k, the row's k-th largest group maximum, among the gathered (warp 0: k
-  // rounds of a warp argmax; lane l takes gathered entries l, l + 32, ...)
-  if (w == 0) {
-    const int n0 = s_n;
-    const int per = (n0 - lane + 31) / 32;
-    uint64_t taken = 0;
-    float vk = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = INT_MAX, bm = -1;
-      for (int m = 0; m < per && m < 64; ++m) {
-        const int f = gsel[lane + 32 * m];
-        if (!(taken & (1ull << m)) && better(gval[f], f, bv, bi)) {
-          bv = gval[f];
-          bi = f;
-          bm = m;
-        }
-      }
-      const int own = bi;
-      warp_argmax(bv, bi);
-      if (own == bi && bi != INT_MAX) taken |= 1ull << bm;
-      vk = bv;
-    }
-    if (lane == 0) {
-      // more than 2048 gathered (values tied at theta): theta itself stays the cut
-      s_vk = n0 <= 32 * 64 ? vk : theta;
-      s_n = 0;
-    }
-  }
-  __syncthreads();
-  const float vk = s_vk;  // k distinct groups reach it: the k best elements all do
-  // the groups that reach v_k (every group with that maximum: a tie keeps them all)
-  for (int m = 0; m < (F + kFinalizeThreads - 1) / kFinalizeThreads; ++m) {
-    const int f = tid + m * kFinalizeThreads;
-    const bool take = f < F && gval[f] >= vk;
-    const unsigned mask = __ballot_sync(0xffffffffu, take);
-    if (mask) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&s_n, __popc(mask));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (take) gsel[base + __popc(mask & lanes_below)] = f;
-    }
-  }
-  __syncthreads();
   const int ng = s_n;
-  // their elements that reach v_k: a vector a thread
+  // their elements that reach theta: a vector a thread
   for (int i = tid; i < ng * kStreamVpt; i += kFinalizeThreads) {
     const int f = gsel[i / kStreamVpt], u = i % kStreamVpt;
     const long long gv = (long long)(uf + f / 32) * kUnitVecs + f % 32 + u * 32;
@@ -651,7 +606,7 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
 #pragma unroll
       for (int q = 0; q < E; ++q) {
         const float v = VecOps<T>::at(x, q);
-        if (v >= vk) {
+        if (v >= theta) {
           const int pos = atomicAdd(&s_ne, 1);
           if (pos < kElemCap) {
             el_v[pos] = v;
@@ -690,9 +645,9 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
         }
       }
     } else {
-      // more than kElemCap elements reach v_k (values tied at the cut): the
+      // more than kElemCap elements reach theta (values tied at the cut): the
       // groups again, through the candidate buffer, 32 at a time
-      float theta = vk;
+      float cut = theta;
       int ncand = 0;
       for (int g0 = 0; g0 < ng; g0 += 32) {
         const int gi = g0 + lane;
@@ -716,7 +671,7 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
           uint32_t bits = 0;
           if (vin & (1u << u)) {
 #pragma unroll
-            for (int q = 0; q < E; ++q) bits |= (VecOps<T>::at(xv[u], q) >= theta ? 1u : 0u) << q;
+            for (int q = 0; q < E; ++q) bits |= (VecOps<T>::at(xv[u], q) >= cut ? 1u : 0u) << q;
           }
           for (;;) {  // one element a lane a round
             const unsigned mask = __ballot_sync(0xffffffffu, bits != 0u);
@@ -726,7 +681,7 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
               stream_merge_candidates(cand_v, cand_i, ncand, k, lv_r, li_r);
               ncand = 0;
               if (__shfl_sync(0xffffffffu, li_r, k - 1) != INT_MAX)  // the list holds k: a tighter bound
-                theta = fmaxf(theta, __shfl_sync(0xffffffffu, lv_r, k - 1));
+                cut = fmaxf(cut, __shfl_sync(0xffffffffu, lv_r, k - 1));
             }
             if (bits) {
               const int q = __ffs(bits) - 1;

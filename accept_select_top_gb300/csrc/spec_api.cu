@@ -502,7 +502,10 @@ int spec_select_topk(int step, int b, int k, int V, int dtype, const void* draft
   p.chunks = sp.chunks;
   p.chunk_elems = sp.chunk_elems;
   p.vec_ok = vec_ok(draft_logits, V, dtype);
-  if (p.vec_ok) {  // rows of whole 16-byte vectors: the streaming kernel, where a row is a batch or longer
+  // rows of whole 16-byte vectors, at least kStreamMinBytes of them: the
+  // streaming pass and the request step (below that the chunked kernel, one
+  // launch with its finalize inside, is faster)
+  if (p.vec_ok && size_t(p.rows) * size_t(V) * elem_bytes(dtype) >= kStreamMinBytes) {
     const StreamGeometry g = select_stream_geometry(p.rows, V, vec_elems(dtype), device_sms());
     p.stream_ctas = g.ctas;
     p.stream_nb = g.nb;

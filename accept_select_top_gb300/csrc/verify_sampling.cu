@@ -264,9 +264,10 @@ __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, 
 
 // Pass 1 on the streaming pass's records (stream_records.cu), one CTA a verify
 // row: the row maximum M, the softmax denominator S (soft rows) and the
-// argmax (the lowest index holding M, found by reloading the groups whose
-// maximum is M) as one chunk's statistics; the CTA whose row is the last of
-// its request to arrive walks the request.
+// argmax (the lowest index holding M, found by reloading, on each thread
+// whose records reach M, the first of its groups that does) as one chunk's
+// statistics; the CTA whose row is the last of its request to arrive walks
+// the request.
 constexpr int kRowThreads = 256;
 
 template <typename T>
@@ -286,7 +287,10 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
   const RowRecords rr(row, a.V / E);
   // this thread's records f = tid + 256 m, eight loads in flight: its maximum
   // and its sum relative to it
+  // (and tf, the first of its groups holding its maximum: its records run
+  // unit by unit, so that group's elements come first in the row)
   float tm = -INFINITY, ts = 0.f;
+  int tf = -1;
   for (int f0 = 0; f0 < rr.F; f0 += 8 * kRowThreads) {
     float2 r[8];
 #pragma unroll
@@ -300,6 +304,7 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
         if (r[q].x > tm) {
           ts = ts * fast_exp2((tm - r[q].x) * c) + r[q].y;
           tm = r[q].x;
+          tf = f0 + q * kRowThreads + tid;
         } else {
           ts += r[q].y * fast_exp2((r[q].x - tm) * c);
         }
@@ -308,27 +313,26 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
   }
   const float M = block_max_f(tm, s_f, kRowThreads / 32);
   const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f, kRowThreads / 32);
-  // the argmax: the first element equal to M in the groups whose maximum is M
+  // the argmax: the first element equal to M among the threads whose first
+  // group holding their maximum holds M
   const uint4* L = static_cast<const uint4*>(a.logits);
-  for (int f = tid; f < rr.F; f += kRowThreads) {
-    const float2 r = __ldcg(&a.rec[rr.slot(f)]);
-    if (r.y >= 0.f && r.x == M) {
-      const long long gv0 = rr.first_vec(f);
-      for (int u = 0; u < kStreamVpt; ++u) {
-        const long long gv = gv0 + u * 32;
-        if (gv < rr.rs || gv >= rr.rend) continue;
-        const uint4 x = __ldcg(L + gv);
-        int q = 0;
-        while (q < E && VecOps<T>::at(x, q) != M) ++q;
-        if (q < E) {
-          atomicMin(&s_arg, int((gv - rr.rs) * E) + q);
-          break;  // (later vectors of the group hold higher indices)
-        }
+  if (tf >= 0 && tm == M) {
+    const long long gv0 = rr.first_vec(tf);
+    for (int u = 0; u < kStreamVpt; ++u) {
+      const long long gv = gv0 + u * 32;
+      if (gv < rr.rs || gv >= rr.rend) continue;
+      const uint4 x = __ldcg(L + gv);
+      int q = 0;
+      while (q < E && VecOps<T>::at(x, q) != M) ++q;
+      if (q < E) {
+        atomicMin(&s_arg, int((gv - rr.rs) * E) + q);
+        break;  // (later vectors of the group hold higher indices)
       }
     }
   }
   __syncthreads();
-  if (tid == 0) reinterpret_cast<StatPart*>(a.partials)[row] = StatPart{M, s_arg, S, 0.f};
+  // (no group holds a finite value: every element is -inf, the first is the argmax)
+  if (tid == 0) reinterpret_cast<StatPart*>(a.partials)[row] = StatPart{M, s_arg == INT_MAX ? 0 : s_arg, S, 0.f};
   if (!arrive_last(a.counters + req, uint32_t(a.n))) return;
   SamplingParams a1 = a;
   a1.chunks = 1;  // a row's statistics are one chunk's

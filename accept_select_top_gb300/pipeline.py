@@ -168,22 +168,39 @@ class VerifyStep:
         return launches_per_step(self.wl, self.mode)
 
 
-def select_launches(wl: Workload) -> int:
-    """Kernels one spec_select_topk call launches: rows of whole 16-byte
-    vectors, at least one streaming unit (256 vectors) and at most 254 units
-    long (the buffers here are aligned), take the streaming kernel and its
-    request step; other rows the chunked kernel alone."""
+STREAM_MIN_BYTES = 32 << 20  # the select's streaming pass from this many bytes of logits a call
+
+
+def select_launches(wl: Workload, step: int) -> int:
+    """Kernels spec_select_topk launches at draft step `step`: rows of whole
+    16-byte vectors, at least one streaming unit (256 vectors) and at most 254
+    units long, and at least 32 MiB of logits in the call (the buffers here
+    are aligned), take the streaming pass and its request step; other calls
+    the chunked kernel alone."""
     elem = 4 if wl.logits_dtype == "f32" else 2
     vecs = wl.V * elem // 16
-    return 2 if (wl.V * elem) % 16 == 0 and 256 <= vecs and (vecs // 256 + 2) <= 256 else 1
+    rows = wl.b * (wl.k if step else 1)
+    ok = (wl.V * elem) % 16 == 0 and 256 <= vecs and (vecs // 256 + 2) <= 256
+    return 2 if ok and rows * wl.V * elem >= STREAM_MIN_BYTES else 1
+
+
+def sampling_launches(wl: Workload) -> int:
+    """Kernels the sampling accept launches: the streaming pass, the row
+    statistics and the terminal pass where its logit rows take the streaming
+    pass, else the chunked statistics pass and the terminal pass."""
+    elem = 4 if wl.logits_dtype == "f32" else 2
+    vecs = wl.V * elem // 16
+    ok = (wl.V * elem) % 16 == 0 and 256 <= vecs and (vecs // 256 + 2) <= 256
+    return 3 if ok else 2
 
 
 def launches_per_step(wl: Workload, mode: str) -> int:
     """Kernels one VerifyStep.run() launches: S selects, the tree build (the
     generic or the chain kernel), the attention (one launch: split key lists
-    are merged inside it), the accept (greedy one launch, sampling two passes)
-    and the KV commit."""
-    return wl.S * select_launches(wl) + 1 + 1 + (1 if mode == "greedy" else 2) + 1
+    are merged inside it), the accept (greedy one launch, sampling two or
+    three) and the KV commit."""
+    selects = sum(select_launches(wl, i) for i in range(wl.S))
+    return selects + 1 + 1 + (1 if mode == "greedy" else sampling_launches(wl)) + 1
 
 
 def _view_from(t: torch.Tensor, offset: int) -> torch.Tensor:

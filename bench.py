@@ -514,7 +514,7 @@ def measure_config(name, args, torch, device, seed, world, peaks, peaks_kind, he
     around them for the headline), the same steps with overlap allowed, the
     per-call pass, e2e and the CPU baseline."""
     from accept_select_top_gb300 import workloads as W
-    from accept_select_top_gb300.pipeline import launches_per_step, select_launches
+    from accept_select_top_gb300.pipeline import launches_per_step, sampling_launches, select_launches
     rank = int(os.environ.get("RANK", 0))
     wl = W.WORKLOADS[name]
     run = ConfigRun(wl, device, seed, torch, args.replicas)
@@ -562,8 +562,8 @@ def measure_config(name, args, torch, device, seed, world, peaks, peaks_kind, he
         roof.update({"traffic": None if tr is None else tr["dram_bytes_per_launch"], "kernel": dom,
                      "kernel_us": kernels[dom]["us"], "algorithmic_bytes": kernels[dom]["algorithmic_bytes"],
                      "peak_kind": kernels[dom]["peak_kind"],
-                     "launches": wl.S * select_launches(wl) if dom == "select" else
-                     (2 if dom == "accept" and run.mode == "sampling" else 1)})
+                     "launches": sum(select_launches(wl, i) for i in range(wl.S)) if dom == "select" else
+                     (sampling_launches(wl) if dom == "accept" and run.mode == "sampling" else 1)})
         if dom == "attention":
             roof["flops"] = flops
     e2e = None if args.no_e2e else run_e2e(args, torch, wl, run.mode, s0, run.stream, device)

@@ -80,17 +80,18 @@ def test_overlap_switch_host_only(lib):
 
 
 def test_launches_per_step_host_only():
-    """S selects (two launches each on rows of whole 16-byte vectors), the
-    tree build, one attention launch, the accept (two passes when sampling)
-    and the commit."""
+    """S selects (two launches each where a call streams at least 32 MiB of
+    whole 16-byte vectors), the tree build, one attention launch, the accept
+    (two or three when sampling) and the commit."""
     import dataclasses
     from accept_select_top_gb300 import workloads as W
     from accept_select_top_gb300.pipeline import launches_per_step
-    wl = W.WORKLOADS["llama8b_greedy"]
-    assert launches_per_step(wl, "greedy") == 2 * wl.S + 4
-    assert launches_per_step(wl, "sampling") == 2 * wl.S + 5
-    odd = dataclasses.replace(wl, V=wl.V + 1)  # bf16 rows of an odd length: the chunked select alone
-    assert launches_per_step(odd, "greedy") == wl.S + 4
+    wl = W.WORKLOADS["llama8b_greedy"]  # 8 MiB a select call: the chunked select
+    assert launches_per_step(wl, "greedy") == wl.S + 4
+    sh = W.WORKLOADS["sampling_heavy"]  # step 0: 8 MiB; later steps: 66 MB, streamed
+    assert launches_per_step(sh, "sampling") == 1 + 2 * (sh.S - 1) + 3 + 3
+    odd = dataclasses.replace(sh, V=sh.V + 1)  # bf16 rows of an odd length: chunked select and accept
+    assert launches_per_step(odd, "sampling") == sh.S + 3 + 2
 
 
 def test_host_argument_checks_without_gpu(lib):
