@@ -522,7 +522,6 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   const int rows_per_req = a.step ? k : 1;
   const int req = row / rows_per_req;
   const long long rowU = a.V / E;
-  const float c = 1.4426950408889634f / a.temperature;
   const float2* rec = reinterpret_cast<const float2*>(a.partials);
   const uint4* logits = static_cast<const uint4*>(a.logits);
   float2* best = reinterpret_cast<float2*>(a.partials + align256(size_t(a.stream_nb) * 2 * 32 * sizeof(float2)));
@@ -540,8 +539,9 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
 
   // one pass over the records (thread tid: f = tid + 256 m, eight loads in
   // flight): the maxima to shared memory, this thread's maximum and its sum
-  // relative to it (fp32: a chain of at most 32 additions here, 8 across the CTA)
-  float tm = -INFINITY, ts = 0.f;
+  // relative to it; the CTA's sum in fp64
+  const ExpScale sc(a.temperature);
+  RecSum rsum;
   for (int f0 = 0; f0 < F; f0 += 8 * kFinalizeThreads) {
     float2 r[8];
 #pragma unroll
@@ -553,18 +553,11 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
     for (int q = 0; q < 8; ++q) {
       const int f = f0 + q * kFinalizeThreads + tid;
       if (f < F) gval[f] = r[q].y >= 0.f ? r[q].x : NAN;
-      if (r[q].y > 0.f) {  // (s = 0: the group is all -inf)
-        if (r[q].x > tm) {
-          ts = ts * fast_exp2((tm - r[q].x) * c) + r[q].y;
-          tm = r[q].x;
-        } else {
-          ts += r[q].y * fast_exp2((r[q].x - tm) * c);
-        }
-      }
+      if (r[q].y > 0.f) rsum.add(r[q].x, r[q].y, sc);  // (s = 0: the group is all -inf)
     }
   }
-  const float M = block_max_f(tm, s_f, kFinalizeWarps);
-  const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f, kFinalizeWarps);
+  const float M = block_max_f(rsum.m, s_f, kFinalizeWarps);
+  const float S = block_sum_f(rsum.rel(M, sc), s_f, kFinalizeWarps);
   // theta: the largest over warps of the k-th largest of the lanes' best group
   // maxima (k distinct groups reach it)
   {

@@ -17,10 +17,18 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) stream_records_k
   const int nu = a.nu;                         // units in all
   const uint4* src = static_cast<const uint4*>(a.logits);
   float2* rec = a.rec;
-  // c = log2(e) / T of a row: one temperature, or one a request (T = 0: greedy, c = 0)
-  auto c_of = [&](unsigned row) {
-    const float temp = a.temperatures ? __ldg(a.temperatures + row / unsigned(a.rows_per_temp)) : a.temperature;
-    return temp > 0.f ? 1.4426950408889634f / temp : 0.f;
+  // c = log2(e) / T of a row: one temperature, or one a request (T = 0:
+  // greedy); formed again only when the row changes
+  unsigned sc_row = 0xffffffffu;
+  ExpScale sc;
+  bool soft = false;
+  auto scale_of = [&](unsigned row) {
+    if (row != sc_row) {
+      const float temp = a.temperatures ? __ldg(a.temperatures + row / unsigned(a.rows_per_temp)) : a.temperature;
+      soft = temp > 0.f;
+      sc = soft ? ExpScale(temp) : ExpScale();
+      sc_row = row;
+    }
   };
   uint4* wring = ring + w * (kStreamStages * kUnitVecs) + lane;
 
@@ -98,10 +106,10 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) stream_records_k
 #pragma unroll
       for (int u = 1; u < kStreamVpt; ++u) gm = VecMax<T>::comb(gm, VecMax<T>::of(x[u]));
       const float g = VecMax<T>::value(gm);
-      // (g = -inf: no element, or all -inf: every term is 0)
-      const float c = c_of(row);
-      // (a greedy row needs no sum: 1 marks the group as holding elements)
-      const float s = c > 0.f ? batch_exp_sum<T>(x, c, g > -INFINITY ? g * c : 0.f) : 1.f;
+      // (g = -inf: no element, or all -inf: every term is 0; a greedy row
+      // needs no sum: 1 marks the group as holding elements)
+      scale_of(row);
+      const float s = soft ? (g > -INFINITY ? batch_exp_sum<T>(x, sc, g) : 0.f) : 1.f;
       if (!waited) {
         pdl_wait();
         waited = true;

@@ -143,30 +143,61 @@ struct VecMax<float> {
   __device__ static float value(type a) { return a; }
 };
 
-// Sum over the batch of 2^(x c - mc), two lanes at a time (packed FMA and
-// add, one ex2 an element).
+// c = log2(e) / T as an unevaluated sum hi + lo, so that d * c for an exact
+// difference d = x - g rounds about once: the exponents of a row's terms
+// then carry no error proportional to the row maximum or to c's own
+// rounding, which over a 128K vocabulary would reach 1e-6 of the softmax
+// denominator.  Formed in fp32: log2(e) = E_HI + E_LO (two floats), hi =
+// E_HI / T rounded toward zero, its remainder E_HI - hi T exact by one FMA,
+// lo = (remainder + E_LO) / T.  hi <= c, so lo > 0: d = -inf then gives
+// -inf, not -inf + inf.
+struct ExpScale {
+  float hi, lo;
+  __device__ __forceinline__ ExpScale() : hi(0.f), lo(0.f) {}
+  __device__ __forceinline__ explicit ExpScale(float T) {
+    constexpr float kE_HI = 1.44269502162933349609375f;  // log2(e) rounded to fp32
+    constexpr float kE_LO = 1.9259629911e-08f;           // log2(e) - kE_HI
+    hi = __fdiv_rz(kE_HI, T);
+    const float rem = fmaf(-hi, T, kE_HI);
+    lo = __fdiv_rn(rem + kE_LO, T);
+  }
+  __device__ __forceinline__ float times(float d) const { return fmaf(d, hi, d * lo); }
+};
+
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Sum over the batch of 2^((x - g) c), two lanes at a time: x - g (exact for
+// bf16 values), times c as hi + lo, one ex2 an element, and the 64 (32) terms
+// added as a tree (depth 6), so that no long chain of roundings builds up.
 template <typename T>
-__device__ __forceinline__ float batch_exp_sum(const uint4 (&x)[kStreamVpt], float c, float mc) {
-  const unsigned long long c2 = f2_pack(c, c), nm2 = f2_pack(-mc, -mc);
-  unsigned long long acc = f2_pack(0.f, 0.f);
+__device__ __forceinline__ float batch_exp_sum(const uint4 (&x)[kStreamVpt], const ExpScale& sc, float g) {
+  const unsigned long long hi2 = f2_pack(sc.hi, sc.hi), lo2 = f2_pack(sc.lo, sc.lo), ng2 = f2_pack(-g, -g);
+  auto term = [&](float a, float b) {
+    const unsigned long long d = f2_add(f2_pack(a, b), ng2);
+    const float2 tt = f2_unpack(f2_fma(d, hi2, f2_mul(d, lo2)));
+    return f2_pack(fast_exp2(tt.x), fast_exp2(tt.y));
+  };
+  unsigned long long vs[kStreamVpt];
 #pragma unroll
   for (int u = 0; u < kStreamVpt; ++u) {
-    const uint32_t wd[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
     if constexpr (sizeof(T) == 2) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 t = f2_unpack(f2_fma(f2_pack(bf16_lo(wd[j]), bf16_hi(wd[j])), c2, nm2));
-        acc = f2_add(acc, f2_pack(fast_exp2(t.x), fast_exp2(t.y)));
-      }
+      const unsigned long long e0 = term(bf16_lo(x[u].x), bf16_hi(x[u].x)), e1 = term(bf16_lo(x[u].y), bf16_hi(x[u].y));
+      const unsigned long long e2 = term(bf16_lo(x[u].z), bf16_hi(x[u].z)), e3 = term(bf16_lo(x[u].w), bf16_hi(x[u].w));
+      vs[u] = f2_add(f2_add(e0, e1), f2_add(e2, e3));
     } else {
-#pragma unroll
-      for (int j = 0; j < 4; j += 2) {
-        const float2 t = f2_unpack(f2_fma(f2_pack(__uint_as_float(wd[j]), __uint_as_float(wd[j + 1])), c2, nm2));
-        acc = f2_add(acc, f2_pack(fast_exp2(t.x), fast_exp2(t.y)));
-      }
+      vs[u] = f2_add(term(__uint_as_float(x[u].x), __uint_as_float(x[u].y)),
+                     term(__uint_as_float(x[u].z), __uint_as_float(x[u].w)));
     }
   }
-  const float2 s = f2_unpack(acc);
+#pragma unroll
+  for (int w = kStreamVpt / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int u = 0; u < w; ++u) vs[u] = f2_add(vs[u], vs[u + w]);
+  const float2 s = f2_unpack(vs[0]);
   return s.x + s.y;
 }
 
@@ -190,6 +221,33 @@ struct RowRecords {
   __device__ __forceinline__ long long first_vec(int f) const { return (long long)(uf + f / 32) * kUnitVecs + f % 32; }
 };
 
+// A thread's running maximum m of records (g, s) and its sum relative to it,
+// sum of s 2^((g - m) c), compensated (Kahan) and rescaled when m grows.
+struct RecSum {
+  float m = -INFINITY, sum = 0.f, comp = 0.f;
+  __device__ __forceinline__ void add_term(float v) {
+    const float y = v - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+  }
+  __device__ __forceinline__ void add(float g, float s, const ExpScale& sc) {
+    if (g > m) {
+      const float f = m > -INFINITY ? fast_exp2(sc.times(m - g)) : 0.f;
+      sum *= f;
+      comp *= f;
+      m = g;
+      add_term(s);
+    } else {
+      add_term(s * fast_exp2(sc.times(g - m)));
+    }
+  }
+  // the sum relative to M (>= m)
+  __device__ __forceinline__ float rel(float M, const ExpScale& sc) const {
+    return sum > 0.f ? (sum - comp) * fast_exp2(sc.times(m - M)) : 0.f;
+  }
+};
+
 // Maximum / sum over a CTA of `nw` warps (scratch: a slot a warp); every
 // thread gets the result.  Both end with a barrier, so the scratch may be
 // reused.
@@ -206,8 +264,10 @@ __device__ __forceinline__ float block_sum_f(float v, float* scratch, int nw) {
   v = warp_sum(v);
   if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
   __syncthreads();
-  float r = 0.f;
-  for (int i = 0; i < nw; ++i) r += scratch[i];
+  // the warps' sums as a tree too (nw a power of two, at most 32)
+  float r = (threadIdx.x & 31) < nw ? scratch[threadIdx.x & 31] : 0.f;
+  for (int o = nw >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  r = __shfl_sync(0xffffffffu, r, 0);
   __syncthreads();
   return r;
 }

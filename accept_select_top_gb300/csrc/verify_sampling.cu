@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
   // and its sum relative to it
   // (and tf, the first of its groups holding its maximum: its records run
   // unit by unit, so that group's elements come first in the row)
-  float tm = -INFINITY, ts = 0.f;
+  const ExpScale sc = soft ? ExpScale(temp) : ExpScale();
+  RecSum rsum;
   int tf = -1;
   for (int f0 = 0; f0 < rr.F; f0 += 8 * kRowThreads) {
     float2 r[8];
@@ -301,18 +302,14 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       if (r[q].y > 0.f) {  // (s = 0: the group is all -inf; s < 0: empty)
-        if (r[q].x > tm) {
-          ts = ts * fast_exp2((tm - r[q].x) * c) + r[q].y;
-          tm = r[q].x;
-          tf = f0 + q * kRowThreads + tid;
-        } else {
-          ts += r[q].y * fast_exp2((r[q].x - tm) * c);
-        }
+        if (r[q].x > rsum.m) tf = f0 + q * kRowThreads + tid;
+        rsum.add(r[q].x, soft ? r[q].y : 0.f, sc);
       }
     }
   }
+  const float tm = rsum.m;
   const float M = block_max_f(tm, s_f, kRowThreads / 32);
-  const float S = block_sum_f(ts > 0.f ? ts * fast_exp2((tm - M) * c) : 0.f, s_f, kRowThreads / 32);
+  const float S = soft ? block_sum_f(rsum.rel(M, sc), s_f, kRowThreads / 32) : 0.f;
   // the argmax: the first element equal to M among the threads whose first
   // group holding their maximum holds M
   const uint4* L = static_cast<const uint4*>(a.logits);

@@ -103,25 +103,17 @@ SAMPLING_ACCEPT_RTOL = 2e-6
 SAMPLING_CDF_ATOL = 1e-6
 
 # The select's top-k probabilities p = exp((v - M)/T) / S against the
-# oracle's fp64 softmax.  The device sums S = sum 2^(x c - M c) in fp32: c =
-# log2(e)/T and M c are rounded to fp32 (together at most (|M c| + w) 2^-23 ln 2
-# of S, w the softmax-weighted mean of |x - M| c, both bounded below), each
-# term goes through the hardware ex2 (2^-22 relative) and the summation is a
-# chain of at most about 60 fp32 additions (a thread's packed pairs, its
-# batches of a row piece, the warp, the CTA and the pieces: 60 * 2^-24); the
-# numerator's expf adds at most 2 ulp.  With |M c| <= 32 and w <= 8 that is at
-# most 40 * 2^-23 * 0.7 + 2 * 2^-22 + 60 * 2^-24, about 7.4e-6, below the
-# bar.  A path score is one more fp32 product of p.
-SELECT_P_RTOL = 1e-5
+# oracle's fp64 softmax: the bar is 1e-6 relative.  The device keeps the
+# denominator's error systematic-free: each term's exponent is (x - g) c with
+# x - g exact (bf16) and c = log2(e)/T carried as hi + lo from fp64, so no
+# error proportional to the row maximum or to c's rounding enters (over a
+# 128K vocabulary, where most of the mass sits 10-15 binary orders below the
+# maximum, those alone reach 1e-6); each term then goes through the hardware
+# ex2 (2^-22 relative), a group's 64 terms are added as a tree, the groups of a
+# thread with compensation, and the CTA in fp64; the numerator is expf (2 ulp).
+# A path score is one more fp32 product of p.
+SELECT_P_RTOL = 1e-6
 SELECT_SCORE_RTOL = SELECT_P_RTOL + 2.0 ** -24
-SELECT_MC_BOUND = 32.0  # |M c| of the rows the bar is stated for
-
-
-def select_rows_within_bound(host_logits: np.ndarray, temperature: float = 1.0) -> bool:
-    """True when every row's |max| * log2(e) / T is within SELECT_MC_BOUND
-    (host_logits: fp32 values, or bf16 bits as uint16)."""
-    x = bf16_to_f64(host_logits) if host_logits.dtype == np.uint16 else host_logits.astype(np.float64)
-    return float(np.abs(x.max(axis=-1)).max()) * 1.4426950408889634 / temperature <= SELECT_MC_BOUND
 
 
 def sampling_divergence(lg_rows: np.ndarray, q_rows: np.ndarray, T: float, u: np.ndarray, u_final: float,

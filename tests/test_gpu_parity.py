@@ -13,7 +13,7 @@ import torch
 import oracle
 from accept_select_top_gb300 import workloads as W
 from tests.cases import (SELECT_P_RTOL, SELECT_SCORE_RTOL, bf16_to_f64, certified_topk_difference, make_case,
-                         sampling_divergence, select_rows_within_bound, target_only_divergence)
+                         sampling_divergence, target_only_divergence)
 
 pytestmark = pytest.mark.gpu
 
@@ -75,7 +75,6 @@ def test_select_topk_parity(cases, name):
         # the oracle on the same inputs (its own scores chain until the first divergence)
         o = oracle.select_topk(i, wl.b, wl.k, c.host_drafts[i], 1.0, None if scores_in is None else _np(scores_in))
         np.testing.assert_array_equal(_np(g["token_blk"]), o["token_blk"])
-        assert select_rows_within_bound(c.host_drafts[i])
         np.testing.assert_allclose(_np(g["topk_p"]), o["topk_p"], rtol=SELECT_P_RTOL, atol=0)
         np.testing.assert_allclose(_np(g["score_blk"]), o["score_blk"], rtol=SELECT_SCORE_RTOL, atol=0)
         if i == 0:
@@ -621,7 +620,6 @@ def test_ragged_vocab_select_and_greedy(V, dtype):
         g = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws)
         o = oracle.select_topk(i, wl.b, wl.k, c.host_drafts[i], 1.0, None if scores_in is None else _np(scores_in))
         np.testing.assert_array_equal(_np(g["token_blk"]), o["token_blk"])
-        assert select_rows_within_bound(c.host_drafts[i])
         np.testing.assert_allclose(_np(g["topk_p"]), o["topk_p"], rtol=SELECT_P_RTOL)
         scores_in = g["scores_out"]
     bufs = _accept_bufs(wl)
