@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   __shared__ int el_i[kElemCap];
   __shared__ float cand_v[kStreamCand];
   __shared__ int cand_i[kStreamCand];
-  __shared__ float s_f[kFinalizeWarps];
+  __shared__ float s_m[kFinalizeWarps], s_s[kFinalizeWarps], s_k[kFinalizeWarps];
   __shared__ int s_n, s_ne;
   pdl_wait();
   pdl_trigger();
@@ -536,6 +536,9 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
     s_n = 0;
     s_ne = 0;
   }
+  // the path step's parent score (lane f < k*k of warp 0: parent f / k), loaded
+  // now so that it is at hand at the end
+  const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
 
   // one pass over the records (thread tid: f = tid + 256 m, eight loads in
   // flight): the maxima to shared memory, this thread's maximum and its sum
@@ -556,27 +559,39 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
       if (r[q].y > 0.f) rsum.add(r[q].x, r[q].y, sc);  // (s = 0: the group is all -inf)
     }
   }
-  const float M = block_max_f(rsum.m, s_f, kFinalizeWarps);
-  const float S = block_sum_f(rsum.rel(M, sc), s_f, kFinalizeWarps);
-  // theta: the largest over warps of the k-th largest of the lanes' best group
-  // maxima (k distinct groups reach it)
+  // one barrier for the row maximum M, the denominator S and theta: per warp
+  // its maximum, its sum relative to it and the k-th largest of its lanes'
+  // best group maxima; theta = the largest of those (k distinct groups reach
+  // it, so the row's k best elements all do)
   {
-    float bv = -INFINITY;
-    for (int m = tid; m < F; m += kFinalizeThreads) bv = fmaxf(bv, gval[m]);
-    float wk = -INFINITY;
+    const float wm = warp_max(rsum.m);
+    const float ws = warp_sum(rsum.rel(wm, sc));
+    float v = rsum.m, wk = -INFINITY;
     for (int j = 0; j < k; ++j) {
-      float wv = bv;
+      float wv = v;
       int wi = lane;
       warp_argmax(wv, wi);
-      if (lane == wi) bv = -INFINITY;
+      if (lane == wi) v = -INFINITY;
       wk = wv;
     }
-    if (lane == 0) s_f[w] = wk;
+    if (lane == 0) {
+      s_m[w] = wm;
+      s_s[w] = ws;
+      s_k[w] = wk;
+    }
   }
   __syncthreads();
-  float theta = -INFINITY;
-  for (int i = 0; i < kFinalizeWarps; ++i) theta = fmaxf(theta, s_f[i]);
-  // the groups that reach theta
+  float M = -INFINITY, theta = -INFINITY;
+  for (int i = 0; i < kFinalizeWarps; ++i) {
+    M = fmaxf(M, s_m[i]);
+    theta = fmaxf(theta, s_k[i]);
+  }
+  float S = 0.f;
+  for (int i = 0; i < kFinalizeWarps; ++i)
+    if (s_s[i] > 0.f) S += s_s[i] * fast_exp2(sc.times(s_m[i] - M));
+  // the groups that reach theta, listed (gsel), then reloaded a vector a
+  // thread (every load of the phase in flight at once); their elements that
+  // reach theta
   for (int m = 0; m < (F + kFinalizeThreads - 1) / kFinalizeThreads; ++m) {
     const int f = tid + m * kFinalizeThreads;
     const bool take = f < F && gval[f] >= theta;
@@ -590,7 +605,6 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   }
   __syncthreads();
   const int ng = s_n;
-  // their elements that reach theta: a vector a thread
   for (int i = tid; i < ng * kStreamVpt; i += kFinalizeThreads) {
     const int f = gsel[i / kStreamVpt], u = i % kStreamVpt;
     const long long gv = (long long)(uf + f / 32) * kUnitVecs + f % 32 + u * 32;
@@ -639,7 +653,7 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
       }
     } else {
       // more than kElemCap elements reach theta (values tied at the cut): the
-      // groups again, through the candidate buffer, 32 at a time
+      // listed groups again, through the candidate buffer, 32 at a time
       float cut = theta;
       int ncand = 0;
       for (int g0 = 0; g0 < ng; g0 += 32) {
@@ -694,7 +708,6 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   }
   // the last row of the request to arrive runs the path step
   if (!arrive_last(a.counters + req, uint32_t(rows_per_req))) return;
-  const float sc_in = (a.step > 0 && w == 0 && lane < kk) ? a.scores_in[size_t(req) * k + lane / k] : 0.f;
   for (int i = tid; i < rows_per_req * k; i += kFinalizeThreads) {
     const float2 v = __ldcg(&best[(size_t(req) * rows_per_req + i / k) * kMaxK + i % k]);
     p_s[i / k][i % k] = v.x;

@@ -248,28 +248,4 @@ struct RecSum {
   }
 };
 
-// Maximum / sum over a CTA of `nw` warps (scratch: a slot a warp); every
-// thread gets the result.  Both end with a barrier, so the scratch may be
-// reused.
-__device__ __forceinline__ float block_max_f(float v, float* scratch, int nw) {
-  v = warp_max(v);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = scratch[0];
-  for (int i = 1; i < nw; ++i) r = fmaxf(r, scratch[i]);
-  __syncthreads();
-  return r;
-}
-__device__ __forceinline__ float block_sum_f(float v, float* scratch, int nw) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  // the warps' sums as a tree too (nw a power of two, at most 32)
-  float r = (threadIdx.x & 31) < nw ? scratch[threadIdx.x & 31] : 0.f;
-  for (int o = nw >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-  r = __shfl_sync(0xffffffffu, r, 0);
-  __syncthreads();
-  return r;
-}
-
 }  // namespace spec

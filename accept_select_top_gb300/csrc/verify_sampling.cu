@@ -273,7 +273,7 @@ constexpr int kRowThreads = 256;
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(SamplingParams a) {
   constexpr int E = LogitTraits<T>::kVec;
-  __shared__ float s_f[kRowThreads / 32];
+  __shared__ float s_m[kRowThreads / 32], s_s[kRowThreads / 32];
   __shared__ int s_arg;
   pdl_wait();
   pdl_trigger();
@@ -308,8 +308,21 @@ __global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(Sampling
     }
   }
   const float tm = rsum.m;
-  const float M = block_max_f(tm, s_f, kRowThreads / 32);
-  const float S = soft ? block_sum_f(rsum.rel(M, sc), s_f, kRowThreads / 32) : 0.f;
+  // one barrier for M and S: per warp its maximum and its sum relative to it
+  {
+    const float wm = warp_max(tm);
+    const float ws = warp_sum(rsum.rel(wm, sc));
+    if ((tid & 31) == 0) {
+      s_m[tid >> 5] = wm;
+      s_s[tid >> 5] = ws;
+    }
+  }
+  __syncthreads();
+  float M = -INFINITY, S = 0.f;
+  for (int i = 0; i < kRowThreads / 32; ++i) M = fmaxf(M, s_m[i]);
+  if (soft)
+    for (int i = 0; i < kRowThreads / 32; ++i)
+      if (s_s[i] > 0.f) S += s_s[i] * fast_exp2(sc.times(s_m[i] - M));
   // the argmax: the first element equal to M among the threads whose first
   // group holding their maximum holds M
   const uint4* L = static_cast<const uint4*>(a.logits);
@@ -538,33 +551,48 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   __syncthreads();
   __shared__ int s_chunk, s_use_res, s_fallback;
   __shared__ double s_before, s_target;
-  if (threadIdx.x == 0) {
-    double zr = 0.0, zp = 0.0;
-    int lr = -1, lp = -1;
-    for (int ch = 0; ch < a.chunks2; ++ch) {
-      zr += s_res[ch];
-      zp += s_p[ch];
-      lr = max(lr, s_lr[ch]);
-      lp = max(lp, s_lp[ch]);
+  if (w == 0) {
+    // warp 0: lane l holds chunks 2l and 2l + 1 (kMaxChunks2 = 64); inclusive
+    // prefix sums of the lanes' pairs (fp64) give each chunk's running mass
+    const int c0 = 2 * lane, c1 = c0 + 1;
+    const double r0 = c0 < a.chunks2 ? s_res[c0] : 0.0, r1 = c1 < a.chunks2 ? s_res[c1] : 0.0;
+    const double p0 = c0 < a.chunks2 ? s_p[c0] : 0.0, p1 = c1 < a.chunks2 ? s_p[c1] : 0.0;
+    double sr = r0 + r1, sp = p0 + p1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double yr = __shfl_up_sync(0xffffffffu, sr, o), yp = __shfl_up_sync(0xffffffffu, sp, o);
+      if (lane >= o) {
+        sr += yr;
+        sp += yp;
+      }
     }
+    const double zr = __shfl_sync(0xffffffffu, sr, 31), zp = __shfl_sync(0xffffffffu, sp, 31);
+    int lr = max(c0 < a.chunks2 ? s_lr[c0] : -1, c1 < a.chunks2 ? s_lr[c1] : -1);
+    int lp = max(c0 < a.chunks2 ? s_lp[c0] : -1, c1 < a.chunks2 ? s_lp[c1] : -1);
+    lr = __reduce_max_sync(0xffffffffu, lr);
+    lp = __reduce_max_sync(0xffffffffu, lp);
     const int use_res = (st.mode == 2 || st.mode == 3) && zr > 0.0;
     const double Z = use_res ? zr : zp;
     const double target = double(a.u_final[req]) * Z;
-    double acc = 0.0;
-    int found = -1;
-    for (int ch = 0; ch < a.chunks2; ++ch) {
-      const double m = use_res ? s_res[ch] : s_p[ch];
-      if (target < acc + m) {
-        found = ch;
-        break;
+    // the first chunk whose running mass passes the target
+    const double m0 = use_res ? r0 : p0, m1 = use_res ? r1 : p1;
+    const double before = (use_res ? sr : sp) - m0 - m1;  // the mass of the chunks ahead of this lane's
+    const int hit = c0 < a.chunks2 && target < before + m0 ? c0 : (c1 < a.chunks2 && target < before + m0 + m1 ? c1 : -1);
+    const unsigned lanes = __ballot_sync(0xffffffffu, hit >= 0);
+    if (lanes == 0u) {
+      if (lane == 0) {
+        s_chunk = -1;
+        s_before = use_res ? zr : zp;
       }
-      acc += m;
+    } else if (lane == __ffs(lanes) - 1) {
+      s_chunk = hit;
+      s_before = hit == c0 ? before : before + m0;
     }
-    s_chunk = found;
-    s_use_res = use_res;
-    s_before = acc;
-    s_target = target;
-    s_fallback = use_res ? lr : lp;
+    if (lane == 0) {
+      s_use_res = use_res;
+      s_target = target;
+      s_fallback = use_res ? lr : lp;
+    }
   }
   __syncthreads();
   __shared__ int s_bonus;
