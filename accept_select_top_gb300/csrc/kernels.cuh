@@ -135,6 +135,9 @@ struct SamplingParams {
   int chunks, chunk_elems;    // pass 1 split of a verify row
   int chunks2, chunk2_elems;  // pass 2 split of the terminal row
   bool vec_ok;
+  // pass 2 may read a thread's 16 tokens (logits and q) with 16-byte loads:
+  // logits mode, V % 16 == 0, 16-byte aligned rows
+  bool vec_term;
   // the streaming pass (logit rows of whole 16-byte vectors): stream_ctas
   // CTAs over stream_nu units, records rec; 0: the chunked pass 1
   int stream_ctas, stream_nu;

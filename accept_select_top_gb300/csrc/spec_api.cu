@@ -668,6 +668,8 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
   p.chunks2 = s2.chunks;
   p.chunk2_elems = s2.chunk_elems;
   p.vec_ok = vec_ok(logits, V, dtype);
+  p.vec_term = !probs && V % 16 == 0 && s2.chunk_elems % 16 == 0 && aligned(logits, 16) &&
+               (target_only || aligned(draft_probs, 16));
   if (!probs && p.vec_ok) {  // logit rows of whole 16-byte vectors: the streaming pass, where it applies
     const StreamGeometry g = stream_geometry(long(b) * n, V, vec_elems(dtype), device_sms());
     if (g.ctas > 0) {

@@ -452,6 +452,52 @@ __device__ __forceinline__ void chunk_mass(const SamplingParams& a, const ReqSta
   ps = double(kp.sum) - double(kp.comp);
 }
 
+// As chunk_mass, for logit rows of whole 16-token vectors (a.vec_term):
+// thread t takes the 16 consecutive tokens [begin + 16 t, + 16) with 16-byte
+// loads (two or four of logits, four of q).  The chunk's tokens come in
+// whole 16-token vectors (V % 16 == 0).
+template <typename T>
+__device__ __forceinline__ void chunk_mass_vec(const SamplingParams& a, const ReqState& st, const Excluded& ex,
+                                               int begin, int end, double& res, double& ps, int& last_res,
+                                               int& last_p) {
+  constexpr int E = LogitTraits<T>::kVec;
+  const int v0 = begin + kTermPer * int(threadIdx.x);
+  const TermP tp(st, false);
+  Kahan kr, kp;
+  if (v0 < end) {
+    const uint4* lrow = reinterpret_cast<const uint4*>(static_cast<const T*>(a.logits) + size_t(st.row) * a.V + v0);
+    uint4 lx[kTermPer / E];
+#pragma unroll
+    for (int j = 0; j < kTermPer / E; ++j) lx[j] = __ldg(lrow + j);
+    float4 qx[kTermPer / 4];
+    if (st.mode == 2) {
+      const float4* qrow = reinterpret_cast<const float4*>(a.draft_probs + size_t(st.row) * a.V + v0);
+#pragma unroll
+      for (int j = 0; j < kTermPer / 4; ++j) qx[j] = __ldg(qrow + j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kTermPer / 4; ++j) qx[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kTermPer; ++u) {
+      const int v = v0 + u;
+      const float l = VecOps<T>::at(lx[u / E], u % E);
+      const float4 q4 = qx[u / 4];
+      const float qv = (u & 3) == 0 ? q4.x : (u & 3) == 1 ? q4.y : (u & 3) == 2 ? q4.z : q4.w;
+      const float p = tp.p(l);
+      float r = 0.f;
+      if (st.mode == 2) r = p > qv ? p - qv : 0.f;
+      else if (st.mode == 3) r = ex.has(v, begin) ? 0.f : p;
+      kr.add(r);
+      kp.add(p);
+      if (r > 0.f) last_res = v;
+      if (p > 0.f) last_p = v;
+    }
+  }
+  res = double(kr.sum) - double(kr.comp);
+  ps = double(kp.sum) - double(kp.comp);
+}
+
 template <typename T, bool PROBS>
 __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams a) {
   pdl_wait();
@@ -506,7 +552,12 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   }
   double res = 0.0, ps = 0.0;
   int last_res = -1, last_p = -1;
-  chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
+  if constexpr (!PROBS) {
+    if (a.vec_term) chunk_mass_vec<T>(a, st, ex, begin, end, res, ps, last_res, last_p);
+    else chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
+  } else {
+    chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
+  }
   __shared__ double sres[kThreads / 32], sps[kThreads / 32];
   __shared__ int slr[kThreads / 32], slp[kThreads / 32];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
