@@ -139,9 +139,9 @@ struct SamplingParams {
   // logits mode, V % 16 == 0, 16-byte aligned rows
   bool vec_term;
   // the streaming pass (logit rows of whole 16-byte vectors): stream_ctas
-  // CTAs over stream_nu units, records rec; 0: the chunked pass 1
+  // CTAs over stream_nu units, unit summaries usum; 0: the chunked pass 1
   int stream_ctas, stream_nu;
-  float2* rec;
+  float2* usum;
   uint32_t* queue;
   uint32_t* error;
   uint32_t* counters;
@@ -266,7 +266,8 @@ struct StreamRecParams {
   int rows_per_temp;
   int nu;                     // units
   int cu;                     // units a queue answer hands out (set by launch_stream_records)
-  float2* rec;                // records [nu][2 row parities][32 lanes]
+  float2* rec;                // records [nu][2 row parities][32 lanes], or null
+  float2* usum;               // unit summaries [nu][2 row parities], or null
   uint32_t* queue;            // the unit queue (0 at launch)
   bool early;                 // reads may start before the grid before is done
 };

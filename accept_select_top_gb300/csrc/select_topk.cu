@@ -205,29 +205,32 @@ __device__ __forceinline__ void write_request(const SelectParams& a, int req, in
     }
     if (a.parent_blk)
       for (int j = threadIdx.x; j <= k; j += blockDim.x) a.parent_blk[size_t(req) * a.parent_ld + j] = j - 1;
-  } else if (w == 0 && kk <= 32) {
-    // lane f: expansion f = (parent f / k, its j = f % k); rank among the k*k
-    // by shuffles
-    const bool on = lane < kk;
-    const float ex = on ? __fmul_rn(sc_in, p_s[lane / k][lane % k]) : -INFINITY;
-    const int id = on ? id_s[lane / k][lane % k] : 0;
-    if (on) {
-      a.score_blk[sb + lane] = ex;
-      a.token_blk[sb + lane] = id;
-    }
-    int rank = 0;
+  } else if (kk <= 32) {
+    if (w == 0) {
+      // lane f: expansion f = (parent f / k, its j = f % k); rank among the
+      // k*k by shuffles
+      const bool on = lane < kk;
+      const float ex = on ? __fmul_rn(sc_in, p_s[lane / k][lane % k]) : -INFINITY;
+      const int id = on ? id_s[lane / k][lane % k] : 0;
+      if (on) {
+        a.score_blk[sb + lane] = ex;
+        a.token_blk[sb + lane] = id;
+      }
+      int rank = 0;
 #pragma unroll
-    for (int g = 0; g < 32; ++g) {  // all lanes shuffle; lanes past k*k hold -inf
-      const float o = __shfl_sync(0xffffffffu, ex, g);
-      rank += (g < kk && better(o, g, ex, lane)) ? 1 : 0;
-    }
-    if (on && rank < k) {
-      if (a.parent_blk) a.parent_blk[size_t(req) * a.parent_ld + rank] = lane + kk * (a.step - 1) + k;
-      a.scores_out[size_t(req) * k + rank] = ex;
-      a.next_ids[size_t(req) * k + rank] = id;
+      for (int g = 0; g < 32; ++g) {  // all lanes shuffle; lanes past k*k hold -inf
+        const float o = __shfl_sync(0xffffffffu, ex, g);
+        rank += (g < kk && better(o, g, ex, lane)) ? 1 : 0;
+      }
+      if (on && rank < k) {
+        if (a.parent_blk) a.parent_blk[size_t(req) * a.parent_ld + rank] = lane + kk * (a.step - 1) + k;
+        a.scores_out[size_t(req) * k + rank] = ex;
+        a.next_ids[size_t(req) * k + rank] = id;
+      }
     }
   } else {
-    // more than 32 expansions: one a thread of the CTA (k*k <= 256)
+    // more than 32 expansions: one a thread of the CTA (k*k <= 256); every
+    // thread of the CTA takes this branch, so the barrier is the CTA's
     __shared__ float ex[kMaxK * kMaxK];
     for (int f = threadIdx.x; f < kk; f += blockDim.x) {
       ex[f] = __fmul_rn(a.scores_in[size_t(req) * k + f / k], p_s[f / k][f % k]);

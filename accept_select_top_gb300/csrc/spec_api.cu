@@ -675,7 +675,7 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
     if (g.ctas > 0) {
       p.stream_ctas = g.ctas;
       p.stream_nu = g.nb;
-      p.rec = reinterpret_cast<float2*>(v.partials + sampling_partial_bytes(b * n, 1));
+      p.usum = reinterpret_cast<float2*>(v.partials + sampling_partial_bytes(b * n, 1));
       p.queue = v.counters + sampling_queue_word(b);
     }
   }

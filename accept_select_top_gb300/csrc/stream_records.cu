@@ -114,7 +114,12 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) stream_records_k
         pdl_wait();
         waited = true;
       }
-      __stcg(&rec[stream_slot(unit, row & 1, lane)], make_float2(g, any ? s : -1.f));
+      if (rec) __stcg(&rec[stream_slot(unit, row & 1, lane)], make_float2(g, any ? s : -1.f));
+      if (a.usum) {  // the unit summary of this row: over its groups, the maximum and the sum relative to it
+        const float gu = warp_max(g);
+        const float su = warp_sum(any && s > 0.f ? s * fast_exp2(sc.times(g - gu)) : 0.f);
+        if (lane == 0) __stcg(&a.usum[unit * 2 + (row & 1)], make_float2(gu, su));
+      }
       cur = seg;
       ++row;
     }

@@ -15,7 +15,10 @@
 // s = sum over the group of 2^((x - g) c), c = log2(e) / T of the row (s = -1
 // where the lane has no vector in that row of the unit; s = 1 in a greedy
 // row, T = 0, which needs no sum).  A unit spans at most two rows, so the record slot
-// is (unit, row parity, lane).
+// is (unit, row parity, lane).  On request the warp also writes a unit
+// summary a row it touches: over the unit's groups of that row, the maximum gu
+// and the sum of s 2^((g - gu) c) (a warp maximum and a warp sum); a caller
+// that needs only those writes no records.
 //
 // From a row's records: the row maximum is the largest g, the softmax
 // denominator sum of s 2^((g - M) c); and the row's k best elements lie in its
@@ -203,23 +206,6 @@ __device__ __forceinline__ float batch_exp_sum(const uint4 (&x)[kStreamVpt], con
 
 // The record slot of (unit, row parity, lane).
 __device__ __forceinline__ int stream_slot(int unit, int parity, int lane) { return (unit * 2 + parity) * 32 + lane; }
-
-// The records of row `row` (of rows of rowU vectors): flat index f = (unit -
-// first unit) * 32 + lane over the units the row touches.
-struct RowRecords {
-  int uf, F, par;
-  long long rs, rend;  // the row's vectors
-  __device__ __forceinline__ RowRecords(int row, long long rowU) {
-    rs = (long long)row * rowU;
-    rend = rs + rowU;
-    uf = int(rs / kUnitVecs);
-    F = (int((rend - 1) / kUnitVecs) - uf + 1) * 32;
-    par = row & 1;
-  }
-  __device__ __forceinline__ int slot(int f) const { return stream_slot(uf + f / 32, par, f % 32); }
-  // the first vector of group f (its vectors: + 32 u, those inside [rs, rend))
-  __device__ __forceinline__ long long first_vec(int f) const { return (long long)(uf + f / 32) * kUnitVecs + f % 32; }
-};
 
 // A thread's running maximum m of records (g, s) and its sum relative to it,
 // sum of s 2^((g - m) c), compensated (Kahan) and rescaled when m grows.

@@ -262,88 +262,83 @@ __device__ __forceinline__ void sampling_walk(const SamplingParams& a, int req, 
   counter_reset(a.counters + req);
 }
 
-// Pass 1 on the streaming pass's records (stream_records.cu), one CTA a verify
-// row: the row maximum M, the softmax denominator S (soft rows) and the
-// argmax (the lowest index holding M, found by reloading, on each thread
-// whose records reach M, the first of its groups that does) as one chunk's
-// statistics; the CTA whose row is the last of its request to arrive walks
-// the request.
-constexpr int kRowThreads = 256;
+// Pass 1 on the streaming pass's unit summaries (stream_records.cu), one
+// warp a verify row, the CTAs of a request holding only its rows (rpc =
+// min(8, n) rows a CTA): the row maximum M (the largest unit maximum), the
+// softmax denominator S = sum of su 2^((gu - M) c) (soft rows) and, for a
+// greedy row, the argmax (the lowest index holding M: in the first unit whose
+// maximum is M, reloaded) as one chunk's statistics; the CTA whose rows are
+// the last of its request to arrive walks the request.
+constexpr int kRowWarpsMax = 8;
+constexpr int kSumPer = kRowRecordsMax / 32 / 32;  // unit summaries a lane reads (a row spans <= 256 units)
 
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads) sampling_rowstats_kernel(SamplingParams a) {
+__global__ void __launch_bounds__(32 * kRowWarpsMax, 1) sampling_rowstats_kernel(SamplingParams a) {
   constexpr int E = LogitTraits<T>::kVec;
-  __shared__ float s_m[kRowThreads / 32], s_s[kRowThreads / 32];
-  __shared__ int s_arg;
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const int req = row / a.n;
+  const int rpc = int(blockDim.x) >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cpr = (a.n + rpc - 1) / rpc;  // CTAs a request
+  const int req = blockIdx.x / cpr, rin = (blockIdx.x % cpr) * rpc + w;
   const float temp = a.temperatures[req];
   const bool soft = temp > 0.f;
   const float c = soft ? 1.4426950408889634f / temp : 0.f;
-  if (row == 0 && tid == 0) *a.queue = 0u;  // the streaming grid is done with the queue: ready for the next call
-  if (tid == 0) s_arg = INT_MAX;
-  const RowRecords rr(row, a.V / E);
-  // this thread's records f = tid + 256 m, eight loads in flight: its maximum
-  // and its sum relative to it
-  // (and tf, the first of its groups holding its maximum: its records run
-  // unit by unit, so that group's elements come first in the row)
-  const ExpScale sc = soft ? ExpScale(temp) : ExpScale();
-  RecSum rsum;
-  int tf = -1;
-  for (int f0 = 0; f0 < rr.F; f0 += 8 * kRowThreads) {
-    float2 r[8];
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.queue = 0u;  // the streaming grid is done with the queue: ready for the next call
+  if (rin < a.n) {
+    const int row = req * a.n + rin;
+    const long long rowU = a.V / E;
+    const long long rs = (long long)row * rowU, rend = rs + rowU;  // the row's vectors
+    const int uf = int(rs / kUnitVecs), nun = int((rend - 1) / kUnitVecs) - uf + 1;
+    const int par = row & 1;
+    // lane l: units l, l + 32, ... (all loads in flight)
+    float2 us[kSumPer];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int f = f0 + q * kRowThreads + tid;
-      r[q] = f < rr.F ? __ldcg(&a.rec[rr.slot(f)]) : make_float2(NAN, -1.f);
+    for (int t = 0; t < kSumPer; ++t) {
+      const int m = lane + 32 * t;
+      us[t] = m < nun ? __ldcg(&a.usum[(uf + m) * 2 + par]) : make_float2(-INFINITY, 0.f);
     }
+    const ExpScale sc = soft ? ExpScale(temp) : ExpScale();
+    RecSum rsum;
+    float lm = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (r[q].y > 0.f) {  // (s = 0: the group is all -inf; s < 0: empty)
-        if (r[q].x > rsum.m) tf = f0 + q * kRowThreads + tid;
-        rsum.add(r[q].x, soft ? r[q].y : 0.f, sc);
+    for (int t = 0; t < kSumPer; ++t) {
+      lm = fmaxf(lm, us[t].x);
+      if (soft && us[t].y > 0.f) rsum.add(us[t].x, us[t].y, sc);  // (0: the unit's part of the row is all -inf)
+    }
+    const float M = warp_max(lm);
+    const float S = soft ? warp_sum(rsum.rel(M, sc)) : 0.f;
+    int arg = 0;  // (every element -inf: the first is the argmax)
+    if (!soft && M > -INFINITY) {
+      // the first unit whose maximum is M, then its first element equal to M
+      int mf = INT_MAX;
+#pragma unroll
+      for (int t = kSumPer - 1; t >= 0; --t)
+        if (lane + 32 * t < nun && us[t].x == M) mf = lane + 32 * t;
+      mf = __reduce_min_sync(0xffffffffu, mf);
+      const uint4* L = static_cast<const uint4*>(a.logits);
+      uint4 x[kStreamVpt];
+      bool in[kStreamVpt];
+#pragma unroll
+      for (int u = 0; u < kStreamVpt; ++u) {
+        const long long gv = (long long)(uf + mf) * kUnitVecs + lane + u * 32;
+        in[u] = gv >= rs && gv < rend;
+        x[u] = in[u] ? __ldcg(L + gv) : make_uint4(0u, 0u, 0u, 0u);
       }
-    }
-  }
-  const float tm = rsum.m;
-  // one barrier for M and S: per warp its maximum and its sum relative to it
-  {
-    const float wm = warp_max(tm);
-    const float ws = warp_sum(rsum.rel(wm, sc));
-    if ((tid & 31) == 0) {
-      s_m[tid >> 5] = wm;
-      s_s[tid >> 5] = ws;
-    }
-  }
-  __syncthreads();
-  float M = -INFINITY, S = 0.f;
-  for (int i = 0; i < kRowThreads / 32; ++i) M = fmaxf(M, s_m[i]);
-  if (soft)
-    for (int i = 0; i < kRowThreads / 32; ++i)
-      if (s_s[i] > 0.f) S += s_s[i] * fast_exp2(sc.times(s_m[i] - M));
-  // the argmax: the first element equal to M among the threads whose first
-  // group holding their maximum holds M
-  const uint4* L = static_cast<const uint4*>(a.logits);
-  if (tf >= 0 && tm == M) {
-    const long long gv0 = rr.first_vec(tf);
-    for (int u = 0; u < kStreamVpt; ++u) {
-      const long long gv = gv0 + u * 32;
-      if (gv < rr.rs || gv >= rr.rend) continue;
-      const uint4 x = __ldcg(L + gv);
-      int q = 0;
-      while (q < E && VecOps<T>::at(x, q) != M) ++q;
-      if (q < E) {
-        atomicMin(&s_arg, int((gv - rr.rs) * E) + q);
-        break;  // (later vectors of the group hold higher indices)
+      int first = INT_MAX;
+#pragma unroll
+      for (int u = kStreamVpt - 1; u >= 0; --u) {  // (later vectors hold higher indices)
+        if (!in[u]) continue;
+        const long long gv = (long long)(uf + mf) * kUnitVecs + lane + u * 32;
+#pragma unroll
+        for (int q = E - 1; q >= 0; --q)
+          if (VecOps<T>::at(x[u], q) == M) first = int((gv - rs) * E) + q;
       }
+      arg = __reduce_min_sync(0xffffffffu, first);
+      if (arg == INT_MAX) arg = 0;  // (not reached: the unit holds its maximum)
     }
+    if (lane == 0) reinterpret_cast<StatPart*>(a.partials)[row] = StatPart{M, arg, S, 0.f};
   }
-  __syncthreads();
-  // (no group holds a finite value: every element is -inf, the first is the argmax)
-  if (tid == 0) reinterpret_cast<StatPart*>(a.partials)[row] = StatPart{M, s_arg == INT_MAX ? 0 : s_arg, S, 0.f};
-  if (!arrive_last(a.counters + req, uint32_t(a.n))) return;
+  if (!arrive_last(a.counters + req, uint32_t(cpr))) return;
   SamplingParams a1 = a;
   a1.chunks = 1;  // a row's statistics are one chunk's
   sampling_walk<T, false, 1>(a1, req, temp, soft, c);
@@ -735,15 +730,18 @@ int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
     r.temperatures = p.temperatures;
     r.rows_per_temp = p.n;
     r.nu = p.stream_nu;
-    r.rec = p.rec;
+    r.rec = nullptr;  // the row statistics need only the unit summaries
+    r.usum = p.usum;
     r.queue = p.queue;
     r.early = false;
     if (launch_stream_records(r, p.stream_ctas, p.dtype, stream) != SPEC_OK) return SPEC_ERR_LAUNCH;
+    const int rpc = p.n < kRowWarpsMax ? p.n : kRowWarpsMax;  // rows a CTA
+    const dim3 gr(p.b * ((p.n + rpc - 1) / rpc)), br(32 * rpc);
     if (p.dtype == SPEC_F32) {
-      e = launch_pdl(sampling_rowstats_kernel<float>, dim3(p.b * p.n), dim3(kRowThreads), 0, stream, p);
+      e = launch_pdl(sampling_rowstats_kernel<float>, gr, br, 0, stream, p);
       if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, false>, g2, dim3(kThreads), 0, stream, p);
     } else {
-      e = launch_pdl(sampling_rowstats_kernel<uint16_t>, dim3(p.b * p.n), dim3(kRowThreads), 0, stream, p);
+      e = launch_pdl(sampling_rowstats_kernel<uint16_t>, gr, br, 0, stream, p);
       if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t, false>, g2, dim3(kThreads), 0, stream, p);
     }
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;

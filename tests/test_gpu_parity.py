@@ -592,6 +592,69 @@ def test_back_to_back_calls_on_one_workspace(cases):
         assert torch.equal(getattr(twice, k_), getattr(once, k_)), k_
 
 
+def test_back_to_back_streamed_selects(cases):
+    """Overlap allowed, the streaming select (66 MB calls): three selects of
+    one step enqueued back to back with no synchronisation (the second on the
+    other half of the select's area, the third on the first one's half again,
+    so it must not start before the first has finished).  Every call's outputs
+    equal those of a call run alone on a fresh workspace."""
+    c = cases("sampling_heavy", "greedy")
+    wl, ops = c.wl, _ops()
+    size = ops.spec_workspace_size(ops.OP_SELECT_TOPK, wl.b, wl.n, wl.k, wl.V)
+    ws = ops.Workspace(size)
+    ws.set_overlap(True)
+    runs, scores_in = [], None
+    for i in range(wl.S):
+        runs.append([_gpu_select_step(wl, i, c.drafts[i], scores_in, ws) for _ in range(3)])
+        scores_in = runs[-1][0]["scores_out"]
+    torch.cuda.synchronize()
+    assert ws.last_error() == 0
+    ws_ref, scores_in = ops.Workspace(size), None
+    for i, trio in enumerate(runs):
+        ref = _gpu_select_step(wl, i, c.drafts[i], scores_in, ws_ref)
+        torch.cuda.synchronize()
+        for j, got in enumerate(trio):
+            for k_, v in ref.items():
+                assert torch.equal(got[k_], v), (i, j, k_)
+        scores_in = ref["scores_out"]
+
+
+def test_select_streamed_ties_and_masked_rows():
+    """A streamed select (256 rows of 128256 bf16 logits, 66 MB) whose rows
+    test the row step's fast path and leave it: logits on a coarse grid
+    (ties at a row's maximum; in row 4 about 170 of them), a constant row,
+    and rows with fewer finite logits than k (-inf elsewhere).  Tokens are bit-exact with the
+    oracle (equal logits rank by lowest index), probabilities within the
+    softmax bar, and the path step bit-exact on the GPU's own probabilities."""
+    import dataclasses
+    ops = _ops()
+    wl = dataclasses.replace(W.WORKLOADS["sampling_heavy"])
+    b, k, V = wl.b, wl.k, wl.V
+    gen = torch.Generator().manual_seed(11)
+    x = torch.round(torch.randn(b * k, V, generator=gen) * 1.5) / 2
+    x[0] = 0.0
+    x[1] = -float("inf")
+    x[1, torch.tensor([5, 77777, V - 1])] = torch.tensor([1.0, 3.0, -2.0])
+    x[2] = -float("inf")
+    x[2, ::6000] = torch.round(torch.randn(x[2, ::6000].shape, generator=gen) * 4) / 4
+    x[3, : V // 2] = -float("inf")
+    x[4] = torch.round(torch.randn(V, generator=gen) * 0.5) / 2
+    logits = x.to(torch.bfloat16).cuda()
+    scores_in = (torch.rand(b, k, generator=gen) * 0.5 + 0.1).cuda()
+    ws = ops.Workspace(ops.spec_workspace_size(ops.OP_SELECT_TOPK, b, wl.n, k, V))
+    g = _gpu_select_step(wl, 1, logits, scores_in, ws)
+    torch.cuda.synchronize()
+    assert ws.last_error() == 0
+    o = oracle.select_topk(1, b, k, W.host(logits), 1.0, _np(scores_in))
+    np.testing.assert_array_equal(_np(g["token_blk"]), o["token_blk"])
+    np.testing.assert_allclose(_np(g["topk_p"]), o["topk_p"], rtol=SELECT_P_RTOL, atol=0)
+    ids = _np(g["token_blk"]).reshape(b * k, k)
+    ch = oracle.path_step(1, b, k, _np(g["topk_p"]), ids, _np(scores_in))
+    for k_ in ("score_blk", "parent_blk", "scores_out"):
+        np.testing.assert_array_equal(_np(g[k_]), ch[k_], err_msg=k_)
+    np.testing.assert_array_equal(_np(g["next_ids"]).reshape(b, k), ch["next_ids"])
+
+
 # ------------------------------------------------------------- edge cases
 
 def test_idle_batch_and_bad_workspace():
