@@ -134,6 +134,7 @@ struct SamplingParams {
   int32_t* next_root;
   int chunks, chunk_elems;    // pass 1 split of a verify row
   int chunks2, chunk2_elems;  // pass 2 split of the terminal row
+  int term_ctas;              // pass 2 CTAs a request (each takes chunks term_ctas apart)
   bool vec_ok;
   // pass 2 may read a thread's 16 tokens (logits and q) with 16-byte loads:
   // logits mode, V % 16 == 0, 16-byte aligned rows

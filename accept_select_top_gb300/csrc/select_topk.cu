@@ -499,6 +499,32 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
 // The row's k probabilities and tokens are stored; the CTA whose row is the
 // last of its request to arrive runs the path step of the request.
 
+// The value of rank k - 1 among the nt (<= 32 NS) slots top[0, nt) by (value
+// desc, slot asc), for every lane of the warp: lane l ranks slots l + 32 i by
+// counting, in one pass over the slots.
+template <int NS>
+__device__ __forceinline__ float kth_slot(const float* top, int nt, int k) {
+  const int lane = threadIdx.x & 31;
+  float v[NS];
+  int rank[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    v[i] = lane + 32 * i < nt ? top[lane + 32 * i] : -INFINITY;
+    rank[i] = 0;
+  }
+#pragma unroll 8
+  for (int o = 0; o < nt; ++o) {
+    const float u = top[o];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) rank[i] += (u > v[i] || (u == v[i] && o < lane + 32 * i)) ? 1 : 0;
+  }
+  float th = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NS; ++i)
+    if (lane + 32 * i < nt && rank[i] == k - 1) th = v[i];
+  return warp_max(th);  // (one slot has rank k - 1)
+}
+
 // The request step after the streaming kernel: one CTA a row.
 constexpr int kFinalizeThreads = 256;
 constexpr int kFinalizeWarps = kFinalizeThreads / 32;
@@ -516,7 +542,8 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
   __shared__ int el_i[kElemCap];
   __shared__ float cand_v[kStreamCand];
   __shared__ int cand_i[kStreamCand];
-  __shared__ float s_m[kFinalizeWarps], s_s[kFinalizeWarps], s_k[kFinalizeWarps];
+  __shared__ float s_m[kFinalizeWarps], s_s[kFinalizeWarps];
+  __shared__ float s_top[kFinalizeWarps * kMaxK];  // each warp's k best lane maxima: [w * k + j]
   __shared__ int s_n, s_ne;
   pdl_wait();
   pdl_trigger();
@@ -563,47 +590,62 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
     }
   }
   // one barrier for the row maximum M, the denominator S and theta: per warp
-  // its maximum, its sum relative to it and the k-th largest of its lanes'
-  // best group maxima; theta = the largest of those (k distinct groups reach
-  // it, so the row's k best elements all do)
+  // its maximum, its sum relative to it and its k best lane maxima
   {
     const float wm = warp_max(rsum.m);
     const float ws = warp_sum(rsum.rel(wm, sc));
-    float v = rsum.m, wk = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-      float wv = v;
-      int wi = lane;
-      warp_argmax(wv, wi);
-      if (lane == wi) v = -INFINITY;
-      wk = wv;
-    }
+    // the lanes' maxima sorted descending across the warp (a bitonic sort,
+    // 15 exchange steps): lane j < k then holds the j-th largest
+    float v = rsum.m;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+        const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+        v = desc == lower ? fmaxf(v, o) : fminf(v, o);
+      }
+    if (lane < k) s_top[w * k + lane] = v;
     if (lane == 0) {
       s_m[w] = wm;
       s_s[w] = ws;
-      s_k[w] = wk;
     }
   }
   __syncthreads();
-  float M = -INFINITY, theta = -INFINITY;
-  for (int i = 0; i < kFinalizeWarps; ++i) {
-    M = fmaxf(M, s_m[i]);
-    theta = fmaxf(theta, s_k[i]);
-  }
+  float M = -INFINITY;
+  for (int i = 0; i < kFinalizeWarps; ++i) M = fmaxf(M, s_m[i]);
   float S = 0.f;
   for (int i = 0; i < kFinalizeWarps; ++i)
     if (s_s[i] > 0.f) S += s_s[i] * fast_exp2(sc.times(s_m[i] - M));
-  // the groups that reach theta, listed (gsel), then reloaded a vector a
-  // thread (every load of the phase in flight at once); their elements that
-  // reach theta
-  for (int m = 0; m < (F + kFinalizeThreads - 1) / kFinalizeThreads; ++m) {
-    const int f = tid + m * kFinalizeThreads;
-    const bool take = f < F && gval[f] >= theta;
-    const unsigned mask = __ballot_sync(0xffffffffu, take);
-    if (mask) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&s_n, __popc(mask));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (take) gsel[base + __popc(mask & lanes_below)] = f;
+  // theta = the k-th largest lane maximum of the CTA (the k best are among
+  // the warps' k best; k distinct groups reach it, so the row's k best
+  // elements all do): each warp ranks the nt = 8 k slots by counting, by
+  // (value desc, slot asc) -- lane l holds slots l + 32 i, one pass over the
+  // slots -- and takes the value of rank k - 1
+  const int nt = kFinalizeWarps * k;
+  const float theta = nt <= 32 ? kth_slot<1>(s_top, nt, k) : nt <= 64 ? kth_slot<2>(s_top, nt, k) : kth_slot<4>(s_top, nt, k);
+  // the groups that reach theta, listed (gsel: one shared atomic a warp),
+  // then reloaded a vector a thread (every load of the phase in flight at
+  // once); their elements that reach theta
+  {
+    const int nm = (F + kFinalizeThreads - 1) / kFinalizeThreads;
+    int cnt = 0;
+    for (int m = 0; m < nm; ++m) {
+      const int f = tid + m * kFinalizeThreads;
+      cnt += (f < F && gval[f] >= theta) ? 1 : 0;
+    }
+    int inc = cnt;  // inclusive scan over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&s_n, inc);
+    int pos = __shfl_sync(0xffffffffu, base, 31) + inc - cnt;
+    for (int m = 0; m < nm; ++m) {
+      const int f = tid + m * kFinalizeThreads;
+      if (f < F && gval[f] >= theta) gsel[pos++] = f;
     }
   }
   __syncthreads();
@@ -631,7 +673,23 @@ __global__ void __launch_bounds__(kFinalizeThreads, 1) select_finalize_kernel(Se
     const int ne = s_ne;
     float lv_r = -INFINITY;  // lane j < k: entry j of the row's k best
     int li_r = INT_MAX;
-    if (ne <= kElemCap) {
+    if (ne <= 32) {
+      // one element a lane, ranked by counting the elements ahead of it
+      // (indices are unique); the entries of rank < k to their slots
+      const float v = lane < ne ? el_v[lane] : -INFINITY;
+      const int i = lane < ne ? el_i[lane] : INT_MAX;
+      int rank = 0;
+      for (int o = 0; o < ne; ++o) rank += better(el_v[o], el_i[o], v, i) ? 1 : 0;
+      if (lane < ne && rank < k) {
+        cand_v[rank] = v;
+        cand_i[rank] = i;
+      }
+      __syncwarp();
+      if (lane < k && lane < ne) {
+        lv_r = cand_v[lane];
+        li_r = cand_i[lane];
+      }
+    } else if (ne <= kElemCap) {
       // k rounds of a warp argmax over the gathered elements (lane l: entries l, l + 32, ...)
       uint32_t taken = 0;
       const int per = (ne - lane + 31) / 32;

@@ -667,6 +667,14 @@ int sampling_call(bool target_only, int b, int n, int S, int V, int dtype, const
   p.chunk_elems = s1.chunk_elems;
   p.chunks2 = s2.chunks;
   p.chunk2_elems = s2.chunk_elems;
+  {  // terminal-pass CTAs a request: a CTA a chunk up to four waves of two
+     // CTAs a SM; past that one wave, each CTA looping over its chunks
+     // (measured: 32 requests x 32 chunks faster as 1024 CTAs, 256 x 32
+     // as 512)
+    const long wave = 2L * device_sms();
+    const long per = long(b) * s2.chunks <= 4 * wave ? s2.chunks : (wave + b - 1) / b;
+    p.term_ctas = int(per < 1 ? 1 : per > s2.chunks ? s2.chunks : per);
+  }
   p.vec_ok = vec_ok(logits, V, dtype);
   p.vec_term = !probs && V % 16 == 0 && s2.chunk_elems % 16 == 0 && aligned(logits, 16) &&
                (target_only || aligned(draft_probs, 16));

@@ -19,9 +19,10 @@
 // terminal from p, 2 = sample it from the residual max(0, p - q), 3 = sample
 // it from p without the terminal node's rejected children (target-only:
 // relu(p - buffer), the buffer holding those children's p).
-// Pass 2, grid (chunks, b): for requests of mode 1 or 2 each CTA sums, in fp64,
-// the residual and p over one chunk of the terminal row; the last CTA finds the
-// chunk where u_final * Z falls and the token inside it by an in-order scan.
+// Pass 2, grid (term_ctas, b), one wave: for requests of mode 1 to 3 each CTA
+// sums, in fp64, the residual and p over chunks of the terminal row (chunk
+// c by CTA c mod term_ctas); the last CTA of the request finds the chunk
+// where u_final * Z falls and the token inside it by an in-order scan.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "stream_records.cuh"
@@ -499,7 +500,6 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
   pdl_trigger();
   using Tr = LogitTraits<T>;
   const int req = blockIdx.y;
-  const int chunk = blockIdx.x;
   const ReqState st = reinterpret_cast<const ReqState*>(a.state)[req];
   if (st.mode == 0) return;  // every CTA of this request agrees: nothing to sample
   // The state comes from the workspace.  One the stats pass did not write (a
@@ -516,8 +516,6 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
       return;
     }
   }
-  const int begin = chunk * a.chunk2_elems;
-  const int end = min(a.V, begin + a.chunk2_elems);
   // mode 3: the tokens of the terminal node's children (all rejected), read
   // from the tree arrays in one round of loads and walked in shared memory
   __shared__ int s_tok[kMaxN], s_ns[kMaxN], s_excl[kMaxN];
@@ -543,46 +541,52 @@ __global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams
     }
     __syncthreads();
     ex.n = s_nexcl;
-    ex.mark(begin);
-  }
-  double res = 0.0, ps = 0.0;
-  int last_res = -1, last_p = -1;
-  if constexpr (!PROBS) {
-    if (a.vec_term) chunk_mass_vec<T>(a, st, ex, begin, end, res, ps, last_res, last_p);
-    else chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
-  } else {
-    chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
   }
   __shared__ double sres[kThreads / 32], sps[kThreads / 32];
   __shared__ int slr[kThreads / 32], slp[kThreads / 32];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  res = warp_sum_d(res);
-  ps = warp_sum_d(ps);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    last_res = max(last_res, __shfl_xor_sync(0xffffffffu, last_res, o));
-    last_p = max(last_p, __shfl_xor_sync(0xffffffffu, last_p, o));
-  }
-  if (lane == 0) {
-    sres[w] = res;
-    sps[w] = ps;
-    slr[w] = last_res;
-    slp[w] = last_p;
-  }
-  __syncthreads();
   MassPart* parts = reinterpret_cast<MassPart*>(a.partials2) + size_t(req) * a.chunks2;
-  if (threadIdx.x == 0) {
-    MassPart mp{0.0, 0.0, -1, -1, {0, 0}};
-    for (int i = 0; i < nw; ++i) {
-      mp.res += sres[i];
-      mp.p += sps[i];
-      mp.last_res = max(mp.last_res, slr[i]);
-      mp.last_p = max(mp.last_p, slp[i]);
+  // this CTA's chunks: blockIdx.x, + gridDim.x, ...
+  for (int chunk = blockIdx.x; chunk < a.chunks2; chunk += gridDim.x) {
+    const int begin = chunk * a.chunk2_elems;
+    const int end = min(a.V, begin + a.chunk2_elems);
+    if (st.mode == 3) ex.mark(begin);
+    double res = 0.0, ps = 0.0;
+    int last_res = -1, last_p = -1;
+    if constexpr (!PROBS) {
+      if (a.vec_term) chunk_mass_vec<T>(a, st, ex, begin, end, res, ps, last_res, last_p);
+      else chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
+    } else {
+      chunk_mass<T, PROBS>(a, st, ex, begin, end, res, ps, last_res, last_p);
     }
-    parts[chunk] = mp;
+    res = warp_sum_d(res);
+    ps = warp_sum_d(ps);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      last_res = max(last_res, __shfl_xor_sync(0xffffffffu, last_res, o));
+      last_p = max(last_p, __shfl_xor_sync(0xffffffffu, last_p, o));
+    }
+    if (lane == 0) {
+      sres[w] = res;
+      sps[w] = ps;
+      slr[w] = last_res;
+      slp[w] = last_p;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      MassPart mp{0.0, 0.0, -1, -1, {0, 0}};
+      for (int i = 0; i < nw; ++i) {
+        mp.res += sres[i];
+        mp.p += sps[i];
+        mp.last_res = max(mp.last_res, slr[i]);
+        mp.last_p = max(mp.last_p, slp[i]);
+      }
+      parts[chunk] = mp;
+    }
+    __syncthreads();  // the chunk's sums and bitmap are read before the next chunk writes them
   }
 
-  if (!arrive_last(a.counters + req, uint32_t(a.chunks2))) return;
+  if (!arrive_last(a.counters + req, uint32_t(gridDim.x))) return;
 
   // ---- finalize: locate u_final * Z on the cumulative mass ----
   // every chunk's partial in one round of loads, then the prefix in shared memory
@@ -720,7 +724,7 @@ size_t sampling_state_bytes(int b) { return align256(size_t(b) * sizeof(ReqState
 size_t sampling_partial2_bytes(int b, int chunks2) { return align256(size_t(b) * chunks2 * sizeof(MassPart)); }
 
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
-  dim3 g1(p.chunks, p.b * p.n), g2(p.chunks2, p.b);
+  dim3 g1(p.chunks, p.b * p.n), g2(p.term_ctas, p.b);
   cudaError_t e;
   if (!p.probs && p.stream_ctas > 0) {  // the streaming pass, then the row statistics and the walk
     StreamRecParams r{};
