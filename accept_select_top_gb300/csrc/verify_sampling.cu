@@ -494,8 +494,11 @@ __device__ __forceinline__ void chunk_mass_vec(const SamplingParams& a, const Re
   ps = double(kp.sum) - double(kp.comp);
 }
 
-template <typename T, bool PROBS>
-__global__ void __launch_bounds__(kThreads) sampling_bonus_kernel(SamplingParams a) {
+// MINB: CTAs a SM the registers must allow -- 4 for the grid of a CTA a chunk
+// (more CTAs resident, fewer waves), 2 for the looping grid (its one wave of
+// two CTAs a SM; a tighter cap makes the loop spill).
+template <typename T, bool PROBS, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) sampling_bonus_kernel(SamplingParams a) {
   pdl_wait();
   pdl_trigger();
   using Tr = LogitTraits<T>;
@@ -723,8 +726,16 @@ size_t sampling_partial_bytes(int rows, int chunks) { return align256(size_t(row
 size_t sampling_state_bytes(int b) { return align256(size_t(b) * sizeof(ReqState)); }
 size_t sampling_partial2_bytes(int b, int chunks2) { return align256(size_t(b) * chunks2 * sizeof(MassPart)); }
 
+template <typename T, bool PROBS>
+cudaError_t launch_bonus(const SamplingParams& p, cudaStream_t stream) {
+  const dim3 g2(p.term_ctas, p.b);
+  return p.term_ctas == p.chunks2
+             ? launch_pdl(sampling_bonus_kernel<T, PROBS, 4>, g2, dim3(kThreads), 0, stream, p)
+             : launch_pdl(sampling_bonus_kernel<T, PROBS, 2>, g2, dim3(kThreads), 0, stream, p);
+}
+
 int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
-  dim3 g1(p.chunks, p.b * p.n), g2(p.term_ctas, p.b);
+  dim3 g1(p.chunks, p.b * p.n);
   cudaError_t e;
   if (!p.probs && p.stream_ctas > 0) {  // the streaming pass, then the row statistics and the walk
     StreamRecParams r{};
@@ -743,22 +754,22 @@ int launch_verify_sampling(const SamplingParams& p, cudaStream_t stream) {
     const dim3 gr(p.b * ((p.n + rpc - 1) / rpc)), br(32 * rpc);
     if (p.dtype == SPEC_F32) {
       e = launch_pdl(sampling_rowstats_kernel<float>, gr, br, 0, stream, p);
-      if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, false>, g2, dim3(kThreads), 0, stream, p);
+      if (e == cudaSuccess) e = launch_bonus<float, false>(p, stream);
     } else {
       e = launch_pdl(sampling_rowstats_kernel<uint16_t>, gr, br, 0, stream, p);
-      if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t, false>, g2, dim3(kThreads), 0, stream, p);
+      if (e == cudaSuccess) e = launch_bonus<uint16_t, false>(p, stream);
     }
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
   }
   if (p.probs) {  // fp32 probabilities
     e = launch_pdl(sampling_stats_kernel<float, true>, g1, dim3(kThreads), 0, stream, p);
-    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, true>, g2, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_bonus<float, true>(p, stream);
   } else if (p.dtype == SPEC_F32) {
     e = launch_pdl(sampling_stats_kernel<float, false>, g1, dim3(kThreads), 0, stream, p);
-    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<float, false>, g2, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_bonus<float, false>(p, stream);
   } else {
     e = launch_pdl(sampling_stats_kernel<uint16_t, false>, g1, dim3(kThreads), 0, stream, p);
-    if (e == cudaSuccess) e = launch_pdl(sampling_bonus_kernel<uint16_t, false>, g2, dim3(kThreads), 0, stream, p);
+    if (e == cudaSuccess) e = launch_bonus<uint16_t, false>(p, stream);
   }
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
