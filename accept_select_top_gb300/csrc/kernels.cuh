@@ -31,11 +31,11 @@ struct SelectParams {
   // neither.
   bool early;
   int half;
-  // streaming kernel (rows 16-byte aligned, at least one batch of vectors
-  // long): stream_ctas persistent CTAs taking the stream_nb batches from a
-  // queue, group records [stream_nb][2 row parities][256 threads] in the
-  // partials, then each row's k best [rows][kMaxK]; 0 selects the chunked
-  // kernel
+  // streaming pass (rows of whole 16-byte vectors, at least one unit long,
+  // at least kStreamMinBytes of logits): stream_ctas persistent CTAs taking
+  // the stream_nb units of 256 vectors from a queue, group records
+  // [stream_nb][2 row parities][32 lanes] in the partials, then each row's k
+  // best [rows][kMaxK]; 0 selects the chunked kernel
   int stream_ctas, stream_nb;
   uint32_t* error;
   uint32_t* counters;    // this call's half: b counters

@@ -491,11 +491,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(SelectParams a) {
 // The streaming select: the logits streaming pass (stream_records.cu: one
 // record, maximum and exp sum, a group of a lane's 8 vectors of a unit), then
 // select_finalize_kernel, one CTA a row.  From the row's records: the row
-// maximum M, the denominator S = sum of s 2^((g - M) c); theta = the largest
-// over warps of the k-th largest of the lanes' best group maxima (k distinct
-// groups reach it, so the k best elements all do); the groups that reach
-// theta are reloaded, a vector a thread, and their elements that reach it
-// ranked by warp 0 (the k best elements lie in the k best groups).
+// maximum M, the denominator S = sum of s 2^((g - M) c); theta = the k-th
+// largest of the CTA's thread maxima, each the best of that thread's groups
+// (k distinct groups reach it, so the k best elements all do); the groups
+// that reach theta are reloaded, a vector a thread, and their elements that
+// reach it ranked by warp 0 (the k best elements lie in the k best groups).
 // The row's k probabilities and tokens are stored; the CTA whose row is the
 // last of its request to arrive runs the path step of the request.
 
