@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) stream_records_k
     }
   };
   uint4* wring = ring + w * (kStreamStages * kUnitVecs) + lane;
+  const unsigned long long pol = stream_read_policy();
 
   // Without overlap: wait for the grid before, then let the grid after (the
   // request step) launch; it waits for this grid to finish before it reads a
@@ -54,13 +55,13 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamPerSm) stream_records_k
       const unsigned o0 = unsigned(unit) * kUnitVecs + lane;
       if (o0 + (kStreamVpt - 1) * 32 < U) {  // the whole unit exists
 #pragma unroll
-        for (int u = 0; u < kStreamVpt; ++u) stream_cp16(st + u * 32, src + o0 + u * 32, 16u);
+        for (int u = 0; u < kStreamVpt; ++u) stream_cp16(st + u * 32, src + o0 + u * 32, 16u, pol);
       } else {
 #pragma unroll
         for (int u = 0; u < kStreamVpt; ++u) {
           const unsigned o = o0 + u * 32;
           const bool ok = o < U;
-          stream_cp16(st + u * 32, ok ? src + o : src, ok ? 16u : 0u);
+          stream_cp16(st + u * 32, ok ? src + o : src, ok ? 16u : 0u, pol);
         }
       }
     }

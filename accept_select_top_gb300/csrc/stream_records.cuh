@@ -40,10 +40,22 @@ constexpr int kStreamVpt = 8;                     // 16-byte vectors a lane hold
 constexpr int kUnitVecs = kStreamVpt * 32;        // vectors a unit
 constexpr int kStreamCand = 32;                   // candidate elements a warp buffers (one a lane)
 
-// 16-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing.
-__device__ __forceinline__ void stream_cp16(void* dst, const void* src, uint32_t src_bytes) {
+// The L2 policy of the streaming reads: every logit is read once, so its
+// lines go first, and what later steps read again (records, summaries, the
+// rows a request step or a terminal pass reloads) stays longer.
+__device__ __forceinline__ unsigned long long stream_read_policy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte global -> shared copy under L2 policy pol; src_bytes 0 writes zeros
+// and reads nothing.
+__device__ __forceinline__ void stream_cp16(void* dst, const void* src, uint32_t src_bytes, unsigned long long pol) {
   const uint32_t d = uint32_t(__cvta_generic_to_shared(dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(d), "l"(src), "r"(src_bytes),
+               "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
